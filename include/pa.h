@@ -1,0 +1,155 @@
+/*
+ * pa.h - C ABI of libpagedattn: attention over a paged KV cache on GB300 (sm_103a).
+ *
+ * The method is the one "Inside vLLM: Anatomy of a High-Throughput LLM Inference
+ * System" describes: KV lives in fixed-size physical blocks drawn from a pool of
+ * free blocks (§Engine core, "free_block_queue"); each sequence reaches its tokens'
+ * K/V through a block table (§Engine core: blocks are the index from tokens to
+ * their KV; §Worker procedures: the input batch holds the block tables); a block
+ * of a standard layer holds 2*block_size*num_kv_heads*head_size*dtype_bytes bytes
+ * (§Block size); the forward pass sees the batch as one flattened sequence
+ * (§Generate function) and long prompts arrive in chunks (chunked prefill, listed
+ * under the post's advanced features).
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *     never allocates or frees device memory and never synchronises: every call
+ *     only enqueues work on `stream` and returns.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *   - bf16 tensors are raw IEEE bfloat16 (2 bytes).  Every bf16 pointer must be
+ *     16-byte aligned; integer arrays 4-byte aligned.
+ *   - KV pool layout: bf16 [num_blocks][2][num_kv_heads][block_size][head_size],
+ *     contiguous; index 0 of the second axis is K, 1 is V.  One physical block is
+ *     therefore one contiguous run of pa_kv_block_bytes() bytes.
+ *   - A slot is physical_block * block_size + offset_in_block.
+ *   - Query head h uses KV head h / (num_heads / num_kv_heads) (grouped-query
+ *     attention, contiguous groups).
+ *   - Supported shapes: head_size 64 or 128; block_size 8, 16 or 32;
+ *     num_heads / num_kv_heads from 1 to 8.  Others return PA_ERR_UNSUPPORTED.
+ *   - Host-checkable faults return PA_ERR_INVALID_ARG or PA_ERR_UNSUPPORTED and
+ *     enqueue nothing.  A failed launch returns PA_ERR_CUDA.  Device-side data
+ *     (slots, block ids, lengths) is a precondition: the kernels check block ids
+ *     and slots against the pool, skip what lies outside and record it in a
+ *     device error word that pa_error_check() reads (PA_ERR_OOB).  Nothing on
+ *     the device traps.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *pa_stream_t;
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, negative size, bad scale ...   */
+    PA_ERR_UNSUPPORTED = 2, /* valid but outside the supported shapes listed above    */
+    PA_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed            */
+    PA_ERR_OOB = 4,         /* a kernel met a block id or slot outside the pool       */
+    PA_ERR_TIMEOUT = 5,     /* a kernel's bounded wait on its own copies gave up      */
+    PA_ERR_WORKSPACE = 6    /* workspace pointer null/misaligned or smaller than asked */
+} pa_status;
+
+/* Human-readable name of a status; never NULL. */
+const char *pa_status_string(pa_status status);
+
+/*
+ * Bytes of one KV block, 2 * block_size * num_kv_heads * head_size * 2 (bf16),
+ * the formula of §Block size.  Returns 0 for non-positive arguments.
+ */
+size_t pa_kv_block_bytes(int block_size, int num_kv_heads, int head_size);
+
+/*
+ * pa_cache_write - scatter new tokens' K and V rows into their slots.
+ *
+ * Follows §Engine core (a token's KV lives in the block its sequence was given).
+ *   kv_cache      [num_blocks][2][num_kv_heads][block_size][head_size] bf16, in/out
+ *   k_new, v_new  [num_tokens][num_kv_heads][head_size] bf16 rows; row i starts
+ *                 at element i * new_row_stride (new_row_stride >= num_kv_heads *
+ *                 head_size, a multiple of 8), heads contiguous inside a row
+ *   slot_mapping  [num_tokens] int32; slot < 0 skips the row (padding); a slot
+ *                 >= num_blocks*block_size is skipped and flagged PA_ERR_OOB
+ * Bit-exact copy.  Two rows with the same slot in one call are a precondition
+ * violation (which one lands is unspecified).  num_tokens == 0 is a no-op.
+ */
+pa_status pa_cache_write(void *kv_cache, int num_blocks, int block_size, int num_kv_heads,
+                         int head_size, const void *k_new, const void *v_new,
+                         int64_t new_row_stride, const int32_t *slot_mapping, int num_tokens,
+                         pa_stream_t stream);
+
+/*
+ * Workspace pa_decode needs on the current device for this shape, in bytes
+ * (partial softmax states of split contexts plus a small table).  Depends on
+ * the device's SM count.  Returns 0 for invalid arguments.
+ */
+size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, int head_size);
+
+/*
+ * pa_decode - one query token per sequence against its paged context.
+ *
+ * Sequence s attends to its tokens 0 .. seq_lens[s]-1, found through
+ * block_tables[s][t / block_size] at offset t % block_size; the new token's own
+ * K/V must already be written (pa_cache_write), so seq_lens[s] counts it.
+ *   out           [num_seqs][num_heads][head_size] bf16, written
+ *   q             [num_seqs][num_heads][head_size] bf16
+ *   block_tables  [num_seqs][max_blocks_per_seq] int32 physical block ids
+ *   seq_lens      [num_seqs] int32, 0 <= seq_lens[s] <= max_blocks_per_seq*block_size;
+ *                 0 yields a zero output row
+ *   max_seq_len   host-side upper bound of seq_lens (sizes the launch only)
+ *   scale         softmax scale applied to q.k (e.g. 1/sqrt(head_size)), finite
+ *   workspace     device scratch of >= pa_decode_workspace_bytes(...) bytes,
+ *                 256-byte aligned, owned by the caller, contents need no
+ *                 initialisation; two calls that overlap on the GPU must not
+ *                 share one workspace
+ * out[s][h] = sum_t softmax_t(scale * q[s][h].K[t][h/G]) V[t][h/G], computed
+ * with an online softmax in fp32 over bf16 products; contexts are split evenly
+ * over the whole GPU and the pieces merged by log-sum-exp.  num_seqs == 0 is a
+ * no-op.
+ */
+pa_status pa_decode(void *out, const void *q, const void *kv_cache, int num_blocks,
+                    int block_size, int num_heads, int num_kv_heads, int head_size,
+                    const int32_t *block_tables, int max_blocks_per_seq,
+                    const int32_t *seq_lens, int num_seqs, int max_seq_len, float scale,
+                    void *workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * pa_prefill_chunk - chunked-prefill attention of query chunks against their
+ * cached context and themselves, causal.
+ *
+ * The batch is flattened (§Generate function): chunk s owns query rows
+ * cu_q_lens[s] .. cu_q_lens[s+1]-1.  Its q_len = cu_q_lens[s+1]-cu_q_lens[s]
+ * new tokens sit at positions seq_lens[s]-q_len .. seq_lens[s]-1 and their K/V
+ * must already be written to the pool; row i sees tokens 0 .. seq_lens[s]-q_len+i.
+ *   out           [total_q][num_heads][head_size] bf16, written
+ *   q             [total_q][num_heads][head_size] bf16
+ *   cu_q_lens     [num_chunks+1] int32, cu_q_lens[0] == 0, non-decreasing
+ *   max_q_len     host-side upper bound of any chunk's q_len (sizes the launch)
+ *   block_tables  [num_chunks][max_blocks_per_seq] int32
+ *   seq_lens      [num_chunks] int32 context + chunk, >= that chunk's q_len
+ * Tensor cores compute q.K^T and P.V in bf16 with fp32 accumulation.
+ * num_chunks == 0 or max_q_len == 0 is a no-op.
+ */
+pa_status pa_prefill_chunk(void *out, const void *q, const int32_t *cu_q_lens, int num_chunks,
+                           int max_q_len, const void *kv_cache, int num_blocks, int block_size,
+                           int num_heads, int num_kv_heads, int head_size,
+                           const int32_t *block_tables, int max_blocks_per_seq,
+                           const int32_t *seq_lens, float scale, pa_stream_t stream);
+
+/*
+ * Synchronise `stream`, then read and clear the device error word the kernels
+ * of this library set on the current device.  Returns PA_OK, PA_ERR_OOB,
+ * PA_ERR_TIMEOUT, or PA_ERR_CUDA if the synchronisation itself failed.
+ */
+pa_status pa_error_check(pa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H */

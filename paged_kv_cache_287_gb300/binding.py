@@ -1,0 +1,167 @@
+"""Thin ctypes binding of libpagedattn (the C ABI in ``include/pa.h``).
+
+Argument marshalling only: every step of the computation runs in the library's
+CUDA kernels.  Functions keep the C names; tensors are PyTorch CUDA tensors
+whose data pointers are passed through, and the stream defaults to PyTorch's
+current stream.  If the library is missing this module raises on first use:
+there is no fallback path.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libpagedattn.so")
+
+STATUS = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_CUDA",
+          4: "PA_ERR_OOB", 5: "PA_ERR_TIMEOUT", 6: "PA_ERR_WORKSPACE"}
+
+# Every symbol include/pa.h declares.
+EXPORTS = ("pa_status_string", "pa_kv_block_bytes", "pa_cache_write",
+           "pa_decode_workspace_bytes", "pa_decode", "pa_prefill_chunk", "pa_error_check")
+
+
+class PaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+
+
+_lib = None
+
+
+def lib(path: Optional[str] = None):
+    """Load libpagedattn.so and declare its entry points (raises if absent)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(
+            f"{p} not found: build it with `python -c 'import __graft_entry__ as g; g.build()'`")
+    L = ctypes.CDLL(p)
+    P, i, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    L.pa_status_string.restype = ctypes.c_char_p
+    L.pa_status_string.argtypes = [i]
+    L.pa_kv_block_bytes.restype = sz
+    L.pa_kv_block_bytes.argtypes = [i, i, i]
+    L.pa_cache_write.restype = i
+    L.pa_cache_write.argtypes = [P, i, i, i, i, P, P, i64, P, i, P]
+    L.pa_decode_workspace_bytes.restype = sz
+    L.pa_decode_workspace_bytes.argtypes = [i, i, i, i]
+    L.pa_decode.restype = i
+    L.pa_decode.argtypes = [P, P, P, i, i, i, i, i, P, i, P, i, i, ctypes.c_float, P, sz, P]
+    L.pa_prefill_chunk.restype = i
+    L.pa_prefill_chunk.argtypes = [P, P, P, i, i, P, i, i, i, i, i, P, i, P, ctypes.c_float, P]
+    L.pa_error_check.restype = i
+    L.pa_error_check.argtypes = [P]
+    if path is None:
+        _lib = L
+    return L
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise PaError(status, where)
+
+
+def _need(t: torch.Tensor, name: str, dtype, dims: Optional[int] = None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if dims is not None and t.dim() != dims:
+        raise ValueError(f"{name} must have {dims} dims, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _pool_geom(kv_cache: torch.Tensor):
+    _need(kv_cache, "kv_cache", torch.bfloat16, 5)
+    NB, two, Hkv, bs, D = kv_cache.shape
+    if two != 2:
+        raise ValueError("kv_cache must be [num_blocks, 2, num_kv_heads, block_size, head_size]")
+    return NB, bs, Hkv, D
+
+
+def pa_kv_block_bytes(block_size: int, num_kv_heads: int, head_size: int) -> int:
+    return int(lib().pa_kv_block_bytes(block_size, num_kv_heads, head_size))
+
+
+def pa_cache_write(kv_cache: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                   slot_mapping: torch.Tensor, stream=None) -> None:
+    """Scatter k_new/v_new [N, Hkv, D] rows into kv_cache at slot_mapping [N]."""
+    NB, bs, Hkv, D = _pool_geom(kv_cache)
+    _need(k_new, "k_new", torch.bfloat16, 3)
+    _need(v_new, "v_new", torch.bfloat16, 3)
+    _need(slot_mapping, "slot_mapping", torch.int32, 1)
+    N = slot_mapping.shape[0]
+    if k_new.shape != (N, Hkv, D) or v_new.shape != (N, Hkv, D):
+        raise ValueError("k_new/v_new must be [num_tokens, num_kv_heads, head_size]")
+    _check(lib().pa_cache_write(kv_cache.data_ptr(), NB, bs, Hkv, D, k_new.data_ptr(),
+                                v_new.data_ptr(), Hkv * D, slot_mapping.data_ptr(), N,
+                                _stream(stream)), "pa_cache_write")
+
+
+def pa_decode_workspace_bytes(num_seqs: int, num_heads: int, num_kv_heads: int,
+                              head_size: int) -> int:
+    return int(lib().pa_decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_size))
+
+
+def pa_decode(out: torch.Tensor, q: torch.Tensor, kv_cache: torch.Tensor,
+              block_tables: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+              scale: float, workspace: torch.Tensor, stream=None) -> None:
+    """Decode attention: q/out [B, Hq, D], block_tables [B, MB], seq_lens [B]."""
+    NB, bs, Hkv, D = _pool_geom(kv_cache)
+    _need(q, "q", torch.bfloat16, 3)
+    _need(out, "out", torch.bfloat16, 3)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(workspace, "workspace", torch.uint8, 1)
+    B, Hq, Dq = q.shape
+    if Dq != D or out.shape != q.shape or seq_lens.shape[0] != B or block_tables.shape[0] != B:
+        raise ValueError("inconsistent decode shapes")
+    _check(lib().pa_decode(out.data_ptr(), q.data_ptr(), kv_cache.data_ptr(), NB, bs, Hq, Hkv, D,
+                           block_tables.data_ptr(), block_tables.shape[1], seq_lens.data_ptr(),
+                           B, int(max_seq_len), float(scale), workspace.data_ptr(),
+                           workspace.numel(), _stream(stream)), "pa_decode")
+
+
+def pa_prefill_chunk(out: torch.Tensor, q: torch.Tensor, cu_q_lens: torch.Tensor,
+                     max_q_len: int, kv_cache: torch.Tensor, block_tables: torch.Tensor,
+                     seq_lens: torch.Tensor, scale: float, stream=None) -> None:
+    """Chunked-prefill attention: q/out [sum q_len, Hq, D], cu_q_lens [n+1]."""
+    NB, bs, Hkv, D = _pool_geom(kv_cache)
+    _need(q, "q", torch.bfloat16, 3)
+    _need(out, "out", torch.bfloat16, 3)
+    _need(cu_q_lens, "cu_q_lens", torch.int32, 1)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    n = seq_lens.shape[0]
+    Hq = q.shape[1]
+    if q.shape[2] != D or out.shape != q.shape or cu_q_lens.shape[0] != n + 1 or \
+            block_tables.shape[0] != n:
+        raise ValueError("inconsistent prefill shapes")
+    _check(lib().pa_prefill_chunk(out.data_ptr(), q.data_ptr(), cu_q_lens.data_ptr(), n,
+                                  int(max_q_len), kv_cache.data_ptr(), NB, bs, Hq, Hkv, D,
+                                  block_tables.data_ptr(), block_tables.shape[1],
+                                  seq_lens.data_ptr(), float(scale), _stream(stream)),
+           "pa_prefill_chunk")
+
+
+def pa_error_check(stream=None) -> None:
+    """Synchronise the stream and raise if a kernel flagged bad device data."""
+    _check(lib().pa_error_check(_stream(stream)), "pa_error_check")

@@ -1,0 +1,189 @@
+// pa_api.cu - the C ABI declared in include/pa.h: host-side argument checks,
+// launch configuration and the device error word.  Allocates nothing.
+#include <cudaTypedefs.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "pa.h"
+#include "pa_internal.h"
+
+namespace pa {
+
+int device_sm_count() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
+    return sms > 0 ? sms : 1;
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool encode_kv_map(CUtensorMap *map, const void *kv_cache, const KvGeom &g, int box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t rows =
+        (cuuint64_t)g.num_blocks * 2u * (cuuint64_t)g.num_kv_heads * (cuuint64_t)g.block_size;
+    cuuint64_t dims[2] = {(cuuint64_t)g.head_size, rows};
+    cuuint64_t strides[1] = {(cuuint64_t)g.head_size * 2u};
+    cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(kv_cache), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace pa
+
+namespace {
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Checks common to every entry point that reads the pool.
+pa_status check_pool(const void *kv_cache, int num_blocks, int block_size, int num_kv_heads,
+                     int head_size) {
+    if (!kv_cache || !aligned(kv_cache, 16)) return PA_ERR_INVALID_ARG;
+    if (num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 || head_size <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (head_size != 64 && head_size != 128) return PA_ERR_UNSUPPORTED;
+    if (block_size != 8 && block_size != 16 && block_size != 32) return PA_ERR_UNSUPPORTED;
+    if (num_kv_heads > 255) return PA_ERR_UNSUPPORTED;
+    // Pool rows must fit the signed 32-bit TMA row coordinate.
+    const long long rows = (long long)num_blocks * 2 * num_kv_heads * block_size;
+    if (rows >= (1LL << 30)) return PA_ERR_UNSUPPORTED;
+    return PA_OK;
+}
+
+pa_status check_heads(int num_heads, int num_kv_heads) {
+    if (num_heads <= 0 || num_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    const int group = num_heads / num_kv_heads;
+    if (group > 8) return PA_ERR_UNSUPPORTED;
+    return PA_OK;
+}
+
+pa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char *pa_status_string(pa_status status) {
+    switch (status) {
+        case PA_OK: return "PA_OK";
+        case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+        case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+        case PA_ERR_CUDA: return "PA_ERR_CUDA";
+        case PA_ERR_OOB: return "PA_ERR_OOB";
+        case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT";
+        case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
+    }
+    return "PA_ERR_UNKNOWN";
+}
+
+size_t pa_kv_block_bytes(int block_size, int num_kv_heads, int head_size) {
+    if (block_size <= 0 || num_kv_heads <= 0 || head_size <= 0) return 0;
+    return (size_t)2 * (size_t)block_size * (size_t)num_kv_heads * (size_t)head_size * 2u;
+}
+
+pa_status pa_cache_write(void *kv_cache, int num_blocks, int block_size, int num_kv_heads,
+                         int head_size, const void *k_new, const void *v_new,
+                         int64_t new_row_stride, const int32_t *slot_mapping, int num_tokens,
+                         pa_stream_t stream) {
+    pa_status st = check_pool(kv_cache, num_blocks, block_size, num_kv_heads, head_size);
+    if (st != PA_OK) return st;
+    if (num_tokens < 0) return PA_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PA_OK;
+    if (!k_new || !v_new || !slot_mapping || !aligned(k_new, 16) || !aligned(v_new, 16) ||
+        !aligned(slot_mapping, 4))
+        return PA_ERR_INVALID_ARG;
+    if (new_row_stride < (int64_t)num_kv_heads * head_size || new_row_stride % 8 != 0)
+        return PA_ERR_INVALID_ARG;
+    pa::KvGeom g{num_blocks, block_size, num_kv_heads, head_size};
+    return from_cuda(pa::launch_cache_write(kv_cache, g, k_new, v_new, new_row_stride,
+                                            slot_mapping, num_tokens,
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, int head_size) {
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_size <= 0) return 0;
+    if (num_heads % num_kv_heads != 0) return 0;
+    return pa::decode_workspace_bytes(num_seqs, head_size, pa::device_sm_count());
+}
+
+pa_status pa_decode(void *out, const void *q, const void *kv_cache, int num_blocks,
+                    int block_size, int num_heads, int num_kv_heads, int head_size,
+                    const int32_t *block_tables, int max_blocks_per_seq,
+                    const int32_t *seq_lens, int num_seqs, int max_seq_len, float scale,
+                    void *workspace, size_t workspace_bytes, pa_stream_t stream) {
+    pa_status st = check_pool(kv_cache, num_blocks, block_size, num_kv_heads, head_size);
+    if (st != PA_OK) return st;
+    if ((st = check_heads(num_heads, num_kv_heads)) != PA_OK) return st;
+    if (num_seqs < 0 || max_seq_len < 0 || max_blocks_per_seq <= 0) return PA_ERR_INVALID_ARG;
+    if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f) return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !q || !block_tables || !seq_lens || !aligned(out, 16) || !aligned(q, 16) ||
+        !aligned(block_tables, 4) || !aligned(seq_lens, 4))
+        return PA_ERR_INVALID_ARG;
+    if (max_seq_len > max_blocks_per_seq * block_size) return PA_ERR_INVALID_ARG;
+    if (num_seqs > pa::decode_max_seqs(head_size)) return PA_ERR_UNSUPPORTED;
+    if ((long long)num_seqs * num_kv_heads * (((long long)max_seq_len + 15) / 16) >= (1LL << 31))
+        return PA_ERR_UNSUPPORTED;
+    const size_t need = pa::decode_workspace_bytes(num_seqs, head_size, pa::device_sm_count());
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return PA_ERR_WORKSPACE;
+    pa::KvGeom g{num_blocks, block_size, num_kv_heads, head_size};
+    return from_cuda(pa::launch_decode(out, q, kv_cache, g, num_heads, block_tables,
+                                       max_blocks_per_seq, seq_lens, num_seqs, max_seq_len, scale,
+                                       workspace, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+pa_status pa_prefill_chunk(void *out, const void *q, const int32_t *cu_q_lens, int num_chunks,
+                           int max_q_len, const void *kv_cache, int num_blocks, int block_size,
+                           int num_heads, int num_kv_heads, int head_size,
+                           const int32_t *block_tables, int max_blocks_per_seq,
+                           const int32_t *seq_lens, float scale, pa_stream_t stream) {
+    pa_status st = check_pool(kv_cache, num_blocks, block_size, num_kv_heads, head_size);
+    if (st != PA_OK) return st;
+    if ((st = check_heads(num_heads, num_kv_heads)) != PA_OK) return st;
+    if (num_chunks < 0 || max_q_len < 0 || max_blocks_per_seq <= 0) return PA_ERR_INVALID_ARG;
+    if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f) return PA_ERR_INVALID_ARG;
+    if (num_chunks == 0 || max_q_len == 0) return PA_OK;
+    if (!out || !q || !cu_q_lens || !block_tables || !seq_lens || !aligned(out, 16) ||
+        !aligned(q, 16) || !aligned(cu_q_lens, 4) || !aligned(block_tables, 4) ||
+        !aligned(seq_lens, 4))
+        return PA_ERR_INVALID_ARG;
+    if (num_chunks > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+    pa::KvGeom g{num_blocks, block_size, num_kv_heads, head_size};
+    return from_cuda(pa::launch_prefill(out, q, cu_q_lens, num_chunks, max_q_len, kv_cache, g,
+                                        num_heads, block_tables, max_blocks_per_seq, seq_lens,
+                                        scale, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+pa_status pa_error_check(pa_stream_t stream) {
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return PA_ERR_CUDA;
+    unsigned bits = 0, b = 0;
+    if (pa::take_error_cache_write(&b) != cudaSuccess) return PA_ERR_CUDA;
+    bits |= b;
+    if (pa::take_error_decode(&b) != cudaSuccess) return PA_ERR_CUDA;
+    bits |= b;
+    if (pa::take_error_prefill(&b) != cudaSuccess) return PA_ERR_CUDA;
+    bits |= b;
+    if (bits & 2u) return PA_ERR_TIMEOUT;
+    if (bits & 1u) return PA_ERR_OOB;
+    return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,529 @@
+// pa_decode.cu - paged decode attention: one query token per sequence.
+//
+// The method: "Inside vLLM: Anatomy of a High-Throughput LLM Inference System"
+// (§Engine core: a sequence's tokens are found through the blocks its block table
+// names; §Block size: one block holds K and V of block_size tokens for every KV
+// head).  Each sequence's query attends to all its cached tokens.
+//
+// GB300 design
+//   * Work = the flattened list of 16-token tiles over (sequence, KV head).  The
+//     list is cut into equal contiguous ranges, one per warp of a persistent grid
+//     (152 SMs x W warps), so skewed lengths cost nothing in balance.  A
+//     (sequence, head) segment that falls across ranges is finished in pieces whose
+//     (max, sum, acc) states are merged by log-sum-exp in a second small kernel.
+//   * Every warp runs its own pipeline: lane 0 issues 128B-swizzled 2-D TMA
+//     copies of the K and V tiles named by the block table into an S-stage ring in
+//     shared memory (plus the segment's G query rows with a bulk copy); the warp
+//     waits on the stage's mbarrier, computes, and refills the stage.  No
+//     CTA-wide synchronisation inside the loop.
+//   * Per tile the warp computes S^T = K.Q^T (16 tokens x 8 query heads of the GQA
+//     group) with one m16n8k16 bf16 MMA per 16 dims, runs the online softmax in
+//     fp32 (log2 domain), transposes P in registers (movmatrix) and accumulates
+//     O^T += V^T.P^T with ldmatrix.trans.  The math is a few hundred instructions
+//     per 8 KB tile, far below what HBM delivers per SM, so the kernel is
+//     HBM-bound.
+#include <algorithm>
+
+#include "pa_common.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+__device__ unsigned g_err_decode;
+
+constexpr int kTile = 16;         // tokens per tile (the MMA's M)
+constexpr int kHeadsPad = 8;      // query heads per KV head, padded to the MMA's N
+constexpr int kDecodeWarps = 4;   // warps per CTA, one CTA per SM
+constexpr int kDecodeStages = 4;  // ring depth per warp
+
+template <int D>
+struct Lay {
+    static constexpr int kPanels = D / 64;             // 128-byte-wide column panels
+    static constexpr int kPanelBytes = kTile * 128;    // 16 rows of one panel
+    static constexpr int kKvBytes = kPanels * kPanelBytes;
+    static constexpr int kQBytes = kHeadsPad * D * 2;  // query rows / output staging
+    static constexpr int kStageBytes = 2 * kKvBytes + kQBytes;
+};
+
+struct DecodeArgs {
+    __nv_bfloat16 *out;
+    const __nv_bfloat16 *q;
+    const int32_t *block_tables;
+    const int32_t *seq_lens;
+    float *part_acc;   // [2*total_warps][8][D]
+    float *part_ml;    // [2*total_warps][8][2]  (max in log2 units, sum)
+    int32_t *prefix;   // [num_seqs+1] tile prefix over sequences
+    int num_seqs, num_heads, num_kv_heads, group;
+    int block_size, max_blocks, num_blocks;
+    int total_warps;
+    float scale_log2;  // scale * log2(e)
+};
+
+__host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+template <int D>
+__host__ __device__ constexpr size_t decode_smem_bytes(int num_seqs) {
+    return 1024 /* alignment slack */ + (size_t)kDecodeWarps * kDecodeStages * Lay<D>::kStageBytes +
+           (size_t)kDecodeWarps * kDecodeStages * 8 + (size_t)(2 * num_seqs + 1) * 4;
+}
+
+// TMA row of (block, K, head, offset) in the pool viewed as rows of head_size.
+__device__ __forceinline__ int kv_row(int blk, int h, int off, const DecodeArgs &a) {
+    if (blk < 0 || blk >= a.num_blocks) {
+        atomicOr(&g_err_decode, kErrOob);
+        return -(1 << 30);  // wholly outside the map: TMA fills zeros, nothing is read
+    }
+    return ((blk * 2) * a.num_kv_heads + h) * a.block_size + off;
+}
+
+template <int D, int W, int S>
+__global__ void __launch_bounds__(W * 32, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
+    using L = Lay<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(align_up(reinterpret_cast<size_t>(smem_raw), 1024));
+    uint8_t *ring = smem;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)W * S * L::kStageBytes);
+    int *s_len = reinterpret_cast<int *>(bars + W * S);
+    int *s_pre = s_len + a.num_seqs;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int B = a.num_seqs, Hkv = a.num_kv_heads, G = a.group, bs = a.block_size;
+
+    if (tid == 0) prefetch_tensormap(&kv_map);
+    // Lengths (clamped to what the table can hold) and the tile prefix over sequences.
+    const int max_len = a.max_blocks * bs;
+    for (int s = tid; s < B; s += W * 32) {
+        int len = a.seq_lens[s];
+        if (len < 0 || len > max_len) {
+            atomicOr(&g_err_decode, kErrOob);
+            len = len < 0 ? 0 : max_len;
+        }
+        s_len[s] = len;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int carry = 0;
+        for (int base = 0; base < B; base += 32) {
+            const int s = base + lane;
+            const int nt = s < B ? (s_len[s] + kTile - 1) / kTile : 0;
+            int v = nt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += u;
+            }
+            if (s < B) s_pre[s] = carry + v - nt;
+            carry += __shfl_sync(0xffffffffu, v, 31);
+        }
+        if (lane == 0) s_pre[B] = carry;
+    }
+    if (lane == 0) {
+        for (int st = 0; st < S; ++st) mbar_init(&bars[warp * S + st], 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (blockIdx.x == 0)
+        for (int s = tid; s <= B; s += W * 32) a.prefix[s] = s_pre[s];
+
+    // This warp's equal share of the flattened tile list.
+    const long long T = (long long)s_pre[B] * Hkv;
+    const long long NW = a.total_warps;
+    const long long g = (long long)blockIdx.x * W + warp;
+    const int t_begin = (int)((g * T) / NW);
+    const int t_end = (int)(((g + 1) * T) / NW);
+    const int n = t_end - t_begin;
+    if (n <= 0) return;
+
+    uint8_t *wring = ring + (size_t)warp * S * L::kStageBytes;
+    uint64_t *wbar = bars + warp * S;
+
+    // Tile descriptors, one tile per lane, for two batches of 32 tiles.
+    //   rk0 / rk1: TMA row of the K rows of the tile's first / second box (-1: none)
+    //   seg: (sequence << 8) | kv head;   jt: tile index inside the segment
+    auto make_desc = [&](int batch, int &rk0, int &rk1, int &seg, int &jt) {
+        const int x = t_begin + batch * 32 + lane;
+        rk0 = -1;
+        rk1 = -1;
+        seg = -1;
+        jt = 0;
+        if (batch * 32 + lane >= n) return;
+        int lo = 0, hi = B - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (Hkv * s_pre[mid] <= x) lo = mid; else hi = mid - 1;
+        }
+        const int s = lo;
+        const int nt = s_pre[s + 1] - s_pre[s];
+        const int r = x - Hkv * s_pre[s];
+        const int h = r / nt;
+        const int j = r - h * nt;
+        seg = (s << 8) | h;
+        jt = j;
+        const int32_t *bt = a.block_tables + (size_t)s * a.max_blocks;
+        const int tok0 = j * kTile;
+        if (bs >= kTile) {
+            rk0 = kv_row(bt[tok0 / bs], h, tok0 % bs, a);
+        } else {  // block_size 8: two blocks per tile, the second only if it holds tokens
+            rk0 = kv_row(bt[tok0 / bs], h, 0, a);
+            if (tok0 + bs < s_len[s]) rk1 = kv_row(bt[tok0 / bs + 1], h, 0, a);
+        }
+    };
+
+    int dA0, dA1, dA2, dA3, dB0, dB1, dB2, dB3;
+    make_desc(0, dA0, dA1, dA2, dA3);
+    make_desc(1, dB0, dB1, dB2, dB3);
+    int cur_batch = 0;
+
+    const int box_rows = bs >= kTile ? kTile : bs;
+    const uint32_t box_bytes = (uint32_t)box_rows * 128u;
+    const uint32_t q_bytes = (uint32_t)G * D * 2u;
+    const int v_row_off = Hkv * bs;
+    const uint64_t policy = policy_evict_first();
+
+    auto issue = [&](int i) {
+        const bool in_a = (i >> 5) == cur_batch;
+        const int src = i & 31;
+        const int rk0 = __shfl_sync(0xffffffffu, in_a ? dA0 : dB0, src);
+        const int rk1 = __shfl_sync(0xffffffffu, in_a ? dA1 : dB1, src);
+        const int seg = __shfl_sync(0xffffffffu, in_a ? dA2 : dB2, src);
+        int prev = -1;
+        if (i > 0) {
+            const bool pa_ = ((i - 1) >> 5) == cur_batch;
+            prev = __shfl_sync(0xffffffffu, pa_ ? dA2 : dB2, (i - 1) & 31);
+        }
+        if (lane == 0) {
+            uint8_t *stg = wring + (size_t)(i % S) * L::kStageBytes;
+            uint64_t *bar = wbar + (i % S);
+            const bool new_seg = seg != prev;
+            const int nbox = rk1 >= 0 ? 2 : 1;
+            const uint32_t bytes =
+                (uint32_t)(2 * L::kPanels * nbox) * box_bytes + (new_seg ? q_bytes : 0u);
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(bar, bytes);
+#pragma unroll
+            for (int p = 0; p < L::kPanels; ++p) {
+                tma_load_2d_hint(stg + p * L::kPanelBytes, &kv_map, bar, 64 * p, rk0, policy);
+                tma_load_2d_hint(stg + L::kKvBytes + p * L::kPanelBytes, &kv_map, bar, 64 * p,
+                                 rk0 + v_row_off, policy);
+                if (rk1 >= 0) {
+                    tma_load_2d_hint(stg + p * L::kPanelBytes + bs * 128, &kv_map, bar, 64 * p,
+                                     rk1, policy);
+                    tma_load_2d_hint(stg + L::kKvBytes + p * L::kPanelBytes + bs * 128, &kv_map,
+                                     bar, 64 * p, rk1 + v_row_off, policy);
+                }
+            }
+            if (new_seg) {
+                const int s = seg >> 8, h = seg & 255;
+                bulk_load(stg + 2 * L::kKvBytes,
+                          a.q + ((size_t)s * a.num_heads + (size_t)h * G) * D, q_bytes, bar);
+            }
+        }
+    };
+
+    const int first_issue = n < S ? n : S;
+    for (int i = 0; i < first_issue; ++i) issue(i);
+    int issued = first_issue;
+
+    float acc[D / 16][4];
+    uint32_t qf[D / 16][2];
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    int prev_seg = -1, first_j = 0;
+    bool first_piece = true;
+    const int hq_row = lane >> 2;          // query head (MMA column) this lane feeds
+    const int hh0 = 2 * (lane & 3);        // query heads whose results this lane holds
+    const int tr0 = lane >> 2;             // tokens whose scores this lane holds: tr0, tr0+8
+
+    for (int c = 0; c < n; ++c) {
+        const int st = c % S;
+        uint8_t *stg = wring + (size_t)st * L::kStageBytes;
+        if (!mbar_wait_bounded(wbar + st, (uint32_t)(c / S) & 1u)) {
+            if (lane == 0) atomicOr(&g_err_decode, kErrTimeout);
+            // Give the copies still in flight a bounded chance to land, then leave.
+            for (int k = c + 1; k < issued; ++k)
+                mbar_wait_bounded(wbar + (k % S), (uint32_t)(k / S) & 1u);
+            return;
+        }
+        const int src = c & 31;
+        const int seg = __shfl_sync(0xffffffffu, dA2, src);
+        const int j = __shfl_sync(0xffffffffu, dA3, src);
+        int next_seg = -2;
+        if (c + 1 < n) {
+            const bool in_a = ((c + 1) >> 5) == cur_batch;
+            next_seg = __shfl_sync(0xffffffffu, in_a ? dA2 : dB2, (c + 1) & 31);
+        }
+        const int s = seg >> 8, h = seg & 255;
+        const __nv_bfloat16 *qslot = reinterpret_cast<const __nv_bfloat16 *>(stg + 2 * L::kKvBytes);
+        if (seg != prev_seg) {
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k) {
+                if (hq_row < G) {
+                    const __nv_bfloat16 *qr = qslot + hq_row * D + 16 * k + 2 * (lane & 3);
+                    qf[k][0] = *reinterpret_cast<const uint32_t *>(qr);
+                    qf[k][1] = *reinterpret_cast<const uint32_t *>(qr + 8);
+                } else {
+                    qf[k][0] = 0u;
+                    qf[k][1] = 0u;
+                }
+            }
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
+            m0 = m1 = -INFINITY;
+            l0 = l1 = 0.f;
+            first_j = j;
+        }
+        const int len = s_len[s];
+        const int valid = min(kTile, len - j * kTile);
+        bool wrote_smem = false;
+        if (valid < kTile) {
+            // Stale rows past the sequence end may hold anything (NaN included):
+            // zero their V so P=0 contributes exactly nothing.
+            const int rows = kTile - valid;
+            for (int e = lane; e < rows * 8 * L::kPanels; e += 32) {
+                const int p = e / (rows * 8);
+                const int rr = (e / 8) % rows;
+                const int ch = e & 7;
+                *reinterpret_cast<uint4 *>(stg + L::kKvBytes + p * L::kPanelBytes +
+                                           (valid + rr) * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+            }
+            wrote_smem = true;
+            __syncwarp();
+        }
+
+        // S^T[token][head] = K . Q^T
+        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint32_t kbase = smem_u32(stg);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+            const uint32_t panel = kbase + (k >> 2) * L::kPanelBytes;
+            const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
+            const int chunk = 2 * (k & 3) + (lane >> 4);
+            uint32_t af[4];
+            ldsm_x4(af, swz128(panel, row, chunk));
+            mma_bf16(sc, af, qf[k][0], qf[k][1]);
+        }
+        const float x0 = tr0 < valid ? sc[0] * a.scale_log2 : -INFINITY;
+        const float x1 = tr0 < valid ? sc[1] * a.scale_log2 : -INFINITY;
+        const float x2 = tr0 + 8 < valid ? sc[2] * a.scale_log2 : -INFINITY;
+        const float x3 = tr0 + 8 < valid ? sc[3] * a.scale_log2 : -INFINITY;
+        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+        }
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float cr0 = fast_exp2(m0 - mn0), cr1 = fast_exp2(m1 - mn1);
+        const uint32_t plo = pack_bf16(fast_exp2(x0 - mn0), fast_exp2(x1 - mn1));
+        const uint32_t phi = pack_bf16(fast_exp2(x2 - mn0), fast_exp2(x3 - mn1));
+        float ps0 = bf16_lo(plo) + bf16_lo(phi), ps1 = bf16_hi(plo) + bf16_hi(phi);
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            ps0 += __shfl_xor_sync(0xffffffffu, ps0, o);
+            ps1 += __shfl_xor_sync(0xffffffffu, ps1, o);
+        }
+        l0 = l0 * cr0 + ps0;
+        l1 = l1 * cr1 + ps1;
+        m0 = mn0;
+        m1 = mn1;
+        const uint32_t b0 = movmatrix_t(plo), b1 = movmatrix_t(phi);
+
+        // O^T[dim][head] += V^T . P^T
+        const uint32_t vbase = kbase + L::kKvBytes;
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+            acc[mt][0] *= cr0;
+            acc[mt][1] *= cr1;
+            acc[mt][2] *= cr0;
+            acc[mt][3] *= cr1;
+            const uint32_t panel = vbase + (mt >> 2) * L::kPanelBytes;
+            const int mi = lane >> 3;
+            const int row = (lane & 7) + (mi >> 1) * 8;
+            const int chunk = 2 * (mt & 3) + (mi & 1);
+            uint32_t af[4];
+            ldsm_x4_t(af, swz128(panel, row, chunk));
+            mma_bf16(acc[mt], af, b0, b1);
+        }
+
+        if (next_seg != seg) {
+            const int nt = s_pre[s + 1] - s_pre[s];
+            if (first_j == 0 && j == nt - 1) {
+                // Whole segment in this warp: normalise and write bf16 rows, staged in
+                // the stage's query slot for 16-byte stores.
+                __nv_bfloat16 *stage_out =
+                    reinterpret_cast<__nv_bfloat16 *>(stg + 2 * L::kKvBytes);
+                const float i0 = 1.f / l0, i1 = 1.f / l1;
+#pragma unroll
+                for (int mt = 0; mt < D / 16; ++mt) {
+                    const int d0 = mt * 16 + tr0;
+                    stage_out[hh0 * D + d0] = __float2bfloat16_rn(acc[mt][0] * i0);
+                    stage_out[(hh0 + 1) * D + d0] = __float2bfloat16_rn(acc[mt][1] * i1);
+                    stage_out[hh0 * D + d0 + 8] = __float2bfloat16_rn(acc[mt][2] * i0);
+                    stage_out[(hh0 + 1) * D + d0 + 8] = __float2bfloat16_rn(acc[mt][3] * i1);
+                }
+                __syncwarp();
+                uint4 *dst = reinterpret_cast<uint4 *>(
+                    a.out + ((size_t)s * a.num_heads + (size_t)h * G) * D);
+                const uint4 *srcv = reinterpret_cast<const uint4 *>(stage_out);
+                for (int v = lane; v < G * D / 8; v += 32) dst[v] = srcv[v];
+                wrote_smem = true;
+            } else {
+                const size_t rec = (size_t)g * 2 + (first_piece ? 0 : 1);
+                float *pacc = a.part_acc + rec * kHeadsPad * D;
+#pragma unroll
+                for (int mt = 0; mt < D / 16; ++mt) {
+                    const int d0 = mt * 16 + tr0;
+                    pacc[hh0 * D + d0] = acc[mt][0];
+                    pacc[(hh0 + 1) * D + d0] = acc[mt][1];
+                    pacc[hh0 * D + d0 + 8] = acc[mt][2];
+                    pacc[(hh0 + 1) * D + d0 + 8] = acc[mt][3];
+                }
+                if (lane < 4) {
+                    float *pml = a.part_ml + rec * kHeadsPad * 2;
+                    pml[hh0 * 2 + 0] = m0;
+                    pml[hh0 * 2 + 1] = l0;
+                    pml[(hh0 + 1) * 2 + 0] = m1;
+                    pml[(hh0 + 1) * 2 + 1] = l1;
+                }
+            }
+            first_piece = false;
+        }
+        prev_seg = seg;
+        if (wrote_smem) fence_proxy_async_smem();
+        __syncwarp();
+        if (c + S < n) {
+            issue(c + S);
+            issued = c + S + 1;
+        }
+        if ((c & 31) == 31) {
+            dA0 = dB0;
+            dA1 = dB1;
+            dA2 = dB2;
+            dA3 = dB3;
+            ++cur_batch;
+            make_desc(cur_batch + 1, dB0, dB1, dB2, dB3);
+        }
+    }
+}
+
+// Merge the pieces of segments that were split across warps; zero empty sequences.
+template <int D>
+__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
+    const int k = blockIdx.x;
+    const int Hkv = a.num_kv_heads, G = a.group;
+    const int s = k / Hkv, h = k - s * Hkv;
+    const int pre = a.prefix[s];
+    const int nt = a.prefix[s + 1] - pre;
+    __nv_bfloat16 *orow = a.out + ((size_t)s * a.num_heads + (size_t)h * G) * D;
+    if (nt == 0) {
+        for (int i = threadIdx.x; i < G * D; i += blockDim.x) orow[i] = __float2bfloat16_rn(0.f);
+        return;
+    }
+    const long long T = (long long)a.prefix[a.num_seqs] * Hkv;
+    const long long NW = a.total_warps;
+    const long long S0 = (long long)Hkv * pre + (long long)h * nt, S1 = S0 + nt;
+    const long long g0 = ((S0 + 1) * NW - 1) / T;
+    const long long g1 = (S1 * NW - 1) / T;
+    if (g0 == g1) return;  // written whole by one warp
+    for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
+        const int hh = i / D, d = i - hh * D;
+        float M = -INFINITY;
+        for (long long gw = g0; gw <= g1; ++gw) {
+            const long long b = (gw * T) / NW, e = ((gw + 1) * T) / NW;
+            if (max(b, S0) >= min(e, S1)) continue;
+            const size_t rec = (size_t)gw * 2 + (b >= S0 ? 0 : 1);
+            M = fmaxf(M, a.part_ml[(rec * kHeadsPad + hh) * 2]);
+        }
+        float num = 0.f, den = 0.f;
+        for (long long gw = g0; gw <= g1; ++gw) {
+            const long long b = (gw * T) / NW, e = ((gw + 1) * T) / NW;
+            if (max(b, S0) >= min(e, S1)) continue;
+            const size_t rec = (size_t)gw * 2 + (b >= S0 ? 0 : 1);
+            const float w = exp2f(a.part_ml[(rec * kHeadsPad + hh) * 2] - M);
+            num += w * a.part_acc[(rec * kHeadsPad + hh) * D + d];
+            den += w * a.part_ml[(rec * kHeadsPad + hh) * 2 + 1];
+        }
+        orow[i] = __float2bfloat16_rn(num / den);
+    }
+}
+
+template <int D>
+cudaError_t launch_decode_d(const DecodeArgs &a0, const CUtensorMap &map, int grid,
+                            size_t smem, cudaStream_t stream) {
+    auto kern = decode_kernel<D, kDecodeWarps, kDecodeStages>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kDecodeWarps * 32, smem, stream>>>(map, a0);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    decode_merge_kernel<D><<<a0.num_seqs * a0.num_kv_heads, 128, 0, stream>>>(a0);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int decode_max_seqs(int head_size) {
+    const size_t limit = 227 * 1024;
+    const size_t fixed = head_size == 128 ? decode_smem_bytes<128>(0) : decode_smem_bytes<64>(0);
+    return (int)((limit - fixed) / 8);
+}
+
+size_t decode_workspace_bytes(int num_seqs, int head_size, int sm_count) {
+    const size_t nw = (size_t)sm_count * kDecodeWarps;
+    return align_up((size_t)(num_seqs + 1) * 4, 256) + align_up(nw * 2 * kHeadsPad * 2 * 4, 256) +
+           align_up(nw * 2 * kHeadsPad * (size_t)head_size * 4, 256);
+}
+
+cudaError_t take_error_decode(unsigned *bits) {
+    unsigned zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(bits, g_err_decode, sizeof(unsigned));
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_err_decode, &zero, sizeof(unsigned));
+    return e;
+}
+
+cudaError_t launch_decode(void *out, const void *q, const void *kv_cache, const KvGeom &g,
+                          int num_heads, const int32_t *block_tables, int max_blocks_per_seq,
+                          const int32_t *seq_lens, int num_seqs, int max_seq_len, float scale,
+                          void *workspace, cudaStream_t stream) {
+    const int sms = device_sm_count();
+    const int D = g.head_size;
+    CUtensorMap map;
+    if (!encode_kv_map(&map, kv_cache, g, g.block_size >= kTile ? kTile : g.block_size))
+        return cudaErrorInvalidValue;
+    // Enough warps that each gets >= ~8 tiles at the largest possible length, at
+    // most one CTA per SM.
+    const long long tmax =
+        (long long)num_seqs * g.num_kv_heads * ((std::max(max_seq_len, 1) + kTile - 1) / kTile);
+    long long ctas = (tmax / 8 + kDecodeWarps - 1) / kDecodeWarps;
+    ctas = std::max(1LL, std::min<long long>(ctas, sms));
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const size_t nw_max = (size_t)sms * kDecodeWarps;
+    DecodeArgs a;
+    a.out = static_cast<__nv_bfloat16 *>(out);
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.block_tables = block_tables;
+    a.seq_lens = seq_lens;
+    a.prefix = reinterpret_cast<int32_t *>(ws);
+    ws += align_up((size_t)(num_seqs + 1) * 4, 256);
+    a.part_ml = reinterpret_cast<float *>(ws);
+    ws += align_up(nw_max * 2 * kHeadsPad * 2 * 4, 256);
+    a.part_acc = reinterpret_cast<float *>(ws);
+    a.num_seqs = num_seqs;
+    a.num_heads = num_heads;
+    a.num_kv_heads = g.num_kv_heads;
+    a.group = num_heads / g.num_kv_heads;
+    a.block_size = g.block_size;
+    a.max_blocks = max_blocks_per_seq;
+    a.num_blocks = g.num_blocks;
+    a.total_warps = (int)ctas * kDecodeWarps;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    if (D == 128)
+        return launch_decode_d<128>(a, map, (int)ctas, decode_smem_bytes<128>(num_seqs), stream);
+    return launch_decode_d<64>(a, map, (int)ctas, decode_smem_bytes<64>(num_seqs), stream);
+}
+
+}  // namespace pa

@@ -1,0 +1,50 @@
+// pa_internal.h - declarations shared by the translation units of libpagedattn.
+// Not part of the public ABI (include/pa.h is).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pa {
+
+// Geometry of the KV pool [num_blocks][2][num_kv_heads][block_size][head_size].
+struct KvGeom {
+    int num_blocks;
+    int block_size;
+    int num_kv_heads;
+    int head_size;
+};
+
+// Each translation unit owns a device error word; these read and clear it.
+cudaError_t take_error_cache_write(unsigned *bits);
+cudaError_t take_error_decode(unsigned *bits);
+cudaError_t take_error_prefill(unsigned *bits);
+
+// Encode a 2-D TMA map over the pool viewed as rows of head_size bf16 elements,
+// box = 64 elements x box_rows rows, 128-byte swizzle.  False on failure.
+bool encode_kv_map(CUtensorMap *map, const void *kv_cache, const KvGeom &g, int box_rows);
+
+int device_sm_count();
+
+cudaError_t launch_cache_write(void *kv_cache, const KvGeom &g, const void *k_new,
+                               const void *v_new, int64_t new_row_stride,
+                               const int32_t *slot_mapping, int num_tokens, cudaStream_t stream);
+
+// Decode workspace bytes for num_seqs sequences on a device with sm_count SMs.
+size_t decode_workspace_bytes(int num_seqs, int head_size, int sm_count);
+// Largest num_seqs the decode kernel's shared-memory tables hold.
+int decode_max_seqs(int head_size);
+
+cudaError_t launch_decode(void *out, const void *q, const void *kv_cache, const KvGeom &g,
+                          int num_heads, const int32_t *block_tables, int max_blocks_per_seq,
+                          const int32_t *seq_lens, int num_seqs, int max_seq_len, float scale,
+                          void *workspace, cudaStream_t stream);
+
+cudaError_t launch_prefill(void *out, const void *q, const int32_t *cu_q_lens, int num_chunks,
+                           int max_q_len, const void *kv_cache, const KvGeom &g, int num_heads,
+                           const int32_t *block_tables, int max_blocks_per_seq,
+                           const int32_t *seq_lens, float scale, cudaStream_t stream);
+
+}  // namespace pa

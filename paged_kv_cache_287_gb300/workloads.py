@@ -39,7 +39,8 @@ from typing import List, Optional, Sequence
 
 import torch
 
-__all__ = ["PagedBatch", "make_batch", "make_config", "CONFIG_NAMES", "config_seed"]
+__all__ = ["PagedBatch", "make_batch", "make_config", "config_spec", "sample_of_config",
+           "CONFIG_NAMES", "config_seed"]
 
 CONFIG_NAMES = {
     1: "tiny-decode-tinyllama-b4",
@@ -213,8 +214,8 @@ def _uniform_int(gen: torch.Generator, lo: int, hi: int, n: int) -> List[int]:
     return torch.randint(lo, hi + 1, (n,), generator=gen).tolist()
 
 
-def make_config(n: int, device="cpu", seed: Optional[int] = None, poison: bool = True) -> PagedBatch:
-    """The five numbered workloads.
+def config_spec(n: int, seed: Optional[int] = None) -> dict:
+    """Keyword arguments of ``make_batch`` for numbered workload ``n``.
 
     1 tiny decode: TinyLlama-1.1B heads (32 q / 4 kv / 64), 4 sequences,
       lengths U{1..128}, a 64-block pool, scale 1/8.
@@ -232,38 +233,50 @@ def make_config(n: int, device="cpu", seed: Optional[int] = None, poison: bool =
     """
     seed = config_seed(n) if seed is None else seed
     g = torch.Generator(device="cpu").manual_seed(seed)
-    common = dict(seed=seed, device=device, poison=poison)
+    llama = dict(num_kv_heads=8, head_size=128, block_size=16, scale=1.0 / math.sqrt(128))
     if n == 1:
         lens = _uniform_int(g, 1, 128, 4)
-        return make_batch(name=CONFIG_NAMES[1], seq_lens=lens, q_lens=[1] * 4, num_heads=32,
-                          num_kv_heads=4, head_size=64, block_size=16, scale=1.0 / 8,
-                          num_blocks=64, max_blocks_per_seq=8, **common)
+        return dict(name=CONFIG_NAMES[1], seq_lens=lens, q_lens=[1] * 4, num_heads=32,
+                    num_kv_heads=4, head_size=64, block_size=16, scale=1.0 / 8, num_blocks=64,
+                    max_blocks_per_seq=8, seed=seed)
     if n == 2:
         lens = _uniform_int(g, 512, 4096, 256)
-        return make_batch(name=CONFIG_NAMES[2], seq_lens=lens, q_lens=[1] * 256, num_heads=32,
-                          num_kv_heads=8, head_size=128, block_size=16,
-                          scale=1.0 / math.sqrt(128), max_blocks_per_seq=256, **common)
+        return dict(name=CONFIG_NAMES[2], seq_lens=lens, q_lens=[1] * 256, num_heads=32,
+                    max_blocks_per_seq=256, seed=seed, **llama)
     if n == 3:
         u = torch.rand(32, generator=g, dtype=torch.float64)
         lo, hi = math.log(1024), math.log(131072)
         lens = [int(math.floor(math.exp(lo + (hi - lo) * float(x)))) for x in u]
-        return make_batch(name=CONFIG_NAMES[3], seq_lens=lens, q_lens=[1] * 32, num_heads=32,
-                          num_kv_heads=8, head_size=128, block_size=16,
-                          scale=1.0 / math.sqrt(128), q_scale=2.0, max_blocks_per_seq=8192,
-                          **common)
+        return dict(name=CONFIG_NAMES[3], seq_lens=lens, q_lens=[1] * 32, num_heads=32,
+                    q_scale=2.0, max_blocks_per_seq=8192, seed=seed, **llama)
     if n == 4:
         ctx = _uniform_int(g, 0, 8192, 8)
         dec = _uniform_int(g, 256, 4096, 248)
-        lens = [c + 512 for c in ctx] + dec
-        qls = [512] * 8 + [1] * 248
-        return make_batch(name=CONFIG_NAMES[4], seq_lens=lens, q_lens=qls, num_heads=32,
-                          num_kv_heads=8, head_size=128, block_size=16,
-                          scale=1.0 / math.sqrt(128), max_blocks_per_seq=544, **common)
+        return dict(name=CONFIG_NAMES[4], seq_lens=[c + 512 for c in ctx] + dec,
+                    q_lens=[512] * 8 + [1] * 248, num_heads=32, max_blocks_per_seq=544,
+                    seed=seed, **llama)
     if n == 5:
         suffix = _uniform_int(g, 64, 1024, 128)
-        lens = [2048 + x for x in suffix]
-        return make_batch(name=CONFIG_NAMES[5], seq_lens=lens, q_lens=[1] * 128, num_heads=64,
-                          num_kv_heads=8, head_size=128, block_size=16,
-                          scale=1.0 / math.sqrt(128), shared_prefix_blocks=128,
-                          max_blocks_per_seq=192, **common)
+        return dict(name=CONFIG_NAMES[5], seq_lens=[2048 + x for x in suffix],
+                    q_lens=[1] * 128, num_heads=64, shared_prefix_blocks=128,
+                    max_blocks_per_seq=192, seed=seed, **llama)
     raise ValueError(f"unknown workload {n}")
+
+
+def make_config(n: int, device="cpu", seed: Optional[int] = None, poison: bool = True) -> PagedBatch:
+    """Numbered workload ``n`` (see ``config_spec``) with its values drawn on ``device``."""
+    return make_batch(device=device, poison=poison, **config_spec(n, seed))
+
+
+def sample_of_config(n: int, first: int, device="cpu", seed: Optional[int] = None) -> PagedBatch:
+    """The first ``first`` sequences of workload ``n``, with a pool of their own.
+
+    Same shapes, lengths and value distribution as the full workload; used where
+    a bounded sample of the workload is wanted (CPU timings).
+    """
+    spec = config_spec(n, seed)
+    spec["seq_lens"] = spec["seq_lens"][:first]
+    spec["q_lens"] = spec["q_lens"][:first]
+    spec.pop("num_blocks", None)
+    spec["name"] = f"{spec['name']}[:{first}]"
+    return make_batch(device=device, **spec)

@@ -1,0 +1,93 @@
+"""The C ABI library loads, exports every declared symbol, and rejects bad host
+arguments before touching the GPU (no compute calls; runs without a GPU)."""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_kv_cache_287_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(binding.LIB_PATH):
+        from paged_kv_cache_287_gb300 import build
+        build.build()
+    return binding.lib()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "pa.h")).read()
+    return set(re.findall(r"^\S[^;(]*?\b(pa_[a-z_0-9]+)\s*\(", src, re.M))
+
+
+def test_header_and_binding_agree():
+    assert _declared() == set(binding.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_block_bytes_formula(lib):
+    assert lib.pa_kv_block_bytes(16, 4, 64) == 16384
+    assert lib.pa_kv_block_bytes(16, 8, 128) == 65536
+    assert lib.pa_kv_block_bytes(0, 8, 128) == 0
+
+
+def test_status_strings(lib):
+    for code, name in binding.STATUS.items():
+        assert lib.pa_status_string(code).decode() == name
+
+
+FAKE = 1 << 20  # 16-byte aligned, never dereferenced: every call below fails host checks
+
+
+def test_cache_write_host_checks(lib):
+    ok = (FAKE, 10, 16, 8, 128, FAKE, FAKE, 8 * 128, FAKE, 4, None)
+    assert lib.pa_cache_write(None, *ok[1:]) == 1                      # null pool
+    assert lib.pa_cache_write(FAKE + 2, *ok[1:]) == 1                  # misaligned pool
+    assert lib.pa_cache_write(FAKE, 10, 16, 8, 96, *ok[5:]) == 2       # head_size 96
+    assert lib.pa_cache_write(FAKE, 10, 12, 8, 128, *ok[5:]) == 2      # block_size 12
+    assert lib.pa_cache_write(*ok[:7], 100, *ok[8:]) == 1              # row stride too small
+    assert lib.pa_cache_write(*ok[:9], -1, None) == 1                  # negative count
+    assert lib.pa_cache_write(*ok[:9], 0, None) == 0                   # empty: no-op
+
+
+def test_decode_host_checks(lib):
+    args = [FAKE, FAKE, FAKE, 10, 16, 32, 8, 128, FAKE, 4, FAKE, 3, 64, 0.1, FAKE, 1 << 30, None]
+    bad = list(args)
+    bad[6] = 5                                  # 32 heads over 5 kv heads
+    assert lib.pa_decode(*bad) == 1
+    bad = list(args)
+    bad[5], bad[6] = 64, 4                      # group 16 unsupported
+    assert lib.pa_decode(*bad) == 2
+    bad = list(args)
+    bad[13] = float("nan")
+    assert lib.pa_decode(*bad) == 1
+    bad = list(args)
+    bad[12] = 4 * 16 + 1                        # max_seq_len beyond the table
+    assert lib.pa_decode(*bad) == 1
+    bad = list(args)
+    bad[11] = 0                                 # no sequences: no-op
+    assert lib.pa_decode(*bad) == 0
+
+
+def test_prefill_host_checks(lib):
+    args = [FAKE, FAKE, FAKE, 2, 64, FAKE, 10, 16, 32, 8, 128, FAKE, 4, FAKE, 0.1, None]
+    bad = list(args)
+    bad[10] = 256
+    assert lib.pa_prefill_chunk(*bad) == 2
+    bad = list(args)
+    bad[1] = FAKE + 8                           # misaligned q
+    assert lib.pa_prefill_chunk(*bad) == 1
+    bad = list(args)
+    bad[4] = 0                                  # empty: no-op
+    assert lib.pa_prefill_chunk(*bad) == 0
