@@ -1,0 +1,533 @@
+"""Benchmark: paged decode attention on GB300 through the C ABI.
+
+One step = one pass of the hot path over one batch: the cache write of every
+sequence's new token (pa_cache_write) followed by decode attention over the
+paged KV cache (pa_decode: the split-context kernel plus its merge kernel).
+Default workload: the Llama-3-8B-shaped decode layer (256 sequences, 32 query /
+8 KV heads, head_size 128, block_size 16, lengths U{512..4096}).
+
+Printed (rank 0, one JSON line): KV bytes read per second over the timed
+steps (device time, inputs resident in HBM), seqs/s, the decode kernel's
+roofline against the measured HBM copy bandwidth, an end-to-end figure with the
+step's inputs copied from pinned host memory and the output copied back, SM
+clocks sampled during the timed region, and the CPU oracle timed on a bounded
+sample of the same workload.
+
+Multi-GPU: the path needs no exchange (sequences are independent), so each rank
+runs its own replica of the workload (weak scaling); timing is the max over
+ranks.  ``--impl reference`` times the CPU fp64 oracle instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged-attn decode: achieved KV-read GB/s (% of HBM peak) and seqs/s"
+UNIT = "GB/s"
+DEFAULT_WORKLOAD = 2
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def kv_read_bytes(seq_lens, num_kv_heads: int, head_size: int) -> int:
+    """Token-granular K+V bytes decode reads: sum_s 2*L_s*Hkv*D*2."""
+    return int(sum(int(L) for L in seq_lens)) * 2 * num_kv_heads * head_size * 2
+
+
+def decode_algorithmic_bytes(b) -> int:
+    """KV read + q read + out write + tables and lengths read, per decode launch."""
+    kv = kv_read_bytes(b.seq_lens.tolist(), b.num_kv_heads, b.head_size)
+    qo = 2 * b.q.numel() * 2
+    nblk = sum(-(-int(L) // b.block_size) for L in b.seq_lens.tolist())
+    return kv + qo + nblk * 4 + b.num_seqs * 4
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def profile_traffic(name: str):
+    """DRAM bytes per launch from a committed ncu summary, if its kernel source is unchanged."""
+    path = os.path.join(ROOT, "profiles", name)
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                fields[k.strip()] = v.strip()
+    src = os.path.join(ROOT, "paged_kv_cache_287_gb300", "csrc", fields.get("source", ""))
+    if not os.path.exists(src):
+        return None
+    with open(src, "rb") as f:
+        digest = hashlib.sha256(f.read()).hexdigest()
+    if digest != fields.get("source_sha256"):
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """Samples SM clock, power and clock-event reasons through NVML (read only)."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device: torch.device):
+        self.ok = False
+        self.samples = []
+        self.max_mhz = None
+        try:
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            props = torch.cuda.get_device_properties(device)
+            bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+            if self.nvml.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(self.h)) != 0:
+                if self.nvml.nvmlDeviceGetHandleByIndex_v2(device.index or 0,
+                                                           ctypes.byref(self.h)) != 0:
+                    return
+            mx = ctypes.c_uint()
+            if self.nvml.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = int(mx.value)
+            self._reasons_fn = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) \
+                or self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.ok = True
+        except (OSError, AttributeError):
+            self.ok = False
+
+    def _poll(self):
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        pw = ctypes.c_uint()
+        while not self._stop.is_set():
+            if self.nvml.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk)) == 0:
+                self._reasons_fn(self.h, ctypes.byref(rs))
+                self.nvml.nvmlDeviceGetPowerUsage(self.h, ctypes.byref(pw))
+                self.samples.append((int(clk.value), int(rs.value), pw.value / 1000.0))
+            time.sleep(0.002)
+
+    def __enter__(self):
+        if self.ok:
+            self._stop = threading.Event()
+            self._t = threading.Thread(target=self._poll, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self.ok:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [],
+                    "samples": 0, "source": "nvml" if self.ok else "unavailable"}
+        reasons = set()
+        for _, r, _ in self.samples:
+            for bit, name in self.REASONS.items():
+                if r & bit:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(s[0] for s in self.samples),
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(reasons),
+                "power_w_max": max(s[2] for s in self.samples),
+                "samples": len(self.samples), "source": "nvml"}
+
+
+def rejected_clocks(c) -> bool:
+    bad = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}
+    if bad & set(c.get("reasons", [])):
+        return True
+    if c.get("sm_mhz") and c.get("sm_max_mhz") and not c["reasons"]:
+        return c["sm_mhz"] < 0.6 * c["sm_max_mhz"]
+    return False
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device=device if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def cpu_oracle_rate(n: int, budget_s: float = 12.0, seed=None, first: int = 64):
+    """Time the oracle (cache write + attention) on the first sequences of workload n.
+
+    Sequences are processed one at a time, cycling over the sample, until about
+    budget_s seconds of wall time are spent.  Returns (GB/s of KV read, seqs/s,
+    sequences timed, sample size, threads).
+    """
+    import numpy as np
+
+    import oracle
+    from paged_kv_cache_287_gb300.workloads import config_spec, sample_of_config
+
+    k = min(len(config_spec(n)["seq_lens"]), first)
+    b = sample_of_config(n, k, device="cpu", seed=seed)
+    lib = oracle.load()
+    threads = oracle.max_threads(lib)
+    lens = b.seq_lens.tolist()
+    pool = oracle._u16(b.kv_cache).copy()
+    done_bytes = 0
+    done = 0
+    spent = 0.0
+    while spent < budget_s:
+        s = done % k
+        one = slice(s, s + 1)
+        r0, r1 = int(b.cu_q_lens[s]), int(b.cu_q_lens[s + 1])
+        t = time.perf_counter()
+        oracle.cache_write(pool, b.k_new[r0:r1], b.v_new[r0:r1], b.slot_mapping[r0:r1], lib=lib,
+                           inplace=True)
+        oracle.attention(b.q[r0:r1], np.array([0, r1 - r0], np.int32), pool,
+                         b.block_tables[one], b.seq_lens[one], b.num_heads, b.scale, lib=lib)
+        spent += time.perf_counter() - t
+        done_bytes += kv_read_bytes(lens[s:s + 1], b.num_kv_heads, b.head_size)
+        done += 1
+    return done_bytes / spent / 1e9, done / spent, done, k, threads
+
+
+# ----------------------------------------------------------------------------- arms
+
+def run_reference(args, world, rank):
+    """The oracle as it stands, on the host cores: each step a bounded sample."""
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    from paged_kv_cache_287_gb300.workloads import CONFIG_NAMES, config_spec, sample_of_config
+
+    n = args.workload
+    spec = config_spec(n)
+    per_step = 2
+    b = sample_of_config(n, per_step, device="cpu")
+    lib = oracle.load()
+    threads = oracle.max_threads(lib)
+    kv = kv_read_bytes(b.seq_lens.tolist(), b.num_kv_heads, b.head_size)
+
+    pool = oracle._u16(b.kv_cache).copy()
+
+    def step():
+        oracle.cache_write(pool, b.k_new, b.v_new, b.slot_mapping, lib=lib, inplace=True)
+        oracle.attention(b.q, b.cu_q_lens, pool, b.block_tables, b.seq_lens, b.num_heads,
+                         b.scale, lib=lib)
+
+    for _ in range(args.warmup):
+        step()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t
+    value = kv * args.steps / el / 1e9
+    sample = (f"first {per_step} of {len(spec['seq_lens'])} sequences of {CONFIG_NAMES[n]} "
+              f"per step (cache write + fp64 attention, all heads)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(n),
+        "seqs_per_s": per_step * args.steps / el,
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(n: int, first: int = 0):
+    from paged_kv_cache_287_gb300.workloads import CONFIG_NAMES, config_spec
+    s = config_spec(n)
+    if first:
+        s["seq_lens"] = s["seq_lens"][:first]
+    return {"workload": CONFIG_NAMES[n] + (f"[:{first}]" if first else ""),
+            "num_seqs": len(s["seq_lens"]),
+            "num_heads": s["num_heads"], "num_kv_heads": s["num_kv_heads"],
+            "head_size": s["head_size"], "block_size": s["block_size"],
+            "seq_len_mean": sum(s["seq_lens"]) / len(s["seq_lens"]),
+            "seq_len_max": max(s["seq_lens"]),
+            "l2": "inputs larger than L2 (KV pool >> 129 MB); no flush",
+            "parallelism": "replicas (one independent batch per GPU)"}
+
+
+def run_ours(args, world, rank, local):
+    from paged_kv_cache_287_gb300 import binding
+    from paged_kv_cache_287_gb300.workloads import make_config
+
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device (the library has no CPU path)")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    n = args.workload
+    if n == 4:
+        return run_mixed(args, world, rank, local)
+    seed = None if rank == 0 else 287 + n + 7919 * rank
+    if args.seqs:
+        from paged_kv_cache_287_gb300.workloads import sample_of_config
+        b = sample_of_config(n, args.seqs, device=dev, seed=seed)
+    else:
+        b = make_config(n, device=dev, seed=seed)
+    binding.lib()
+    stream = torch.cuda.current_stream(dev)
+    out = torch.empty_like(b.q)
+    ws = torch.empty(binding.pa_decode_workspace_bytes(b.num_seqs, b.num_heads, b.num_kv_heads,
+                                                       b.head_size), dtype=torch.uint8, device=dev)
+    max_len = b.max_seq_len
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        binding.pa_cache_write(b.kv_cache, b.k_new, b.v_new, b.slot_mapping, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        binding.pa_decode(out, b.q, b.kv_cache, b.block_tables, b.seq_lens, max_len, b.scale, ws,
+                          stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    binding.pa_error_check(stream)
+
+    def timed():
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+        start = torch.cuda.Event(enable_timing=True)
+        stop = torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        sampler = ClockSampler(dev) if rank == 0 else None
+        if sampler:
+            sampler.__enter__()
+        start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        stop.record(stream)
+        torch.cuda.synchronize(dev)
+        if sampler:
+            sampler.__exit__(None, None, None)
+        barrier(world)
+        total_ms = start.elapsed_time(stop)
+        write_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
+        decode_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
+        return total_ms, write_ms, decode_ms, (sampler.summary() if sampler else {})
+
+    total_ms, write_ms, decode_ms, clocks = timed()
+    if rank == 0 and rejected_clocks(clocks):
+        total_ms, write_ms, decode_ms, clocks = timed()
+        clocks["remeasured"] = True
+    binding.pa_error_check(stream)
+    total_ms = max_over_ranks(total_ms, world, dev)
+
+    # End to end: the step's inputs from pinned host memory, output back to host.
+    host = {k: getattr(b, k).to("cpu").pin_memory()
+            for k in ("q", "k_new", "v_new", "slot_mapping", "block_tables", "seq_lens")}
+    dev_in = {k: torch.empty_like(getattr(b, k)) for k in host}
+    out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        for k, t in host.items():
+            dev_in[k].copy_(t, non_blocking=True)
+        binding.pa_cache_write(b.kv_cache, dev_in["k_new"], dev_in["v_new"],
+                               dev_in["slot_mapping"], stream)
+        binding.pa_decode(out, dev_in["q"], b.kv_cache, dev_in["block_tables"],
+                          dev_in["seq_lens"], max_len, b.scale, ws, stream)
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(max(args.warmup, 3)):
+        e2e_step()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
+    barrier(world)
+
+    if rank != 0:
+        return
+    kv = kv_read_bytes(b.seq_lens.tolist(), b.num_kv_heads, b.head_size)
+    value = world * kv * args.steps / (total_ms / 1e3) / 1e9
+    seqs_s = world * b.num_seqs * args.steps / (total_ms / 1e3)
+    peak, peak_src = measured_peaks()
+    alg = decode_algorithmic_bytes(b)
+    achieved = alg / (decode_ms / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(n, args.seqs),
+        "seqs_per_s": seqs_s,
+        "hbm_frac_of_step": value / world / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": profile_traffic(
+                         f"decode_{b.name}.traffic.txt"),
+                     "kernel": "pa_decode (split-context kernel + merge kernel)",
+                     "algorithmic_bytes_per_launch": alg, "launch_ms": decode_ms,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_src == "measured" else "fallback 6.8 TB/s"},
+        "kernels_ms": {"pa_cache_write": write_ms, "pa_decode": decode_ms},
+        "e2e": {"value": world * kv * args.steps / e2e_s / 1e9, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "note": "KV pool resident in HBM (the cache); per-step inputs copied in, "
+                        "output copied out"},
+        "clocks": clocks,
+        "gpu_launches": 3 * args.steps,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        gbs, sps, done, k, threads = cpu_oracle_rate(n)
+        line["cpu_baseline"] = {"value": gbs, "unit": UNIT, "cores": threads, "kind": "oracle",
+                                "seqs_per_s": sps,
+                                "sample": f"{done} sequence-steps cycling over the first {k} "
+                                          f"sequences of {b.name} (cache write + fp64 "
+                                          f"attention, all heads, one sequence per call)"}
+    print(json.dumps(line), flush=True)
+
+
+def prefill_flops(b, lo: int, hi: int) -> int:
+    """4*Hq*D per causally visible (query, key) pair: q_len*ctx + q_len*(q_len+1)/2."""
+    pairs = 0
+    for s in range(lo, hi):
+        ql = int(b.q_lens[s])
+        ctx = int(b.seq_lens[s]) - ql
+        pairs += ql * ctx + ql * (ql + 1) // 2
+    return 4 * b.num_heads * b.head_size * pairs
+
+
+def run_mixed(args, world, rank, local):
+    """Workload 4: write all new tokens, then chunked prefill of the 8 chunks and
+    decode of the 248 sequences; per-kernel device times (informational line)."""
+    from paged_kv_cache_287_gb300 import binding
+    from paged_kv_cache_287_gb300.workloads import make_config
+
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    b = make_config(4, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    n_pre = int((b.q_lens > 1).sum())
+    r_pre = int(b.cu_q_lens[n_pre])
+    q_pre, q_dec = b.q[:r_pre], b.q[r_pre:]
+    out_pre, out_dec = torch.empty_like(q_pre), torch.empty_like(q_dec)
+    cu_pre = b.cu_q_lens[:n_pre + 1].contiguous()
+    bt_pre, bt_dec = b.block_tables[:n_pre], b.block_tables[n_pre:]
+    sl_pre, sl_dec = b.seq_lens[:n_pre], b.seq_lens[n_pre:]
+    max_q = int(b.q_lens[:n_pre].max())
+    max_dec = int(sl_dec.max())
+    ws = torch.empty(binding.pa_decode_workspace_bytes(b.num_seqs - n_pre, b.num_heads,
+                                                       b.num_kv_heads, b.head_size),
+                     dtype=torch.uint8, device=dev)
+
+    def step(ev=None):
+        if ev: ev[0].record(stream)
+        binding.pa_cache_write(b.kv_cache, b.k_new, b.v_new, b.slot_mapping, stream)
+        if ev: ev[1].record(stream)
+        binding.pa_prefill_chunk(out_pre, q_pre, cu_pre, max_q, b.kv_cache, bt_pre, sl_pre,
+                                 b.scale, stream)
+        if ev: ev[2].record(stream)
+        binding.pa_decode(out_dec, q_dec, b.kv_cache, bt_dec, sl_dec, max_dec, b.scale, ws, stream)
+        if ev: ev[3].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    binding.pa_error_check(stream)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev) as sampler:
+        for i in range(args.steps):
+            step(evs[i])
+        torch.cuda.synchronize(dev)
+    ms = [sum(e[j].elapsed_time(e[j + 1]) for e in evs) / args.steps for j in range(3)]
+    if rank != 0:
+        return
+    flops = prefill_flops(b, 0, n_pre)
+    kv_dec = kv_read_bytes(sl_dec.tolist(), b.num_kv_heads, b.head_size)
+    with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+        pk = json.load(f)
+    line = {"metric": "mixed chunked-prefill + decode step", "value": sum(ms), "unit": "ms",
+            "higher_is_better": False, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "dtype": "bf16", "data": "synthetic",
+            "config": workload_config(4),
+            "kernels_ms": {"pa_cache_write": ms[0], "pa_prefill_chunk": ms[1], "pa_decode": ms[2]},
+            "prefill": {"tflops": flops / (ms[1] / 1e3) / 1e12, "flops_per_launch": flops,
+                        "peak_tflops": pk["bf16_tflops"],
+                        "frac": flops / (ms[1] / 1e3) / 1e12 / pk["bf16_tflops"]},
+            "decode": {"kv_gbs": kv_dec / (ms[2] / 1e3) / 1e9,
+                       "frac": kv_dec / (ms[2] / 1e3) / 1e9 / pk["hbm_gbs"]},
+            "cache_write": {"gbs": 2 * b.k_new.numel() * 2 * 2 / (ms[0] / 1e3) / 1e9},
+            "clocks": sampler.summary(), "gpu_launches": 4 * args.steps}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seqs", type=int, default=0,
+                    help="profile only the first N sequences of the workload (not a bench line)")
+    args = ap.parse_args(argv)
+    world, rank, local = dist_setup()
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -95,9 +95,18 @@ def kv_block_bytes(block_size: int, num_kv_heads: int, head_size: int,
                                                      dtype_bytes))
 
 
-def cache_write(kv_cache, k_new, v_new, slot_mapping, lib=None) -> np.ndarray:
-    """Return a copy of the pool (uint16 bits) with the new rows written."""
-    pool = _u16(kv_cache).copy()
+def cache_write(kv_cache, k_new, v_new, slot_mapping, lib=None, inplace: bool = False) -> np.ndarray:
+    """Return the pool (uint16 bits) with the new rows written.
+
+    By default the input is copied first; with ``inplace=True`` ``kv_cache`` must
+    already be a contiguous uint16 array and is written directly.
+    """
+    if inplace:
+        assert isinstance(kv_cache, np.ndarray) and kv_cache.dtype == np.uint16
+        assert kv_cache.flags["C_CONTIGUOUS"]
+        pool = kv_cache
+    else:
+        pool = _u16(kv_cache).copy()
     NB, two, Hkv, bs, D = pool.shape
     assert two == 2
     kn, vn, sm = _u16(k_new), _u16(v_new), _i32(slot_mapping)
