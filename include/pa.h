@@ -119,6 +119,31 @@ pa_status pa_decode(void *out, const void *q, const void *kv_cache, int num_bloc
                     void *workspace, size_t workspace_bytes, pa_stream_t stream);
 
 /*
+ * pa_decode_noalloc - pa_decode without a caller-provided workspace.
+ *
+ * The pages have no counterpart to this call; it exists for callers that cannot
+ * allocate device memory on this path: an engine that has already reserved
+ * nearly all of HBM for its KV-cache pool, a host program that only receives
+ * device pointers and owns no allocator, or a decode loop that cannot afford
+ * cudaMalloc/cudaFree (they may synchronise the device).
+ *   Arguments and results are those of pa_decode, minus workspace.
+ *   Scratch comes from a 16 MiB array in this library's device image, held by
+ *   every GPU that loads the library until the process exits.  A shape whose
+ *   pa_decode_workspace_bytes() exceeds 16 MiB returns PA_ERR_UNSUPPORTED.
+ *   The call allocates nothing.  Its first call on a device (with that device
+ *   current) looks up the array's device address; make that first call before
+ *   any stream capture.
+ *   All calls share the one array: calls that overlap on the GPU (other
+ *   streams, other threads) race and must be serialised by the caller.  No
+ *   byte of the array needs to start at zero: each call writes before it reads.
+ */
+pa_status pa_decode_noalloc(void *out, const void *q, const void *kv_cache, int num_blocks,
+                            int block_size, int num_heads, int num_kv_heads, int head_size,
+                            const int32_t *block_tables, int max_blocks_per_seq,
+                            const int32_t *seq_lens, int num_seqs, int max_seq_len, float scale,
+                            pa_stream_t stream);
+
+/*
  * pa_prefill_chunk - chunked-prefill attention of query chunks against their
  * cached context and themselves, causal.
  *
