@@ -320,20 +320,30 @@ def run_ours(args, world, rank, local):
                                                        b.head_size), dtype=torch.uint8, device=dev)
     max_len = b.max_seq_len
 
-    def step(ev=None):
+    def step(ev=None, st=None):
+        st = stream if st is None else st
         if ev is not None:
-            ev[0].record(stream)
-        binding.pa_cache_write(b.kv_cache, b.k_new, b.v_new, b.slot_mapping, stream)
+            ev[0].record(st)
+        binding.pa_cache_write(b.kv_cache, b.k_new, b.v_new, b.slot_mapping, st)
         if ev is not None:
-            ev[1].record(stream)
+            ev[1].record(st)
         binding.pa_decode(out, b.q, b.kv_cache, b.block_tables, b.seq_lens, max_len, b.scale, ws,
-                          stream)
+                          st)
         if ev is not None:
-            ev[2].record(stream)
+            ev[2].record(st)
 
     for _ in range(max(args.warmup, 3)):
         step()
     binding.pa_error_check(stream)
+    graph = None
+    if args.graph:
+        # One captured step (cache write + decode kernels) replayed per timed step.
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        torch.cuda.synchronize(dev)
+        with torch.cuda.graph(graph, stream=cap):
+            step(st=cap)
+        torch.cuda.synchronize(dev)
 
     def timed():
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
@@ -346,15 +356,24 @@ def run_ours(args, world, rank, local):
             sampler.__enter__()
         start.record(stream)
         for i in range(args.steps):
-            step(evs[i])
+            if graph is not None:
+                evs[i][0].record(stream)
+                graph.replay()
+                evs[i][2].record(stream)
+            else:
+                step(evs[i])
         stop.record(stream)
         torch.cuda.synchronize(dev)
         if sampler:
             sampler.__exit__(None, None, None)
         barrier(world)
         total_ms = start.elapsed_time(stop)
-        write_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
-        decode_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
+        if graph is not None:  # the per-kernel split is not visible inside a replay
+            write_ms = float("nan")
+            decode_ms = sum(e[0].elapsed_time(e[2]) for e in evs) / args.steps
+        else:
+            write_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
+            decode_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
         return total_ms, write_ms, decode_ms, (sampler.summary() if sampler else {})
 
     total_ms, write_ms, decode_ms, clocks = timed()
@@ -404,7 +423,7 @@ def run_ours(args, world, rank, local):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": workload_config(n, args.seqs),
+        "config": dict(workload_config(n, args.seqs), launch="cuda-graph" if graph else "eager"),
         "seqs_per_s": seqs_s,
         "hbm_frac_of_step": value / world / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -514,6 +533,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="replay one CUDA-graph-captured step per timed step")
     ap.add_argument("--seqs", type=int, default=0,
                     help="profile only the first N sequences of the workload (not a bench line)")
     args = ap.parse_args(argv)

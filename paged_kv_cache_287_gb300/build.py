@@ -38,14 +38,18 @@ def _flags(debug: bool):
     return f
 
 
-def build(verbose: bool = False, debug: bool = False, ptxas_info: bool = False) -> str:
-    """Compile every translation unit and link ``libpagedattn.so``; returns its path."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, debug: bool = False, ptxas_info: bool = False,
+          defines=(), out: str = LIB, build_dir: str = BUILD) -> str:
+    """Compile every translation unit and link the library (default
+    ``libpagedattn.so`` in the package); returns its path.  ``defines`` are
+    extra ``NAME=VALUE`` preprocessor definitions (kernel tuning parameters)."""
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
-    flags = _flags(debug) + (["-Xptxas", "-v"] if ptxas_info else [])
+    flags = _flags(debug) + (["-Xptxas", "-v"] if ptxas_info else []) + \
+        [f"-D{d}" for d in defines]
 
     def compile_one(src):
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(build_dir, src.replace(".cu", ".o"))
         cmd = [cc, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -59,14 +63,14 @@ def build(verbose: bool = False, debug: bool = False, ptxas_info: bool = False) 
             if err.strip():
                 sys.stderr.write(err)
     objs = [o for o, _ in results]
-    tmp = LIB + ".tmp"
+    tmp = out + ".tmp"
     cmd = [cc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
            "-Xlinker", "-rpath,/usr/local/cuda/lib64"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":

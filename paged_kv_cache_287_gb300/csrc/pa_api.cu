@@ -138,7 +138,8 @@ pa_status pa_decode(void *out, const void *q, const void *kv_cache, int num_bloc
         !aligned(block_tables, 4) || !aligned(seq_lens, 4))
         return PA_ERR_INVALID_ARG;
     if (max_seq_len > max_blocks_per_seq * block_size) return PA_ERR_INVALID_ARG;
-    if (num_seqs > pa::decode_max_seqs(head_size)) return PA_ERR_UNSUPPORTED;
+    if (num_seqs > pa::decode_max_seqs(head_size, num_heads / num_kv_heads))
+        return PA_ERR_UNSUPPORTED;
     if ((long long)num_seqs * num_kv_heads * (((long long)max_seq_len + 15) / 16) >= (1LL << 31))
         return PA_ERR_UNSUPPORTED;
     const size_t need = pa::decode_workspace_bytes(num_seqs, head_size, pa::device_sm_count());

@@ -32,19 +32,37 @@ namespace {
 
 __device__ unsigned g_err_decode;
 
-constexpr int kTile = 16;         // tokens per tile (the MMA's M)
-constexpr int kHeadsPad = 8;      // query heads per KV head, padded to the MMA's N
-constexpr int kDecodeWarps = 4;   // warps per CTA, one CTA per SM
-constexpr int kDecodeStages = 4;  // ring depth per warp
+// Warps per CTA and ring depth per warp (one CTA per SM).  Measured on GB300:
+// 12 warps with one stage each keeps the most bytes in flight for the smallest
+// issue cost; more warps help only when the context is served from L2.
+#ifndef PA_DECODE_WARPS
+#define PA_DECODE_WARPS 12
+#endif
+#ifndef PA_DECODE_STAGES
+#define PA_DECODE_STAGES 1
+#endif
+
+constexpr int kTile = 16;                        // tokens per tile (the MMA's M)
+constexpr int kHeadsPad = 8;                     // query heads per KV head, padded to the MMA's N
+constexpr int kDecodeWarps = PA_DECODE_WARPS;
+constexpr int kDecodeStages = PA_DECODE_STAGES;
+// The running max used as the exponent reference is only raised when a score
+// exceeds it by more than this (log2 units), so P stays <= 2^8 and the
+// accumulator is rescaled rarely.
+constexpr float kRescaleSlack = 8.0f;
 
 template <int D>
 struct Lay {
     static constexpr int kPanels = D / 64;             // 128-byte-wide column panels
     static constexpr int kPanelBytes = kTile * 128;    // 16 rows of one panel
     static constexpr int kKvBytes = kPanels * kPanelBytes;
-    static constexpr int kQBytes = kHeadsPad * D * 2;  // query rows / output staging
-    static constexpr int kStageBytes = 2 * kKvBytes + kQBytes;
 };
+
+// A stage: K panels, V panels, then the segment's G query rows (also used to
+// stage a finished segment's output), rounded up to keep stages 1024-aligned.
+__host__ __device__ constexpr int q_slot_bytes(int group, int head_size) {
+    return (group * head_size * 2 + 1023) / 1024 * 1024;
+}
 
 struct DecodeArgs {
     __nv_bfloat16 *out;
@@ -57,14 +75,16 @@ struct DecodeArgs {
     int num_seqs, num_heads, num_kv_heads, group;
     int block_size, max_blocks, num_blocks;
     int total_warps;
+    int stage_bytes;   // 2 * K/V tile bytes + query slot
     float scale_log2;  // scale * log2(e)
 };
 
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 template <int D>
-__host__ __device__ constexpr size_t decode_smem_bytes(int num_seqs) {
-    return 1024 /* alignment slack */ + (size_t)kDecodeWarps * kDecodeStages * Lay<D>::kStageBytes +
+__host__ __device__ constexpr size_t decode_smem_bytes(int num_seqs, int group) {
+    return 1024 /* alignment slack */ +
+           (size_t)kDecodeWarps * kDecodeStages * (2 * Lay<D>::kKvBytes + q_slot_bytes(group, D)) +
            (size_t)kDecodeWarps * kDecodeStages * 8 + (size_t)(2 * num_seqs + 1) * 4;
 }
 
@@ -83,8 +103,9 @@ __global__ void __launch_bounds__(W * 32, 1)
     using L = Lay<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(align_up(reinterpret_cast<size_t>(smem_raw), 1024));
+    const int stage_bytes = a.stage_bytes;
     uint8_t *ring = smem;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)W * S * L::kStageBytes);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)W * S * stage_bytes);
     int *s_len = reinterpret_cast<int *>(bars + W * S);
     int *s_pre = s_len + a.num_seqs;
 
@@ -126,6 +147,8 @@ __global__ void __launch_bounds__(W * 32, 1)
     __syncthreads();
     if (blockIdx.x == 0)
         for (int s = tid; s <= B; s += W * 32) a.prefix[s] = s_pre[s];
+    // The merge kernel may be scheduled now; it waits for this grid to finish.
+    asm volatile("griddepcontrol.launch_dependents;" :::);
 
     // This warp's equal share of the flattened tile list.
     const long long T = (long long)s_pre[B] * Hkv;
@@ -136,7 +159,7 @@ __global__ void __launch_bounds__(W * 32, 1)
     const int n = t_end - t_begin;
     if (n <= 0) return;
 
-    uint8_t *wring = ring + (size_t)warp * S * L::kStageBytes;
+    uint8_t *wring = ring + (size_t)warp * S * stage_bytes;
     uint64_t *wbar = bars + warp * S;
 
     // Tile descriptors, one tile per lane, for two batches of 32 tiles.
@@ -194,7 +217,7 @@ __global__ void __launch_bounds__(W * 32, 1)
             prev = __shfl_sync(0xffffffffu, pa_ ? dA2 : dB2, (i - 1) & 31);
         }
         if (lane == 0) {
-            uint8_t *stg = wring + (size_t)(i % S) * L::kStageBytes;
+            uint8_t *stg = wring + (size_t)(i % S) * stage_bytes;
             uint64_t *bar = wbar + (i % S);
             const bool new_seg = seg != prev;
             const int nbox = rk1 >= 0 ? 2 : 1;
@@ -237,7 +260,7 @@ __global__ void __launch_bounds__(W * 32, 1)
 
     for (int c = 0; c < n; ++c) {
         const int st = c % S;
-        uint8_t *stg = wring + (size_t)st * L::kStageBytes;
+        uint8_t *stg = wring + (size_t)st * stage_bytes;
         if (!mbar_wait_bounded(wbar + st, (uint32_t)(c / S) & 1u)) {
             if (lane == 0) atomicOr(&g_err_decode, kErrTimeout);
             // Give the copies still in flight a bounded chance to land, then leave.
@@ -293,8 +316,9 @@ __global__ void __launch_bounds__(W * 32, 1)
             __syncwarp();
         }
 
-        // S^T[token][head] = K . Q^T
+        // S^T[token][head] = K . Q^T, as two independent accumulation chains
         float sc[4] = {0.f, 0.f, 0.f, 0.f};
+        float sd[4] = {0.f, 0.f, 0.f, 0.f};
         const uint32_t kbase = smem_u32(stg);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
@@ -303,42 +327,60 @@ __global__ void __launch_bounds__(W * 32, 1)
             const int chunk = 2 * (k & 3) + (lane >> 4);
             uint32_t af[4];
             ldsm_x4(af, swz128(panel, row, chunk));
-            mma_bf16(sc, af, qf[k][0], qf[k][1]);
+            if (k & 1)
+                mma_bf16(sd, af, qf[k][0], qf[k][1]);
+            else
+                mma_bf16(sc, af, qf[k][0], qf[k][1]);
         }
-        const float x0 = tr0 < valid ? sc[0] * a.scale_log2 : -INFINITY;
-        const float x1 = tr0 < valid ? sc[1] * a.scale_log2 : -INFINITY;
-        const float x2 = tr0 + 8 < valid ? sc[2] * a.scale_log2 : -INFINITY;
-        const float x3 = tr0 + 8 < valid ? sc[3] * a.scale_log2 : -INFINITY;
-        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+        for (int e = 0; e < 4; ++e) sc[e] += sd[e];
+        // Scores in log2 units; tokens past the sequence end get -inf.
+        float x0 = sc[0] * a.scale_log2, x1 = sc[1] * a.scale_log2;
+        float x2 = sc[2] * a.scale_log2, x3 = sc[3] * a.scale_log2;
+        if (valid < kTile) {
+            if (tr0 >= valid) x0 = x1 = -INFINITY;
+            if (tr0 + 8 >= valid) x2 = x3 = -INFINITY;
         }
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float cr0 = fast_exp2(m0 - mn0), cr1 = fast_exp2(m1 - mn1);
-        const uint32_t plo = pack_bf16(fast_exp2(x0 - mn0), fast_exp2(x1 - mn1));
-        const uint32_t phi = pack_bf16(fast_exp2(x2 - mn0), fast_exp2(x3 - mn1));
-        float ps0 = bf16_lo(plo) + bf16_lo(phi), ps1 = bf16_hi(plo) + bf16_hi(phi);
+        // The exponent reference m only moves when some score exceeds it by the
+        // slack (first tile, sharp rises): one warp vote decides, and only then is
+        // the tile max reduced across lanes and the accumulator rescaled.
+        const bool grow = fmaxf(x0, x2) > m0 + kRescaleSlack || fmaxf(x1, x3) > m1 + kRescaleSlack;
+        float cr0 = 1.f, cr1 = 1.f;
+        const bool rescale = __any_sync(0xffffffffu, grow);
+        if (rescale) {
+            float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-            ps0 += __shfl_xor_sync(0xffffffffu, ps0, o);
-            ps1 += __shfl_xor_sync(0xffffffffu, ps1, o);
+            for (int o = 4; o < 32; o <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+            }
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            cr0 = fast_exp2(m0 - mn0);
+            cr1 = fast_exp2(m1 - mn1);
+            m0 = mn0;
+            m1 = mn1;
         }
-        l0 = l0 * cr0 + ps0;
-        l1 = l1 * cr1 + ps1;
-        m0 = mn0;
-        m1 = mn1;
+        const uint32_t plo = pack_bf16(fast_exp2(x0 - m0), fast_exp2(x1 - m1));
+        const uint32_t phi = pack_bf16(fast_exp2(x2 - m0), fast_exp2(x3 - m1));
+        // Per-lane partial sums of the bf16 P actually multiplied; the head's 8
+        // lanes are summed once, at the end of the segment.
+        l0 = l0 * cr0 + (bf16_lo(plo) + bf16_lo(phi));
+        l1 = l1 * cr1 + (bf16_hi(plo) + bf16_hi(phi));
         const uint32_t b0 = movmatrix_t(plo), b1 = movmatrix_t(phi);
 
         // O^T[dim][head] += V^T . P^T
         const uint32_t vbase = kbase + L::kKvBytes;
+        if (rescale) {
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+                acc[mt][0] *= cr0;
+                acc[mt][1] *= cr1;
+                acc[mt][2] *= cr0;
+                acc[mt][3] *= cr1;
+            }
+        }
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt) {
-            acc[mt][0] *= cr0;
-            acc[mt][1] *= cr1;
-            acc[mt][2] *= cr0;
-            acc[mt][3] *= cr1;
             const uint32_t panel = vbase + (mt >> 2) * L::kPanelBytes;
             const int mi = lane >> 3;
             const int row = (lane & 7) + (mi >> 1) * 8;
@@ -349,20 +391,31 @@ __global__ void __launch_bounds__(W * 32, 1)
         }
 
         if (next_seg != seg) {
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+                l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+            }
             const int nt = s_pre[s + 1] - s_pre[s];
             if (first_j == 0 && j == nt - 1) {
                 // Whole segment in this warp: normalise and write bf16 rows, staged in
-                // the stage's query slot for 16-byte stores.
+                // the stage's query slot (G rows) for 16-byte stores.  Only the G real
+                // heads are staged: the slot holds no room for the padding heads.
                 __nv_bfloat16 *stage_out =
                     reinterpret_cast<__nv_bfloat16 *>(stg + 2 * L::kKvBytes);
                 const float i0 = 1.f / l0, i1 = 1.f / l1;
+                const bool w0 = hh0 < G, w1 = hh0 + 1 < G;
 #pragma unroll
                 for (int mt = 0; mt < D / 16; ++mt) {
                     const int d0 = mt * 16 + tr0;
-                    stage_out[hh0 * D + d0] = __float2bfloat16_rn(acc[mt][0] * i0);
-                    stage_out[(hh0 + 1) * D + d0] = __float2bfloat16_rn(acc[mt][1] * i1);
-                    stage_out[hh0 * D + d0 + 8] = __float2bfloat16_rn(acc[mt][2] * i0);
-                    stage_out[(hh0 + 1) * D + d0 + 8] = __float2bfloat16_rn(acc[mt][3] * i1);
+                    if (w0) {
+                        stage_out[hh0 * D + d0] = __float2bfloat16_rn(acc[mt][0] * i0);
+                        stage_out[hh0 * D + d0 + 8] = __float2bfloat16_rn(acc[mt][2] * i0);
+                    }
+                    if (w1) {
+                        stage_out[(hh0 + 1) * D + d0] = __float2bfloat16_rn(acc[mt][1] * i1);
+                        stage_out[(hh0 + 1) * D + d0 + 8] = __float2bfloat16_rn(acc[mt][3] * i1);
+                    }
                 }
                 __syncwarp();
                 uint4 *dst = reinterpret_cast<uint4 *>(
@@ -410,16 +463,24 @@ __global__ void __launch_bounds__(W * 32, 1)
 }
 
 // Merge the pieces of segments that were split across warps; zero empty sequences.
+// One CTA per (sequence, KV head); one thread per (query head, 4 dims).  Launched
+// as a programmatic dependent of the split kernel: it may start early and waits
+// for that grid's completion before reading anything it wrote.
 template <int D>
-__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kHeadsPad * D / 4) decode_merge_kernel(const DecodeArgs a) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int k = blockIdx.x;
     const int Hkv = a.num_kv_heads, G = a.group;
     const int s = k / Hkv, h = k - s * Hkv;
     const int pre = a.prefix[s];
     const int nt = a.prefix[s + 1] - pre;
-    __nv_bfloat16 *orow = a.out + ((size_t)s * a.num_heads + (size_t)h * G) * D;
+    const int i = threadIdx.x;
+    if (i >= G * D / 4) return;
+    const int hh = i / (D / 4), d4 = i - hh * (D / 4);
+    uint2 *orow =
+        reinterpret_cast<uint2 *>(a.out + ((size_t)s * a.num_heads + (size_t)h * G + hh) * D);
     if (nt == 0) {
-        for (int i = threadIdx.x; i < G * D; i += blockDim.x) orow[i] = __float2bfloat16_rn(0.f);
+        orow[d4] = make_uint2(0u, 0u);
         return;
     }
     const long long T = (long long)a.prefix[a.num_seqs] * Hkv;
@@ -428,26 +489,37 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
     const long long g0 = ((S0 + 1) * NW - 1) / T;
     const long long g1 = (S1 * NW - 1) / T;
     if (g0 == g1) return;  // written whole by one warp
-    for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
-        const int hh = i / D, d = i - hh * D;
-        float M = -INFINITY;
-        for (long long gw = g0; gw <= g1; ++gw) {
-            const long long b = (gw * T) / NW, e = ((gw + 1) * T) / NW;
-            if (max(b, S0) >= min(e, S1)) continue;
+    float M = -INFINITY;
+    long long b = (g0 * T) / NW;
+    for (long long gw = g0; gw <= g1; ++gw) {
+        const long long e = ((gw + 1) * T) / NW;
+        if (max(b, S0) < min(e, S1)) {
             const size_t rec = (size_t)gw * 2 + (b >= S0 ? 0 : 1);
             M = fmaxf(M, a.part_ml[(rec * kHeadsPad + hh) * 2]);
         }
-        float num = 0.f, den = 0.f;
-        for (long long gw = g0; gw <= g1; ++gw) {
-            const long long b = (gw * T) / NW, e = ((gw + 1) * T) / NW;
-            if (max(b, S0) >= min(e, S1)) continue;
-            const size_t rec = (size_t)gw * 2 + (b >= S0 ? 0 : 1);
-            const float w = exp2f(a.part_ml[(rec * kHeadsPad + hh) * 2] - M);
-            num += w * a.part_acc[(rec * kHeadsPad + hh) * D + d];
-            den += w * a.part_ml[(rec * kHeadsPad + hh) * 2 + 1];
-        }
-        orow[i] = __float2bfloat16_rn(num / den);
+        b = e;
     }
+    float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+    float den = 0.f;
+    b = (g0 * T) / NW;
+    for (long long gw = g0; gw <= g1; ++gw) {
+        const long long e = ((gw + 1) * T) / NW;
+        if (max(b, S0) < min(e, S1)) {
+            const size_t rec = (size_t)gw * 2 + (b >= S0 ? 0 : 1);
+            const float2 ml = reinterpret_cast<const float2 *>(a.part_ml)[rec * kHeadsPad + hh];
+            const float4 v =
+                reinterpret_cast<const float4 *>(a.part_acc + (rec * kHeadsPad + hh) * D)[d4];
+            const float w = exp2f(ml.x - M);
+            num.x += w * v.x;
+            num.y += w * v.y;
+            num.z += w * v.z;
+            num.w += w * v.w;
+            den += w * ml.y;
+        }
+        b = e;
+    }
+    const float inv = 1.f / den;
+    orow[d4] = make_uint2(pack_bf16(num.x * inv, num.y * inv), pack_bf16(num.z * inv, num.w * inv));
 }
 
 template <int D>
@@ -460,16 +532,26 @@ cudaError_t launch_decode_d(const DecodeArgs &a0, const CUtensorMap &map, int gr
     kern<<<grid, kDecodeWarps * 32, smem, stream>>>(map, a0);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    decode_merge_kernel<D><<<a0.num_seqs * a0.num_kv_heads, 128, 0, stream>>>(a0);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(a0.num_seqs * a0.num_kv_heads));
+    cfg.blockDim = dim3((unsigned)(a0.group * D / 4));
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_merge_kernel<D>, a0);
 }
 
 }  // namespace
 
-int decode_max_seqs(int head_size) {
+int decode_max_seqs(int head_size, int group) {
     const size_t limit = 227 * 1024;
-    const size_t fixed = head_size == 128 ? decode_smem_bytes<128>(0) : decode_smem_bytes<64>(0);
-    return (int)((limit - fixed) / 8);
+    const size_t fixed =
+        head_size == 128 ? decode_smem_bytes<128>(0, group) : decode_smem_bytes<64>(0, group);
+    return fixed >= limit ? 0 : (int)((limit - fixed) / 8);
 }
 
 size_t decode_workspace_bytes(int num_seqs, int head_size, int sm_count) {
@@ -520,10 +602,13 @@ cudaError_t launch_decode(void *out, const void *q, const void *kv_cache, const 
     a.max_blocks = max_blocks_per_seq;
     a.num_blocks = g.num_blocks;
     a.total_warps = (int)ctas * kDecodeWarps;
+    a.stage_bytes = 2 * (D / 64) * kTile * 128 + q_slot_bytes(a.group, D);
     a.scale_log2 = scale * 1.4426950408889634f;
     if (D == 128)
-        return launch_decode_d<128>(a, map, (int)ctas, decode_smem_bytes<128>(num_seqs), stream);
-    return launch_decode_d<64>(a, map, (int)ctas, decode_smem_bytes<64>(num_seqs), stream);
+        return launch_decode_d<128>(a, map, (int)ctas, decode_smem_bytes<128>(num_seqs, a.group),
+                                    stream);
+    return launch_decode_d<64>(a, map, (int)ctas, decode_smem_bytes<64>(num_seqs, a.group),
+                               stream);
 }
 
 }  // namespace pa

@@ -35,7 +35,7 @@ cudaError_t launch_cache_write(void *kv_cache, const KvGeom &g, const void *k_ne
 // Decode workspace bytes for num_seqs sequences on a device with sm_count SMs.
 size_t decode_workspace_bytes(int num_seqs, int head_size, int sm_count);
 // Largest num_seqs the decode kernel's shared-memory tables hold.
-int decode_max_seqs(int head_size);
+int decode_max_seqs(int head_size, int group);
 
 cudaError_t launch_decode(void *out, const void *q, const void *kv_cache, const KvGeom &g,
                           int num_heads, const int32_t *block_tables, int max_blocks_per_seq,

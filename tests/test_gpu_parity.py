@@ -242,3 +242,20 @@ def test_mixed_workload_full_size():
     compare(pre[torch.as_tensor(pre_rows, device=DEV).long()], oracle_rows(b, pool, pre_rows),
             "mixed: prefill chunks (sampled rows)")
     compare(dec, oracle_rows(b, pool, np.arange(4096, 4344, dtype=np.int32)), "mixed: decode")
+
+
+@pytest.mark.parametrize("scale", [-0.125, 0.0])
+def test_negative_and_zero_softmax_scale(scale):
+    """The scale is a free parameter: a negative one flips which keys win, zero
+    gives the mean of the visible values."""
+    b = make_batch(name="sc", seq_lens=[150, 40, 260], q_lens=[70, 1, 129], num_heads=16,
+                   num_kv_heads=4, head_size=128, block_size=16, scale=scale, seed=77,
+                   device=DEV)
+    pool = oracle_pool(b)
+    gpu_write(b)
+    compare(gpu_prefill(b), oracle_rows(b, pool), f"prefill, scale {scale}")
+    d = make_batch(name="scd", seq_lens=[150, 40, 260], q_lens=[1, 1, 1], num_heads=16,
+                   num_kv_heads=4, head_size=64, block_size=16, scale=scale, seed=78, device=DEV)
+    pool = oracle_pool(d)
+    gpu_write(d)
+    compare(gpu_decode(d), oracle_rows(d, pool), f"decode, scale {scale}")
