@@ -7,15 +7,24 @@
 // batch is flattened (§Generate function): chunk s owns query rows
 // cu_q_lens[s] .. cu_q_lens[s+1]-1.
 //
-// Design: one CTA per (query tile, KV head, chunk).  The CTA's rows are the
-// query tile's tokens for every query head of the KV head's GQA group, so each
-// K/V tile is fetched once for the whole group.  A producer warp streams 64-key
-// K/V tiles through the block table with 128B-swizzled 2-D TMA copies into a
-// 3-stage ring (full/empty mbarriers); up to 8 consumer warps each own 16 rows
-// and run QK^T, an fp32 online softmax and PV on bf16 warp MMAs with P kept in
-// registers.  Keys past a row's position are masked; tiles past the CTA's
-// causal limit are never fetched.
+// Design (tcgen05): one CTA per (128-row query tile, KV head, chunk); the rows
+// are the tile's tokens times the G query heads of the KV head, so each K/V tile
+// is fetched once for the whole GQA group.
+//   warp 0     streams 128-key K/V tiles through the block table with
+//              128B-swizzled 2-D TMA copies into a 2-stage ring;
+//   warp 1     owns the tensor memory and is the only issuer of tcgen05.mma:
+//              S = Q.K^T (A and B K-major from shared memory) and O += P.V
+//              (P from tensor memory, V MN-major from shared memory);
+//   warps 2-5  (one warpgroup) load the query tile, run the softmax with one
+//              thread per row, write P (bf16) to tensor memory, and normalise O.
+// Tensor memory (512 columns x 128 lanes): S0 [0,128) and S1 [128,256)
+// double-buffer the scores so S_{j+1} runs on the tensor cores while the softmax
+// works on S_j; P0 [256,320) and P1 [320,384) hold bf16 probabilities; O
+// [384, 384+D) accumulates P.V.  Nothing aliases, so no MMA ever writes a
+// region that a pending MMA still reads.  Keys past a row's position are
+// masked; tiles past the CTA's causal limit are never fetched.
 #include <algorithm>
+#include <cmath>
 
 #include "pa_common.cuh"
 #include "pa_internal.h"
@@ -25,17 +34,14 @@ namespace {
 
 __device__ unsigned g_err_prefill;
 
-constexpr int kKeys = 64;         // keys per K/V tile
-constexpr int kStages = 3;
-constexpr int kMaxWarps = 8;      // consumer warps
+// The softmax reference max is raised only when a row max exceeds it by more
+// than this (log2 units): P stays <= 2^8 and O is rescaled rarely.
+constexpr float kRescaleSlack = 8.0f;
 
-template <int D>
-struct PLay {
-    static constexpr int kPanels = D / 64;
-    static constexpr int kPanelBytes = kKeys * 128;   // 64 rows of one 128-byte panel
-    static constexpr int kTileBytes = kPanels * kPanelBytes;
-    static constexpr int kStageBytes = 2 * kTileBytes;  // K then V
-};
+constexpr int kTcRows = 128;    // query rows per CTA (the MMA's M)
+constexpr int kTcKeys = 128;    // keys per K/V tile
+constexpr int kTcStages = 2;
+constexpr uint32_t kTmemCols = 512, kColS = 0, kColP = 256, kColO = 384;
 
 struct PrefillArgs {
     __nv_bfloat16 *out;
@@ -45,40 +51,59 @@ struct PrefillArgs {
     const int32_t *seq_lens;
     int num_heads, num_kv_heads, group;
     int block_size, max_blocks, num_blocks;
-    int q_tile;        // query tokens per CTA (16 * (8 / group))
-    int warps;         // consumer warps = group * q_tile / 16
-    float scale_log2;
+    int q_tile;        // query tokens per CTA: floor(128 / group)
+    int negate_q;      // 1 if the softmax scale is negative (Q is negated instead)
+    float scale_log2;  // |scale| * log2(e), at least 1e-30
 };
 
 template <int D>
-constexpr size_t prefill_smem_bytes() {
-    return 1024 + (size_t)kStages * PLay<D>::kStageBytes + 2 * kStages * 8;
-}
+struct TcLay {
+    static constexpr int kPanels = D / 64;
+    static constexpr int kQPanel = kTcRows * 128;     // 16 KB: one 64-dim panel of Q
+    static constexpr int kQBytes = kPanels * kQPanel;
+    static constexpr int kKvPanel = kTcKeys * 128;
+    static constexpr int kKBytes = kPanels * kKvPanel;
+    static constexpr int kStageBytes = 2 * kKBytes;   // K then V
+    static constexpr int kPad = 16 * 1024;            // slack past the last operand
+    static constexpr int kOperands = kQBytes + kTcStages * kStageBytes + kPad;
+    static constexpr size_t kSmem = 1024 + (size_t)kOperands + 16 * 8;
+};
 
 __device__ __forceinline__ int prefill_row(int blk, int h, int off, const PrefillArgs &a) {
     if (blk < 0 || blk >= a.num_blocks) {
         atomicOr(&g_err_prefill, kErrOob);
-        return -(1 << 30);
+        return -(1 << 30);  // wholly outside the map: TMA fills zeros, nothing is read
     }
     return ((blk * 2) * a.num_kv_heads + h) * a.block_size + off;
 }
 
+// Bounded wait whose outcome is the same on every lane of the warp (the warp's
+// later tcgen05.ld/st are warp-collective, so a timeout must be warp-uniform).
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity));
+}
+
 template <int D>
-__global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
-    prefill_kernel(const __grid_constant__ CUtensorMap kv_map, const PrefillArgs a) {
-    using L = PLay<D>;
+__global__ void __launch_bounds__(192, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const PrefillArgs a) {
+    using L = TcLay<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<size_t>(smem_raw) + 1023) & ~static_cast<size_t>(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * L::kStageBytes);
-    uint64_t *empty = full + kStages;
+    uint8_t *sQ = smem;
+    uint8_t *sKV = smem + L::kQBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kOperands);
+    uint64_t *kv_full = bars, *kv_empty = bars + 2, *s_full = bars + 4, *p_full = bars + 6;
+    uint64_t *o_done = bars + 8, *q_full = bars + 9, *drain = bars + 10;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 11);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int s = blockIdx.z, h = blockIdx.y;
     const int qt = gridDim.x - 1 - blockIdx.x;  // longest tiles first
     const int q0 = a.cu_q_lens[s];
     const int q_len = a.cu_q_lens[s + 1] - q0;
-    const int t0 = qt * a.q_tile;
+    const int QT = a.q_tile, G = a.group;
+    const int t0 = qt * QT;
     if (t0 >= q_len) return;
     int len = a.seq_lens[s];
     const int max_len = a.max_blocks * a.block_size;
@@ -87,238 +112,286 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
         len = std::min(std::max(len, q_len), max_len);
     }
     const int ctx = len - q_len;
-    const int t_last = std::min(t0 + a.q_tile, q_len) - 1;   // last valid token of the tile
-    const int n_keys = ctx + t_last + 1;                      // keys any row of the CTA sees
-    const int n_kt = (n_keys + kKeys - 1) / kKeys;
-    const int G = a.group;
+    const int t_last = std::min(t0 + QT, q_len) - 1;
+    const int n_keys = ctx + t_last + 1;
+    const int n_kt = (n_keys + kTcKeys - 1) / kTcKeys;
 
     if (threadIdx.x == 0) {
         prefetch_tensormap(&kv_map);
-        for (int st = 0; st < kStages; ++st) {
-            mbar_init(&full[st], 1);
-            mbar_init(&empty[st], a.warps);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&kv_full[i], 1);
+            mbar_init(&kv_empty[i], 1);
+            mbar_init(&s_full[i], 1);
+            mbar_init(&p_full[i], 4);
         }
+        mbar_init(o_done, 1);
+        mbar_init(q_full, 4);
+        mbar_init(drain, 1);
         fence_barrier_init();
     }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
 
-    if (warp == a.warps) {
-        // ------------------------------------------------------------ producer warp
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
         const int bs = a.block_size;
         const int box_rows = bs >= 16 ? 16 : bs;
-        const int boxes = kKeys / box_rows;   // 4 or 8
+        const int nbox = kTcKeys / box_rows;  // 8 or 16 boxes per tile
         const int32_t *bt = a.block_tables + (size_t)s * a.max_blocks;
         const int v_off = a.num_kv_heads * bs;
-        const uint32_t box_bytes = (uint32_t)box_rows * 128u;
         const uint64_t policy = policy_evict_first();
         auto box_row = [&](int kt) {
-            int r = -1;
-            const int tok = kt * kKeys + lane * box_rows;
-            if (lane < boxes && tok < len) r = prefill_row(bt[tok / bs], h, tok % bs, a);
-            return r;
+            const int tok = kt * kTcKeys + lane * box_rows;
+            if (lane >= nbox) return 0;
+            if (tok >= len) return -(1 << 30);  // past the sequence: TMA fills zeros
+            return prefill_row(bt[tok / bs], h, tok % bs, a);
         };
         int nxt = box_row(0);
+        int issued = 0;
         for (int kt = 0; kt < n_kt; ++kt) {
             const int cur = nxt;
             if (kt + 1 < n_kt) nxt = box_row(kt + 1);
-            const int st = kt % kStages;
-            if (kt >= kStages) {
-                if (!mbar_wait_bounded(&empty[st], (uint32_t)((kt / kStages) - 1) & 1u)) {
-                    if (lane == 0) atomicOr(&g_err_prefill, kErrTimeout);
-                    return;  // consumers time out on the full barrier in turn
-                }
+            const int st = kt & 1;
+            if (kt >= kTcStages && !warp_wait(&kv_empty[st], (uint32_t)((kt >> 1) - 1) & 1u)) {
+                if (lane == 0) atomicOr(&g_err_prefill, kErrTimeout);
+                break;
             }
-            const unsigned have = __ballot_sync(0xffffffffu, cur != -1);
-            if (lane == 0)
-                mbar_arrive_expect_tx(&full[st],
-                                      (uint32_t)__popc(have) * 2u * L::kPanels * box_bytes);
+            if (lane == 0) mbar_arrive_expect_tx(&kv_full[st], (uint32_t)(2 * L::kKBytes));
             __syncwarp();
-            if (cur != -1) {
-                uint8_t *stg = smem + (size_t)st * L::kStageBytes;
+            if (lane < nbox) {
+                uint8_t *stg = sKV + (size_t)st * L::kStageBytes;
 #pragma unroll
                 for (int p = 0; p < L::kPanels; ++p) {
-                    tma_load_2d_hint(stg + p * L::kPanelBytes + lane * box_rows * 128, &kv_map,
-                                     &full[st], 64 * p, cur, policy);
-                    tma_load_2d_hint(stg + L::kTileBytes + p * L::kPanelBytes +
-                                         lane * box_rows * 128,
-                                     &kv_map, &full[st], 64 * p, cur + v_off, policy);
+                    tma_load_2d_hint(stg + p * L::kKvPanel + lane * box_rows * 128, &kv_map,
+                                     &kv_full[st], 64 * p, cur, policy);
+                    tma_load_2d_hint(stg + L::kKBytes + p * L::kKvPanel + lane * box_rows * 128,
+                                     &kv_map, &kv_full[st], 64 * p, cur + v_off, policy);
                 }
             }
+            issued = kt + 1;
         }
-        return;
-    }
-
-    // ---------------------------------------------------------------- consumer warps
-    const int sub = a.q_tile / 16;           // 16-token sub-tiles per query tile
-    const int gh = warp / sub;               // query head inside the group
-    const int ts = warp - gh * sub;
-    const int hq = h * G + gh;
-    const int tw = t0 + ts * 16;             // first token of this warp's rows
-    const int r0 = lane >> 2;                // rows r0 and r0+8 of the warp
-    // Causal limit of row r: min(ctx + tw + r, len - 1).
-    const int lim0 = std::min(ctx + tw + r0, len - 1);
-    const int lim1 = std::min(ctx + tw + r0 + 8, len - 1);
-    const int warp_lo = std::min(ctx + tw, len - 1);
-    const int warp_hi = std::min(ctx + tw + 15, len - 1);
-
-    uint32_t qf[D / 16][4];
-    {
-        const int ta = tw + r0, tb = tw + r0 + 8;
-        const __nv_bfloat16 *qa = a.q + ((size_t)(q0 + ta) * a.num_heads + hq) * D;
-        const __nv_bfloat16 *qb = a.q + ((size_t)(q0 + tb) * a.num_heads + hq) * D;
+        // Never leave with copies in flight into this CTA's shared memory.
+        for (int kt = std::max(0, issued - kTcStages); kt < issued; ++kt)
+            mbar_wait_bounded(&kv_full[kt & 1], (uint32_t)(kt >> 1) & 1u);
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        const uint32_t idesc_s = tc_idesc_bf16(kTcRows, kTcKeys, 0);
+        const uint32_t idesc_pv = tc_idesc_bf16(kTcRows, D, 1);
+        const uint32_t q_base = smem_u32(sQ), kv_base = smem_u32(sKV);
+        bool ok = warp_wait(q_full, 0);
+        auto issue_s = [&](int j) -> bool {
+            const int st = j & 1;
+            if (!warp_wait(&kv_full[st], (uint32_t)(j >> 1) & 1u)) return false;
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t kb = kv_base + st * L::kStageBytes;
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-            const int d = 16 * k + 2 * (lane & 3);
-            qf[k][0] = ta < q_len ? *reinterpret_cast<const uint32_t *>(qa + d) : 0u;
-            qf[k][1] = tb < q_len ? *reinterpret_cast<const uint32_t *>(qb + d) : 0u;
-            qf[k][2] = ta < q_len ? *reinterpret_cast<const uint32_t *>(qa + d + 8) : 0u;
-            qf[k][3] = tb < q_len ? *reinterpret_cast<const uint32_t *>(qb + d + 8) : 0u;
-        }
-    }
-    float o[D / 8][4];
-#pragma unroll
-    for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-
-    for (int kt = 0; kt < n_kt; ++kt) {
-        const int st = kt % kStages;
-        if (!mbar_wait_bounded(&full[st], (uint32_t)(kt / kStages) & 1u)) {
-            if (lane == 0) atomicOr(&g_err_prefill, kErrTimeout);
-            return;
-        }
-        const int k0 = kt * kKeys;
-        if (k0 <= warp_hi) {
-            const uint32_t kb = smem_u32(smem + (size_t)st * L::kStageBytes);
-            const uint32_t vb = kb + L::kTileBytes;
-            float sacc[8][4];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.f;
-#pragma unroll
-            for (int k = 0; k < D / 16; ++k) {
-                const uint32_t panel = kb + (k >> 2) * L::kPanelBytes;
-#pragma unroll
-                for (int np = 0; np < 4; ++np) {
-                    const int mi = lane >> 3;
-                    const int row = np * 16 + (lane & 7) + (mi >> 1) * 8;
-                    const int chunk = 2 * (k & 3) + (mi & 1);
-                    uint32_t bf[4];
-                    ldsm_x4(bf, swz128(panel, row, chunk));
-                    mma_bf16(sacc[2 * np], qf[k], bf[0], bf[1]);
-                    mma_bf16(sacc[2 * np + 1], qf[k], bf[2], bf[3]);
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = (k >> 2) * L::kQPanel + (k & 3) * 32;
+                    const uint64_t ad = tc_desc_sw128(q_base + off, 16, 1024);
+                    const uint64_t bd = tc_desc_sw128(kb + (k >> 2) * L::kKvPanel + (k & 3) * 32,
+                                                      16, 1024);
+                    tc_mma_ss(tmem + kColS + st * kTcKeys, ad, bd, idesc_s, k > 0 ? 1u : 0u);
                 }
+                tc_commit(&s_full[st]);
             }
-            const bool need_mask = (k0 + kKeys - 1 > warp_lo);
-            float mx0 = -INFINITY, mx1 = -INFINITY;
+            __syncwarp();
+            return true;
+        };
+        if (ok) ok = issue_s(0);
+        for (int j = 0; ok && j < n_kt; ++j) {
+            if (j + 1 < n_kt && !(ok = issue_s(j + 1))) break;
+            if (!(ok = warp_wait(&p_full[j & 1], (uint32_t)(j >> 1) & 1u))) break;
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t vb = kv_base + (j & 1) * L::kStageBytes + L::kKBytes;
 #pragma unroll
-            for (int nt = 0; nt < 8; ++nt) {
-                const int key = k0 + nt * 8 + 2 * (lane & 3);
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    float x0 = sacc[nt][e] * a.scale_log2;
-                    float x1 = sacc[nt][2 + e] * a.scale_log2;
-                    if (need_mask) {
-                        x0 = key + e <= lim0 ? x0 : -INFINITY;
-                        x1 = key + e <= lim1 ? x1 : -INFINITY;
-                    }
-                    sacc[nt][e] = x0;
-                    sacc[nt][2 + e] = x1;
-                    mx0 = fmaxf(mx0, x0);
-                    mx1 = fmaxf(mx1, x1);
+                for (int kk = 0; kk < kTcKeys / 16; ++kk) {
+                    const uint64_t bd = tc_desc_sw128(vb + kk * 16 * 128, L::kKvPanel, 1024);
+                    tc_mma_ts(tmem + kColO, tmem + kColP + (j & 1) * 64 + kk * 8, bd, idesc_pv,
+                              (j > 0 || kk > 0) ? 1u : 0u);
                 }
+                tc_commit(&kv_empty[j & 1]);
+                tc_commit(o_done);
             }
-#pragma unroll
-            for (int o_ = 1; o_ < 4; o_ <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o_));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o_));
-            }
-            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-            const float cr0 = fast_exp2(m0 - mn0), cr1 = fast_exp2(m1 - mn1);
-            m0 = mn0;
-            m1 = mn1;
-            uint32_t pa[4][4];
-            float rs0 = 0.f, rs1 = 0.f;
-#pragma unroll
-            for (int nt = 0; nt < 8; ++nt) {
-                const uint32_t lo = pack_bf16(fast_exp2(sacc[nt][0] - mn0),
-                                              fast_exp2(sacc[nt][1] - mn0));
-                const uint32_t hi = pack_bf16(fast_exp2(sacc[nt][2] - mn1),
-                                              fast_exp2(sacc[nt][3] - mn1));
-                rs0 += bf16_lo(lo) + bf16_hi(lo);
-                rs1 += bf16_lo(hi) + bf16_hi(hi);
-                pa[nt >> 1][(nt & 1) * 2 + 0] = lo;
-                pa[nt >> 1][(nt & 1) * 2 + 1] = hi;
-            }
-#pragma unroll
-            for (int o_ = 1; o_ < 4; o_ <<= 1) {
-                rs0 += __shfl_xor_sync(0xffffffffu, rs0, o_);
-                rs1 += __shfl_xor_sync(0xffffffffu, rs1, o_);
-            }
-            l0 = l0 * cr0 + rs0;
-            l1 = l1 * cr1 + rs1;
-#pragma unroll
-            for (int i = 0; i < D / 8; ++i) {
-                o[i][0] *= cr0;
-                o[i][1] *= cr0;
-                o[i][2] *= cr1;
-                o[i][3] *= cr1;
-            }
-            // Keys at or past the sequence end (stale rows, unfetched boxes): their V
-            // must contribute exactly zero even if the stale data is not finite.
-            const int kv_valid = len - k0;  // keys of this tile inside the sequence
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-#pragma unroll
-                for (int dp = 0; dp < D / 16; ++dp) {
-                    const uint32_t panel = vb + (dp >> 2) * L::kPanelBytes;
-                    const int mi = lane >> 3;
-                    const int row = kk * 16 + (lane & 7) + (mi & 1) * 8;
-                    const int chunk = 2 * (dp & 3) + (mi >> 1);
-                    uint32_t bf[4];
-                    ldsm_x4_t(bf, swz128(panel, row, chunk));
-                    if (kv_valid < kKeys) {
-                        const int kr = kk * 16 + 2 * (lane & 3);
-                        const uint32_t m_lo = (kr < kv_valid ? 0xffffu : 0u) |
-                                              (kr + 1 < kv_valid ? 0xffff0000u : 0u);
-                        const uint32_t m_hi = (kr + 8 < kv_valid ? 0xffffu : 0u) |
-                                              (kr + 9 < kv_valid ? 0xffff0000u : 0u);
-                        bf[0] &= m_lo;
-                        bf[1] &= m_hi;
-                        bf[2] &= m_lo;
-                        bf[3] &= m_hi;
-                    }
-                    mma_bf16(o[2 * dp], pa[kk], bf[0], bf[1]);
-                    mma_bf16(o[2 * dp + 1], pa[kk], bf[2], bf[3]);
-                }
-            }
+            __syncwarp();
         }
+        if (!ok && lane == 0) atomicOr(&g_err_prefill, kErrTimeout);
+        // Wait for every issued MMA before the tensor memory is released.
+        if (lane == 0) tc_commit(drain);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st]);
-    }
-
-    // Normalise and store the rows this warp owns.
-    const float i0 = 1.f / l0, i1 = 1.f / l1;
-    const int ta = tw + r0, tb = tw + r0 + 8;
+        mbar_wait_bounded(drain, 0);
+    } else {
+        // ------------------------------------------------------------ softmax warpgroup
+        const int row = 32 * (warp & 3) + lane;   // this thread's TMEM lane = query row
+        const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+        const int t = row / G, gq = row - t * G;
+        const bool real = row < QT * G && t0 + t < q_len;
+        // Query row -> shared memory in the 128B-swizzled K-major layout.  Loads
+        // are bounds-checked: the host does not know the total number of rows.
+        {
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                a.q + ((size_t)(q0 + t0 + t) * a.num_heads + (size_t)h * G + gq) * D);
+            const uint32_t flip = a.negate_q ? 0x80008000u : 0u;  // exact bf16 negation
 #pragma unroll
-    for (int i = 0; i < D / 8; ++i) {
-        const int d = i * 8 + 2 * (lane & 3);
-        if (ta < q_len)
-            *reinterpret_cast<uint32_t *>(a.out + ((size_t)(q0 + ta) * a.num_heads + hq) * D + d) =
-                pack_bf16(o[i][0] * i0, o[i][1] * i0);
-        if (tb < q_len)
-            *reinterpret_cast<uint32_t *>(a.out + ((size_t)(q0 + tb) * a.num_heads + hq) * D + d) =
-                pack_bf16(o[i][2] * i1, o[i][3] * i1);
+            for (int p = 0; p < L::kPanels; ++p)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint4 v = real ? src[p * 8 + c] : make_uint4(0, 0, 0, 0);
+                    v.x ^= flip;
+                    v.y ^= flip;
+                    v.z ^= flip;
+                    v.w ^= flip;
+                    *reinterpret_cast<uint4 *>(sQ + p * L::kQPanel + row * 128 +
+                                               ((c ^ (row & 7)) << 4)) = v;
+                }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(q_full);
+        }
+        const int lim = real ? std::min(ctx + t0 + t, len - 1) : len - 1;
+        const float sl2 = a.scale_log2;  // > 0: a negative scale was moved into Q
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_kt; ++j) {
+            const int sb = j & 1;
+            if (!(ok = warp_wait(&s_full[sb], (uint32_t)(j >> 1) & 1u))) break;
+            tc_fence_after();
+            float x[kTcKeys];
+#pragma unroll
+            for (int c = 0; c < kTcKeys / 32; ++c)
+                tmem_ld32(trow + kColS + sb * kTcKeys + 32 * c,
+                          *reinterpret_cast<float(*)[32]>(&x[32 * c]));
+            tc_wait_ld();
+            const int k0 = j * kTcKeys;
+            if (k0 + kTcKeys - 1 > lim) {
+                // Diagonal / last tile: keys past this row's limit get -inf.
+#pragma unroll
+                for (int c = 0; c < kTcKeys; ++c)
+                    if (k0 + c > lim) x[c] = -INFINITY;
+            }
+            // The scale is folded into the exponent below, so the max is taken over
+            // raw scores (four independent chains).
+            float r0m = -INFINITY, r1m = -INFINITY, r2m = -INFINITY, r3m = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kTcKeys; c += 4) {
+                r0m = fmaxf(r0m, x[c]);
+                r1m = fmaxf(r1m, x[c + 1]);
+                r2m = fmaxf(r2m, x[c + 2]);
+                r3m = fmaxf(r3m, x[c + 3]);
+            }
+            const float mx = fmaxf(fmaxf(r0m, r1m), fmaxf(r2m, r3m)) * sl2;
+            const bool grow = mx > m + kRescaleSlack;
+            if (__any_sync(0xffffffffu, grow)) {
+                const float mn = grow ? fmaxf(m, mx) : m;
+                const float cr = fast_exp2(m - mn);
+                l *= cr;
+                if (j > 0) {
+                    // O holds P_0..P_{j-1} . V: wait for the last of those products.
+                    if (!(ok = warp_wait(o_done, (uint32_t)(j - 1) & 1u))) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        float o[32];
+                        tmem_ld32(trow + kColO + 32 * c, o);
+                        tc_wait_ld();
+                        uint32_t r[32];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(o[e] * cr);
+                        tmem_st32(trow + kColO + 32 * c, r);
+                    }
+                }
+                m = mn;
+            }
+            // P = 2^(x*scale - m) <= 2^8; the row sum is kept in fp32 before the
+            // bf16 rounding of P (relative effect ~2^-9 per term, averaging out).
+            const float nm = -m;
+            float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int c = 0; c < 32; c += 2) {
+                    const float p0 = fast_exp2(fmaf(x[64 * half + 2 * c], sl2, nm));
+                    const float p1 = fast_exp2(fmaf(x[64 * half + 2 * c + 1], sl2, nm));
+                    const float p2 = fast_exp2(fmaf(x[64 * half + 2 * c + 2], sl2, nm));
+                    const float p3 = fast_exp2(fmaf(x[64 * half + 2 * c + 3], sl2, nm));
+                    s0 += p0;
+                    s1 += p1;
+                    s2 += p2;
+                    s3 += p3;
+                    pk[c] = pack_bf16(p0, p1);
+                    pk[c + 1] = pack_bf16(p2, p3);
+                }
+                tmem_st32(trow + kColP + sb * 64 + 32 * half, pk);
+            }
+            tc_wait_st();
+            l += (s0 + s1) + (s2 + s3);
+            if (k0 + kTcKeys > len) {
+                // Keys at or past the sequence end: zero their V rows so P=0 adds
+                // exactly nothing whatever the stale data is.
+                if (!(ok = warp_wait(&kv_full[sb], (uint32_t)(j >> 1) & 1u))) break;
+                const int r0 = len - k0, nr = kTcKeys - r0;
+                uint8_t *vs = sKV + (size_t)sb * L::kStageBytes + L::kKBytes;
+                for (int e = row; e < nr * 8 * L::kPanels; e += 128) {
+                    const int p = e / (nr * 8), rr = (e >> 3) % nr, ch = e & 7;
+                    *reinterpret_cast<uint4 *>(vs + p * L::kKvPanel + (r0 + rr) * 128 + ch * 16) =
+                        make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[sb]);
+        }
+        if (ok) ok = warp_wait(o_done, (uint32_t)(n_kt - 1) & 1u);
+        if (!ok) {
+            if (lane == 0) atomicOr(&g_err_prefill, kErrTimeout);
+        } else {
+            tc_fence_after();
+            const float inv = 1.f / l;
+            uint4 *dst = reinterpret_cast<uint4 *>(
+                a.out + ((size_t)(q0 + t0 + t) * a.num_heads + (size_t)h * G + gq) * D);
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                float o[32];
+                tmem_ld32(trow + kColO + 32 * c, o);
+                tc_wait_ld();
+                if (real) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        dst[c * 4 + e] = make_uint4(
+                            pack_bf16(o[8 * e + 0] * inv, o[8 * e + 1] * inv),
+                            pack_bf16(o[8 * e + 2] * inv, o[8 * e + 3] * inv),
+                            pack_bf16(o[8 * e + 4] * inv, o[8 * e + 5] * inv),
+                            pack_bf16(o[8 * e + 6] * inv, o[8 * e + 7] * inv));
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
     }
 }
 
 template <int D>
-cudaError_t launch_prefill_d(const PrefillArgs &a, const CUtensorMap &map, dim3 grid,
-                             cudaStream_t stream) {
-    const size_t smem = prefill_smem_bytes<D>();
-    auto kern = prefill_kernel<D>;
+cudaError_t launch_prefill_tc(const PrefillArgs &a, const CUtensorMap &map, dim3 grid,
+                              cudaStream_t stream) {
+    const size_t smem = TcLay<D>::kSmem;
+    auto kern = prefill_tc_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, (a.warps + 1) * 32, smem, stream>>>(map, a);
+    kern<<<grid, 192, smem, stream>>>(map, a);
     return cudaGetLastError();
 }
 
@@ -350,13 +423,16 @@ cudaError_t launch_prefill(void *out, const void *q, const int32_t *cu_q_lens, i
     a.block_size = g.block_size;
     a.max_blocks = max_blocks_per_seq;
     a.num_blocks = g.num_blocks;
-    a.q_tile = 16 * (kMaxWarps / a.group);
-    a.warps = a.group * (a.q_tile / 16);
-    a.scale_log2 = scale * 1.4426950408889634f;
+    // The kernel folds a positive scale into the exponent; a negative scale is
+    // applied by negating Q (exact in bf16), and a zero scale is replaced by a
+    // positive value far too small to change any finite score.
+    a.negate_q = scale < 0.f ? 1 : 0;
+    a.scale_log2 = std::max(std::fabs(scale) * 1.4426950408889634f, 1e-30f);
+    a.q_tile = kTcRows / a.group;
     dim3 grid((unsigned)((max_q_len + a.q_tile - 1) / a.q_tile), (unsigned)g.num_kv_heads,
               (unsigned)num_chunks);
-    if (g.head_size == 128) return launch_prefill_d<128>(a, map, grid, stream);
-    return launch_prefill_d<64>(a, map, grid, stream);
+    if (g.head_size == 128) return launch_prefill_tc<128>(a, map, grid, stream);
+    return launch_prefill_tc<64>(a, map, grid, stream);
 }
 
 }  // namespace pa
