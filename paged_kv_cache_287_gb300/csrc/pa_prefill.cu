@@ -7,22 +7,22 @@
 // batch is flattened (§Generate function): chunk s owns query rows
 // cu_q_lens[s] .. cu_q_lens[s+1]-1.
 //
-// Design (tcgen05): one CTA per (128-row query tile, KV head, chunk); the rows
-// are the tile's tokens times the G query heads of the KV head, so each K/V tile
-// is fetched once for the whole GQA group.
+// Design (tcgen05): one CTA per (two 128-row query tiles, KV head, chunk); a
+// tile's rows are its tokens times the G query heads of the KV head, so each K/V
+// tile is fetched once for 256 rows of the whole GQA group.
 //   warp 0     streams 128-key K/V tiles through the block table with
 //              128B-swizzled 2-D TMA copies into a 2-stage ring;
 //   warp 1     owns the tensor memory and is the only issuer of tcgen05.mma:
-//              S = Q.K^T (A and B K-major from shared memory) and O += P.V
-//              (P from tensor memory, V MN-major from shared memory);
-//   warps 2-5  (one warpgroup) load the query tile, run the softmax with one
-//              thread per row, write P (bf16) to tensor memory, and normalise O.
-// Tensor memory (512 columns x 128 lanes): S0 [0,128) and S1 [128,256)
-// double-buffer the scores so S_{j+1} runs on the tensor cores while the softmax
-// works on S_j; P0 [256,320) and P1 [320,384) hold bf16 probabilities; O
-// [384, 384+D) accumulates P.V.  Nothing aliases, so no MMA ever writes a
-// region that a pending MMA still reads.  Keys past a row's position are
-// masked; tiles past the CTA's causal limit are never fetched.
+//              S_t = Q_t.K^T (A and B K-major from shared memory) and
+//              O_t += P_t.V (P from tensor memory, V MN-major in shared memory);
+//   warps 2-5  and 6-9: one warpgroup per query tile; each loads its tile,
+//              runs the softmax with one thread per row, writes P (bf16) into
+//              tensor memory over its own scores, and normalises O.
+// Tensor memory (512 columns x 128 lanes): S_0/P_0 [0,128), S_1/P_1 [128,256),
+// O_0 [256,384), O_1 [384,512).  P_t overwrites S_t, so S_t for the next K/V
+// tile is issued only after O_t += P_t.V has completed; meanwhile the tensor
+// cores work on the other tile.  Keys past a row's position are masked; tiles
+// past the CTA's causal limit are never fetched.
 #include <algorithm>
 #include <cmath>
 
@@ -38,10 +38,12 @@ __device__ unsigned g_err_prefill;
 // than this (log2 units): P stays <= 2^8 and O is rescaled rarely.
 constexpr float kRescaleSlack = 8.0f;
 
-constexpr int kTcRows = 128;    // query rows per CTA (the MMA's M)
+constexpr int kTcRows = 128;    // query rows per tile (the MMA's M)
+constexpr int kTcTiles = 2;     // query tiles per CTA
 constexpr int kTcKeys = 128;    // keys per K/V tile
 constexpr int kTcStages = 2;
-constexpr uint32_t kTmemCols = 512, kColS = 0, kColP = 256, kColO = 384;
+constexpr int kTcThreads = (2 + 4 * kTcTiles) * 32;
+constexpr uint32_t kTmemCols = 512, kColO = 256;
 
 struct PrefillArgs {
     __nv_bfloat16 *out;
@@ -51,7 +53,7 @@ struct PrefillArgs {
     const int32_t *seq_lens;
     int num_heads, num_kv_heads, group;
     int block_size, max_blocks, num_blocks;
-    int q_tile;        // query tokens per CTA: floor(128 / group)
+    int q_tile;        // query tokens per 128-row tile: floor(128 / group)
     int negate_q;      // 1 if the softmax scale is negative (Q is negated instead)
     float scale_log2;  // |scale| * log2(e), at least 1e-30
 };
@@ -59,8 +61,9 @@ struct PrefillArgs {
 template <int D>
 struct TcLay {
     static constexpr int kPanels = D / 64;
-    static constexpr int kQPanel = kTcRows * 128;     // 16 KB: one 64-dim panel of Q
-    static constexpr int kQBytes = kPanels * kQPanel;
+    static constexpr int kQPanel = kTcRows * 128;     // 16 KB: one 64-dim panel of a tile
+    static constexpr int kQTile = kPanels * kQPanel;
+    static constexpr int kQBytes = kTcTiles * kQTile;
     static constexpr int kKvPanel = kTcKeys * 128;
     static constexpr int kKBytes = kPanels * kKvPanel;
     static constexpr int kStageBytes = 2 * kKBytes;   // K then V
@@ -84,7 +87,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const PrefillArgs a) {
     using L = TcLay<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -93,9 +96,10 @@ __global__ void __launch_bounds__(192, 1)
     uint8_t *sQ = smem;
     uint8_t *sKV = smem + L::kQBytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kOperands);
-    uint64_t *kv_full = bars, *kv_empty = bars + 2, *s_full = bars + 4, *p_full = bars + 6;
-    uint64_t *o_done = bars + 8, *q_full = bars + 9, *drain = bars + 10;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 11);
+    uint64_t *kv_full = bars, *kv_empty = bars + 2;
+    uint64_t *s_full = bars + 4, *p_full = bars + 6, *pv_done = bars + 8, *q_full = bars + 10;
+    uint64_t *drain = bars + 12;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 13);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int s = blockIdx.z, h = blockIdx.y;
@@ -103,8 +107,9 @@ __global__ void __launch_bounds__(192, 1)
     const int q0 = a.cu_q_lens[s];
     const int q_len = a.cu_q_lens[s + 1] - q0;
     const int QT = a.q_tile, G = a.group;
-    const int t0 = qt * QT;
+    const int t0 = qt * kTcTiles * QT;
     if (t0 >= q_len) return;
+    const bool has1 = t0 + QT < q_len;  // the second tile holds at least one token
     int len = a.seq_lens[s];
     const int max_len = a.max_blocks * a.block_size;
     if (len < q_len || len > max_len) {
@@ -112,7 +117,7 @@ __global__ void __launch_bounds__(192, 1)
         len = std::min(std::max(len, q_len), max_len);
     }
     const int ctx = len - q_len;
-    const int t_last = std::min(t0 + QT, q_len) - 1;
+    const int t_last = std::min(t0 + kTcTiles * QT, q_len) - 1;
     const int n_keys = ctx + t_last + 1;
     const int n_kt = (n_keys + kTcKeys - 1) / kTcKeys;
 
@@ -123,9 +128,9 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(&kv_empty[i], 1);
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], 4);
+            mbar_init(&pv_done[i], 1);
+            mbar_init(&q_full[i], 4);
         }
-        mbar_init(o_done, 1);
-        mbar_init(q_full, 4);
         mbar_init(drain, 1);
         fence_barrier_init();
     }
@@ -184,61 +189,85 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t idesc_s = tc_idesc_bf16(kTcRows, kTcKeys, 0);
         const uint32_t idesc_pv = tc_idesc_bf16(kTcRows, D, 1);
         const uint32_t q_base = smem_u32(sQ), kv_base = smem_u32(sKV);
-        bool ok = warp_wait(q_full, 0);
-        auto issue_s = [&](int j) -> bool {
-            const int st = j & 1;
-            if (!warp_wait(&kv_full[st], (uint32_t)(j >> 1) & 1u)) return false;
-            tc_fence_after();
+        const int ntiles = has1 ? 2 : 1;
+        // S_t = Q_t . K_j^T into tensor-memory columns [128 t, 128 t + 128).
+        auto issue_s = [&](int j, int t) {
             if (lane == 0) {
-                const uint32_t kb = kv_base + st * L::kStageBytes;
+                const uint32_t kb = kv_base + (j & 1) * L::kStageBytes;
+                const uint32_t qb = q_base + t * L::kQTile;
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint32_t off = (k >> 2) * L::kQPanel + (k & 3) * 32;
-                    const uint64_t ad = tc_desc_sw128(q_base + off, 16, 1024);
+                    const uint64_t ad = tc_desc_sw128(qb + off, 16, 1024);
                     const uint64_t bd = tc_desc_sw128(kb + (k >> 2) * L::kKvPanel + (k & 3) * 32,
                                                       16, 1024);
-                    tc_mma_ss(tmem + kColS + st * kTcKeys, ad, bd, idesc_s, k > 0 ? 1u : 0u);
+                    tc_mma_ss(tmem + t * kTcRows, ad, bd, idesc_s, k > 0 ? 1u : 0u);
                 }
-                tc_commit(&s_full[st]);
+                tc_commit(&s_full[t]);
             }
             __syncwarp();
-            return true;
         };
-        if (ok) ok = issue_s(0);
-        for (int j = 0; ok && j < n_kt; ++j) {
-            if (j + 1 < n_kt && !(ok = issue_s(j + 1))) break;
-            if (!(ok = warp_wait(&p_full[j & 1], (uint32_t)(j >> 1) & 1u))) break;
-            tc_fence_after();
+        // O_t += P_t . V_j, P_t in the first 64 columns of tile t's score region.
+        auto issue_pv = [&](int j, int t) {
             if (lane == 0) {
                 const uint32_t vb = kv_base + (j & 1) * L::kStageBytes + L::kKBytes;
 #pragma unroll
                 for (int kk = 0; kk < kTcKeys / 16; ++kk) {
                     const uint64_t bd = tc_desc_sw128(vb + kk * 16 * 128, L::kKvPanel, 1024);
-                    tc_mma_ts(tmem + kColO, tmem + kColP + (j & 1) * 64 + kk * 8, bd, idesc_pv,
-                              (j > 0 || kk > 0) ? 1u : 0u);
+                    tc_mma_ts(tmem + kColO + t * kTcRows, tmem + t * kTcRows + kk * 8, bd,
+                              idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
                 }
-                tc_commit(&kv_empty[j & 1]);
-                tc_commit(o_done);
+                tc_commit(&pv_done[t]);
             }
             __syncwarp();
+        };
+        bool ok = warp_wait(&q_full[0], 0) && (!has1 || warp_wait(&q_full[1], 0));
+        ok = ok && warp_wait(&kv_full[0], 0);
+        if (ok) {
+            tc_fence_after();
+            for (int t = 0; t < ntiles; ++t) issue_s(0, t);
+        }
+        for (int j = 0; ok && j < n_kt; ++j) {
+            for (int t = 0; t < ntiles; ++t) {
+                if (!(ok = warp_wait(&p_full[t], (uint32_t)j & 1u))) break;
+                tc_fence_after();
+                issue_pv(j, t);
+            }
+            if (!ok) break;
+            if (lane == 0) tc_commit(&kv_empty[j & 1]);
+            __syncwarp();
+            if (j + 1 < n_kt) {
+                if (!(ok = warp_wait(&kv_full[(j + 1) & 1], (uint32_t)((j + 1) >> 1) & 1u)))
+                    break;
+                for (int t = 0; t < ntiles; ++t) {
+                    // P_t lives where S_t will be written: wait for O_t += P_t.V.
+                    if (!(ok = warp_wait(&pv_done[t], (uint32_t)j & 1u))) break;
+                    tc_fence_after();
+                    issue_s(j + 1, t);
+                }
+            }
         }
         if (!ok && lane == 0) atomicOr(&g_err_prefill, kErrTimeout);
         // Wait for every issued MMA before the tensor memory is released.
         if (lane == 0) tc_commit(drain);
         __syncwarp();
         mbar_wait_bounded(drain, 0);
-    } else {
-        // ------------------------------------------------------------ softmax warpgroup
+    } else if ((warp - 2) / 4 == 0 || has1) {
+        // ------------------------------------------------------------ softmax warpgroups
+        const int t = (warp - 2) / 4;             // query tile of this warpgroup
         const int row = 32 * (warp & 3) + lane;   // this thread's TMEM lane = query row
         const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-        const int t = row / G, gq = row - t * G;
-        const bool real = row < QT * G && t0 + t < q_len;
+        const uint32_t cs = trow + t * kTcRows;   // this tile's score / P columns
+        const uint32_t co = trow + kColO + t * kTcRows;
+        const int tok = t * QT + row / G, gq = row % G;
+        const bool real = row < QT * G && t0 + tok < q_len;
         // Query row -> shared memory in the 128B-swizzled K-major layout.  Loads
         // are bounds-checked: the host does not know the total number of rows.
         {
             const uint4 *src = reinterpret_cast<const uint4 *>(
-                a.q + ((size_t)(q0 + t0 + t) * a.num_heads + (size_t)h * G + gq) * D);
+                a.q + ((size_t)(q0 + t0 + tok) * a.num_heads + (size_t)h * G + gq) * D);
             const uint32_t flip = a.negate_q ? 0x80008000u : 0u;  // exact bf16 negation
+            uint8_t *qt_smem = sQ + t * L::kQTile;
 #pragma unroll
             for (int p = 0; p < L::kPanels; ++p)
 #pragma unroll
@@ -248,97 +277,105 @@ __global__ void __launch_bounds__(192, 1)
                     v.y ^= flip;
                     v.z ^= flip;
                     v.w ^= flip;
-                    *reinterpret_cast<uint4 *>(sQ + p * L::kQPanel + row * 128 +
+                    *reinterpret_cast<uint4 *>(qt_smem + p * L::kQPanel + row * 128 +
                                                ((c ^ (row & 7)) << 4)) = v;
                 }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(q_full);
+            if (lane == 0) mbar_arrive(&q_full[t]);
         }
-        const int lim = real ? std::min(ctx + t0 + t, len - 1) : len - 1;
+        const int lim = real ? std::min(ctx + t0 + tok, len - 1) : len - 1;
         const float sl2 = a.scale_log2;  // > 0: a negative scale was moved into Q
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < n_kt; ++j) {
-            const int sb = j & 1;
-            if (!(ok = warp_wait(&s_full[sb], (uint32_t)(j >> 1) & 1u))) break;
+            if (!(ok = warp_wait(&s_full[t], (uint32_t)j & 1u))) break;
             tc_fence_after();
-            float x[kTcKeys];
-#pragma unroll
-            for (int c = 0; c < kTcKeys / 32; ++c)
-                tmem_ld32(trow + kColS + sb * kTcKeys + 32 * c,
-                          *reinterpret_cast<float(*)[32]>(&x[32 * c]));
-            tc_wait_ld();
             const int k0 = j * kTcKeys;
-            if (k0 + kTcKeys - 1 > lim) {
-                // Diagonal / last tile: keys past this row's limit get -inf.
+            const bool masked = k0 + kTcKeys - 1 > lim;
+            // Pass 1: row max of the raw scores, two 32-column chunks at a time.
+            float mxa = -INFINITY, mxb = -INFINITY;
 #pragma unroll
-                for (int c = 0; c < kTcKeys; ++c)
-                    if (k0 + c > lim) x[c] = -INFINITY;
-            }
-            // The scale is folded into the exponent below, so the max is taken over
-            // raw scores (four independent chains).
-            float r0m = -INFINITY, r1m = -INFINITY, r2m = -INFINITY, r3m = -INFINITY;
+            for (int c2 = 0; c2 < kTcKeys / 64; ++c2) {
+                float xa[32], xb[32];
+                tmem_ld32(cs + 64 * c2, xa);
+                tmem_ld32(cs + 64 * c2 + 32, xb);
+                tc_wait_ld();
 #pragma unroll
-            for (int c = 0; c < kTcKeys; c += 4) {
-                r0m = fmaxf(r0m, x[c]);
-                r1m = fmaxf(r1m, x[c + 1]);
-                r2m = fmaxf(r2m, x[c + 2]);
-                r3m = fmaxf(r3m, x[c + 3]);
+                for (int c = 0; c < 32; ++c) {
+                    float va = xa[c], vb = xb[c];
+                    if (masked) {
+                        if (k0 + 64 * c2 + c > lim) va = -INFINITY;
+                        if (k0 + 64 * c2 + 32 + c > lim) vb = -INFINITY;
+                    }
+                    mxa = fmaxf(mxa, va);
+                    mxb = fmaxf(mxb, vb);
+                }
             }
-            const float mx = fmaxf(fmaxf(r0m, r1m), fmaxf(r2m, r3m)) * sl2;
+            const float mx = fmaxf(mxa, mxb) * sl2;
             const bool grow = mx > m + kRescaleSlack;
             if (__any_sync(0xffffffffu, grow)) {
                 const float mn = grow ? fmaxf(m, mx) : m;
                 const float cr = fast_exp2(m - mn);
                 l *= cr;
                 if (j > 0) {
-                    // O holds P_0..P_{j-1} . V: wait for the last of those products.
-                    if (!(ok = warp_wait(o_done, (uint32_t)(j - 1) & 1u))) break;
-                    tc_fence_after();
+                    // O_t += P_{j-1}.V completed before S_t for this tile was issued.
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
                         float o[32];
-                        tmem_ld32(trow + kColO + 32 * c, o);
+                        tmem_ld32(co + 32 * c, o);
                         tc_wait_ld();
                         uint32_t r[32];
 #pragma unroll
                         for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(o[e] * cr);
-                        tmem_st32(trow + kColO + 32 * c, r);
+                        tmem_st32(co + 32 * c, r);
                     }
                 }
                 m = mn;
             }
-            // P = 2^(x*scale - m) <= 2^8; the row sum is kept in fp32 before the
-            // bf16 rounding of P (relative effect ~2^-9 per term, averaging out).
+            // Pass 2: P = 2^(x*scale - m) <= 2^8, packed to bf16 over the scores
+            // already consumed (chunk c's 16 P columns lie in columns < 32 c + 32).
+            // The row sum is kept in fp32 before rounding (~2^-9 per term, averaging).
             const float nm = -m;
             float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t pk[32];
+            for (int c = 0; c < kTcKeys / 32; ++c) {
+                float x[32];
+                tmem_ld32(cs + 32 * c, x);
+                tc_wait_ld();
+                uint32_t pk[16];
 #pragma unroll
-                for (int c = 0; c < 32; c += 2) {
-                    const float p0 = fast_exp2(fmaf(x[64 * half + 2 * c], sl2, nm));
-                    const float p1 = fast_exp2(fmaf(x[64 * half + 2 * c + 1], sl2, nm));
-                    const float p2 = fast_exp2(fmaf(x[64 * half + 2 * c + 2], sl2, nm));
-                    const float p3 = fast_exp2(fmaf(x[64 * half + 2 * c + 3], sl2, nm));
+                for (int e = 0; e < 32; e += 4) {
+                    float v0 = x[e], v1 = x[e + 1], v2 = x[e + 2], v3 = x[e + 3];
+                    if (masked) {
+                        const int kb = k0 + 32 * c + e;
+                        if (kb > lim) v0 = -INFINITY;
+                        if (kb + 1 > lim) v1 = -INFINITY;
+                        if (kb + 2 > lim) v2 = -INFINITY;
+                        if (kb + 3 > lim) v3 = -INFINITY;
+                    }
+                    const float p0 = fast_exp2(fmaf(v0, sl2, nm));
+                    const float p1 = fast_exp2(fmaf(v1, sl2, nm));
+                    const float p2 = fast_exp2(fmaf(v2, sl2, nm));
+                    const float p3 = fast_exp2(fmaf(v3, sl2, nm));
                     s0 += p0;
                     s1 += p1;
                     s2 += p2;
                     s3 += p3;
-                    pk[c] = pack_bf16(p0, p1);
-                    pk[c + 1] = pack_bf16(p2, p3);
+                    pk[e / 2] = pack_bf16(p0, p1);
+                    pk[e / 2 + 1] = pack_bf16(p2, p3);
                 }
-                tmem_st32(trow + kColP + sb * 64 + 32 * half, pk);
+                tmem_st16(cs + 16 * c, pk);
             }
             tc_wait_st();
             l += (s0 + s1) + (s2 + s3);
-            if (k0 + kTcKeys > len) {
+            if (t == 0 && k0 + kTcKeys > len) {
                 // Keys at or past the sequence end: zero their V rows so P=0 adds
-                // exactly nothing whatever the stale data is.
-                if (!(ok = warp_wait(&kv_full[sb], (uint32_t)(j >> 1) & 1u))) break;
+                // exactly nothing whatever the stale data is.  Tile 0's product is
+                // issued first, so zeroing here covers both tiles.
+                if (!(ok = warp_wait(&kv_full[j & 1], (uint32_t)(j >> 1) & 1u))) break;
                 const int r0 = len - k0, nr = kTcKeys - r0;
-                uint8_t *vs = sKV + (size_t)sb * L::kStageBytes + L::kKBytes;
+                uint8_t *vs = sKV + (size_t)(j & 1) * L::kStageBytes + L::kKBytes;
                 for (int e = row; e < nr * 8 * L::kPanels; e += 128) {
                     const int p = e / (nr * 8), rr = (e >> 3) % nr, ch = e & 7;
                     *reinterpret_cast<uint4 *>(vs + p * L::kKvPanel + (r0 + rr) * 128 + ch * 16) =
@@ -348,20 +385,20 @@ __global__ void __launch_bounds__(192, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[sb]);
+            if (lane == 0) mbar_arrive(&p_full[t]);
         }
-        if (ok) ok = warp_wait(o_done, (uint32_t)(n_kt - 1) & 1u);
+        if (ok) ok = warp_wait(&pv_done[t], (uint32_t)(n_kt - 1) & 1u);
         if (!ok) {
             if (lane == 0) atomicOr(&g_err_prefill, kErrTimeout);
         } else {
             tc_fence_after();
             const float inv = 1.f / l;
             uint4 *dst = reinterpret_cast<uint4 *>(
-                a.out + ((size_t)(q0 + t0 + t) * a.num_heads + (size_t)h * G + gq) * D);
+                a.out + ((size_t)(q0 + t0 + tok) * a.num_heads + (size_t)h * G + gq) * D);
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 float o[32];
-                tmem_ld32(trow + kColO + 32 * c, o);
+                tmem_ld32(co + 32 * c, o);
                 tc_wait_ld();
                 if (real) {
 #pragma unroll
@@ -391,7 +428,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, const CUtensorMap &map, dim3
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, 192, smem, stream>>>(map, a);
+    kern<<<grid, kTcThreads, smem, stream>>>(map, a);
     return cudaGetLastError();
 }
 
@@ -429,7 +466,8 @@ cudaError_t launch_prefill(void *out, const void *q, const int32_t *cu_q_lens, i
     a.negate_q = scale < 0.f ? 1 : 0;
     a.scale_log2 = std::max(std::fabs(scale) * 1.4426950408889634f, 1e-30f);
     a.q_tile = kTcRows / a.group;
-    dim3 grid((unsigned)((max_q_len + a.q_tile - 1) / a.q_tile), (unsigned)g.num_kv_heads,
+    const int per_cta = kTcTiles * a.q_tile;
+    dim3 grid((unsigned)((max_q_len + per_cta - 1) / per_cta), (unsigned)g.num_kv_heads,
               (unsigned)num_chunks);
     if (g.head_size == 128) return launch_prefill_tc<128>(a, map, grid, stream);
     return launch_prefill_tc<64>(a, map, grid, stream);
