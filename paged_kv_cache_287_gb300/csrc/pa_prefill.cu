@@ -16,12 +16,15 @@
 //              S_t = Q_t.K^T (A and B K-major from shared memory) and
 //              O_t += P_t.V (P from tensor memory, V MN-major in shared memory);
 //   warps 2-5  and 6-9: one warpgroup per query tile; each loads its tile,
-//              runs the softmax with one thread per row, writes P (bf16) into
+//              runs the softmax with one thread per row (the row's 128 scores
+//              read from tensor memory in one batch), writes P (bf16) into
 //              tensor memory over its own scores, and normalises O.
 // Tensor memory (512 columns x 128 lanes): S_0/P_0 [0,128), S_1/P_1 [128,256),
 // O_0 [256,384), O_1 [384,512).  P_t overwrites S_t, so S_t for the next K/V
-// tile is issued only after O_t += P_t.V has completed; meanwhile the tensor
-// cores work on the other tile.  Keys past a row's position are masked; tiles
+// tile is issued only after O_t += P_t.V has completed; the issue order per K/V
+// tile is P_0.V, Q_0.K', P_1.V, Q_1.K', so each softmax warpgroup gets its next
+// scores one product pair after handing over P while the tensor cores serve
+// the other tile.  Keys past a row's position are masked; tiles
 // past the CTA's causal limit are never fetched.
 #include <algorithm>
 #include <cmath>
@@ -41,9 +44,13 @@ constexpr float kRescaleSlack = 8.0f;
 constexpr int kTcRows = 128;    // query rows per tile (the MMA's M)
 constexpr int kTcTiles = 2;     // query tiles per CTA
 constexpr int kTcKeys = 128;    // keys per K/V tile
-constexpr int kTcStages = 2;
+constexpr int kKSlots = 3;      // K ring: a slot frees once both Q.K^T products are done
+constexpr int kVSlots = 2;      // V ring: a slot frees once both P.V products are done
 constexpr int kTcThreads = (2 + 4 * kTcTiles) * 32;
 constexpr uint32_t kTmemCols = 512, kColO = 256;
+// Chunks are taken longest cached context first (ranked on the device) when
+// there are at most this many; more keep the order of the batch.
+constexpr int kRankMax = 256;
 
 struct PrefillArgs {
     __nv_bfloat16 *out;
@@ -65,11 +72,9 @@ struct TcLay {
     static constexpr int kQTile = kPanels * kQPanel;
     static constexpr int kQBytes = kTcTiles * kQTile;
     static constexpr int kKvPanel = kTcKeys * 128;
-    static constexpr int kKBytes = kPanels * kKvPanel;
-    static constexpr int kStageBytes = 2 * kKBytes;   // K then V
-    static constexpr int kPad = 16 * 1024;            // slack past the last operand
-    static constexpr int kOperands = kQBytes + kTcStages * kStageBytes + kPad;
-    static constexpr size_t kSmem = 1024 + (size_t)kOperands + 16 * 8;
+    static constexpr int kKBytes = kPanels * kKvPanel;  // one K (or V) tile
+    static constexpr int kOperands = kQBytes + (kKSlots + kVSlots) * kKBytes;
+    static constexpr size_t kSmem = 1024 + (size_t)kOperands + 24 * 8;
 };
 
 __device__ __forceinline__ int prefill_row(int blk, int h, int off, const PrefillArgs &a) {
@@ -94,16 +99,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<size_t>(smem_raw) + 1023) & ~static_cast<size_t>(1023));
     uint8_t *sQ = smem;
-    uint8_t *sKV = smem + L::kQBytes;
+    uint8_t *sK = smem + L::kQBytes;
+    uint8_t *sV = sK + kKSlots * L::kKBytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kOperands);
-    uint64_t *kv_full = bars, *kv_empty = bars + 2;
-    uint64_t *s_full = bars + 4, *p_full = bars + 6, *pv_done = bars + 8, *q_full = bars + 10;
-    uint64_t *drain = bars + 12;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 13);
+    uint64_t *k_full = bars, *k_empty = bars + 3, *v_full = bars + 6, *v_empty = bars + 8;
+    uint64_t *s_full = bars + 10, *p_full = bars + 12, *pv_done = bars + 14, *q_full = bars + 16;
+    uint64_t *drain = bars + 18;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 19);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int s = blockIdx.z, h = blockIdx.y;
-    const int qt = gridDim.x - 1 - blockIdx.x;  // longest tiles first
+    // Grid (query tile, head, chunk rank): CTAs are dispatched in that order, so
+    // the chunk with the longest cached context, and within a chunk the latest
+    // query tiles, start first (longest work first keeps the tail short).
+    __shared__ int s_ctx[kRankMax];
+    __shared__ int s_pick;
+    int s = blockIdx.z;
+    const int nchunks = gridDim.z;
+    if (nchunks <= kRankMax) {
+        for (int i = threadIdx.x; i < nchunks; i += blockDim.x)
+            s_ctx[i] = a.seq_lens[i] - (a.cu_q_lens[i + 1] - a.cu_q_lens[i]);
+        __syncthreads();
+        for (int i = threadIdx.x; i < nchunks; i += blockDim.x) {
+            const int ci = s_ctx[i];
+            int rank = 0;
+            for (int k = 0; k < nchunks; ++k) {
+                const int ck = s_ctx[k];
+                rank += (ck > ci) || (ck == ci && k < i);
+            }
+            if (rank == (int)blockIdx.z) s_pick = i;
+        }
+        __syncthreads();
+        s = s_pick;
+    }
+    const int h = blockIdx.y;
+    const int qt = gridDim.x - 1 - blockIdx.x;  // latest query tiles first
     const int q0 = a.cu_q_lens[s];
     const int q_len = a.cu_q_lens[s + 1] - q0;
     const int QT = a.q_tile, G = a.group;
@@ -123,9 +152,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (threadIdx.x == 0) {
         prefetch_tensormap(&kv_map);
+        for (int i = 0; i < kKSlots; ++i) {
+            mbar_init(&k_full[i], 1);
+            mbar_init(&k_empty[i], 1);
+        }
+        for (int i = 0; i < kVSlots; ++i) {
+            mbar_init(&v_full[i], 1);
+            mbar_init(&v_empty[i], 1);
+        }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&kv_full[i], 1);
-            mbar_init(&kv_empty[i], 1);
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], 4);
             mbar_init(&pv_done[i], 1);
@@ -159,41 +194,54 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         };
         int nxt = box_row(0);
         int issued = 0;
+        auto load = [&](uint8_t *dst, uint64_t *bar, int row) {
+            if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)L::kKBytes);
+            __syncwarp();
+            if (lane < nbox) {
+#pragma unroll
+                for (int p = 0; p < L::kPanels; ++p)
+                    tma_load_2d_hint(dst + p * L::kKvPanel + lane * box_rows * 128, &kv_map, bar,
+                                     64 * p, row, policy);
+            }
+        };
         for (int kt = 0; kt < n_kt; ++kt) {
             const int cur = nxt;
             if (kt + 1 < n_kt) nxt = box_row(kt + 1);
-            const int st = kt & 1;
-            if (kt >= kTcStages && !warp_wait(&kv_empty[st], (uint32_t)((kt >> 1) - 1) & 1u)) {
+            const int ks = kt % kKSlots, vs = kt % kVSlots;
+            if (kt >= kKSlots &&
+                !warp_wait(&k_empty[ks], (uint32_t)(kt / kKSlots - 1) & 1u)) {
                 if (lane == 0) atomicOr(&g_err_prefill, kErrTimeout);
                 break;
             }
-            if (lane == 0) mbar_arrive_expect_tx(&kv_full[st], (uint32_t)(2 * L::kKBytes));
-            __syncwarp();
-            if (lane < nbox) {
-                uint8_t *stg = sKV + (size_t)st * L::kStageBytes;
-#pragma unroll
-                for (int p = 0; p < L::kPanels; ++p) {
-                    tma_load_2d_hint(stg + p * L::kKvPanel + lane * box_rows * 128, &kv_map,
-                                     &kv_full[st], 64 * p, cur, policy);
-                    tma_load_2d_hint(stg + L::kKBytes + p * L::kKvPanel + lane * box_rows * 128,
-                                     &kv_map, &kv_full[st], 64 * p, cur + v_off, policy);
-                }
+            load(sK + ks * L::kKBytes, &k_full[ks], cur);
+            if (kt >= kVSlots &&
+                !warp_wait(&v_empty[vs], (uint32_t)(kt / kVSlots - 1) & 1u)) {
+                if (lane == 0) atomicOr(&g_err_prefill, kErrTimeout);
+                issued = -(kt + 1);  // K of tile kt is in flight, V is not
+                break;
             }
+            load(sV + vs * L::kKBytes, &v_full[vs], cur < -(1 << 29) ? cur : cur + v_off);
             issued = kt + 1;
         }
         // Never leave with copies in flight into this CTA's shared memory.
-        for (int kt = std::max(0, issued - kTcStages); kt < issued; ++kt)
-            mbar_wait_bounded(&kv_full[kt & 1], (uint32_t)(kt >> 1) & 1u);
+        {
+            const int last = issued < 0 ? -issued : issued;   // tiles whose K was issued
+            const int vlast = issued < 0 ? last - 1 : last;    // tiles whose V was issued
+            for (int kt = std::max(0, last - kKSlots); kt < last; ++kt)
+                mbar_wait_bounded(&k_full[kt % kKSlots], (uint32_t)(kt / kKSlots) & 1u);
+            for (int kt = std::max(0, vlast - kVSlots); kt < vlast; ++kt)
+                mbar_wait_bounded(&v_full[kt % kVSlots], (uint32_t)(kt / kVSlots) & 1u);
+        }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         const uint32_t idesc_s = tc_idesc_bf16(kTcRows, kTcKeys, 0);
         const uint32_t idesc_pv = tc_idesc_bf16(kTcRows, D, 1);
-        const uint32_t q_base = smem_u32(sQ), kv_base = smem_u32(sKV);
+        const uint32_t q_base = smem_u32(sQ), k_base = smem_u32(sK), v_base = smem_u32(sV);
         const int ntiles = has1 ? 2 : 1;
         // S_t = Q_t . K_j^T into tensor-memory columns [128 t, 128 t + 128).
         auto issue_s = [&](int j, int t) {
             if (lane == 0) {
-                const uint32_t kb = kv_base + (j & 1) * L::kStageBytes;
+                const uint32_t kb = k_base + (j % kKSlots) * L::kKBytes;
                 const uint32_t qb = q_base + t * L::kQTile;
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
@@ -204,13 +252,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tc_mma_ss(tmem + t * kTcRows, ad, bd, idesc_s, k > 0 ? 1u : 0u);
                 }
                 tc_commit(&s_full[t]);
+                if (t == ntiles - 1) tc_commit(&k_empty[j % kKSlots]);
             }
             __syncwarp();
         };
         // O_t += P_t . V_j, P_t in the first 64 columns of tile t's score region.
         auto issue_pv = [&](int j, int t) {
             if (lane == 0) {
-                const uint32_t vb = kv_base + (j & 1) * L::kStageBytes + L::kKBytes;
+                const uint32_t vb = v_base + (j % kVSlots) * L::kKBytes;
 #pragma unroll
                 for (int kk = 0; kk < kTcKeys / 16; ++kk) {
                     const uint64_t bd = tc_desc_sw128(vb + kk * 16 * 128, L::kKvPanel, 1024);
@@ -218,29 +267,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                               idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc_commit(&pv_done[t]);
+                if (t == ntiles - 1) tc_commit(&v_empty[j % kVSlots]);
             }
             __syncwarp();
         };
         bool ok = warp_wait(&q_full[0], 0) && (!has1 || warp_wait(&q_full[1], 0));
-        ok = ok && warp_wait(&kv_full[0], 0);
+        ok = ok && warp_wait(&k_full[0], 0);
         if (ok) {
             tc_fence_after();
             for (int t = 0; t < ntiles; ++t) issue_s(0, t);
         }
+        // Per K/V tile j and query tile t: O_t += P_t.V_j as soon as P_t is ready,
+        // then (once that product is done, since P_t sits where S_t is written)
+        // S_t = Q_t.K_{j+1}^T, so tile t's softmax restarts after one P.V and one
+        // Q.K^T while the tensor cores move on to the other tile.
         for (int j = 0; ok && j < n_kt; ++j) {
+            const bool more = j + 1 < n_kt;
             for (int t = 0; t < ntiles; ++t) {
                 if (!(ok = warp_wait(&p_full[t], (uint32_t)j & 1u))) break;
+                if (t == 0 && !(ok = warp_wait(&v_full[j % kVSlots], (uint32_t)(j / kVSlots) & 1u)))
+                    break;
                 tc_fence_after();
                 issue_pv(j, t);
-            }
-            if (!ok) break;
-            if (lane == 0) tc_commit(&kv_empty[j & 1]);
-            __syncwarp();
-            if (j + 1 < n_kt) {
-                if (!(ok = warp_wait(&kv_full[(j + 1) & 1], (uint32_t)((j + 1) >> 1) & 1u)))
-                    break;
-                for (int t = 0; t < ntiles; ++t) {
-                    // P_t lives where S_t will be written: wait for O_t += P_t.V.
+                if (more) {
+                    if (t == 0 && !(ok = warp_wait(&k_full[(j + 1) % kKSlots],
+                                                   (uint32_t)((j + 1) / kKSlots) & 1u)))
+                        break;
                     if (!(ok = warp_wait(&pv_done[t], (uint32_t)j & 1u))) break;
                     tc_fence_after();
                     issue_s(j + 1, t);
@@ -292,27 +344,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (!(ok = warp_wait(&s_full[t], (uint32_t)j & 1u))) break;
             tc_fence_after();
             const int k0 = j * kTcKeys;
-            const bool masked = k0 + kTcKeys - 1 > lim;
-            // Pass 1: row max of the raw scores, two 32-column chunks at a time.
-            float mxa = -INFINITY, mxb = -INFINITY;
+            // The whole row of scores in one batch of tensor-memory loads.
+            float x[kTcKeys];
 #pragma unroll
-            for (int c2 = 0; c2 < kTcKeys / 64; ++c2) {
-                float xa[32], xb[32];
-                tmem_ld32(cs + 64 * c2, xa);
-                tmem_ld32(cs + 64 * c2 + 32, xb);
-                tc_wait_ld();
+            for (int c = 0; c < kTcKeys / 32; ++c)
+                tmem_ld32(cs + 32 * c, *reinterpret_cast<float(*)[32]>(&x[32 * c]));
+            tc_wait_ld();
+            if (k0 + kTcKeys - 1 > lim) {
+                // Diagonal / last tile: keys past this row's limit get -inf.
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    float va = xa[c], vb = xb[c];
-                    if (masked) {
-                        if (k0 + 64 * c2 + c > lim) va = -INFINITY;
-                        if (k0 + 64 * c2 + 32 + c > lim) vb = -INFINITY;
-                    }
-                    mxa = fmaxf(mxa, va);
-                    mxb = fmaxf(mxb, vb);
-                }
+                for (int c = 0; c < kTcKeys; ++c)
+                    if (k0 + c > lim) x[c] = -INFINITY;
             }
-            const float mx = fmaxf(mxa, mxb) * sl2;
+            // The scale is folded into the exponent below, so the max is taken over
+            // raw scores (four independent chains).
+            float r0m = x[0], r1m = x[1], r2m = x[2], r3m = x[3];
+#pragma unroll
+            for (int c = 4; c < kTcKeys; c += 4) {
+                r0m = fmaxf(r0m, x[c]);
+                r1m = fmaxf(r1m, x[c + 1]);
+                r2m = fmaxf(r2m, x[c + 2]);
+                r3m = fmaxf(r3m, x[c + 3]);
+            }
+            const float mx = fmaxf(fmaxf(r0m, r1m), fmaxf(r2m, r3m)) * sl2;
             const bool grow = mx > m + kRescaleSlack;
             if (__any_sync(0xffffffffu, grow)) {
                 const float mn = grow ? fmaxf(m, mx) : m;
@@ -320,52 +374,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 l *= cr;
                 if (j > 0) {
                     // O_t += P_{j-1}.V completed before S_t for this tile was issued.
-#pragma unroll
+#pragma unroll 1
                     for (int c = 0; c < D / 32; ++c) {
                         float o[32];
                         tmem_ld32(co + 32 * c, o);
                         tc_wait_ld();
-                        uint32_t r[32];
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(o[e] * cr);
-                        tmem_st32(co + 32 * c, r);
+                        for (int e = 0; e < 32; ++e) o[e] *= cr;
+                        tmem_st32(co + 32 * c, *reinterpret_cast<const uint32_t(*)[32]>(o));
                     }
                 }
                 m = mn;
             }
-            // Pass 2: P = 2^(x*scale - m) <= 2^8, packed to bf16 over the scores
-            // already consumed (chunk c's 16 P columns lie in columns < 32 c + 32).
-            // The row sum is kept in fp32 before rounding (~2^-9 per term, averaging).
+            // P = 2^(x*scale - m) <= 2^8, packed to bf16 over the first 64 score
+            // columns (already read).  The row sum is kept in fp32 before rounding
+            // (~2^-9 relative per term, averaging out).
             const float nm = -m;
             float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
-            for (int c = 0; c < kTcKeys / 32; ++c) {
-                float x[32];
-                tmem_ld32(cs + 32 * c, x);
-                tc_wait_ld();
+            for (int qr = 0; qr < 4; ++qr) {
                 uint32_t pk[16];
 #pragma unroll
-                for (int e = 0; e < 32; e += 4) {
-                    float v0 = x[e], v1 = x[e + 1], v2 = x[e + 2], v3 = x[e + 3];
-                    if (masked) {
-                        const int kb = k0 + 32 * c + e;
-                        if (kb > lim) v0 = -INFINITY;
-                        if (kb + 1 > lim) v1 = -INFINITY;
-                        if (kb + 2 > lim) v2 = -INFINITY;
-                        if (kb + 3 > lim) v3 = -INFINITY;
-                    }
-                    const float p0 = fast_exp2(fmaf(v0, sl2, nm));
-                    const float p1 = fast_exp2(fmaf(v1, sl2, nm));
-                    const float p2 = fast_exp2(fmaf(v2, sl2, nm));
-                    const float p3 = fast_exp2(fmaf(v3, sl2, nm));
+                for (int c = 0; c < 16; c += 2) {
+                    const float p0 = fast_exp2(fmaf(x[32 * qr + 2 * c], sl2, nm));
+                    const float p1 = fast_exp2(fmaf(x[32 * qr + 2 * c + 1], sl2, nm));
+                    const float p2 = fast_exp2(fmaf(x[32 * qr + 2 * c + 2], sl2, nm));
+                    const float p3 = fast_exp2(fmaf(x[32 * qr + 2 * c + 3], sl2, nm));
                     s0 += p0;
                     s1 += p1;
                     s2 += p2;
                     s3 += p3;
-                    pk[e / 2] = pack_bf16(p0, p1);
-                    pk[e / 2 + 1] = pack_bf16(p2, p3);
+                    pk[c] = pack_bf16(p0, p1);
+                    pk[c + 1] = pack_bf16(p2, p3);
                 }
-                tmem_st16(cs + 16 * c, pk);
+                tmem_st16(cs + 16 * qr, pk);
             }
             tc_wait_st();
             l += (s0 + s1) + (s2 + s3);
@@ -373,9 +415,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // Keys at or past the sequence end: zero their V rows so P=0 adds
                 // exactly nothing whatever the stale data is.  Tile 0's product is
                 // issued first, so zeroing here covers both tiles.
-                if (!(ok = warp_wait(&kv_full[j & 1], (uint32_t)(j >> 1) & 1u))) break;
+                if (!(ok = warp_wait(&v_full[j % kVSlots], (uint32_t)(j / kVSlots) & 1u))) break;
                 const int r0 = len - k0, nr = kTcKeys - r0;
-                uint8_t *vs = sKV + (size_t)(j & 1) * L::kStageBytes + L::kKBytes;
+                uint8_t *vs = sV + (size_t)(j % kVSlots) * L::kKBytes;
                 for (int e = row; e < nr * 8 * L::kPanels; e += 128) {
                     const int p = e / (nr * 8), rr = (e >> 3) % nr, ch = e & 7;
                     *reinterpret_cast<uint4 *>(vs + p * L::kKvPanel + (r0 + rr) * 128 + ch * 16) =
