@@ -357,16 +357,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (k0 + c > lim) x[c] = -INFINITY;
             }
             // The scale is folded into the exponent below, so the max is taken over
-            // raw scores (four independent chains).
-            float r0m = x[0], r1m = x[1], r2m = x[2], r3m = x[3];
+            // raw scores (three-input max, two independent chains).
+            float r0m = -INFINITY, r1m = -INFINITY;
 #pragma unroll
-            for (int c = 4; c < kTcKeys; c += 4) {
-                r0m = fmaxf(r0m, x[c]);
-                r1m = fmaxf(r1m, x[c + 1]);
-                r2m = fmaxf(r2m, x[c + 2]);
-                r3m = fmaxf(r3m, x[c + 3]);
+            for (int c = 0; c < kTcKeys; c += 4) {
+                r0m = fmax3(r0m, x[c], x[c + 1]);
+                r1m = fmax3(r1m, x[c + 2], x[c + 3]);
             }
-            const float mx = fmaxf(fmaxf(r0m, r1m), fmaxf(r2m, r3m)) * sl2;
+            const float mx = fmaxf(r0m, r1m) * sl2;
             const bool grow = mx > m + kRescaleSlack;
             if (__any_sync(0xffffffffu, grow)) {
                 const float mn = grow ? fmaxf(m, mx) : m;
@@ -389,6 +387,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // P = 2^(x*scale - m) <= 2^8, packed to bf16 over the first 64 score
             // columns (already read).  The row sum is kept in fp32 before rounding
             // (~2^-9 relative per term, averaging out).
+            // Packed fp32 pairs: one FFMA for (x*scale - m) and one add for the
+            // row sums per two scores.
             const float nm = -m;
             float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
@@ -396,14 +396,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 uint32_t pk[16];
 #pragma unroll
                 for (int c = 0; c < 16; c += 2) {
-                    const float p0 = fast_exp2(fmaf(x[32 * qr + 2 * c], sl2, nm));
-                    const float p1 = fast_exp2(fmaf(x[32 * qr + 2 * c + 1], sl2, nm));
-                    const float p2 = fast_exp2(fmaf(x[32 * qr + 2 * c + 2], sl2, nm));
-                    const float p3 = fast_exp2(fmaf(x[32 * qr + 2 * c + 3], sl2, nm));
-                    s0 += p0;
-                    s1 += p1;
-                    s2 += p2;
-                    s3 += p3;
+                    float t0, t1, t2, t3;
+                    fma2(t0, t1, x[32 * qr + 2 * c], x[32 * qr + 2 * c + 1], sl2, sl2, nm, nm);
+                    fma2(t2, t3, x[32 * qr + 2 * c + 2], x[32 * qr + 2 * c + 3], sl2, sl2, nm, nm);
+                    const float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
+                    const float p2 = fast_exp2(t2), p3 = fast_exp2(t3);
+                    add2(s0, s1, p0, p1);
+                    add2(s2, s3, p2, p3);
                     pk[c] = pack_bf16(p0, p1);
                     pk[c + 1] = pack_bf16(p2, p3);
                 }
