@@ -503,6 +503,7 @@ def run_mixed(args, world, rank, local):
         for i in range(args.steps):
             step(evs[i])
         torch.cuda.synchronize(dev)
+    binding.pa_error_check(stream)
     ms = [sum(e[j].elapsed_time(e[j + 1]) for e in evs) / args.steps for j in range(3)]
     if rank != 0:
         return

@@ -12,19 +12,18 @@
 // tile is fetched once for 256 rows of the whole GQA group.
 //   warp 0     streams 128-key K/V tiles through the block table with
 //              128B-swizzled 2-D TMA copies into a 2-stage ring;
-//   warp 1     owns the tensor memory and is the only issuer of tcgen05.mma:
-//              S_t = Q_t.K^T (A and B K-major from shared memory) and
-//              O_t += P_t.V (P from tensor memory, V MN-major in shared memory);
+//   warps 1, 10  issue tcgen05.mma, one warp per query tile (warp 1 also owns
+//              the tensor memory): S_t = Q_t.K^T (A and B K-major from shared
+//              memory) and O_t += P_t.V (P from tensor memory, V MN-major);
 //   warps 2-5  and 6-9: one warpgroup per query tile; each loads its tile,
 //              runs the softmax with one thread per row (the row's 128 scores
 //              read from tensor memory in one batch), writes P (bf16) into
 //              tensor memory over its own scores, and normalises O.
 // Tensor memory (512 columns x 128 lanes): S_0/P_0 [0,128), S_1/P_1 [128,256),
 // O_0 [256,384), O_1 [384,512).  P_t overwrites S_t, so S_t for the next K/V
-// tile is issued only after O_t += P_t.V has completed; the issue order per K/V
-// tile is P_0.V, Q_0.K', P_1.V, Q_1.K', so each softmax warpgroup gets its next
-// scores one product pair after handing over P while the tensor cores serve
-// the other tile.  Keys past a row's position are masked; tiles
+// tile is issued only after O_t += P_t.V has completed; each tile's issuer runs
+// P_t.V then Q_t.K' as soon as its own tile allows, and the two streams share
+// the tensor cores, so one tile's wait is the other tile's work.  Keys past a row's position are masked; tiles
 // past the CTA's causal limit are never fetched.
 #include <algorithm>
 #include <cmath>
@@ -46,7 +45,11 @@ constexpr int kTcTiles = 2;     // query tiles per CTA
 constexpr int kTcKeys = 128;    // keys per K/V tile
 constexpr int kKSlots = 3;      // K ring: a slot frees once both Q.K^T products are done
 constexpr int kVSlots = 2;      // V ring: a slot frees once both P.V products are done
-constexpr int kTcThreads = (2 + 4 * kTcTiles) * 32;
+// warp 0: TMA producer; warps 2..9: softmax warpgroups; warps 1 and 10: one MMA
+// issuer per query tile.  With 11 warps one scheduler holds three, which caps a
+// thread at 168 registers.
+constexpr int kTcWarps = 3 + 4 * kTcTiles;
+constexpr int kTcThreads = kTcWarps * 32;
 constexpr uint32_t kTmemCols = 512, kColO = 256;
 // Chunks are taken longest cached context first (ranked on the device) when
 // there are at most this many; more keep the order of the batch.
@@ -74,7 +77,7 @@ struct TcLay {
     static constexpr int kKvPanel = kTcKeys * 128;
     static constexpr int kKBytes = kPanels * kKvPanel;  // one K (or V) tile
     static constexpr int kOperands = kQBytes + (kKSlots + kVSlots) * kKBytes;
-    static constexpr size_t kSmem = 1024 + (size_t)kOperands + 24 * 8;
+    static constexpr size_t kSmem = 1024 + (size_t)kOperands + 24 * 8;  // + barriers, TMEM slot
 };
 
 __device__ __forceinline__ int prefill_row(int blk, int h, int off, const PrefillArgs &a) {
@@ -104,8 +107,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kOperands);
     uint64_t *k_full = bars, *k_empty = bars + 3, *v_full = bars + 6, *v_empty = bars + 8;
     uint64_t *s_full = bars + 10, *p_full = bars + 12, *pv_done = bars + 14, *q_full = bars + 16;
-    uint64_t *drain = bars + 18;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 19);
+    uint64_t *drain = bars + 18;  // [2], one per issuer
+    volatile int *s1_issued = reinterpret_cast<volatile int *>(bars + 20);  // Q_1.K^T products issued
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 21);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // Grid (query tile, head, chunk rank): CTAs are dispatched in that order, so
@@ -152,13 +156,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (threadIdx.x == 0) {
         prefetch_tensormap(&kv_map);
+        // A K or V slot is free once every active issuer has committed its
+        // products that read it.
+        const uint32_t issuers = has1 ? 2u : 1u;
         for (int i = 0; i < kKSlots; ++i) {
             mbar_init(&k_full[i], 1);
-            mbar_init(&k_empty[i], 1);
+            mbar_init(&k_empty[i], issuers);
         }
         for (int i = 0; i < kVSlots; ++i) {
             mbar_init(&v_full[i], 1);
-            mbar_init(&v_empty[i], 1);
+            mbar_init(&v_empty[i], issuers);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
@@ -166,7 +173,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&pv_done[i], 1);
             mbar_init(&q_full[i], 4);
         }
-        mbar_init(drain, 1);
+        mbar_init(&drain[0], 1);
+        mbar_init(&drain[1], 1);
+        *s1_issued = 0;
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -232,32 +241,37 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int kt = std::max(0, vlast - kVSlots); kt < vlast; ++kt)
                 mbar_wait_bounded(&v_full[kt % kVSlots], (uint32_t)(kt / kVSlots) & 1u);
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == 1 || (warp == kTcWarps - 1 && has1)) {
+        // ------------------------------------------------------------ MMA issuers
+        // Warp 1 issues for query tile 0, the last warp for tile 1: each waits only
+        // on its own tile, so one tile's products never queue behind the other's
+        // hand-over, and while one issuer waits for its P.V to finish the other's
+        // products keep the tensor cores busy.
+        const int t = warp == 1 ? 0 : 1;
         const uint32_t idesc_s = tc_idesc_bf16(kTcRows, kTcKeys, 0);
         const uint32_t idesc_pv = tc_idesc_bf16(kTcRows, D, 1);
-        const uint32_t q_base = smem_u32(sQ), k_base = smem_u32(sK), v_base = smem_u32(sV);
-        const int ntiles = has1 ? 2 : 1;
+        const uint32_t q_base = smem_u32(sQ) + t * L::kQTile;
+        const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV);
         // S_t = Q_t . K_j^T into tensor-memory columns [128 t, 128 t + 128).
-        auto issue_s = [&](int j, int t) {
+        auto issue_s = [&](int j) {
             if (lane == 0) {
                 const uint32_t kb = k_base + (j % kKSlots) * L::kKBytes;
-                const uint32_t qb = q_base + t * L::kQTile;
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint32_t off = (k >> 2) * L::kQPanel + (k & 3) * 32;
-                    const uint64_t ad = tc_desc_sw128(qb + off, 16, 1024);
+                    const uint64_t ad = tc_desc_sw128(q_base + off, 16, 1024);
                     const uint64_t bd = tc_desc_sw128(kb + (k >> 2) * L::kKvPanel + (k & 3) * 32,
                                                       16, 1024);
                     tc_mma_ss(tmem + t * kTcRows, ad, bd, idesc_s, k > 0 ? 1u : 0u);
                 }
                 tc_commit(&s_full[t]);
-                if (t == ntiles - 1) tc_commit(&k_empty[j % kKSlots]);
+                tc_commit(&k_empty[j % kKSlots]);
+                if (t == 1) *s1_issued = j + 1;
             }
             __syncwarp();
         };
         // O_t += P_t . V_j, P_t in the first 64 columns of tile t's score region.
-        auto issue_pv = [&](int j, int t) {
+        auto issue_pv = [&](int j) {
             if (lane == 0) {
                 const uint32_t vb = v_base + (j % kVSlots) * L::kKBytes;
 #pragma unroll
@@ -267,44 +281,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                               idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc_commit(&pv_done[t]);
-                if (t == ntiles - 1) tc_commit(&v_empty[j % kVSlots]);
+                tc_commit(&v_empty[j % kVSlots]);
             }
             __syncwarp();
         };
-        bool ok = warp_wait(&q_full[0], 0) && (!has1 || warp_wait(&q_full[1], 0));
-        ok = ok && warp_wait(&k_full[0], 0);
+        bool ok = warp_wait(&q_full[t], 0) && warp_wait(&k_full[0], 0);
+        // Tile 1 starts once tile 0's first softmax is done: the two chains then
+        // run half a period apart, so each softmax overlaps the other tile's
+        // products instead of competing with the other softmax.
+        if (ok && t == 1) ok = warp_wait(&p_full[0], 0);
         if (ok) {
             tc_fence_after();
-            for (int t = 0; t < ntiles; ++t) issue_s(0, t);
+            issue_s(0);
         }
-        // Per K/V tile j and query tile t: O_t += P_t.V_j as soon as P_t is ready,
-        // then (once that product is done, since P_t sits where S_t is written)
-        // S_t = Q_t.K_{j+1}^T, so tile t's softmax restarts after one P.V and one
-        // Q.K^T while the tensor cores move on to the other tile.
+        // O_t += P_t.V_j as soon as P_t is ready; then, once that product is done
+        // (P_t sits where S_t is written), S_t = Q_t.K_{j+1}^T.
         for (int j = 0; ok && j < n_kt; ++j) {
-            const bool more = j + 1 < n_kt;
-            for (int t = 0; t < ntiles; ++t) {
-                if (!(ok = warp_wait(&p_full[t], (uint32_t)j & 1u))) break;
-                if (t == 0 && !(ok = warp_wait(&v_full[j % kVSlots], (uint32_t)(j / kVSlots) & 1u)))
+            if (!(ok = warp_wait(&p_full[t], (uint32_t)j & 1u))) break;
+            if (!(ok = warp_wait(&v_full[j % kVSlots], (uint32_t)(j / kVSlots) & 1u))) break;
+            tc_fence_after();
+            issue_pv(j);
+            if (j + 1 < n_kt) {
+                if (!(ok = warp_wait(&k_full[(j + 1) % kKSlots],
+                                     (uint32_t)((j + 1) / kKSlots) & 1u)))
+                    break;
+                if (!(ok = warp_wait(&pv_done[t], (uint32_t)j & 1u))) break;
+                // Keep tile 0 at most half a period ahead of tile 1.
+                if (t == 0 && has1 &&
+                    !(ok = __all_sync(0xffffffffu, smem_counter_wait(s1_issued, j + 1))))
                     break;
                 tc_fence_after();
-                issue_pv(j, t);
-                if (more) {
-                    if (t == 0 && !(ok = warp_wait(&k_full[(j + 1) % kKSlots],
-                                                   (uint32_t)((j + 1) / kKSlots) & 1u)))
-                        break;
-                    if (!(ok = warp_wait(&pv_done[t], (uint32_t)j & 1u))) break;
-                    tc_fence_after();
-                    issue_s(j + 1, t);
-                }
+                issue_s(j + 1);
             }
         }
         if (!ok && lane == 0) atomicOr(&g_err_prefill, kErrTimeout);
-        // Wait for every issued MMA before the tensor memory is released.
-        if (lane == 0) tc_commit(drain);
+        // Wait for every product this thread issued before tensor memory is freed.
+        if (lane == 0) tc_commit(&drain[t]);
         __syncwarp();
-        mbar_wait_bounded(drain, 0);
-    } else if ((warp - 2) / 4 == 0 || has1) {
+        mbar_wait_bounded(&drain[t], 0);
+    } else if (warp >= 2 && warp < 2 + 4 * kTcTiles && ((warp - 2) / 4 == 0 || has1)) {
         // ------------------------------------------------------------ softmax warpgroups
         const int t = (warp - 2) / 4;             // query tile of this warpgroup
         const int row = 32 * (warp & 3) + lane;   // this thread's TMEM lane = query row
@@ -410,10 +425,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             tc_wait_st();
             l += (s0 + s1) + (s2 + s3);
-            if (t == 0 && k0 + kTcKeys > len) {
+            if (k0 + kTcKeys > len) {
                 // Keys at or past the sequence end: zero their V rows so P=0 adds
-                // exactly nothing whatever the stale data is.  Tile 0's product is
-                // issued first, so zeroing here covers both tiles.
+                // exactly nothing whatever the stale data is.  Each tile's warpgroup
+                // zeroes them before its own hand-over (the two write the same
+                // zeros), since the two tiles' products are issued independently.
                 if (!(ok = warp_wait(&v_full[j % kVSlots], (uint32_t)(j / kVSlots) & 1u))) break;
                 const int r0 = len - k0, nr = kTcKeys - r0;
                 uint8_t *vs = sV + (size_t)(j % kVSlots) * L::kKBytes;
