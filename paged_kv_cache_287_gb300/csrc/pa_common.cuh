@@ -83,22 +83,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     }
 }
 
-// Wait until a shared-memory counter written by another warp reaches `target`;
-// false after kWaitLimitNs.  A counter never wraps, so unlike a phase parity it
-// cannot be mistaken when the writer runs ahead.
-__device__ __forceinline__ bool smem_counter_wait(const volatile int *counter, int target) {
-    if (*counter >= target) return true;
-    const unsigned long long t0 = globaltimer_ns();
-    for (;;) {
-#pragma unroll 1
-        for (int i = 0; i < 64; ++i) {
-            if (*counter >= target) return true;
-            __nanosleep(20);
-        }
-        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
-    }
-}
-
 // ------------------------------------------------------------------ TMA / bulk copies
 // 2-D tiled tensor load into shared memory, completing on an mbarrier.
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar,

@@ -576,11 +576,12 @@ cudaError_t launch_decode(void *out, const void *q, const void *kv_cache, const 
     CUtensorMap map;
     if (!encode_kv_map(&map, kv_cache, g, g.block_size >= kTile ? kTile : g.block_size))
         return cudaErrorInvalidValue;
-    // Enough warps that each gets >= ~8 tiles at the largest possible length, at
-    // most one CTA per SM.
+    // As many warps as there can be tiles, at most one CTA per SM.  A warp has a
+    // single stage, so a small batch finishes soonest with one tile per warp; a
+    // large one fills every SM and each warp streams its share.
     const long long tmax =
         (long long)num_seqs * g.num_kv_heads * ((std::max(max_seq_len, 1) + kTile - 1) / kTile);
-    long long ctas = (tmax / 8 + kDecodeWarps - 1) / kDecodeWarps;
+    long long ctas = (tmax + kDecodeWarps - 1) / kDecodeWarps;
     ctas = std::max(1LL, std::min<long long>(ctas, sms));
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     const size_t nw_max = (size_t)sms * kDecodeWarps;

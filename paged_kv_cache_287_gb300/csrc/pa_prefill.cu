@@ -11,20 +11,21 @@
 // tile's rows are its tokens times the G query heads of the KV head, so each K/V
 // tile is fetched once for 256 rows of the whole GQA group.
 //   warp 0     streams 128-key K/V tiles through the block table with
-//              128B-swizzled 2-D TMA copies into a 2-stage ring;
+//              128B-swizzled 2-D TMA copies into a 3-slot K ring and a 2-slot
+//              V ring;
 //   warps 1, 10  issue tcgen05.mma, one warp per query tile (warp 1 also owns
 //              the tensor memory): S_t = Q_t.K^T (A and B K-major from shared
 //              memory) and O_t += P_t.V (P from tensor memory, V MN-major);
-//   warps 2-5  and 6-9: one warpgroup per query tile; each loads its tile,
-//              runs the softmax with one thread per row (the row's 128 scores
-//              read from tensor memory in one batch), writes P (bf16) into
-//              tensor memory over its own scores, and normalises O.
+//   warps 2-5  and 6-9: one warpgroup per query tile, one thread per row: the
+//              softmax, P (bf16) written into tensor memory over its own
+//              scores, and the final normalisation of O.
 // Tensor memory (512 columns x 128 lanes): S_0/P_0 [0,128), S_1/P_1 [128,256),
-// O_0 [256,384), O_1 [384,512).  P_t overwrites S_t, so S_t for the next K/V
-// tile is issued only after O_t += P_t.V has completed; each tile's issuer runs
-// P_t.V then Q_t.K' as soon as its own tile allows, and the two streams share
-// the tensor cores, so one tile's wait is the other tile's work.  Keys past a row's position are masked; tiles
-// past the CTA's causal limit are never fetched.
+// O_0 [256,384), O_1 [384,512).  Each K/V tile is worked in two 64-key halves
+// with their own hand-overs: while the softmax runs on one half, the tensor
+// cores compute the other half's scores or its P.V.  P of a half overwrites its
+// own scores, so that half's next scores are issued only after its P.V is done.
+// Keys past a row's position are masked; tiles past the CTA's causal limit are
+// never fetched.
 #include <algorithm>
 #include <cmath>
 
@@ -43,6 +44,7 @@ constexpr float kRescaleSlack = 8.0f;
 constexpr int kTcRows = 128;    // query rows per tile (the MMA's M)
 constexpr int kTcTiles = 2;     // query tiles per CTA
 constexpr int kTcKeys = 128;    // keys per K/V tile
+constexpr int kHalf = 64;       // keys per score half: S, softmax and P.V run per half
 constexpr int kKSlots = 3;      // K ring: a slot frees once both Q.K^T products are done
 constexpr int kVSlots = 2;      // V ring: a slot frees once both P.V products are done
 // warp 0: TMA producer; warps 2..9: softmax warpgroups; warps 1 and 10: one MMA
@@ -77,7 +79,7 @@ struct TcLay {
     static constexpr int kKvPanel = kTcKeys * 128;
     static constexpr int kKBytes = kPanels * kKvPanel;  // one K (or V) tile
     static constexpr int kOperands = kQBytes + (kKSlots + kVSlots) * kKBytes;
-    static constexpr size_t kSmem = 1024 + (size_t)kOperands + 24 * 8;  // + barriers, TMEM slot
+    static constexpr size_t kSmem = 1024 + (size_t)kOperands + 32 * 8;  // + barriers, TMEM slot
 };
 
 __device__ __forceinline__ int prefill_row(int blk, int h, int off, const PrefillArgs &a) {
@@ -106,10 +108,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint8_t *sV = sK + kKSlots * L::kKBytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kOperands);
     uint64_t *k_full = bars, *k_empty = bars + 3, *v_full = bars + 6, *v_empty = bars + 8;
-    uint64_t *s_full = bars + 10, *p_full = bars + 12, *pv_done = bars + 14, *q_full = bars + 16;
-    uint64_t *drain = bars + 18;  // [2], one per issuer
-    volatile int *s1_issued = reinterpret_cast<volatile int *>(bars + 20);  // Q_1.K^T products issued
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 21);
+    // Per (query tile t, key half f), index 2 t + f: scores ready, P written, P.V done.
+    uint64_t *s_full = bars + 10, *p_full = bars + 14, *pv_done = bars + 18;
+    uint64_t *q_full = bars + 22;  // [2]
+    uint64_t *drain = bars + 24;   // [2], one per issuer
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 26);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // Grid (query tile, head, chunk rank): CTAs are dispatched in that order, so
@@ -167,15 +170,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], issuers);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < 2 * kTcTiles; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], 4);
             mbar_init(&pv_done[i], 1);
-            mbar_init(&q_full[i], 4);
         }
-        mbar_init(&drain[0], 1);
-        mbar_init(&drain[1], 1);
-        *s1_issued = 0;
+        for (int i = 0; i < kTcTiles; ++i) {
+            mbar_init(&q_full[i], 4);
+            mbar_init(&drain[i], 1);
+        }
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -248,70 +251,77 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // hand-over, and while one issuer waits for its P.V to finish the other's
         // products keep the tensor cores busy.
         const int t = warp == 1 ? 0 : 1;
-        const uint32_t idesc_s = tc_idesc_bf16(kTcRows, kTcKeys, 0);
+        const uint32_t idesc_s = tc_idesc_bf16(kTcRows, kHalf, 0);
         const uint32_t idesc_pv = tc_idesc_bf16(kTcRows, D, 1);
         const uint32_t q_base = smem_u32(sQ) + t * L::kQTile;
         const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV);
-        // S_t = Q_t . K_j^T into tensor-memory columns [128 t, 128 t + 128).
-        auto issue_s = [&](int j) {
+        // S_t,f = Q_t . K_j[64 f, 64 f + 64)^T into tensor-memory columns
+        // [128 t + 64 f, 128 t + 64 f + 64).
+        auto issue_s = [&](int j, int f) {
             if (lane == 0) {
-                const uint32_t kb = k_base + (j % kKSlots) * L::kKBytes;
+                const uint32_t kb = k_base + (j % kKSlots) * L::kKBytes + f * kHalf * 128;
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint32_t off = (k >> 2) * L::kQPanel + (k & 3) * 32;
                     const uint64_t ad = tc_desc_sw128(q_base + off, 16, 1024);
                     const uint64_t bd = tc_desc_sw128(kb + (k >> 2) * L::kKvPanel + (k & 3) * 32,
                                                       16, 1024);
-                    tc_mma_ss(tmem + t * kTcRows, ad, bd, idesc_s, k > 0 ? 1u : 0u);
+                    tc_mma_ss(tmem + t * kTcRows + f * kHalf, ad, bd, idesc_s, k > 0 ? 1u : 0u);
                 }
-                tc_commit(&s_full[t]);
-                tc_commit(&k_empty[j % kKSlots]);
-                if (t == 1) *s1_issued = j + 1;
+                tc_commit(&s_full[2 * t + f]);
+                if (f == 1) tc_commit(&k_empty[j % kKSlots]);
             }
             __syncwarp();
         };
-        // O_t += P_t . V_j, P_t in the first 64 columns of tile t's score region.
-        auto issue_pv = [&](int j) {
+        // O_t += P_t,f . V_j[64 f, 64 f + 64); P_t,f is packed bf16 in the first 32
+        // columns of its own score half.
+        auto issue_pv = [&](int j, int f) {
             if (lane == 0) {
-                const uint32_t vb = v_base + (j % kVSlots) * L::kKBytes;
+                const uint32_t vb = v_base + (j % kVSlots) * L::kKBytes + f * kHalf * 128;
 #pragma unroll
-                for (int kk = 0; kk < kTcKeys / 16; ++kk) {
+                for (int kk = 0; kk < kHalf / 16; ++kk) {
                     const uint64_t bd = tc_desc_sw128(vb + kk * 16 * 128, L::kKvPanel, 1024);
-                    tc_mma_ts(tmem + kColO + t * kTcRows, tmem + t * kTcRows + kk * 8, bd,
-                              idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                    tc_mma_ts(tmem + kColO + t * kTcRows, tmem + t * kTcRows + f * kHalf + kk * 8,
+                              bd, idesc_pv, (j > 0 || f > 0 || kk > 0) ? 1u : 0u);
                 }
-                tc_commit(&pv_done[t]);
-                tc_commit(&v_empty[j % kVSlots]);
+                tc_commit(&pv_done[2 * t + f]);
+                if (f == 1) tc_commit(&v_empty[j % kVSlots]);
             }
             __syncwarp();
         };
         bool ok = warp_wait(&q_full[t], 0) && warp_wait(&k_full[0], 0);
-        // Tile 1 starts once tile 0's first softmax is done: the two chains then
-        // run half a period apart, so each softmax overlaps the other tile's
-        // products instead of competing with the other softmax.
+        // Tile 1 starts once tile 0's first softmax half is done, so the two
+        // softmax warpgroups start out of step.
         if (ok && t == 1) ok = warp_wait(&p_full[0], 0);
         if (ok) {
             tc_fence_after();
-            issue_s(0);
+            issue_s(0, 0);
+            issue_s(0, 1);
         }
-        // O_t += P_t.V_j as soon as P_t is ready; then, once that product is done
-        // (P_t sits where S_t is written), S_t = Q_t.K_{j+1}^T.
+        // Per half f: O_t += P_t,f.V_j as soon as P_t,f is ready, then, once that
+        // product is done (P_t,f sits where S_t,f is written), S_t,f for the next
+        // K tile.  The other half's softmax runs meanwhile, so the tensor cores
+        // work under the softmax instead of after it.
         for (int j = 0; ok && j < n_kt; ++j) {
-            if (!(ok = warp_wait(&p_full[t], (uint32_t)j & 1u))) break;
+            if (!(ok = warp_wait(&p_full[2 * t], (uint32_t)j & 1u))) break;
             if (!(ok = warp_wait(&v_full[j % kVSlots], (uint32_t)(j / kVSlots) & 1u))) break;
             tc_fence_after();
-            issue_pv(j);
+            issue_pv(j, 0);
             if (j + 1 < n_kt) {
                 if (!(ok = warp_wait(&k_full[(j + 1) % kKSlots],
                                      (uint32_t)((j + 1) / kKSlots) & 1u)))
                     break;
-                if (!(ok = warp_wait(&pv_done[t], (uint32_t)j & 1u))) break;
-                // Keep tile 0 at most half a period ahead of tile 1.
-                if (t == 0 && has1 &&
-                    !(ok = __all_sync(0xffffffffu, smem_counter_wait(s1_issued, j + 1))))
-                    break;
+                if (!(ok = warp_wait(&pv_done[2 * t], (uint32_t)j & 1u))) break;
                 tc_fence_after();
-                issue_s(j + 1);
+                issue_s(j + 1, 0);
+            }
+            if (!(ok = warp_wait(&p_full[2 * t + 1], (uint32_t)j & 1u))) break;
+            tc_fence_after();
+            issue_pv(j, 1);
+            if (j + 1 < n_kt) {
+                if (!(ok = warp_wait(&pv_done[2 * t + 1], (uint32_t)j & 1u))) break;
+                tc_fence_after();
+                issue_s(j + 1, 1);
             }
         }
         if (!ok && lane == 0) atomicOr(&g_err_prefill, kErrTimeout);
@@ -355,96 +365,109 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float sl2 = a.scale_log2;  // > 0: a negative scale was moved into Q
         float m = -INFINITY, l = 0.f;
         bool ok = true;
-        for (int j = 0; j < n_kt; ++j) {
-            if (!(ok = warp_wait(&s_full[t], (uint32_t)j & 1u))) break;
-            tc_fence_after();
-            const int k0 = j * kTcKeys;
-            // The whole row of scores in one batch of tensor-memory loads.
-            float x[kTcKeys];
-#pragma unroll
-            for (int c = 0; c < kTcKeys / 32; ++c)
-                tmem_ld32(cs + 32 * c, *reinterpret_cast<float(*)[32]>(&x[32 * c]));
-            tc_wait_ld();
-            if (k0 + kTcKeys - 1 > lim) {
-                // Diagonal / last tile: keys past this row's limit get -inf.
-#pragma unroll
-                for (int c = 0; c < kTcKeys; ++c)
-                    if (k0 + c > lim) x[c] = -INFINITY;
-            }
-            // The scale is folded into the exponent below, so the max is taken over
-            // raw scores (three-input max, two independent chains).
-            float r0m = -INFINITY, r1m = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < kTcKeys; c += 4) {
-                r0m = fmax3(r0m, x[c], x[c + 1]);
-                r1m = fmax3(r1m, x[c + 2], x[c + 3]);
-            }
-            const float mx = fmaxf(r0m, r1m) * sl2;
-            const bool grow = mx > m + kRescaleSlack;
-            if (__any_sync(0xffffffffu, grow)) {
-                const float mn = grow ? fmaxf(m, mx) : m;
-                const float cr = fast_exp2(m - mn);
-                l *= cr;
-                if (j > 0) {
-                    // O_t += P_{j-1}.V completed before S_t for this tile was issued.
+        for (int j = 0; ok && j < n_kt; ++j) {
 #pragma unroll 1
-                    for (int c = 0; c < D / 32; ++c) {
-                        float o[32];
-                        tmem_ld32(co + 32 * c, o);
-                        tc_wait_ld();
+            for (int f = 0; f < 2; ++f) {
+                const uint32_t cf = cs + f * kHalf;  // this half's score / P columns
+                if (!(ok = warp_wait(&s_full[2 * t + f], (uint32_t)j & 1u))) break;
+                tc_fence_after();
+                const int k0 = j * kTcKeys + f * kHalf;
+                float x[kHalf];
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] *= cr;
-                        tmem_st32(co + 32 * c, *reinterpret_cast<const uint32_t(*)[32]>(o));
+                for (int c = 0; c < kHalf / 32; ++c)
+                    tmem_ld32(cf + 32 * c, *reinterpret_cast<float(*)[32]>(&x[32 * c]));
+                tc_wait_ld();
+                if (k0 + kHalf - 1 > lim) {
+                    // Diagonal / last keys: those past this row's limit get -inf.
+#pragma unroll
+                    for (int c = 0; c < kHalf; ++c)
+                        if (k0 + c > lim) x[c] = -INFINITY;
+                }
+                // The scale is folded into the exponent below, so the max is taken
+                // over raw scores (three-input max, two independent chains).
+                float r0m = -INFINITY, r1m = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < kHalf; c += 4) {
+                    r0m = fmax3(r0m, x[c], x[c + 1]);
+                    r1m = fmax3(r1m, x[c + 2], x[c + 3]);
+                }
+                const float mx = fmaxf(r0m, r1m) * sl2;
+                const bool grow = mx > m + kRescaleSlack;
+                if (__any_sync(0xffffffffu, grow)) {
+                    const float mn = grow ? fmaxf(m, mx) : m;
+                    const float cr = fast_exp2(m - mn);
+                    l *= cr;
+                    if (j > 0 || f > 0) {
+                        // Every earlier P.V of this tile must be done before O is
+                        // rescaled.  The other half's previous product is the only
+                        // one not already implied by this half's scores being ready
+                        // (each half's S is issued after its own previous P.V).
+                        ok = f == 0 ? warp_wait(&pv_done[2 * t + 1], (uint32_t)(j - 1) & 1u)
+                                    : warp_wait(&pv_done[2 * t], (uint32_t)j & 1u);
+                        if (!ok) break;
+                        tc_fence_after();
+#pragma unroll 1
+                        for (int c = 0; c < D / 32; ++c) {
+                            float o[32];
+                            tmem_ld32(co + 32 * c, o);
+                            tc_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) o[e] *= cr;
+                            tmem_st32(co + 32 * c, *reinterpret_cast<const uint32_t(*)[32]>(o));
+                        }
                     }
+                    m = mn;
                 }
-                m = mn;
-            }
-            // P = 2^(x*scale - m) <= 2^8, packed to bf16 over the first 64 score
-            // columns (already read).  The row sum is kept in fp32 before rounding
-            // (~2^-9 relative per term, averaging out).
-            // Packed fp32 pairs: one FFMA for (x*scale - m) and one add for the
-            // row sums per two scores.
-            const float nm = -m;
-            float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+                // P = 2^(x*scale - m) <= 2^8, packed to bf16 into the half's first 32
+                // columns (already read).  Packed fp32 pairs: one FFMA for
+                // (x*scale - m) and one add for the row sums per two scores; the row
+                // sum is kept in fp32 before the bf16 rounding.
+                const float nm = -m;
+                float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
-            for (int qr = 0; qr < 4; ++qr) {
-                uint32_t pk[16];
+                for (int qr = 0; qr < kHalf / 32; ++qr) {
+                    uint32_t pk[16];
 #pragma unroll
-                for (int c = 0; c < 16; c += 2) {
-                    float t0, t1, t2, t3;
-                    fma2(t0, t1, x[32 * qr + 2 * c], x[32 * qr + 2 * c + 1], sl2, sl2, nm, nm);
-                    fma2(t2, t3, x[32 * qr + 2 * c + 2], x[32 * qr + 2 * c + 3], sl2, sl2, nm, nm);
-                    const float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
-                    const float p2 = fast_exp2(t2), p3 = fast_exp2(t3);
-                    add2(s0, s1, p0, p1);
-                    add2(s2, s3, p2, p3);
-                    pk[c] = pack_bf16(p0, p1);
-                    pk[c + 1] = pack_bf16(p2, p3);
+                    for (int c = 0; c < 16; c += 2) {
+                        float t0, t1, t2, t3;
+                        fma2(t0, t1, x[32 * qr + 2 * c], x[32 * qr + 2 * c + 1], sl2, sl2, nm, nm);
+                        fma2(t2, t3, x[32 * qr + 2 * c + 2], x[32 * qr + 2 * c + 3], sl2, sl2, nm,
+                             nm);
+                        const float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
+                        const float p2 = fast_exp2(t2), p3 = fast_exp2(t3);
+                        add2(s0, s1, p0, p1);
+                        add2(s2, s3, p2, p3);
+                        pk[c] = pack_bf16(p0, p1);
+                        pk[c + 1] = pack_bf16(p2, p3);
+                    }
+                    tmem_st16(cf + 16 * qr, pk);
                 }
-                tmem_st16(cs + 16 * qr, pk);
-            }
-            tc_wait_st();
-            l += (s0 + s1) + (s2 + s3);
-            if (k0 + kTcKeys > len) {
-                // Keys at or past the sequence end: zero their V rows so P=0 adds
-                // exactly nothing whatever the stale data is.  Each tile's warpgroup
-                // zeroes them before its own hand-over (the two write the same
-                // zeros), since the two tiles' products are issued independently.
-                if (!(ok = warp_wait(&v_full[j % kVSlots], (uint32_t)(j / kVSlots) & 1u))) break;
-                const int r0 = len - k0, nr = kTcKeys - r0;
-                uint8_t *vs = sV + (size_t)(j % kVSlots) * L::kKBytes;
-                for (int e = row; e < nr * 8 * L::kPanels; e += 128) {
-                    const int p = e / (nr * 8), rr = (e >> 3) % nr, ch = e & 7;
-                    *reinterpret_cast<uint4 *>(vs + p * L::kKvPanel + (r0 + rr) * 128 + ch * 16) =
-                        make_uint4(0, 0, 0, 0);
+                tc_wait_st();
+                l += (s0 + s1) + (s2 + s3);
+                if (f == 0 && j * kTcKeys + kTcKeys > len) {
+                    // Keys at or past the sequence end: zero their V rows so P=0 adds
+                    // exactly nothing whatever the stale data is.  Each tile's
+                    // warpgroup zeroes them before its first hand-over of the tile
+                    // (the two write the same zeros), since the two tiles' products
+                    // are issued independently.
+                    if (!(ok = warp_wait(&v_full[j % kVSlots], (uint32_t)(j / kVSlots) & 1u)))
+                        break;
+                    const int r0 = len - j * kTcKeys, nr = kTcKeys - r0;
+                    uint8_t *vs = sV + (size_t)(j % kVSlots) * L::kKBytes;
+                    for (int e = row; e < nr * 8 * L::kPanels; e += 128) {
+                        const int p = e / (nr * 8), rr = (e >> 3) % nr, ch = e & 7;
+                        *reinterpret_cast<uint4 *>(vs + p * L::kKvPanel + (r0 + rr) * 128 +
+                                                   ch * 16) = make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
                 }
-                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&p_full[2 * t + f]);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[t]);
         }
-        if (ok) ok = warp_wait(&pv_done[t], (uint32_t)(n_kt - 1) & 1u);
+        // The last half's P.V completes after every earlier product of the tile.
+        if (ok) ok = warp_wait(&pv_done[2 * t + 1], (uint32_t)(n_kt - 1) & 1u);
         if (!ok) {
             if (lane == 0) atomicOr(&g_err_prefill, kErrTimeout);
         } else {
