@@ -57,6 +57,16 @@ def decode_algorithmic_bytes(b) -> int:
     return kv + qo + nblk * 4 + b.num_seqs * 4
 
 
+def cascade_algorithmic_bytes(b, shared_len: int) -> int:
+    """Bytes a shared-prefix decode must move: the shared tokens' K+V once, each
+    sequence's own tokens, q, out and the tables; the prefix partials stay in L2."""
+    own = [int(L) - shared_len for L in b.seq_lens.tolist()]
+    kv = kv_read_bytes([shared_len] + own, b.num_kv_heads, b.head_size)
+    qo = 2 * b.q.numel() * 2
+    nblk = shared_len // b.block_size + sum(-(-L // b.block_size) for L in own)
+    return kv + qo + nblk * 4 + b.num_seqs * 4
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -316,9 +326,24 @@ def run_ours(args, world, rank, local):
     binding.lib()
     stream = torch.cuda.current_stream(dev)
     out = torch.empty_like(b.q)
-    ws = torch.empty(binding.pa_decode_workspace_bytes(b.num_seqs, b.num_heads, b.num_kv_heads,
-                                                       b.head_size), dtype=torch.uint8, device=dev)
+    shared = b.shared_prefix_blocks * b.block_size if args.cascade else 0
+    if args.cascade and not shared:
+        raise SystemExit("--cascade needs a workload whose sequences share a prefix (5)")
+    if args.cascade:
+        nbytes = binding.pa_decode_cascade_workspace_bytes(b.num_seqs, b.num_heads,
+                                                           b.num_kv_heads, b.head_size, shared)
+    else:
+        nbytes = binding.pa_decode_workspace_bytes(b.num_seqs, b.num_heads, b.num_kv_heads,
+                                                   b.head_size)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     max_len = b.max_seq_len
+
+    def attend(q, tables, lens, st):
+        if args.cascade:
+            binding.pa_decode_cascade(out, q, b.kv_cache, tables, lens, max_len, shared, b.scale,
+                                      ws, st)
+        else:
+            binding.pa_decode(out, q, b.kv_cache, tables, lens, max_len, b.scale, ws, st)
 
     def step(ev=None, st=None):
         st = stream if st is None else st
@@ -327,8 +352,7 @@ def run_ours(args, world, rank, local):
         binding.pa_cache_write(b.kv_cache, b.k_new, b.v_new, b.slot_mapping, st)
         if ev is not None:
             ev[1].record(st)
-        binding.pa_decode(out, b.q, b.kv_cache, b.block_tables, b.seq_lens, max_len, b.scale, ws,
-                          st)
+        attend(b.q, b.block_tables, b.seq_lens, st)
         if ev is not None:
             ev[2].record(st)
 
@@ -396,8 +420,7 @@ def run_ours(args, world, rank, local):
             dev_in[k].copy_(t, non_blocking=True)
         binding.pa_cache_write(b.kv_cache, dev_in["k_new"], dev_in["v_new"],
                                dev_in["slot_mapping"], stream)
-        binding.pa_decode(out, dev_in["q"], b.kv_cache, dev_in["block_tables"],
-                          dev_in["seq_lens"], max_len, b.scale, ws, stream)
+        attend(dev_in["q"], dev_in["block_tables"], dev_in["seq_lens"], stream)
         out_host.copy_(out, non_blocking=True)
 
     for _ in range(max(args.warmup, 3)):
@@ -417,19 +440,25 @@ def run_ours(args, world, rank, local):
     value = world * kv * args.steps / (total_ms / 1e3) / 1e9
     seqs_s = world * b.num_seqs * args.steps / (total_ms / 1e3)
     peak, peak_src = measured_peaks()
-    alg = decode_algorithmic_bytes(b)
+    alg = cascade_algorithmic_bytes(b, shared) if args.cascade else decode_algorithmic_bytes(b)
     achieved = alg / (decode_ms / 1e3) / 1e9
+    if args.cascade:
+        kernel = "pa_decode_cascade (prefix pass + suffix decode + merge kernel)"
+        traffic_file = f"cascade_{b.name}.traffic.txt"
+    else:
+        kernel = "pa_decode (split-context kernel + merge kernel)"
+        traffic_file = f"decode_{b.name}.traffic.txt"
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": dict(workload_config(n, args.seqs), launch="cuda-graph" if graph else "eager"),
+        "config": dict(workload_config(n, args.seqs), launch="cuda-graph" if graph else "eager",
+                       **({"cascade_shared_len": shared} if args.cascade else {})),
         "seqs_per_s": seqs_s,
         "hbm_frac_of_step": value / world / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": profile_traffic(
-                         f"decode_{b.name}.traffic.txt"),
-                     "kernel": "pa_decode (split-context kernel + merge kernel)",
+                     "frac": achieved / peak, "traffic": profile_traffic(traffic_file),
+                     "kernel": kernel,
                      "algorithmic_bytes_per_launch": alg, "launch_ms": decode_ms,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s"},
@@ -439,7 +468,7 @@ def run_ours(args, world, rank, local):
                 "note": "KV pool resident in HBM (the cache); per-step inputs copied in, "
                         "output copied out"},
         "clocks": clocks,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": (4 if args.cascade else 3) * args.steps,
     }
     if world == 1 and not args.no_cpu_baseline:
         gbs, sps, done, k, threads = cpu_oracle_rate(n)
@@ -536,6 +565,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph", action="store_true",
                     help="replay one CUDA-graph-captured step per timed step")
+    ap.add_argument("--cascade", action="store_true",
+                    help="shared-prefix decode (pa_decode_cascade) on a prefix-sharing workload")
     ap.add_argument("--seqs", type=int, default=0,
                     help="profile only the first N sequences of the workload (not a bench line)")
     args = ap.parse_args(argv)

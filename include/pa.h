@@ -144,6 +144,42 @@ pa_status pa_decode_noalloc(void *out, const void *q, const void *kv_cache, int 
                             pa_stream_t stream);
 
 /*
+ * Workspace pa_decode_cascade needs on the current device, in bytes: that of
+ * pa_decode plus the shared prefix's partial softmax states.  Depends on the
+ * device's SM count.  Returns 0 for invalid arguments.
+ */
+size_t pa_decode_cascade_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads,
+                                         int head_size, int shared_len);
+
+/*
+ * pa_decode_cascade - pa_decode for a batch whose sequences share a prefix.
+ *
+ * Prefix caching ("Inside vLLM: Anatomy of a High-Throughput LLM Inference
+ * System", advanced features: prefix caching) lets sequences with a common
+ * prompt start hold the same physical KV blocks.  Here the first shared_len
+ * tokens of every sequence are those blocks: block_tables[s][i] equals
+ * block_tables[0][i] for i < shared_len / block_size (a precondition; the
+ * prefix is read through sequence 0's table).  The prefix is attended once per
+ * KV head for all queries of the batch on the tensor cores, each sequence's own
+ * tokens [shared_len, seq_lens[s]) as in pa_decode, and the two softmax states
+ * are merged by log-sum-exp.  The result is pa_decode's up to floating-point
+ * summation order.
+ *   Arguments are those of pa_decode, plus:
+ *   shared_len    tokens shared by every sequence, 0 <= shared_len <= max_seq_len,
+ *                 a multiple of 16 and of block_size (else PA_ERR_UNSUPPORTED);
+ *                 every seq_lens[s] >= shared_len (else PA_ERR_OOB is flagged);
+ *                 0 makes the call pa_decode
+ *   workspace     >= pa_decode_cascade_workspace_bytes(...) bytes, 256-byte
+ *                 aligned, caller-owned, no initialisation needed
+ */
+pa_status pa_decode_cascade(void *out, const void *q, const void *kv_cache, int num_blocks,
+                            int block_size, int num_heads, int num_kv_heads, int head_size,
+                            const int32_t *block_tables, int max_blocks_per_seq,
+                            const int32_t *seq_lens, int num_seqs, int max_seq_len,
+                            int shared_len, float scale, void *workspace,
+                            size_t workspace_bytes, pa_stream_t stream);
+
+/*
  * pa_prefill_chunk - chunked-prefill attention of query chunks against their
  * cached context and themselves, causal.
  *

@@ -23,7 +23,8 @@ STATUS = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_E
 
 # Every symbol include/pa.h declares.
 EXPORTS = ("pa_status_string", "pa_kv_block_bytes", "pa_cache_write",
-           "pa_decode_workspace_bytes", "pa_decode", "pa_decode_noalloc", "pa_prefill_chunk",
+           "pa_decode_workspace_bytes", "pa_decode", "pa_decode_noalloc",
+           "pa_decode_cascade_workspace_bytes", "pa_decode_cascade", "pa_prefill_chunk",
            "pa_error_check")
 
 
@@ -59,6 +60,11 @@ def lib(path: Optional[str] = None):
     L.pa_decode.argtypes = [P, P, P, i, i, i, i, i, P, i, P, i, i, ctypes.c_float, P, sz, P]
     L.pa_decode_noalloc.restype = i
     L.pa_decode_noalloc.argtypes = [P, P, P, i, i, i, i, i, P, i, P, i, i, ctypes.c_float, P]
+    L.pa_decode_cascade_workspace_bytes.restype = sz
+    L.pa_decode_cascade_workspace_bytes.argtypes = [i, i, i, i, i]
+    L.pa_decode_cascade.restype = i
+    L.pa_decode_cascade.argtypes = [P, P, P, i, i, i, i, i, P, i, P, i, i, i, ctypes.c_float, P,
+                                    sz, P]
     L.pa_prefill_chunk.restype = i
     L.pa_prefill_chunk.argtypes = [P, P, P, i, i, P, i, i, i, i, i, P, i, P, ctypes.c_float, P]
     L.pa_error_check.restype = i
@@ -159,6 +165,33 @@ def pa_decode_noalloc(out: torch.Tensor, q: torch.Tensor, kv_cache: torch.Tensor
                                    Hkv, D, block_tables.data_ptr(), block_tables.shape[1],
                                    seq_lens.data_ptr(), B, int(max_seq_len), float(scale),
                                    _stream(stream)), "pa_decode_noalloc")
+
+
+def pa_decode_cascade_workspace_bytes(num_seqs: int, num_heads: int, num_kv_heads: int,
+                                      head_size: int, shared_len: int) -> int:
+    return int(lib().pa_decode_cascade_workspace_bytes(num_seqs, num_heads, num_kv_heads,
+                                                       head_size, shared_len))
+
+
+def pa_decode_cascade(out: torch.Tensor, q: torch.Tensor, kv_cache: torch.Tensor,
+                      block_tables: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                      shared_len: int, scale: float, workspace: torch.Tensor,
+                      stream=None) -> None:
+    """pa_decode for a batch whose first shared_len tokens sit in the same blocks."""
+    NB, bs, Hkv, D = _pool_geom(kv_cache)
+    _need(q, "q", torch.bfloat16, 3)
+    _need(out, "out", torch.bfloat16, 3)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(workspace, "workspace", torch.uint8, 1)
+    B, Hq, Dq = q.shape
+    if Dq != D or out.shape != q.shape or seq_lens.shape[0] != B or block_tables.shape[0] != B:
+        raise ValueError("inconsistent decode shapes")
+    _check(lib().pa_decode_cascade(out.data_ptr(), q.data_ptr(), kv_cache.data_ptr(), NB, bs, Hq,
+                                   Hkv, D, block_tables.data_ptr(), block_tables.shape[1],
+                                   seq_lens.data_ptr(), B, int(max_seq_len), int(shared_len),
+                                   float(scale), workspace.data_ptr(), workspace.numel(),
+                                   _stream(stream)), "pa_decode_cascade")
 
 
 def pa_prefill_chunk(out: torch.Tensor, q: torch.Tensor, cu_q_lens: torch.Tensor,

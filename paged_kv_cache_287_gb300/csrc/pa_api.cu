@@ -150,6 +150,64 @@ pa_status pa_decode(void *out, const void *q, const void *kv_cache, int num_bloc
                                        workspace, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t pa_decode_cascade_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads,
+                                         int head_size, int shared_len) {
+    if (num_seqs <= 0 || num_heads <= 0 || num_kv_heads <= 0 || head_size <= 0 || shared_len < 0)
+        return 0;
+    const int sms = pa::device_sm_count();
+    const int splits = pa::prefix_splits(num_seqs, num_heads, num_kv_heads, shared_len, sms);
+    return pa::decode_workspace_bytes(num_seqs, head_size, sms) +
+           pa::prefix_partial_bytes(splits, num_seqs, num_heads, head_size);
+}
+
+pa_status pa_decode_cascade(void *out, const void *q, const void *kv_cache, int num_blocks,
+                            int block_size, int num_heads, int num_kv_heads, int head_size,
+                            const int32_t *block_tables, int max_blocks_per_seq,
+                            const int32_t *seq_lens, int num_seqs, int max_seq_len,
+                            int shared_len, float scale, void *workspace,
+                            size_t workspace_bytes, pa_stream_t stream) {
+    pa_status st = check_pool(kv_cache, num_blocks, block_size, num_kv_heads, head_size);
+    if (st != PA_OK) return st;
+    if ((st = check_heads(num_heads, num_kv_heads)) != PA_OK) return st;
+    if (num_seqs < 0 || max_seq_len < 0 || max_blocks_per_seq <= 0) return PA_ERR_INVALID_ARG;
+    if (shared_len < 0 || shared_len > max_seq_len) return PA_ERR_INVALID_ARG;
+    if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f) return PA_ERR_INVALID_ARG;
+    if (shared_len % 16 != 0 || shared_len % block_size != 0) return PA_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !q || !block_tables || !seq_lens || !aligned(out, 16) || !aligned(q, 16) ||
+        !aligned(block_tables, 4) || !aligned(seq_lens, 4))
+        return PA_ERR_INVALID_ARG;
+    if (max_seq_len > max_blocks_per_seq * block_size) return PA_ERR_INVALID_ARG;
+    if (num_seqs > pa::decode_max_seqs(head_size, num_heads / num_kv_heads))
+        return PA_ERR_UNSUPPORTED;
+    if ((long long)num_seqs * num_kv_heads * (((long long)max_seq_len + 15) / 16) >= (1LL << 31))
+        return PA_ERR_UNSUPPORTED;
+    if (num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+    const int sms = pa::device_sm_count();
+    const int splits = pa::prefix_splits(num_seqs, num_heads, num_kv_heads, shared_len, sms);
+    const size_t dec = pa::decode_workspace_bytes(num_seqs, head_size, sms);
+    const size_t need = dec + pa::prefix_partial_bytes(splits, num_seqs, num_heads, head_size);
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return PA_ERR_WORKSPACE;
+    pa::KvGeom g{num_blocks, block_size, num_kv_heads, head_size};
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    float *pre_ml = nullptr, *pre_acc = nullptr;
+    if (splits > 0) {
+        // Prefix partials after the decode workspace: (m, l) records, then O rows.
+        uint8_t *base = static_cast<uint8_t *>(workspace) + dec;
+        const size_t rows = (size_t)splits * num_seqs * num_heads;
+        pre_ml = reinterpret_cast<float *>(base);
+        pre_acc = reinterpret_cast<float *>(base + (rows * 2 * 4 + 255) / 256 * 256);
+        cudaError_t e = pa::launch_prefix_partials(q, kv_cache, g, num_heads, block_tables,
+                                                   max_blocks_per_seq, num_seqs, shared_len,
+                                                   scale, splits, pre_ml, pre_acc, s);
+        if (e != cudaSuccess) return from_cuda(e);
+    }
+    return from_cuda(pa::launch_decode_suffix(out, q, kv_cache, g, num_heads, block_tables,
+                                              max_blocks_per_seq, seq_lens, num_seqs,
+                                              max_seq_len, shared_len, scale, workspace, pre_ml,
+                                              pre_acc, splits, s));
+}
+
 pa_status pa_prefill_chunk(void *out, const void *q, const int32_t *cu_q_lens, int num_chunks,
                            int max_q_len, const void *kv_cache, int num_blocks, int block_size,
                            int num_heads, int num_kv_heads, int head_size,

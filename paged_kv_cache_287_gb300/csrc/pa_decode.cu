@@ -77,6 +77,13 @@ struct DecodeArgs {
     int total_warps;
     int stage_bytes;   // 2 * K/V tile bytes + query slot
     float scale_log2;  // scale * log2(e)
+    // Cascade: each sequence's tokens [0, shared_len) were attended by the prefix
+    // pass, whose pre_splits unnormalised partials per (sequence, query head) are
+    // folded in here; this kernel covers tokens [shared_len, seq_len).
+    int shared_len;
+    int pre_splits;
+    const float *pre_ml;   // [pre_splits][num_seqs][num_heads][2]
+    const float *pre_acc;  // [pre_splits][num_seqs][num_heads][D]
 };
 
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -115,13 +122,15 @@ __global__ void __launch_bounds__(W * 32, 1)
     if (tid == 0) prefetch_tensormap(&kv_map);
     // Lengths (clamped to what the table can hold) and the tile prefix over sequences.
     const int max_len = a.max_blocks * bs;
+    // s_len holds the tokens this kernel covers: those past the shared prefix.
+    const int sh = a.shared_len;
     for (int s = tid; s < B; s += W * 32) {
         int len = a.seq_lens[s];
-        if (len < 0 || len > max_len) {
+        if (len < sh || len > max_len) {
             atomicOr(&g_err_decode, kErrOob);
-            len = len < 0 ? 0 : max_len;
+            len = len < sh ? sh : max_len;
         }
-        s_len[s] = len;
+        s_len[s] = len - sh;
     }
     __syncthreads();
     if (warp == 0) {
@@ -185,12 +194,12 @@ __global__ void __launch_bounds__(W * 32, 1)
         seg = (s << 8) | h;
         jt = j;
         const int32_t *bt = a.block_tables + (size_t)s * a.max_blocks;
-        const int tok0 = j * kTile;
+        const int tok0 = sh + j * kTile;  // absolute position of the tile's first token
         if (bs >= kTile) {
             rk0 = kv_row(bt[tok0 / bs], h, tok0 % bs, a);
         } else {  // block_size 8: two blocks per tile, the second only if it holds tokens
             rk0 = kv_row(bt[tok0 / bs], h, 0, a);
-            if (tok0 + bs < s_len[s]) rk1 = kv_row(bt[tok0 / bs + 1], h, 0, a);
+            if (j * kTile + bs < s_len[s]) rk1 = kv_row(bt[tok0 / bs + 1], h, 0, a);
         }
     };
 
@@ -398,6 +407,53 @@ __global__ void __launch_bounds__(W * 32, 1)
             }
             const int nt = s_pre[s + 1] - s_pre[s];
             if (first_j == 0 && j == nt - 1) {
+                if (a.pre_splits > 0) {
+                    // Fold in the shared prefix's partials of this lane's two heads.
+                    const bool w0 = hh0 < G, w1 = hh0 + 1 < G;
+                    const size_t r0 = (size_t)s * a.num_heads + (size_t)h * G + hh0;
+                    const size_t rstride = (size_t)B * a.num_heads;
+                    const float2 *pml = reinterpret_cast<const float2 *>(a.pre_ml);
+                    float M0 = m0, M1 = m1;
+                    for (int k = 0; k < a.pre_splits; ++k) {
+                        if (w0) M0 = fmaxf(M0, pml[k * rstride + r0].x);
+                        if (w1) M1 = fmaxf(M1, pml[k * rstride + r0 + 1].x);
+                    }
+                    const float c0 = fast_exp2(m0 - M0), c1 = fast_exp2(m1 - M1);
+                    l0 *= c0;
+                    l1 *= c1;
+#pragma unroll
+                    for (int mt = 0; mt < D / 16; ++mt) {
+                        acc[mt][0] *= c0;
+                        acc[mt][2] *= c0;
+                        acc[mt][1] *= c1;
+                        acc[mt][3] *= c1;
+                    }
+                    for (int k = 0; k < a.pre_splits; ++k) {
+                        const size_t r = k * rstride + r0;
+                        if (w0) {
+                            const float2 ml = pml[r];
+                            const float wk = fast_exp2(ml.x - M0);
+                            const float *pa = a.pre_acc + r * D;
+                            l0 += wk * ml.y;
+#pragma unroll
+                            for (int mt = 0; mt < D / 16; ++mt) {
+                                acc[mt][0] += wk * pa[mt * 16 + tr0];
+                                acc[mt][2] += wk * pa[mt * 16 + tr0 + 8];
+                            }
+                        }
+                        if (w1) {
+                            const float2 ml = pml[r + 1];
+                            const float wk = fast_exp2(ml.x - M1);
+                            const float *pa = a.pre_acc + (r + 1) * D;
+                            l1 += wk * ml.y;
+#pragma unroll
+                            for (int mt = 0; mt < D / 16; ++mt) {
+                                acc[mt][1] += wk * pa[mt * 16 + tr0];
+                                acc[mt][3] += wk * pa[mt * 16 + tr0 + 8];
+                            }
+                        }
+                    }
+                }
                 // Whole segment in this warp: normalise and write bf16 rows, staged in
                 // the stage's query slot (G rows) for 16-byte stores.  Only the G real
                 // heads are staged: the slot holds no room for the padding heads.
@@ -479,17 +535,28 @@ __global__ void __launch_bounds__(kHeadsPad * D / 4) decode_merge_kernel(const D
     const int hh = i / (D / 4), d4 = i - hh * (D / 4);
     uint2 *orow =
         reinterpret_cast<uint2 *>(a.out + ((size_t)s * a.num_heads + (size_t)h * G + hh) * D);
-    if (nt == 0) {
+    const int P = a.pre_splits;
+    if (nt == 0 && P == 0) {
         orow[d4] = make_uint2(0u, 0u);
         return;
     }
-    const long long T = (long long)a.prefix[a.num_seqs] * Hkv;
+    // Pieces g0..g1 of this segment (none if the sequence has no tokens here).
     const long long NW = a.total_warps;
-    const long long S0 = (long long)Hkv * pre + (long long)h * nt, S1 = S0 + nt;
-    const long long g0 = ((S0 + 1) * NW - 1) / T;
-    const long long g1 = (S1 * NW - 1) / T;
-    if (g0 == g1) return;  // written whole by one warp
+    long long T = 1, S0 = 0, S1 = 0, g0 = 0, g1 = -1;
+    if (nt > 0) {
+        T = (long long)a.prefix[a.num_seqs] * Hkv;
+        S0 = (long long)Hkv * pre + (long long)h * nt;
+        S1 = S0 + nt;
+        g0 = ((S0 + 1) * NW - 1) / T;
+        g1 = (S1 * NW - 1) / T;
+        if (g0 == g1) return;  // written whole by one warp (prefix folded in there)
+    }
+    // Shared-prefix partials of this query head.
+    const size_t pr0 = (size_t)s * a.num_heads + (size_t)h * G + hh;
+    const size_t prs = (size_t)a.num_seqs * a.num_heads;
+    const float2 *pml = reinterpret_cast<const float2 *>(a.pre_ml);
     float M = -INFINITY;
+    for (int sp = 0; sp < P; ++sp) M = fmaxf(M, pml[sp * prs + pr0].x);
     long long b = (g0 * T) / NW;
     for (long long gw = g0; gw <= g1; ++gw) {
         const long long e = ((gw + 1) * T) / NW;
@@ -517,6 +584,17 @@ __global__ void __launch_bounds__(kHeadsPad * D / 4) decode_merge_kernel(const D
             den += w * ml.y;
         }
         b = e;
+    }
+    for (int sp = 0; sp < P; ++sp) {
+        const size_t r = sp * prs + pr0;
+        const float2 ml = pml[r];
+        const float4 v = reinterpret_cast<const float4 *>(a.pre_acc + r * D)[d4];
+        const float w = exp2f(ml.x - M);
+        num.x += w * v.x;
+        num.y += w * v.y;
+        num.z += w * v.z;
+        num.w += w * v.w;
+        den += w * ml.y;
     }
     const float inv = 1.f / den;
     orow[d4] = make_uint2(pack_bf16(num.x * inv, num.y * inv), pack_bf16(num.z * inv, num.w * inv));
@@ -567,10 +645,13 @@ cudaError_t take_error_decode(unsigned *bits) {
     return e;
 }
 
-cudaError_t launch_decode(void *out, const void *q, const void *kv_cache, const KvGeom &g,
-                          int num_heads, const int32_t *block_tables, int max_blocks_per_seq,
-                          const int32_t *seq_lens, int num_seqs, int max_seq_len, float scale,
-                          void *workspace, cudaStream_t stream) {
+namespace {
+
+cudaError_t launch_decode_impl(void *out, const void *q, const void *kv_cache, const KvGeom &g,
+                               int num_heads, const int32_t *block_tables, int max_blocks_per_seq,
+                               const int32_t *seq_lens, int num_seqs, int max_seq_len,
+                               int shared_len, float scale, void *workspace, const float *pre_ml,
+                               const float *pre_acc, int pre_splits, cudaStream_t stream) {
     const int sms = device_sm_count();
     const int D = g.head_size;
     CUtensorMap map;
@@ -579,8 +660,8 @@ cudaError_t launch_decode(void *out, const void *q, const void *kv_cache, const 
     // As many warps as there can be tiles, at most one CTA per SM.  A warp has a
     // single stage, so a small batch finishes soonest with one tile per warp; a
     // large one fills every SM and each warp streams its share.
-    const long long tmax =
-        (long long)num_seqs * g.num_kv_heads * ((std::max(max_seq_len, 1) + kTile - 1) / kTile);
+    const long long tmax = (long long)num_seqs * g.num_kv_heads *
+                           ((std::max(max_seq_len - shared_len, 1) + kTile - 1) / kTile);
     long long ctas = (tmax + kDecodeWarps - 1) / kDecodeWarps;
     ctas = std::max(1LL, std::min<long long>(ctas, sms));
     uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -605,11 +686,42 @@ cudaError_t launch_decode(void *out, const void *q, const void *kv_cache, const 
     a.total_warps = (int)ctas * kDecodeWarps;
     a.stage_bytes = 2 * (D / 64) * kTile * 128 + q_slot_bytes(a.group, D);
     a.scale_log2 = scale * 1.4426950408889634f;
+    a.shared_len = shared_len;
+    a.pre_splits = pre_splits;
+    a.pre_ml = pre_ml;
+    a.pre_acc = pre_acc;
     if (D == 128)
         return launch_decode_d<128>(a, map, (int)ctas, decode_smem_bytes<128>(num_seqs, a.group),
                                     stream);
     return launch_decode_d<64>(a, map, (int)ctas, decode_smem_bytes<64>(num_seqs, a.group),
                                stream);
+}
+
+}  // namespace
+
+cudaError_t launch_decode(void *out, const void *q, const void *kv_cache, const KvGeom &g,
+                          int num_heads, const int32_t *block_tables, int max_blocks_per_seq,
+                          const int32_t *seq_lens, int num_seqs, int max_seq_len, float scale,
+                          void *workspace, cudaStream_t stream) {
+    return launch_decode_impl(out, q, kv_cache, g, num_heads, block_tables, max_blocks_per_seq,
+                              seq_lens, num_seqs, max_seq_len, 0, scale, workspace, nullptr,
+                              nullptr, 0, stream);
+}
+
+cudaError_t launch_decode_suffix(void *out, const void *q, const void *kv_cache, const KvGeom &g,
+                                 int num_heads, const int32_t *block_tables,
+                                 int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs,
+                                 int max_seq_len, int shared_len, float scale, void *workspace,
+                                 const float *pre_ml, const float *pre_acc, int pre_splits,
+                                 cudaStream_t stream) {
+    return launch_decode_impl(out, q, kv_cache, g, num_heads, block_tables, max_blocks_per_seq,
+                              seq_lens, num_seqs, max_seq_len, shared_len, scale, workspace,
+                              pre_ml, pre_acc, pre_splits, stream);
+}
+
+size_t prefix_partial_bytes(int splits, int num_seqs, int num_heads, int head_size) {
+    const size_t rows = (size_t)splits * num_seqs * num_heads;
+    return align_up(rows * 2 * 4, 256) + align_up(rows * (size_t)head_size * 4, 256);
 }
 
 }  // namespace pa

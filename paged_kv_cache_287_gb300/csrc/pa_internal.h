@@ -42,6 +42,26 @@ cudaError_t launch_decode(void *out, const void *q, const void *kv_cache, const 
                           const int32_t *seq_lens, int num_seqs, int max_seq_len, float scale,
                           void *workspace, cudaStream_t stream);
 
+// Shared-prefix (cascade) decode.  The first shared_len tokens of every sequence
+// sit in sequence 0's first blocks.  The prefix pass computes, per key-range split,
+// the unnormalised (m, l, O) of every (sequence, query head) over those tokens.
+int prefix_splits(int num_seqs, int num_heads, int num_kv_heads, int shared_len, int sm_count);
+cudaError_t launch_prefix_partials(const void *q, const void *kv_cache, const KvGeom &g,
+                                   int num_heads, const int32_t *block_tables,
+                                   int max_blocks_per_seq, int num_seqs, int shared_len,
+                                   float scale, int splits, float *part_ml, float *part_acc,
+                                   cudaStream_t stream);
+// Bytes of prefix partials for `splits` splits.
+size_t prefix_partial_bytes(int splits, int num_seqs, int num_heads, int head_size);
+// Decode over each sequence's tokens [shared_len, seq_len), folding in the prefix
+// partials (pre_splits of them at pre_ml / pre_acc) before normalising.
+cudaError_t launch_decode_suffix(void *out, const void *q, const void *kv_cache, const KvGeom &g,
+                                 int num_heads, const int32_t *block_tables,
+                                 int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs,
+                                 int max_seq_len, int shared_len, float scale, void *workspace,
+                                 const float *pre_ml, const float *pre_acc, int pre_splits,
+                                 cudaStream_t stream);
+
 cudaError_t launch_prefill(void *out, const void *q, const int32_t *cu_q_lens, int num_chunks,
                            int max_q_len, const void *kv_cache, const KvGeom &g, int num_heads,
                            const int32_t *block_tables, int max_blocks_per_seq,

@@ -68,6 +68,14 @@ struct PrefillArgs {
     int q_tile;        // query tokens per 128-row tile: floor(128 / group)
     int negate_q;      // 1 if the softmax scale is negative (Q is negated instead)
     float scale_log2;  // |scale| * log2(e), at least 1e-30
+    // Shared-prefix mode (part_ml != nullptr): the "chunk" is the whole decode
+    // batch (row = sequence), every row sees every key of the shared prefix
+    // [0, shared_len) held by sequence 0's blocks, split over blockIdx.z in
+    // ranges of split_tiles K/V tiles; the unnormalised (m, l, O) of each
+    // (split, sequence, query head) go to part_ml / part_acc.
+    float *part_ml;    // [splits][num_seqs][num_heads][2]: m (log2 units), l
+    float *part_acc;   // [splits][num_seqs][num_heads][D]
+    int shared_len, split_tiles, prefix_rows;  // prefix_rows: the batch's sequences
 };
 
 template <int D>
@@ -120,9 +128,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // query tiles, start first (longest work first keeps the tail short).
     __shared__ int s_ctx[kRankMax];
     __shared__ int s_pick;
-    int s = blockIdx.z;
+    const bool prefix = a.part_ml != nullptr;
+    int s = prefix ? 0 : blockIdx.z;
     const int nchunks = gridDim.z;
-    if (nchunks <= kRankMax) {
+    if (!prefix && nchunks <= kRankMax) {
         for (int i = threadIdx.x; i < nchunks; i += blockDim.x)
             s_ctx[i] = a.seq_lens[i] - (a.cu_q_lens[i + 1] - a.cu_q_lens[i]);
         __syncthreads();
@@ -140,22 +149,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     const int h = blockIdx.y;
     const int qt = gridDim.x - 1 - blockIdx.x;  // latest query tiles first
-    const int q0 = a.cu_q_lens[s];
-    const int q_len = a.cu_q_lens[s + 1] - q0;
+    const int q0 = prefix ? 0 : a.cu_q_lens[s];
+    const int q_len = prefix ? a.prefix_rows : a.cu_q_lens[s + 1] - q0;
     const int QT = a.q_tile, G = a.group;
     const int t0 = qt * kTcTiles * QT;
     if (t0 >= q_len) return;
     const bool has1 = t0 + QT < q_len;  // the second tile holds at least one token
-    int len = a.seq_lens[s];
-    const int max_len = a.max_blocks * a.block_size;
-    if (len < q_len || len > max_len) {
-        if (threadIdx.x == 0) atomicOr(&g_err_prefill, kErrOob);
-        len = std::min(std::max(len, q_len), max_len);
+    // Keys [key0, key0 + len) of the sequence are this CTA's; key indices below
+    // are relative to key0.
+    int len, ctx, key0 = 0, n_kt;
+    if (!prefix) {
+        len = a.seq_lens[s];
+        const int max_len = a.max_blocks * a.block_size;
+        if (len < q_len || len > max_len) {
+            if (threadIdx.x == 0) atomicOr(&g_err_prefill, kErrOob);
+            len = std::min(std::max(len, q_len), max_len);
+        }
+        ctx = len - q_len;
+        const int t_last = std::min(t0 + kTcTiles * QT, q_len) - 1;
+        n_kt = (ctx + t_last + 1 + kTcKeys - 1) / kTcKeys;
+    } else {
+        key0 = (int)blockIdx.z * a.split_tiles * kTcKeys;
+        len = std::min(a.shared_len - key0, a.split_tiles * kTcKeys);
+        ctx = len;  // no causal limit: every row sees the whole range
+        n_kt = (len + kTcKeys - 1) / kTcKeys;
+        if (len <= 0) return;
     }
-    const int ctx = len - q_len;
-    const int t_last = std::min(t0 + kTcTiles * QT, q_len) - 1;
-    const int n_keys = ctx + t_last + 1;
-    const int n_kt = (n_keys + kTcKeys - 1) / kTcKeys;
 
     if (threadIdx.x == 0) {
         prefetch_tensormap(&kv_map);
@@ -201,8 +220,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         auto box_row = [&](int kt) {
             const int tok = kt * kTcKeys + lane * box_rows;
             if (lane >= nbox) return 0;
-            if (tok >= len) return -(1 << 30);  // past the sequence: TMA fills zeros
-            return prefill_row(bt[tok / bs], h, tok % bs, a);
+            if (tok >= len) return -(1 << 30);  // past the range: TMA fills zeros
+            return prefill_row(bt[(key0 + tok) / bs], h, (key0 + tok) % bs, a);
         };
         int nxt = box_row(0);
         int issued = 0;
@@ -361,7 +380,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&q_full[t]);
         }
-        const int lim = real ? std::min(ctx + t0 + tok, len - 1) : len - 1;
+        const int lim = real && !prefix ? std::min(ctx + t0 + tok, len - 1) : len - 1;
         const float sl2 = a.scale_log2;  // > 0: a negative scale was moved into Q
         float m = -INFINITY, l = 0.f;
         bool ok = true;
@@ -472,6 +491,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (lane == 0) atomicOr(&g_err_prefill, kErrTimeout);
         } else {
             tc_fence_after();
+            if (prefix) {
+                // Unnormalised partial of this (split, sequence, query head).
+                const size_t rec =
+                    ((size_t)blockIdx.z * q_len + (t0 + tok)) * a.num_heads + (size_t)h * G + gq;
+                float4 *pacc = reinterpret_cast<float4 *>(a.part_acc + rec * D);
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    float o[32];
+                    tmem_ld32(co + 32 * c, o);
+                    tc_wait_ld();
+                    if (real) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            pacc[c * 8 + e] =
+                                make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+                    }
+                }
+                if (real) reinterpret_cast<float2 *>(a.part_ml)[rec] = make_float2(m, l);
+            } else {
             const float inv = 1.f / l;
             uint4 *dst = reinterpret_cast<uint4 *>(
                 a.out + ((size_t)(q0 + t0 + tok) * a.num_heads + (size_t)h * G + gq) * D);
@@ -489,6 +527,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             pack_bf16(o[8 * e + 4] * inv, o[8 * e + 5] * inv),
                             pack_bf16(o[8 * e + 6] * inv, o[8 * e + 7] * inv));
                 }
+            }
             }
         }
     }
@@ -546,9 +585,61 @@ cudaError_t launch_prefill(void *out, const void *q, const int32_t *cu_q_lens, i
     a.negate_q = scale < 0.f ? 1 : 0;
     a.scale_log2 = std::max(std::fabs(scale) * 1.4426950408889634f, 1e-30f);
     a.q_tile = kTcRows / a.group;
+    a.part_ml = nullptr;
+    a.part_acc = nullptr;
+    a.shared_len = a.split_tiles = a.prefix_rows = 0;
     const int per_cta = kTcTiles * a.q_tile;
     dim3 grid((unsigned)((max_q_len + per_cta - 1) / per_cta), (unsigned)g.num_kv_heads,
               (unsigned)num_chunks);
+    if (g.head_size == 128) return launch_prefill_tc<128>(a, map, grid, stream);
+    return launch_prefill_tc<64>(a, map, grid, stream);
+}
+
+int prefix_splits(int num_seqs, int num_heads, int num_kv_heads, int shared_len, int sm_count) {
+    if (shared_len <= 0 || num_seqs <= 0) return 0;
+    const int group = num_heads / num_kv_heads;
+    const int per_cta = kTcTiles * (kTcRows / group);
+    const long long ctas = (long long)((num_seqs + per_cta - 1) / per_cta) * num_kv_heads;
+    const int tiles = (shared_len + kTcKeys - 1) / kTcKeys;
+    // About one wave of CTAs, at least two K/V tiles per CTA.
+    long long want = (sm_count + ctas - 1) / ctas;
+    want = std::min<long long>(want, std::max(1, tiles / 2));
+    const int per = (int)((tiles + want - 1) / want);
+    return (tiles + per - 1) / per;
+}
+
+cudaError_t launch_prefix_partials(const void *q, const void *kv_cache, const KvGeom &g,
+                                   int num_heads, const int32_t *block_tables,
+                                   int max_blocks_per_seq, int num_seqs, int shared_len,
+                                   float scale, int splits, float *part_ml, float *part_acc,
+                                   cudaStream_t stream) {
+    CUtensorMap map;
+    if (!encode_kv_map(&map, kv_cache, g, g.block_size >= 16 ? 16 : g.block_size))
+        return cudaErrorInvalidValue;
+    PrefillArgs a;
+    a.out = nullptr;
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.cu_q_lens = nullptr;
+    a.block_tables = block_tables;
+    a.seq_lens = nullptr;
+    a.num_heads = num_heads;
+    a.num_kv_heads = g.num_kv_heads;
+    a.group = num_heads / g.num_kv_heads;
+    a.block_size = g.block_size;
+    a.max_blocks = max_blocks_per_seq;
+    a.num_blocks = g.num_blocks;
+    a.negate_q = scale < 0.f ? 1 : 0;
+    a.scale_log2 = std::max(std::fabs(scale) * 1.4426950408889634f, 1e-30f);
+    a.q_tile = kTcRows / a.group;
+    a.part_ml = part_ml;
+    a.part_acc = part_acc;
+    a.shared_len = shared_len;
+    const int tiles = (shared_len + kTcKeys - 1) / kTcKeys;
+    a.split_tiles = (tiles + splits - 1) / splits;
+    a.prefix_rows = num_seqs;
+    const int per_cta = kTcTiles * a.q_tile;
+    dim3 grid((unsigned)((num_seqs + per_cta - 1) / per_cta), (unsigned)g.num_kv_heads,
+              (unsigned)splits);
     if (g.head_size == 128) return launch_prefill_tc<128>(a, map, grid, stream);
     return launch_prefill_tc<64>(a, map, grid, stream);
 }

@@ -91,3 +91,21 @@ def test_prefill_host_checks(lib):
     bad = list(args)
     bad[4] = 0                                  # empty: no-op
     assert lib.pa_prefill_chunk(*bad) == 0
+
+
+def test_cascade_host_checks(lib):
+    args = [FAKE, FAKE, FAKE, 10, 16, 32, 8, 128, FAKE, 4, FAKE, 3, 64, 32, 0.1, FAKE, 1 << 30,
+            None]
+    bad = list(args)
+    bad[13] = 65                                # shared_len beyond max_seq_len
+    assert lib.pa_decode_cascade(*bad) == 1
+    bad = list(args)
+    bad[13] = 8                                 # not a multiple of 16
+    assert lib.pa_decode_cascade(*bad) == 2
+    bad = list(args)
+    bad[13] = -16
+    assert lib.pa_decode_cascade(*bad) == 1
+    bad = list(args)
+    bad[11] = 0                                 # no sequences: no-op
+    assert lib.pa_decode_cascade(*bad) == 0
+    assert lib.pa_decode_cascade_workspace_bytes(0, 32, 8, 128, 64) == 0

@@ -1,0 +1,123 @@
+"""Parity of the shared-prefix (cascade) decode with the CPU fp64 oracle.
+
+The oracle knows nothing of the cascade: it gathers each sequence's whole
+context through its own block table and applies the plain definition, so these
+tests check that attending the shared blocks once for the batch and merging
+with each sequence's own tokens gives ordinary decode attention.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_cache_287_gb300 import binding
+from paged_kv_cache_287_gb300.workloads import make_batch, make_config
+from tests._gpu import bits, compare, gpu_decode, gpu_write, oracle_pool, oracle_rows
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(autouse=True)
+def _clean_errors():
+    binding.pa_error_check()
+    yield
+    binding.pa_error_check()
+
+
+def gpu_cascade(b, shared_len: int, seq_lens=None) -> torch.Tensor:
+    lens = b.seq_lens if seq_lens is None else seq_lens
+    out = torch.full_like(b.q, float("nan"))
+    nbytes = binding.pa_decode_cascade_workspace_bytes(b.num_seqs, b.num_heads, b.num_kv_heads,
+                                                       b.head_size, shared_len)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    binding.pa_decode_cascade(out, b.q, b.kv_cache, b.block_tables, lens, int(lens.max()),
+                              shared_len, b.scale, ws)
+    return out
+
+
+CASCADE_SHAPES = [
+    # num_seqs, prefix blocks, suffix range, Hq, Hkv, D, bs
+    (40, 20, (1, 300), 64, 8, 128, 16),     # group 8: two prefix CTAs, 3 key tiles, ragged
+    (7, 9, (1, 40), 8, 8, 128, 16),         # group 1, one short key tile
+    (50, 34, (5, 150), 16, 4, 64, 8),       # group 4, block 8, 272 shared tokens
+    (33, 8, (1, 100), 24, 8, 128, 32),      # group 3, block 32, 256 shared tokens
+    (130, 40, (64, 400), 32, 8, 128, 16),   # many splits over 640 shared tokens
+]
+
+
+@pytest.mark.parametrize("case", range(len(CASCADE_SHAPES)))
+def test_cascade_small_shapes(case):
+    B, pb, (lo, hi), Hq, Hkv, D, bs = CASCADE_SHAPES[case]
+    g = torch.Generator().manual_seed(500 + case)
+    suffix = torch.randint(lo, hi + 1, (B,), generator=g).tolist()
+    lens = [pb * bs + x for x in suffix]
+    b = make_batch(name=f"c{case}", seq_lens=lens, q_lens=[1] * B, num_heads=Hq,
+                   num_kv_heads=Hkv, head_size=D, block_size=bs, scale=D ** -0.5,
+                   seed=600 + case, shared_prefix_blocks=pb, device=DEV)
+    pool = oracle_pool(b)
+    gpu_write(b)
+    out = gpu_cascade(b, pb * bs)
+    binding.pa_error_check()
+    compare(out, oracle_rows(b, pool), f"cascade case {case}")
+
+
+def test_cascade_with_sequences_that_have_no_own_tokens():
+    """A sequence whose length equals the shared length attends to the prefix only."""
+    pb, bs = 12, 16
+    b = make_batch(name="cz", seq_lens=[pb * bs + x for x in (5, 70, 1, 33, 9)],
+                   q_lens=[1] * 5, num_heads=32, num_kv_heads=8, head_size=128, block_size=bs,
+                   scale=128 ** -0.5, seed=71, shared_prefix_blocks=pb, device=DEV)
+    pool = oracle_pool(b)
+    gpu_write(b)
+    lens = b.seq_lens.clone()
+    lens[0] = pb * bs
+    lens[3] = pb * bs
+    out = gpu_cascade(b, pb * bs, lens)
+    binding.pa_error_check()
+    want = oracle_rows(type(b)(**{**b.__dict__, "seq_lens": lens}), pool)
+    compare(out, want, "cascade, empty suffixes")
+
+
+def test_cascade_without_shared_tokens_is_plain_decode_bitwise():
+    b = make_batch(name="c0", seq_lens=[33, 200, 17, 90], q_lens=[1] * 4, num_heads=32,
+                   num_kv_heads=8, head_size=128, block_size=16, scale=0.09, seed=72,
+                   device=DEV)
+    gpu_write(b)
+    assert np.array_equal(bits(gpu_cascade(b, 0)), bits(gpu_decode(b)))
+
+
+def test_cascade_matches_decode_and_is_deterministic():
+    b = make_batch(name="cd", seq_lens=[512 + x for x in (100, 3, 250, 64, 1, 77)],
+                   q_lens=[1] * 6, num_heads=64, num_kv_heads=8, head_size=128, block_size=16,
+                   scale=128 ** -0.5, seed=73, shared_prefix_blocks=32, device=DEV)
+    gpu_write(b)
+    c1 = gpu_cascade(b, 512)
+    c2 = gpu_cascade(b, 512)
+    assert np.array_equal(bits(c1), bits(c2))
+    d = gpu_decode(b)
+    assert (c1.float() - d.float()).abs().max().item() <= 1e-2
+
+
+def test_cascade_prefix_workload_full_size():
+    b = make_config(5, device=DEV)
+    pool = oracle_pool(b)
+    gpu_write(b)
+    out = gpu_cascade(b, b.shared_prefix_blocks * b.block_size)
+    binding.pa_error_check()
+    compare(out, oracle_rows(b, pool), "prefix-shared workload, cascade")
+
+
+def test_cascade_rejects_unaligned_shared_length():
+    b = make_batch(name="cu", seq_lens=[40, 50], q_lens=[1, 1], num_heads=8, num_kv_heads=8,
+                   head_size=64, block_size=8, scale=0.1, seed=74, shared_prefix_blocks=3,
+                   device=DEV)
+    with pytest.raises(binding.PaError) as e:
+        gpu_cascade(b, 24)  # three blocks of 8: not a multiple of 16
+    assert e.value.status == 2
