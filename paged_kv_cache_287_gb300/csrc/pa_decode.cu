@@ -555,11 +555,20 @@ __global__ void __launch_bounds__(kHeadsPad * D / 4) decode_merge_kernel(const D
     const size_t pr0 = (size_t)s * a.num_heads + (size_t)h * G + hh;
     const size_t prs = (size_t)a.num_seqs * a.num_heads;
     const float2 *pml = reinterpret_cast<const float2 *>(a.pre_ml);
+    // Warp gw covers tiles [floor(gw*T/NW), floor((gw+1)*T/NW)); the bounds are
+    // stepped incrementally (T = q*NW + r) instead of divided per warp.
+    const long long tq = T / NW, tr = T % NW;
+    const long long b0 = g0 * tq + (g0 * tr) / NW, f0 = (g0 * tr) % NW;
     float M = -INFINITY;
     for (int sp = 0; sp < P; ++sp) M = fmaxf(M, pml[sp * prs + pr0].x);
-    long long b = (g0 * T) / NW;
+    long long b = b0, f = f0;
     for (long long gw = g0; gw <= g1; ++gw) {
-        const long long e = ((gw + 1) * T) / NW;
+        long long e = b + tq;
+        f += tr;
+        if (f >= NW) {
+            f -= NW;
+            ++e;
+        }
         if (max(b, S0) < min(e, S1)) {
             const size_t rec = (size_t)gw * 2 + (b >= S0 ? 0 : 1);
             M = fmaxf(M, a.part_ml[(rec * kHeadsPad + hh) * 2]);
@@ -568,9 +577,15 @@ __global__ void __launch_bounds__(kHeadsPad * D / 4) decode_merge_kernel(const D
     }
     float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
     float den = 0.f;
-    b = (g0 * T) / NW;
+    b = b0;
+    f = f0;
     for (long long gw = g0; gw <= g1; ++gw) {
-        const long long e = ((gw + 1) * T) / NW;
+        long long e = b + tq;
+        f += tr;
+        if (f >= NW) {
+            f -= NW;
+            ++e;
+        }
         if (max(b, S0) < min(e, S1)) {
             const size_t rec = (size_t)gw * 2 + (b >= S0 ? 0 : 1);
             const float2 ml = reinterpret_cast<const float2 *>(a.part_ml)[rec * kHeadsPad + hh];
