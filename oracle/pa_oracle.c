@@ -24,6 +24,12 @@
  *             index 0 = K, 1 = V;
  *   slot      = physical_block * block_size + offset inside the block;
  *   query head h reads KV head h / (num_heads / num_kv_heads).
+ * FP8 pools (the pages name FP8 among the supported quantisation formats and
+ * give the block size per dtype byte count): one byte per element in the same
+ * layout, each an OCP FP8 E4M3 ("e4m3fn") code; the real value is the code's
+ * value times a per-tensor scale (k_scale for K, v_scale for V).  A new row is
+ * stored as the e4m3 code nearest to (float)x / scale, ties to the even code,
+ * magnitudes beyond the largest finite code (448) saturating to it.
  * Every function here is pinned by the CPU tests (closed forms, brute force
  * on contiguous data, library attention, placement invariance).
  */
@@ -42,6 +48,52 @@ static double bf16_bits_to_double(uint16_t bits)
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/*
+ * OCP FP8 E4M3 (e4m3fn): sign, 4 exponent bits (bias 7), 3 mantissa bits; no
+ * infinities; exponent 15 with mantissa 7 is NaN; exponent 0 is subnormal,
+ * m * 2^-9.  Otherwise (1 + m/8) * 2^(e-7) = (8 + m) * 2^(e-10).
+ */
+double oracle_e4m3_to_double(uint8_t code)
+{
+    const int s = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    if (e == 15 && m == 7)
+        return NAN;
+    const double v = e == 0 ? ldexp((double)m, -9) : ldexp((double)(8 + m), e - 10);
+    return s ? -v : v;
+}
+
+/*
+ * Nearest e4m3 code to x, ties to the code with an even mantissa (its low bit
+ * clear), |x| >= 448 saturating to 448; the sign is kept (so a negative value
+ * that rounds to zero gives the negative-zero code); NaN gives the NaN code.
+ * Plain search over the 127 non-negative finite codes, whose values increase
+ * with the code.
+ */
+uint8_t oracle_e4m3_from_float(float x)
+{
+    if (isnan(x))
+        return 0x7F;
+    const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    const double a = fabs((double)x);
+    if (a >= 448.0)
+        return sign | 0x7E;
+    int lo = 0;
+    for (int c = 0; c <= 0x7E; ++c)
+        if (oracle_e4m3_to_double((uint8_t)c) <= a)
+            lo = c;
+    const double vlo = oracle_e4m3_to_double((uint8_t)lo);
+    const double vhi = oracle_e4m3_to_double((uint8_t)(lo + 1));
+    const double mid = 0.5 * (vlo + vhi); /* exact: both have few significant bits */
+    int c;
+    if (a < mid)
+        c = lo;
+    else if (a > mid)
+        c = lo + 1;
+    else
+        c = (lo & 1) == 0 ? lo : lo + 1;
+    return sign | (uint8_t)c;
 }
 
 /* §Block size: 2 (key and value) * block_size * num_kv_heads * head_size * dtype bytes. */
@@ -91,6 +143,50 @@ int oracle_cache_write(uint16_t *kv_cache, int num_blocks, int block_size, int n
         }
     }
     return status;
+}
+
+/*
+ * FP8 cache write: as oracle_cache_write, but element x of new token i is
+ * stored as oracle_e4m3_from_float((float)x / scale), the division in binary32
+ * (k_scale for K, v_scale for V).
+ */
+int oracle_cache_write_fp8(uint8_t *kv_cache, int num_blocks, int block_size, int num_kv_heads,
+                           int head_size, const uint16_t *k_new, const uint16_t *v_new,
+                           const int32_t *slot_mapping, int num_tokens, float k_scale,
+                           float v_scale)
+{
+    int status = 0;
+    for (int i = 0; i < num_tokens; ++i) {
+        int64_t slot = slot_mapping[i];
+        if (slot < 0)
+            continue;
+        if (slot >= (int64_t)num_blocks * block_size) {
+            status = -1;
+            continue;
+        }
+        int64_t block = slot / block_size;
+        int offset = (int)(slot % block_size);
+        for (int h = 0; h < num_kv_heads; ++h) {
+            for (int d = 0; d < head_size; ++d) {
+                size_t src = ((size_t)i * num_kv_heads + h) * head_size + d;
+                const float k = (float)bf16_bits_to_double(k_new[src]);
+                const float v = (float)bf16_bits_to_double(v_new[src]);
+                kv_cache[pool_index(block, 0, h, offset, d, num_kv_heads, block_size, head_size)] =
+                    oracle_e4m3_from_float(k / k_scale);
+                kv_cache[pool_index(block, 1, h, offset, d, num_kv_heads, block_size, head_size)] =
+                    oracle_e4m3_from_float(v / v_scale);
+            }
+        }
+    }
+    return status;
+}
+
+/* Value of pool element idx: bf16 bits, or an e4m3 code times its scale. */
+static double pool_value(const void *kv_cache, int fp8, size_t idx, double scale)
+{
+    if (fp8)
+        return oracle_e4m3_to_double(((const uint8_t *)kv_cache)[idx]) * scale;
+    return bf16_bits_to_double(((const uint16_t *)kv_cache)[idx]);
 }
 
 /*
@@ -178,11 +274,12 @@ static void attend_row(double *out, const uint16_t *q_row, const double *K, cons
  * Returns 0; -1 on a bad argument or an out-of-pool table entry; -2 on
  * allocation failure.
  */
-int oracle_attention(double *out, const uint16_t *q, const int32_t *cu_q_lens, int num_seqs,
-                     const uint16_t *kv_cache, int num_blocks, int block_size, int num_heads,
-                     int num_kv_heads, int head_size, const int32_t *block_tables,
-                     int max_blocks_per_seq, const int32_t *seq_lens, double scale,
-                     const int32_t *rows, int num_rows, int num_threads)
+static int attention_impl(double *out, const uint16_t *q, const int32_t *cu_q_lens,
+                          int num_seqs, const void *kv_cache, int kv_fp8, double k_scale,
+                          double v_scale, int num_blocks, int block_size, int num_heads,
+                          int num_kv_heads, int head_size, const int32_t *block_tables,
+                          int max_blocks_per_seq, const int32_t *seq_lens, double scale,
+                          const int32_t *rows, int num_rows, int num_threads)
 {
     if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0 || head_size <= 0 ||
         head_size > 512 || block_size <= 0)
@@ -245,10 +342,14 @@ int oracle_attention(double *out, const uint16_t *q, const int32_t *cu_q_lens, i
                     for (int h = 0; h < num_kv_heads; ++h)
                         for (int d = 0; d < head_size; ++d) {
                             size_t dst = ((size_t)t * num_kv_heads + h) * head_size + d;
-                            K[dst] = bf16_bits_to_double(kv_cache[pool_index(
-                                block, 0, h, t - t0, d, num_kv_heads, block_size, head_size)]);
-                            V[dst] = bf16_bits_to_double(kv_cache[pool_index(
-                                block, 1, h, t - t0, d, num_kv_heads, block_size, head_size)]);
+                            K[dst] = pool_value(kv_cache, kv_fp8,
+                                                pool_index(block, 0, h, t - t0, d, num_kv_heads,
+                                                           block_size, head_size),
+                                                k_scale);
+                            V[dst] = pool_value(kv_cache, kv_fp8,
+                                                pool_index(block, 1, h, t - t0, d, num_kv_heads,
+                                                           block_size, head_size),
+                                                v_scale);
                         }
             }
             if (bad) {
@@ -284,6 +385,34 @@ int oracle_attention(double *out, const uint16_t *q, const int32_t *cu_q_lens, i
     }
     free(out_index);
     return status;
+}
+
+int oracle_attention(double *out, const uint16_t *q, const int32_t *cu_q_lens, int num_seqs,
+                     const uint16_t *kv_cache, int num_blocks, int block_size, int num_heads,
+                     int num_kv_heads, int head_size, const int32_t *block_tables,
+                     int max_blocks_per_seq, const int32_t *seq_lens, double scale,
+                     const int32_t *rows, int num_rows, int num_threads)
+{
+    return attention_impl(out, q, cu_q_lens, num_seqs, kv_cache, 0, 1.0, 1.0, num_blocks,
+                          block_size, num_heads, num_kv_heads, head_size, block_tables,
+                          max_blocks_per_seq, seq_lens, scale, rows, num_rows, num_threads);
+}
+
+/*
+ * oracle_attention over an FP8 pool: K = e4m3 value * k_scale, V = e4m3 value *
+ * v_scale (exact in double), then the same definition.
+ */
+int oracle_attention_fp8(double *out, const uint16_t *q, const int32_t *cu_q_lens, int num_seqs,
+                         const uint8_t *kv_cache, double k_scale, double v_scale, int num_blocks,
+                         int block_size, int num_heads, int num_kv_heads, int head_size,
+                         const int32_t *block_tables, int max_blocks_per_seq,
+                         const int32_t *seq_lens, double scale, const int32_t *rows,
+                         int num_rows, int num_threads)
+{
+    return attention_impl(out, q, cu_q_lens, num_seqs, kv_cache, 1, k_scale, v_scale,
+                          num_blocks, block_size, num_heads, num_kv_heads, head_size,
+                          block_tables, max_blocks_per_seq, seq_lens, scale, rows, num_rows,
+                          num_threads);
 }
 
 /* Threads an OpenMP parallel region would use (1 without OpenMP). */

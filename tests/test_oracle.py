@@ -25,6 +25,8 @@ import oracle
 from tests._helpers import Contig, brute_reference, oracle_on, page, random_contig
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+# Altered oracle copies are compiled in a git-ignored folder inside the repository.
+MUT_DIR = os.path.join(os.path.dirname(oracle.__file__), "_build")
 
 
 def _golden_rows(name):
@@ -342,10 +344,11 @@ def test_unmodified_oracle_passes_battery(oracle_lib):
 def test_planted_mistakes_are_caught(name):
     if shutil.which("gcc") is None:
         pytest.skip("no gcc")
+    os.makedirs(MUT_DIR, exist_ok=True)
     src = open(os.path.join(os.path.dirname(oracle.__file__), "pa_oracle.c")).read()
     old, new = MUTATIONS[name]
     assert old in src, f"mutation anchor for {name} not found"
-    with tempfile.TemporaryDirectory() as d:
+    with tempfile.TemporaryDirectory(prefix="_mut_", dir=MUT_DIR) as d:
         p = os.path.join(d, "mut.c")
         with open(p, "w") as f:
             f.write(src.replace(old, new))
