@@ -320,10 +320,10 @@ MUTATIONS = {
     "causal_off_by_one": ("const int pos = context + (r - r0);",
                           "const int pos = context + (r - r0) - 1;"),
     "scale_dropped": ("x[j] = scale * dot;", "x[j] = dot;"),
-    "k_read_from_v": ("K[dst] = bf16_bits_to_double(kv_cache[pool_index(\n"
-                      "                                block, 0,",
-                      "K[dst] = bf16_bits_to_double(kv_cache[pool_index(\n"
-                      "                                block, 1,"),
+    "k_read_from_v": ("K[dst] = pool_value(kv_cache, kv_fp8,\n"
+                      "                                                pool_index(block, 0,",
+                      "K[dst] = pool_value(kv_cache, kv_fp8,\n"
+                      "                                                pool_index(block, 1,"),
     "no_normalisation": ("out[d] /= denom;", "out[d] /= 1.0;"),
     "offset_and_head_swapped": (
         "((((size_t)block * 2 + (size_t)kv) * (size_t)num_kv_heads + (size_t)head) *\n"
