@@ -49,9 +49,9 @@ def kv_read_bytes(seq_lens, num_kv_heads: int, head_size: int) -> int:
     return int(sum(int(L) for L in seq_lens)) * 2 * num_kv_heads * head_size * 2
 
 
-def decode_algorithmic_bytes(b) -> int:
+def decode_algorithmic_bytes(b, elem_bytes: int = 2) -> int:
     """KV read + q read + out write + tables and lengths read, per decode launch."""
-    kv = kv_read_bytes(b.seq_lens.tolist(), b.num_kv_heads, b.head_size)
+    kv = kv_read_bytes(b.seq_lens.tolist(), b.num_kv_heads, b.head_size) * elem_bytes // 2
     qo = 2 * b.q.numel() * 2
     nblk = sum(-(-int(L) // b.block_size) for L in b.seq_lens.tolist())
     return kv + qo + nblk * 4 + b.num_seqs * 4
@@ -326,6 +326,15 @@ def run_ours(args, world, rank, local):
     binding.lib()
     stream = torch.cuda.current_stream(dev)
     out = torch.empty_like(b.q)
+    fp8 = args.kv == "fp8"
+    if fp8 and args.cascade:
+        raise SystemExit("--cascade reads a bf16 pool")
+    pool = b.kv_cache
+    if fp8:
+        from paged_kv_cache_287_gb300.workloads import FP8_K_SCALE, FP8_V_SCALE, fp8_pool_of
+        pool = fp8_pool_of(b)
+        b.kv_cache = torch.empty(0, device=dev)  # the bf16 pool is not read
+        torch.cuda.empty_cache()
     shared = b.shared_prefix_blocks * b.block_size if args.cascade else 0
     if args.cascade and not shared:
         raise SystemExit("--cascade needs a workload whose sequences share a prefix (5)")
@@ -340,16 +349,25 @@ def run_ours(args, world, rank, local):
 
     def attend(q, tables, lens, st):
         if args.cascade:
-            binding.pa_decode_cascade(out, q, b.kv_cache, tables, lens, max_len, shared, b.scale,
+            binding.pa_decode_cascade(out, q, pool, tables, lens, max_len, shared, b.scale,
                                       ws, st)
+        elif fp8:
+            binding.pa_decode_fp8(out, q, pool, tables, lens, max_len, b.scale, FP8_K_SCALE,
+                                  FP8_V_SCALE, ws, st)
         else:
-            binding.pa_decode(out, q, b.kv_cache, tables, lens, max_len, b.scale, ws, st)
+            binding.pa_decode(out, q, pool, tables, lens, max_len, b.scale, ws, st)
+
+    def write(k_new, v_new, slots, st):
+        if fp8:
+            binding.pa_cache_write_fp8(pool, k_new, v_new, slots, FP8_K_SCALE, FP8_V_SCALE, st)
+        else:
+            binding.pa_cache_write(pool, k_new, v_new, slots, st)
 
     def step(ev=None, st=None):
         st = stream if st is None else st
         if ev is not None:
             ev[0].record(st)
-        binding.pa_cache_write(b.kv_cache, b.k_new, b.v_new, b.slot_mapping, st)
+        write(b.k_new, b.v_new, b.slot_mapping, st)
         if ev is not None:
             ev[1].record(st)
         attend(b.q, b.block_tables, b.seq_lens, st)
@@ -418,8 +436,7 @@ def run_ours(args, world, rank, local):
     def e2e_step():
         for k, t in host.items():
             dev_in[k].copy_(t, non_blocking=True)
-        binding.pa_cache_write(b.kv_cache, dev_in["k_new"], dev_in["v_new"],
-                               dev_in["slot_mapping"], stream)
+        write(dev_in["k_new"], dev_in["v_new"], dev_in["slot_mapping"], stream)
         attend(dev_in["q"], dev_in["block_tables"], dev_in["seq_lens"], stream)
         out_host.copy_(out, non_blocking=True)
 
@@ -436,23 +453,29 @@ def run_ours(args, world, rank, local):
 
     if rank != 0:
         return
-    kv = kv_read_bytes(b.seq_lens.tolist(), b.num_kv_heads, b.head_size)
+    kv = kv_read_bytes(b.seq_lens.tolist(), b.num_kv_heads, b.head_size) // (2 if fp8 else 1)
     value = world * kv * args.steps / (total_ms / 1e3) / 1e9
     seqs_s = world * b.num_seqs * args.steps / (total_ms / 1e3)
     peak, peak_src = measured_peaks()
-    alg = cascade_algorithmic_bytes(b, shared) if args.cascade else decode_algorithmic_bytes(b)
+    alg = cascade_algorithmic_bytes(b, shared) if args.cascade else \
+        decode_algorithmic_bytes(b, 1 if fp8 else 2)
     achieved = alg / (decode_ms / 1e3) / 1e9
     if args.cascade:
         kernel = "pa_decode_cascade (prefix pass + suffix decode + merge kernel)"
         traffic_file = f"cascade_{b.name}.traffic.txt"
+    elif fp8:
+        kernel = "pa_decode_fp8 (split-context kernel + merge kernel)"
+        traffic_file = f"decode_fp8_{b.name}.traffic.txt"
     else:
         kernel = "pa_decode (split-context kernel + merge kernel)"
         traffic_file = f"decode_{b.name}.traffic.txt"
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16" if fp8 else "bf16",
+        "data": "synthetic",
         "config": dict(workload_config(n, args.seqs), launch="cuda-graph" if graph else "eager",
+                       kv_cache="fp8-e4m3 (per-tensor k/v scale 1/64)" if fp8 else "bf16",
                        **({"cascade_shared_len": shared} if args.cascade else {})),
         "seqs_per_s": seqs_s,
         "hbm_frac_of_step": value / world / peak,
@@ -470,7 +493,7 @@ def run_ours(args, world, rank, local):
         "clocks": clocks,
         "gpu_launches": (4 if args.cascade else 3) * args.steps,
     }
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and not fp8:
         gbs, sps, done, k, threads = cpu_oracle_rate(n)
         line["cpu_baseline"] = {"value": gbs, "unit": UNIT, "cores": threads, "kind": "oracle",
                                 "seqs_per_s": sps,
@@ -565,6 +588,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph", action="store_true",
                     help="replay one CUDA-graph-captured step per timed step")
+    ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
+                    help="KV-cache element type of the decode workloads")
     ap.add_argument("--cascade", action="store_true",
                     help="shared-prefix decode (pa_decode_cascade) on a prefix-sharing workload")
     ap.add_argument("--seqs", type=int, default=0,

@@ -84,6 +84,49 @@ pa_status pa_cache_write(void *kv_cache, int num_blocks, int block_size, int num
                          pa_stream_t stream);
 
 /*
+ * pa_kv_block_bytes_dtype - the same formula for any element size:
+ * 2 * block_size * num_kv_heads * head_size * dtype_num_bytes (§Block size);
+ * 1 for an FP8 pool.  Returns 0 for non-positive arguments.
+ */
+size_t pa_kv_block_bytes_dtype(int block_size, int num_kv_heads, int head_size,
+                               int dtype_num_bytes);
+
+/*
+ * FP8 KV cache.  The pages list FP8 among the quantisation formats the engine
+ * supports and size a block by its element bytes (§Block size); here an FP8
+ * pool has the bf16 pool's layout, [num_blocks][2][num_kv_heads][block_size]
+ * [head_size], one byte per element holding an OCP FP8 E4M3 ("e4m3fn") code,
+ * and real values are code values times a per-tensor scale: k_scale for every
+ * K element, v_scale for every V element (finite, > 0; else
+ * PA_ERR_INVALID_ARG).
+ *
+ * pa_cache_write_fp8 - pa_cache_write into an FP8 pool: element x of a new
+ * bf16 row is stored as the e4m3 code nearest to x / scale (binary32
+ * division; ties to the even code; magnitudes beyond 448 saturate to +-448).
+ * Arguments as pa_cache_write, plus k_scale / v_scale; kv_cache is the FP8
+ * pool (16-byte aligned).
+ */
+pa_status pa_cache_write_fp8(void *kv_cache, int num_blocks, int block_size, int num_kv_heads,
+                             int head_size, const void *k_new, const void *v_new,
+                             int64_t new_row_stride, const int32_t *slot_mapping, int num_tokens,
+                             float k_scale, float v_scale, pa_stream_t stream);
+
+/*
+ * pa_decode_fp8 - pa_decode over an FP8 pool: K = code value * k_scale,
+ * V = code value * v_scale.  head_size must be 128 (else PA_ERR_UNSUPPORTED).
+ * Codes convert to f16 exactly and the products run on f16 MMAs with fp32
+ * accumulation; each query head is scaled by a power of two into f16 range
+ * first (exact), P is rounded to f16.  Workspace: pa_decode_workspace_bytes.
+ * Other arguments, results and errors as pa_decode.
+ */
+pa_status pa_decode_fp8(void *out, const void *q, const void *kv_cache, int num_blocks,
+                        int block_size, int num_heads, int num_kv_heads, int head_size,
+                        const int32_t *block_tables, int max_blocks_per_seq,
+                        const int32_t *seq_lens, int num_seqs, int max_seq_len, float scale,
+                        float k_scale, float v_scale, void *workspace, size_t workspace_bytes,
+                        pa_stream_t stream);
+
+/*
  * Workspace pa_decode needs on the current device for this shape, in bytes
  * (partial softmax states of split contexts plus a small table).  Depends on
  * the device's SM count.  Returns 0 for invalid arguments.

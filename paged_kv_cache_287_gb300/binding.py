@@ -22,7 +22,8 @@ STATUS = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_E
           4: "PA_ERR_OOB", 5: "PA_ERR_TIMEOUT", 6: "PA_ERR_WORKSPACE"}
 
 # Every symbol include/pa.h declares.
-EXPORTS = ("pa_status_string", "pa_kv_block_bytes", "pa_cache_write",
+EXPORTS = ("pa_status_string", "pa_kv_block_bytes", "pa_kv_block_bytes_dtype", "pa_cache_write",
+           "pa_cache_write_fp8", "pa_decode_fp8",
            "pa_decode_workspace_bytes", "pa_decode", "pa_decode_noalloc",
            "pa_decode_cascade_workspace_bytes", "pa_decode_cascade", "pa_prefill_chunk",
            "pa_error_check")
@@ -52,6 +53,14 @@ def lib(path: Optional[str] = None):
     L.pa_status_string.argtypes = [i]
     L.pa_kv_block_bytes.restype = sz
     L.pa_kv_block_bytes.argtypes = [i, i, i]
+    L.pa_kv_block_bytes_dtype.restype = sz
+    L.pa_kv_block_bytes_dtype.argtypes = [i, i, i, i]
+    L.pa_cache_write_fp8.restype = i
+    L.pa_cache_write_fp8.argtypes = [P, i, i, i, i, P, P, i64, P, i, ctypes.c_float,
+                                     ctypes.c_float, P]
+    L.pa_decode_fp8.restype = i
+    L.pa_decode_fp8.argtypes = [P, P, P, i, i, i, i, i, P, i, P, i, i, ctypes.c_float,
+                                ctypes.c_float, ctypes.c_float, P, sz, P]
     L.pa_cache_write.restype = i
     L.pa_cache_write.argtypes = [P, i, i, i, i, P, P, i64, P, i, P]
     L.pa_decode_workspace_bytes.restype = sz
@@ -123,6 +132,58 @@ def pa_cache_write(kv_cache: torch.Tensor, k_new: torch.Tensor, v_new: torch.Ten
     _check(lib().pa_cache_write(kv_cache.data_ptr(), NB, bs, Hkv, D, k_new.data_ptr(),
                                 v_new.data_ptr(), Hkv * D, slot_mapping.data_ptr(), N,
                                 _stream(stream)), "pa_cache_write")
+
+
+def _pool8_geom(kv_cache: torch.Tensor):
+    _need(kv_cache, "kv_cache", torch.uint8, 5)
+    NB, two, Hkv, bs, D = kv_cache.shape
+    if two != 2:
+        raise ValueError("kv_cache must be [num_blocks, 2, num_kv_heads, block_size, head_size]")
+    return NB, bs, Hkv, D
+
+
+def pa_kv_block_bytes_dtype(block_size: int, num_kv_heads: int, head_size: int,
+                            dtype_num_bytes: int) -> int:
+    return int(lib().pa_kv_block_bytes_dtype(block_size, num_kv_heads, head_size,
+                                             dtype_num_bytes))
+
+
+def pa_cache_write_fp8(kv_cache: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                       slot_mapping: torch.Tensor, k_scale: float, v_scale: float,
+                       stream=None) -> None:
+    """Quantise bf16 k_new/v_new [N, Hkv, D] into an FP8 (uint8 e4m3 codes) pool."""
+    NB, bs, Hkv, D = _pool8_geom(kv_cache)
+    _need(k_new, "k_new", torch.bfloat16, 3)
+    _need(v_new, "v_new", torch.bfloat16, 3)
+    _need(slot_mapping, "slot_mapping", torch.int32, 1)
+    N = slot_mapping.shape[0]
+    if k_new.shape != (N, Hkv, D) or v_new.shape != (N, Hkv, D):
+        raise ValueError("k_new/v_new must be [num_tokens, num_kv_heads, head_size]")
+    _check(lib().pa_cache_write_fp8(kv_cache.data_ptr(), NB, bs, Hkv, D, k_new.data_ptr(),
+                                    v_new.data_ptr(), Hkv * D, slot_mapping.data_ptr(), N,
+                                    float(k_scale), float(v_scale), _stream(stream)),
+           "pa_cache_write_fp8")
+
+
+def pa_decode_fp8(out: torch.Tensor, q: torch.Tensor, kv_cache: torch.Tensor,
+                  block_tables: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                  scale: float, k_scale: float, v_scale: float, workspace: torch.Tensor,
+                  stream=None) -> None:
+    """Decode attention over an FP8 pool (uint8 e4m3 codes times k_scale / v_scale)."""
+    NB, bs, Hkv, D = _pool8_geom(kv_cache)
+    _need(q, "q", torch.bfloat16, 3)
+    _need(out, "out", torch.bfloat16, 3)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(workspace, "workspace", torch.uint8, 1)
+    B, Hq, Dq = q.shape
+    if Dq != D or out.shape != q.shape or seq_lens.shape[0] != B or block_tables.shape[0] != B:
+        raise ValueError("inconsistent decode shapes")
+    _check(lib().pa_decode_fp8(out.data_ptr(), q.data_ptr(), kv_cache.data_ptr(), NB, bs, Hq,
+                               Hkv, D, block_tables.data_ptr(), block_tables.shape[1],
+                               seq_lens.data_ptr(), B, int(max_seq_len), float(scale),
+                               float(k_scale), float(v_scale), workspace.data_ptr(),
+                               workspace.numel(), _stream(stream)), "pa_decode_fp8")
 
 
 def pa_decode_workspace_bytes(num_seqs: int, num_heads: int, num_kv_heads: int,

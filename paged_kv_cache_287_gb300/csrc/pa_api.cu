@@ -46,6 +46,21 @@ bool encode_kv_map(CUtensorMap *map, const void *kv_cache, const KvGeom &g, int 
     return r == CUDA_SUCCESS;
 }
 
+bool encode_kv_map_fp8(CUtensorMap *map, const void *kv_cache, const KvGeom &g, int box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn || g.head_size != 128) return false;
+    const cuuint64_t rows =
+        (cuuint64_t)g.num_blocks * 2u * (cuuint64_t)g.num_kv_heads * (cuuint64_t)g.block_size;
+    cuuint64_t dims[2] = {(cuuint64_t)g.head_size, rows};
+    cuuint64_t strides[1] = {(cuuint64_t)g.head_size};
+    cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(kv_cache), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace pa
 
 namespace {
@@ -115,6 +130,65 @@ pa_status pa_cache_write(void *kv_cache, int num_blocks, int block_size, int num
     return from_cuda(pa::launch_cache_write(kv_cache, g, k_new, v_new, new_row_stride,
                                             slot_mapping, num_tokens,
                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t pa_kv_block_bytes_dtype(int block_size, int num_kv_heads, int head_size,
+                               int dtype_num_bytes) {
+    if (block_size <= 0 || num_kv_heads <= 0 || head_size <= 0 || dtype_num_bytes <= 0) return 0;
+    return (size_t)2 * (size_t)block_size * (size_t)num_kv_heads * (size_t)head_size *
+           (size_t)dtype_num_bytes;
+}
+
+static bool good_scale(float s) { return s == s && s > 0.f && s < 3.0e38f; }
+
+pa_status pa_cache_write_fp8(void *kv_cache, int num_blocks, int block_size, int num_kv_heads,
+                             int head_size, const void *k_new, const void *v_new,
+                             int64_t new_row_stride, const int32_t *slot_mapping, int num_tokens,
+                             float k_scale, float v_scale, pa_stream_t stream) {
+    pa_status st = check_pool(kv_cache, num_blocks, block_size, num_kv_heads, head_size);
+    if (st != PA_OK) return st;
+    if (num_tokens < 0 || !good_scale(k_scale) || !good_scale(v_scale)) return PA_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PA_OK;
+    if (!k_new || !v_new || !slot_mapping || !aligned(k_new, 16) || !aligned(v_new, 16) ||
+        !aligned(slot_mapping, 4))
+        return PA_ERR_INVALID_ARG;
+    if (new_row_stride < (int64_t)num_kv_heads * head_size || new_row_stride % 8 != 0)
+        return PA_ERR_INVALID_ARG;
+    pa::KvGeom g{num_blocks, block_size, num_kv_heads, head_size};
+    return from_cuda(pa::launch_cache_write_fp8(kv_cache, g, k_new, v_new, new_row_stride,
+                                                slot_mapping, num_tokens, k_scale, v_scale,
+                                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
+pa_status pa_decode_fp8(void *out, const void *q, const void *kv_cache, int num_blocks,
+                        int block_size, int num_heads, int num_kv_heads, int head_size,
+                        const int32_t *block_tables, int max_blocks_per_seq,
+                        const int32_t *seq_lens, int num_seqs, int max_seq_len, float scale,
+                        float k_scale, float v_scale, void *workspace, size_t workspace_bytes,
+                        pa_stream_t stream) {
+    pa_status st = check_pool(kv_cache, num_blocks, block_size, num_kv_heads, head_size);
+    if (st != PA_OK) return st;
+    if ((st = check_heads(num_heads, num_kv_heads)) != PA_OK) return st;
+    if (head_size != 128) return PA_ERR_UNSUPPORTED;
+    if (num_seqs < 0 || max_seq_len < 0 || max_blocks_per_seq <= 0) return PA_ERR_INVALID_ARG;
+    if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f) return PA_ERR_INVALID_ARG;
+    if (!good_scale(k_scale) || !good_scale(v_scale)) return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !q || !block_tables || !seq_lens || !aligned(out, 16) || !aligned(q, 16) ||
+        !aligned(block_tables, 4) || !aligned(seq_lens, 4))
+        return PA_ERR_INVALID_ARG;
+    if (max_seq_len > max_blocks_per_seq * block_size) return PA_ERR_INVALID_ARG;
+    if (num_seqs > pa::decode_max_seqs(head_size, num_heads / num_kv_heads, true))
+        return PA_ERR_UNSUPPORTED;
+    if ((long long)num_seqs * num_kv_heads * (((long long)max_seq_len + 15) / 16) >= (1LL << 31))
+        return PA_ERR_UNSUPPORTED;
+    const size_t need = pa::decode_workspace_bytes(num_seqs, head_size, pa::device_sm_count());
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return PA_ERR_WORKSPACE;
+    pa::KvGeom g{num_blocks, block_size, num_kv_heads, head_size};
+    return from_cuda(pa::launch_decode_fp8(out, q, kv_cache, g, num_heads, block_tables,
+                                           max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
+                                           scale, k_scale, v_scale, workspace,
+                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, int head_size) {

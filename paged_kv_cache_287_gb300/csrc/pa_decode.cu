@@ -46,14 +46,20 @@ constexpr int kTile = 16;                        // tokens per tile (the MMA's M
 constexpr int kHeadsPad = 8;                     // query heads per KV head, padded to the MMA's N
 constexpr int kDecodeWarps = PA_DECODE_WARPS;
 constexpr int kDecodeStages = PA_DECODE_STAGES;
+// An FP8 tile is half the bytes, so an FP8 pool gets twice the stages to keep the
+// same bytes in flight per warp.
+constexpr int kDecodeStagesFp8 = 2 * PA_DECODE_STAGES;
 // The running max used as the exponent reference is only raised when a score
 // exceeds it by more than this (log2 units), so P stays <= 2^8 and the
 // accumulator is rescaled rarely.
 constexpr float kRescaleSlack = 8.0f;
 
-template <int D>
+// KV8: an FP8 pool (one e4m3 byte per element) instead of bf16.
+template <int D, bool KV8 = false>
 struct Lay {
-    static constexpr int kPanels = D / 64;             // 128-byte-wide column panels
+    static constexpr int kElemBytes = KV8 ? 1 : 2;
+    static constexpr int kElemsPerPanel = 128 / kElemBytes;  // elements in a 128-byte row
+    static constexpr int kPanels = D * kElemBytes / 128;     // 128-byte-wide column panels
     static constexpr int kPanelBytes = kTile * 128;    // 16 rows of one panel
     static constexpr int kKvBytes = kPanels * kPanelBytes;
 };
@@ -77,6 +83,7 @@ struct DecodeArgs {
     int total_warps;
     int stage_bytes;   // 2 * K/V tile bytes + query slot
     float scale_log2;  // scale * log2(e)
+    float k_scale, v_scale;  // FP8 pool: real K/V = e4m3 value * scale (1 for bf16)
     // Cascade: each sequence's tokens [0, shared_len) were attended by the prefix
     // pass, whose pre_splits unnormalised partials per (sequence, query head) are
     // folded in here; this kernel covers tokens [shared_len, seq_len).
@@ -88,11 +95,11 @@ struct DecodeArgs {
 
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-template <int D>
+template <int D, bool KV8 = false, int S = kDecodeStages>
 __host__ __device__ constexpr size_t decode_smem_bytes(int num_seqs, int group) {
     return 1024 /* alignment slack */ +
-           (size_t)kDecodeWarps * kDecodeStages * (2 * Lay<D>::kKvBytes + q_slot_bytes(group, D)) +
-           (size_t)kDecodeWarps * kDecodeStages * 8 + (size_t)(2 * num_seqs + 1) * 4;
+           (size_t)kDecodeWarps * S * (2 * Lay<D, KV8>::kKvBytes + q_slot_bytes(group, D)) +
+           (size_t)kDecodeWarps * S * 8 + (size_t)(2 * num_seqs + 1) * 4;
 }
 
 // TMA row of (block, K, head, offset) in the pool viewed as rows of head_size.
@@ -104,10 +111,10 @@ __device__ __forceinline__ int kv_row(int blk, int h, int off, const DecodeArgs 
     return ((blk * 2) * a.num_kv_heads + h) * a.block_size + off;
 }
 
-template <int D, int W, int S>
+template <int D, int W, int S, bool KV8>
 __global__ void __launch_bounds__(W * 32, 1)
     decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
-    using L = Lay<D>;
+    using L = Lay<D, KV8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(align_up(reinterpret_cast<size_t>(smem_raw), 1024));
     const int stage_bytes = a.stage_bytes;
@@ -236,14 +243,15 @@ __global__ void __launch_bounds__(W * 32, 1)
             mbar_arrive_expect_tx(bar, bytes);
 #pragma unroll
             for (int p = 0; p < L::kPanels; ++p) {
-                tma_load_2d_hint(stg + p * L::kPanelBytes, &kv_map, bar, 64 * p, rk0, policy);
-                tma_load_2d_hint(stg + L::kKvBytes + p * L::kPanelBytes, &kv_map, bar, 64 * p,
+                const int x = L::kElemsPerPanel * p;
+                tma_load_2d_hint(stg + p * L::kPanelBytes, &kv_map, bar, x, rk0, policy);
+                tma_load_2d_hint(stg + L::kKvBytes + p * L::kPanelBytes, &kv_map, bar, x,
                                  rk0 + v_row_off, policy);
                 if (rk1 >= 0) {
-                    tma_load_2d_hint(stg + p * L::kPanelBytes + bs * 128, &kv_map, bar, 64 * p,
-                                     rk1, policy);
+                    tma_load_2d_hint(stg + p * L::kPanelBytes + bs * 128, &kv_map, bar, x, rk1,
+                                     policy);
                     tma_load_2d_hint(stg + L::kKvBytes + p * L::kPanelBytes + bs * 128, &kv_map,
-                                     bar, 64 * p, rk1 + v_row_off, policy);
+                                     bar, x, rk1 + v_row_off, policy);
                 }
             }
             if (new_seg) {
@@ -260,12 +268,21 @@ __global__ void __launch_bounds__(W * 32, 1)
 
     float acc[D / 16][4];
     uint32_t qf[D / 16][2];
+    // Score multipliers (log2 units) of this lane's two score columns (query
+    // heads 2t, 2t+1): scale*log2(e), times, for an FP8 pool, k_scale and the
+    // power of two that brought the head's query into f16 range.
+    float cs0 = a.scale_log2, cs1 = a.scale_log2;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     int prev_seg = -1, first_j = 0;
     bool first_piece = true;
     const int hq_row = lane >> 2;          // query head (MMA column) this lane feeds
     const int hh0 = 2 * (lane & 3);        // query heads whose results this lane holds
     const int tr0 = lane >> 2;             // tokens whose scores this lane holds: tr0, tr0+8
+    // Output dim of accumulator row tr0 (+8 if hi) of MMA tile mt.
+    auto dim_of = [&](int mt, int hi) {
+        if constexpr (KV8) return 32 * (mt >> 1) + 4 * tr0 + 2 * (mt & 1) + hi;
+        return mt * 16 + tr0 + 8 * hi;
+    };
 
     for (int c = 0; c < n; ++c) {
         const int st = c % S;
@@ -288,16 +305,55 @@ __global__ void __launch_bounds__(W * 32, 1)
         const int s = seg >> 8, h = seg & 255;
         const __nv_bfloat16 *qslot = reinterpret_cast<const __nv_bfloat16 *>(stg + 2 * L::kKvBytes);
         if (seg != prev_seg) {
+            if constexpr (!KV8) {
 #pragma unroll
-            for (int k = 0; k < D / 16; ++k) {
-                if (hq_row < G) {
-                    const __nv_bfloat16 *qr = qslot + hq_row * D + 16 * k + 2 * (lane & 3);
-                    qf[k][0] = *reinterpret_cast<const uint32_t *>(qr);
-                    qf[k][1] = *reinterpret_cast<const uint32_t *>(qr + 8);
-                } else {
-                    qf[k][0] = 0u;
-                    qf[k][1] = 0u;
+                for (int k = 0; k < D / 16; ++k) {
+                    if (hq_row < G) {
+                        const __nv_bfloat16 *qr = qslot + hq_row * D + 16 * k + 2 * (lane & 3);
+                        qf[k][0] = *reinterpret_cast<const uint32_t *>(qr);
+                        qf[k][1] = *reinterpret_cast<const uint32_t *>(qr + 8);
+                    } else {
+                        qf[k][0] = 0u;
+                        qf[k][1] = 0u;
+                    }
                 }
+            } else {
+                // f16 operands.  The K fragment of MMA k-slots (2t, 2t+1, 2t+8, 2t+9)
+                // holds dims 4t..4t+3 of each 16-dim chunk (one 32-bit word of e4m3
+                // codes), so the query fragment takes the same dims.  Each head's
+                // query is scaled by a power of two into [1, 2) at its largest
+                // element (exact; f16 keeps every bf16 significand), and the
+                // scores are scaled back.
+                float qv[D / 16][4];
+                float mx = 0.f;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    uint2 w = make_uint2(0u, 0u);
+                    if (hq_row < G)
+                        w = *reinterpret_cast<const uint2 *>(qslot + hq_row * D + 16 * k +
+                                                             4 * (lane & 3));
+                    qv[k][0] = bf16_lo(w.x);
+                    qv[k][1] = bf16_hi(w.x);
+                    qv[k][2] = bf16_lo(w.y);
+                    qv[k][3] = bf16_hi(w.y);
+                    mx = fmax3(mx, fabsf(qv[k][0]), fabsf(qv[k][1]));
+                    mx = fmax3(mx, fabsf(qv[k][2]), fabsf(qv[k][3]));
+                }
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                int ex = mx > 0.f ? (int)((__float_as_uint(mx) >> 23) & 0xffu) - 127 : 0;
+                ex = max(-126, min(126, ex));
+                const float down = __uint_as_float((uint32_t)(127 - ex) << 23);  // 2^-ex
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    qf[k][0] = pack_f16(qv[k][0] * down, qv[k][1] * down);
+                    qf[k][1] = pack_f16(qv[k][2] * down, qv[k][3] * down);
+                }
+                const int e0 = __shfl_sync(0xffffffffu, ex, 4 * hh0);
+                const int e1 = __shfl_sync(0xffffffffu, ex, 4 * (hh0 + 1));
+                const float base = a.scale_log2 * a.k_scale;
+                cs0 = base * __uint_as_float((uint32_t)(127 + e0) << 23);
+                cs1 = base * __uint_as_float((uint32_t)(127 + e1) << 23);
             }
 #pragma unroll
             for (int mt = 0; mt < D / 16; ++mt)
@@ -329,23 +385,43 @@ __global__ void __launch_bounds__(W * 32, 1)
         float sc[4] = {0.f, 0.f, 0.f, 0.f};
         float sd[4] = {0.f, 0.f, 0.f, 0.f};
         const uint32_t kbase = smem_u32(stg);
+        if constexpr (!KV8) {
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-            const uint32_t panel = kbase + (k >> 2) * L::kPanelBytes;
+            for (int k = 0; k < D / 16; ++k) {
+                const uint32_t panel = kbase + (k >> 2) * L::kPanelBytes;
+                const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
+                const int chunk = 2 * (k & 3) + (lane >> 4);
+                uint32_t af[4];
+                ldsm_x4(af, swz128(panel, row, chunk));
+                if (k & 1)
+                    mma_bf16(sd, af, qf[k][0], qf[k][1]);
+                else
+                    mma_bf16(sc, af, qf[k][0], qf[k][1]);
+            }
+        } else {
+            // One ldmatrix.x4 reads 16 tokens x 32 dims of e4m3 codes: per lane a
+            // word of 4 codes (dims 4t..4t+3 of a 16-dim chunk) for tokens g, g+8
+            // and two chunks; each word becomes the f16 pairs of MMA k-slots
+            // (2t, 2t+1) and (2t+8, 2t+9).
             const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
-            const int chunk = 2 * (k & 3) + (lane >> 4);
-            uint32_t af[4];
-            ldsm_x4(af, swz128(panel, row, chunk));
-            if (k & 1)
-                mma_bf16(sd, af, qf[k][0], qf[k][1]);
-            else
-                mma_bf16(sc, af, qf[k][0], qf[k][1]);
+#pragma unroll
+            for (int k2 = 0; k2 < D / 32; ++k2) {
+                uint32_t w[4];
+                ldsm_x4(w, swz128(kbase, row, 2 * k2 + (lane >> 4)));
+                uint32_t af[4], ag[4];
+                e4m3x4_to_f16x4(w[0], af[0], af[2]);
+                e4m3x4_to_f16x4(w[1], af[1], af[3]);
+                e4m3x4_to_f16x4(w[2], ag[0], ag[2]);
+                e4m3x4_to_f16x4(w[3], ag[1], ag[3]);
+                mma_f16(sc, af, qf[2 * k2][0], qf[2 * k2][1]);
+                mma_f16(sd, ag, qf[2 * k2 + 1][0], qf[2 * k2 + 1][1]);
+            }
         }
 #pragma unroll
         for (int e = 0; e < 4; ++e) sc[e] += sd[e];
         // Scores in log2 units; tokens past the sequence end get -inf.
-        float x0 = sc[0] * a.scale_log2, x1 = sc[1] * a.scale_log2;
-        float x2 = sc[2] * a.scale_log2, x3 = sc[3] * a.scale_log2;
+        float x0 = sc[0] * cs0, x1 = sc[1] * cs1;
+        float x2 = sc[2] * cs0, x3 = sc[3] * cs1;
         if (valid < kTile) {
             if (tr0 >= valid) x0 = x1 = -INFINITY;
             if (tr0 + 8 >= valid) x2 = x3 = -INFINITY;
@@ -369,12 +445,20 @@ __global__ void __launch_bounds__(W * 32, 1)
             m0 = mn0;
             m1 = mn1;
         }
-        const uint32_t plo = pack_bf16(fast_exp2(x0 - m0), fast_exp2(x1 - m1));
-        const uint32_t phi = pack_bf16(fast_exp2(x2 - m0), fast_exp2(x3 - m1));
-        // Per-lane partial sums of the bf16 P actually multiplied; the head's 8
+        // Per-lane partial sums of the rounded P actually multiplied; the head's 8
         // lanes are summed once, at the end of the segment.
-        l0 = l0 * cr0 + (bf16_lo(plo) + bf16_lo(phi));
-        l1 = l1 * cr1 + (bf16_hi(plo) + bf16_hi(phi));
+        uint32_t plo, phi;
+        if constexpr (!KV8) {
+            plo = pack_bf16(fast_exp2(x0 - m0), fast_exp2(x1 - m1));
+            phi = pack_bf16(fast_exp2(x2 - m0), fast_exp2(x3 - m1));
+            l0 = l0 * cr0 + (bf16_lo(plo) + bf16_lo(phi));
+            l1 = l1 * cr1 + (bf16_hi(plo) + bf16_hi(phi));
+        } else {
+            plo = pack_f16(fast_exp2(x0 - m0), fast_exp2(x1 - m1));
+            phi = pack_f16(fast_exp2(x2 - m0), fast_exp2(x3 - m1));
+            l0 = l0 * cr0 + (f16_lo(plo) + f16_lo(phi));
+            l1 = l1 * cr1 + (f16_hi(plo) + f16_hi(phi));
+        }
         const uint32_t b0 = movmatrix_t(plo), b1 = movmatrix_t(phi);
 
         // O^T[dim][head] += V^T . P^T
@@ -388,15 +472,46 @@ __global__ void __launch_bounds__(W * 32, 1)
                 acc[mt][3] *= cr1;
             }
         }
+        if constexpr (!KV8) {
 #pragma unroll
-        for (int mt = 0; mt < D / 16; ++mt) {
-            const uint32_t panel = vbase + (mt >> 2) * L::kPanelBytes;
-            const int mi = lane >> 3;
-            const int row = (lane & 7) + (mi >> 1) * 8;
-            const int chunk = 2 * (mt & 3) + (mi & 1);
-            uint32_t af[4];
-            ldsm_x4_t(af, swz128(panel, row, chunk));
-            mma_bf16(acc[mt], af, b0, b1);
+            for (int mt = 0; mt < D / 16; ++mt) {
+                const uint32_t panel = vbase + (mt >> 2) * L::kPanelBytes;
+                const int mi = lane >> 3;
+                const int row = (lane & 7) + (mi >> 1) * 8;
+                const int chunk = 2 * (mt & 3) + (mi & 1);
+                uint32_t af[4];
+                ldsm_x4_t(af, swz128(panel, row, chunk));
+                mma_bf16(acc[mt], af, b0, b1);
+            }
+        } else {
+            // V^T fragments from e4m3 codes.  MMA row m of tile mt stands for dim
+            // 32*(mt/2) + 4*(m%8) + 2*(mt%2) + m/8, so a lane (m%8 = g) needs dims
+            // 32*q + 4g .. 4g+3 of its four tokens 2t, 2t+1, 2t+8, 2t+9 (the
+            // k-slots of P^T): four 32-bit loads per 32 dims, a 4x4 byte
+            // transpose, and each (dim, token pair) becomes one f16 pair.
+            const int t2 = 2 * (lane & 3), g = lane >> 2;
+#pragma unroll
+            for (int q = 0; q < D / 32; ++q) {
+                const uint32_t off = (uint32_t)(g & 3) << 2;
+                const int chunk = 2 * q + (g >> 2);
+                uint32_t w0, w1, w2, w3;
+                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w0) : "r"(swz128(vbase, t2, chunk) + off));
+                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w1) : "r"(swz128(vbase, t2 + 1, chunk) + off));
+                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w2) : "r"(swz128(vbase, t2 + 8, chunk) + off));
+                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w3) : "r"(swz128(vbase, t2 + 9, chunk) + off));
+                const uint32_t u0 = prmt(w0, w1, 0x5140u), u1 = prmt(w0, w1, 0x7362u);
+                const uint32_t u2 = prmt(w2, w3, 0x5140u), u3 = prmt(w2, w3, 0x7362u);
+                // d_j = codes of dim 32q + 4g + j for tokens (2t, 2t+1, 2t+8, 2t+9)
+                const uint32_t d0 = prmt(u0, u2, 0x5410u), d1 = prmt(u0, u2, 0x7632u);
+                const uint32_t d2 = prmt(u1, u3, 0x5410u), d3 = prmt(u1, u3, 0x7632u);
+                uint32_t af[4], ag[4];
+                e4m3x4_to_f16x4(d0, af[0], af[2]);  // row g: dim 4g + 0
+                e4m3x4_to_f16x4(d1, af[1], af[3]);  // row g + 8: dim 4g + 1
+                e4m3x4_to_f16x4(d2, ag[0], ag[2]);  // tile 2q + 1, row g: dim 4g + 2
+                e4m3x4_to_f16x4(d3, ag[1], ag[3]);  // tile 2q + 1, row g + 8: dim 4g + 3
+                mma_f16(acc[2 * q], af, b0, b1);
+                mma_f16(acc[2 * q + 1], ag, b0, b1);
+            }
         }
 
         if (next_seg != seg) {
@@ -404,6 +519,12 @@ __global__ void __launch_bounds__(W * 32, 1)
             for (int o = 4; o < 32; o <<= 1) {
                 l0 += __shfl_xor_sync(0xffffffffu, l0, o);
                 l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+            }
+            if constexpr (KV8) {
+#pragma unroll
+                for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[mt][e] *= a.v_scale;
             }
             const int nt = s_pre[s + 1] - s_pre[s];
             if (first_j == 0 && j == nt - 1) {
@@ -437,8 +558,8 @@ __global__ void __launch_bounds__(W * 32, 1)
                             l0 += wk * ml.y;
 #pragma unroll
                             for (int mt = 0; mt < D / 16; ++mt) {
-                                acc[mt][0] += wk * pa[mt * 16 + tr0];
-                                acc[mt][2] += wk * pa[mt * 16 + tr0 + 8];
+                                acc[mt][0] += wk * pa[dim_of(mt, 0)];
+                                acc[mt][2] += wk * pa[dim_of(mt, 1)];
                             }
                         }
                         if (w1) {
@@ -448,8 +569,8 @@ __global__ void __launch_bounds__(W * 32, 1)
                             l1 += wk * ml.y;
 #pragma unroll
                             for (int mt = 0; mt < D / 16; ++mt) {
-                                acc[mt][1] += wk * pa[mt * 16 + tr0];
-                                acc[mt][3] += wk * pa[mt * 16 + tr0 + 8];
+                                acc[mt][1] += wk * pa[dim_of(mt, 0)];
+                                acc[mt][3] += wk * pa[dim_of(mt, 1)];
                             }
                         }
                     }
@@ -463,14 +584,14 @@ __global__ void __launch_bounds__(W * 32, 1)
                 const bool w0 = hh0 < G, w1 = hh0 + 1 < G;
 #pragma unroll
                 for (int mt = 0; mt < D / 16; ++mt) {
-                    const int d0 = mt * 16 + tr0;
+                    const int d0 = dim_of(mt, 0), d1 = dim_of(mt, 1);
                     if (w0) {
                         stage_out[hh0 * D + d0] = __float2bfloat16_rn(acc[mt][0] * i0);
-                        stage_out[hh0 * D + d0 + 8] = __float2bfloat16_rn(acc[mt][2] * i0);
+                        stage_out[hh0 * D + d1] = __float2bfloat16_rn(acc[mt][2] * i0);
                     }
                     if (w1) {
                         stage_out[(hh0 + 1) * D + d0] = __float2bfloat16_rn(acc[mt][1] * i1);
-                        stage_out[(hh0 + 1) * D + d0 + 8] = __float2bfloat16_rn(acc[mt][3] * i1);
+                        stage_out[(hh0 + 1) * D + d1] = __float2bfloat16_rn(acc[mt][3] * i1);
                     }
                 }
                 __syncwarp();
@@ -484,11 +605,11 @@ __global__ void __launch_bounds__(W * 32, 1)
                 float *pacc = a.part_acc + rec * kHeadsPad * D;
 #pragma unroll
                 for (int mt = 0; mt < D / 16; ++mt) {
-                    const int d0 = mt * 16 + tr0;
+                    const int d0 = dim_of(mt, 0), d1 = dim_of(mt, 1);
                     pacc[hh0 * D + d0] = acc[mt][0];
                     pacc[(hh0 + 1) * D + d0] = acc[mt][1];
-                    pacc[hh0 * D + d0 + 8] = acc[mt][2];
-                    pacc[(hh0 + 1) * D + d0 + 8] = acc[mt][3];
+                    pacc[hh0 * D + d1] = acc[mt][2];
+                    pacc[(hh0 + 1) * D + d1] = acc[mt][3];
                 }
                 if (lane < 4) {
                     float *pml = a.part_ml + rec * kHeadsPad * 2;
@@ -615,10 +736,12 @@ __global__ void __launch_bounds__(kHeadsPad * D / 4) decode_merge_kernel(const D
     orow[d4] = make_uint2(pack_bf16(num.x * inv, num.y * inv), pack_bf16(num.z * inv, num.w * inv));
 }
 
-template <int D>
+template <int D, bool KV8>
 cudaError_t launch_decode_d(const DecodeArgs &a0, const CUtensorMap &map, int grid,
-                            size_t smem, cudaStream_t stream) {
-    auto kern = decode_kernel<D, kDecodeWarps, kDecodeStages>;
+                            cudaStream_t stream) {
+    constexpr int S = KV8 ? kDecodeStagesFp8 : kDecodeStages;
+    const size_t smem = decode_smem_bytes<D, KV8, S>(a0.num_seqs, a0.group);
+    auto kern = decode_kernel<D, kDecodeWarps, S, KV8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
@@ -640,10 +763,11 @@ cudaError_t launch_decode_d(const DecodeArgs &a0, const CUtensorMap &map, int gr
 
 }  // namespace
 
-int decode_max_seqs(int head_size, int group) {
+int decode_max_seqs(int head_size, int group, bool kv8) {
     const size_t limit = 227 * 1024;
-    const size_t fixed =
-        head_size == 128 ? decode_smem_bytes<128>(0, group) : decode_smem_bytes<64>(0, group);
+    const size_t fixed = kv8 ? decode_smem_bytes<128, true, kDecodeStagesFp8>(0, group)
+                         : head_size == 128 ? decode_smem_bytes<128>(0, group)
+                                            : decode_smem_bytes<64>(0, group);
     return fixed >= limit ? 0 : (int)((limit - fixed) / 8);
 }
 
@@ -666,11 +790,14 @@ cudaError_t launch_decode_impl(void *out, const void *q, const void *kv_cache, c
                                int num_heads, const int32_t *block_tables, int max_blocks_per_seq,
                                const int32_t *seq_lens, int num_seqs, int max_seq_len,
                                int shared_len, float scale, void *workspace, const float *pre_ml,
-                               const float *pre_acc, int pre_splits, cudaStream_t stream) {
+                               const float *pre_acc, int pre_splits, bool kv8, float k_scale,
+                               float v_scale, cudaStream_t stream) {
     const int sms = device_sm_count();
     const int D = g.head_size;
     CUtensorMap map;
-    if (!encode_kv_map(&map, kv_cache, g, g.block_size >= kTile ? kTile : g.block_size))
+    const int box_rows = g.block_size >= kTile ? kTile : g.block_size;
+    if (!(kv8 ? encode_kv_map_fp8(&map, kv_cache, g, box_rows)
+              : encode_kv_map(&map, kv_cache, g, box_rows)))
         return cudaErrorInvalidValue;
     // As many warps as there can be tiles, at most one CTA per SM.  A warp has a
     // single stage, so a small batch finishes soonest with one tile per warp; a
@@ -699,17 +826,17 @@ cudaError_t launch_decode_impl(void *out, const void *q, const void *kv_cache, c
     a.max_blocks = max_blocks_per_seq;
     a.num_blocks = g.num_blocks;
     a.total_warps = (int)ctas * kDecodeWarps;
-    a.stage_bytes = 2 * (D / 64) * kTile * 128 + q_slot_bytes(a.group, D);
+    a.stage_bytes = 2 * (D * (kv8 ? 1 : 2) / 128) * kTile * 128 + q_slot_bytes(a.group, D);
     a.scale_log2 = scale * 1.4426950408889634f;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
     a.shared_len = shared_len;
     a.pre_splits = pre_splits;
     a.pre_ml = pre_ml;
     a.pre_acc = pre_acc;
-    if (D == 128)
-        return launch_decode_d<128>(a, map, (int)ctas, decode_smem_bytes<128>(num_seqs, a.group),
-                                    stream);
-    return launch_decode_d<64>(a, map, (int)ctas, decode_smem_bytes<64>(num_seqs, a.group),
-                               stream);
+    if (kv8) return launch_decode_d<128, true>(a, map, (int)ctas, stream);
+    if (D == 128) return launch_decode_d<128, false>(a, map, (int)ctas, stream);
+    return launch_decode_d<64, false>(a, map, (int)ctas, stream);
 }
 
 }  // namespace
@@ -720,7 +847,16 @@ cudaError_t launch_decode(void *out, const void *q, const void *kv_cache, const 
                           void *workspace, cudaStream_t stream) {
     return launch_decode_impl(out, q, kv_cache, g, num_heads, block_tables, max_blocks_per_seq,
                               seq_lens, num_seqs, max_seq_len, 0, scale, workspace, nullptr,
-                              nullptr, 0, stream);
+                              nullptr, 0, false, 1.f, 1.f, stream);
+}
+
+cudaError_t launch_decode_fp8(void *out, const void *q, const void *kv_cache, const KvGeom &g,
+                              int num_heads, const int32_t *block_tables, int max_blocks_per_seq,
+                              const int32_t *seq_lens, int num_seqs, int max_seq_len, float scale,
+                              float k_scale, float v_scale, void *workspace, cudaStream_t stream) {
+    return launch_decode_impl(out, q, kv_cache, g, num_heads, block_tables, max_blocks_per_seq,
+                              seq_lens, num_seqs, max_seq_len, 0, scale, workspace, nullptr,
+                              nullptr, 0, true, k_scale, v_scale, stream);
 }
 
 cudaError_t launch_decode_suffix(void *out, const void *q, const void *kv_cache, const KvGeom &g,
@@ -731,7 +867,7 @@ cudaError_t launch_decode_suffix(void *out, const void *q, const void *kv_cache,
                                  cudaStream_t stream) {
     return launch_decode_impl(out, q, kv_cache, g, num_heads, block_tables, max_blocks_per_seq,
                               seq_lens, num_seqs, max_seq_len, shared_len, scale, workspace,
-                              pre_ml, pre_acc, pre_splits, stream);
+                              pre_ml, pre_acc, pre_splits, false, 1.f, 1.f, stream);
 }
 
 size_t prefix_partial_bytes(int splits, int num_seqs, int num_heads, int head_size) {

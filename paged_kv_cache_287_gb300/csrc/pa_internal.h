@@ -25,6 +25,8 @@ cudaError_t take_error_prefill(unsigned *bits);
 // Encode a 2-D TMA map over the pool viewed as rows of head_size bf16 elements,
 // box = 64 elements x box_rows rows, 128-byte swizzle.  False on failure.
 bool encode_kv_map(CUtensorMap *map, const void *kv_cache, const KvGeom &g, int box_rows);
+// The same over an FP8 pool (rows of head_size bytes), box = 128 bytes x box_rows.
+bool encode_kv_map_fp8(CUtensorMap *map, const void *kv_cache, const KvGeom &g, int box_rows);
 
 int device_sm_count();
 
@@ -34,8 +36,18 @@ cudaError_t launch_cache_write(void *kv_cache, const KvGeom &g, const void *k_ne
 
 // Decode workspace bytes for num_seqs sequences on a device with sm_count SMs.
 size_t decode_workspace_bytes(int num_seqs, int head_size, int sm_count);
-// Largest num_seqs the decode kernel's shared-memory tables hold.
-int decode_max_seqs(int head_size, int group);
+// Largest num_seqs the decode kernel's shared-memory tables hold (kv8: FP8 pool).
+int decode_max_seqs(int head_size, int group, bool kv8 = false);
+
+// FP8 pool (OCP e4m3 codes; real K/V = code value * k_scale / v_scale); head_size 128.
+cudaError_t launch_cache_write_fp8(void *kv_cache, const KvGeom &g, const void *k_new,
+                                   const void *v_new, int64_t new_row_stride,
+                                   const int32_t *slot_mapping, int num_tokens, float k_scale,
+                                   float v_scale, cudaStream_t stream);
+cudaError_t launch_decode_fp8(void *out, const void *q, const void *kv_cache, const KvGeom &g,
+                              int num_heads, const int32_t *block_tables, int max_blocks_per_seq,
+                              const int32_t *seq_lens, int num_seqs, int max_seq_len, float scale,
+                              float k_scale, float v_scale, void *workspace, cudaStream_t stream);
 
 cudaError_t launch_decode(void *out, const void *q, const void *kv_cache, const KvGeom &g,
                           int num_heads, const int32_t *block_tables, int max_blocks_per_seq,

@@ -280,3 +280,24 @@ def sample_of_config(n: int, first: int, device="cpu", seed: Optional[int] = Non
     spec.pop("num_blocks", None)
     spec["name"] = f"{spec['name']}[:{first}]"
     return make_batch(device=device, **spec)
+
+
+# Per-tensor scales of the FP8 (e4m3) pools built below: N(0,1) values divided by
+# 1/64 stay far inside the format's +-448 range, using most of its exponents.
+FP8_K_SCALE = 1.0 / 64
+FP8_V_SCALE = 1.0 / 64
+
+
+def fp8_pool_of(b: PagedBatch, k_scale: float = FP8_K_SCALE,
+                v_scale: float = FP8_V_SCALE) -> torch.Tensor:
+    """The batch's pool as an FP8 pool: uint8 OCP e4m3 codes of value / scale, in the
+    same layout, drawn through PyTorch's float8_e4m3fn cast of the values clamped
+    to +-448 (input data only; NaN poison stays NaN).  The new tokens' slots still hold NaN codes, to be written
+    by the FP8 cache write."""
+    out = torch.empty(b.kv_cache.shape, dtype=torch.uint8, device=b.kv_cache.device)
+    for side, sc in ((0, k_scale), (1, v_scale)):
+        for lo in range(0, b.num_blocks, 4096):
+            hi = min(b.num_blocks, lo + 4096)
+            x = (b.kv_cache[lo:hi, side].float() / sc).clamp(-448.0, 448.0)  # NaN stays NaN
+            out[lo:hi, side] = x.to(torch.float8_e4m3fn).view(torch.uint8)
+    return out

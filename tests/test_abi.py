@@ -109,3 +109,29 @@ def test_cascade_host_checks(lib):
     bad[11] = 0                                 # no sequences: no-op
     assert lib.pa_decode_cascade(*bad) == 0
     assert lib.pa_decode_cascade_workspace_bytes(0, 32, 8, 128, 64) == 0
+
+
+def test_fp8_host_checks(lib):
+    wr = [FAKE, 10, 16, 8, 128, FAKE, FAKE, 8 * 128, FAKE, 4, 0.5, 0.25, None]
+    bad = list(wr)
+    bad[10] = 0.0                               # k_scale must be > 0
+    assert lib.pa_cache_write_fp8(*bad) == 1
+    bad = list(wr)
+    bad[11] = float("nan")
+    assert lib.pa_cache_write_fp8(*bad) == 1
+    bad = list(wr)
+    bad[9] = 0                                  # empty: no-op
+    assert lib.pa_cache_write_fp8(*bad) == 0
+    dec = [FAKE, FAKE, FAKE, 10, 16, 32, 8, 128, FAKE, 4, FAKE, 3, 64, 0.1, 0.5, 0.5, FAKE,
+           1 << 30, None]
+    bad = list(dec)
+    bad[7] = 64                                 # head_size 64 is bf16-only
+    assert lib.pa_decode_fp8(*bad) == 2
+    bad = list(dec)
+    bad[15] = -1.0                              # v_scale must be > 0
+    assert lib.pa_decode_fp8(*bad) == 1
+    bad = list(dec)
+    bad[11] = 0                                 # no sequences: no-op
+    assert lib.pa_decode_fp8(*bad) == 0
+    assert lib.pa_kv_block_bytes_dtype(16, 8, 128, 1) == 32768
+    assert lib.pa_kv_block_bytes_dtype(16, 8, 128, 2) == lib.pa_kv_block_bytes(16, 8, 128)

@@ -1,0 +1,160 @@
+"""Parity of the FP8 (e4m3) KV-cache path with the CPU fp64 oracle.
+
+The FP8 cache write must match the oracle's quantisation bit for bit over the
+whole pool; FP8 decode must lie within the same 1e-2 max / 1e-3 mean absolute
+error of the oracle's fp64 attention over the dequantised pool as bf16 decode.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_287_gb300 import binding
+from paged_kv_cache_287_gb300.workloads import (FP8_K_SCALE, FP8_V_SCALE, fp8_pool_of,
+                                                make_batch, make_config)
+from tests._gpu import compare, workspace_for
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(autouse=True)
+def _clean_errors():
+    binding.pa_error_check()
+    yield
+    binding.pa_error_check()
+
+
+def _write(b, pool8, ks, vs):
+    want = oracle.cache_write_fp8(pool8, b.k_new, b.v_new, b.slot_mapping, ks, vs)
+    binding.pa_cache_write_fp8(pool8, b.k_new, b.v_new, b.slot_mapping, ks, vs)
+    binding.pa_error_check()
+    return want
+
+
+def _decode(b, pool8, ks, vs):
+    out = torch.full_like(b.q, float("nan"))
+    binding.pa_decode_fp8(out, b.q, pool8, b.block_tables, b.seq_lens, b.max_seq_len, b.scale,
+                          ks, vs, workspace_for(b))
+    binding.pa_error_check()
+    return out
+
+
+def _oracle(b, pool_codes, ks, vs, rows=None):
+    return oracle.attention_fp8(b.q, b.cu_q_lens, pool_codes, ks, vs, b.block_tables,
+                                b.seq_lens, b.num_heads, b.scale, rows=rows)
+
+
+WRITE_SHAPES = [
+    # seq_lens, q_lens, Hkv, D, bs
+    ([40, 7, 90], [5, 1, 33], 2, 64, 8),
+    ([33, 64, 1], [33, 3, 1], 8, 128, 16),
+    ([300], [100], 4, 128, 32),
+]
+
+
+@pytest.mark.parametrize("case", range(len(WRITE_SHAPES)))
+def test_fp8_cache_write_bit_exact(case):
+    lens, qls, Hkv, D, bs = WRITE_SHAPES[case]
+    b = make_batch(name=f"w8{case}", seq_lens=lens, q_lens=qls, num_heads=Hkv, num_kv_heads=Hkv,
+                   head_size=D, block_size=bs, scale=0.1, seed=800 + case, device=DEV)
+    pool8 = fp8_pool_of(b)
+    b.slot_mapping[1] = -1  # a padding row is skipped
+    want = _write(b, pool8, 0.05, 0.0123)
+    assert np.array_equal(pool8.cpu().numpy(), want)
+
+
+def test_fp8_cache_write_saturates_rounds_ties_and_keeps_signs():
+    b = make_batch(name="w8s", seq_lens=[16], q_lens=[16], num_heads=2, num_kv_heads=2,
+                   head_size=64, block_size=16, scale=0.1, seed=810, device=DEV)
+    pool8 = fp8_pool_of(b)
+    # Every bf16 magnitude class: huge (saturates), exact codes, ties, tiny (to +-0).
+    g = torch.Generator().manual_seed(3)
+    e = torch.randint(-40, 40, b.k_new.shape, generator=g).float()
+    x = torch.sign(torch.randn(b.k_new.shape, generator=g)) * torch.exp2(e) * \
+        (1 + torch.randint(0, 16, b.k_new.shape, generator=g).float() / 16)
+    b.k_new.copy_(x.to(torch.bfloat16).to(DEV))
+    b.v_new.copy_((-x).to(torch.bfloat16).to(DEV))
+    want = _write(b, pool8, 1.0, 0.5)
+    assert np.array_equal(pool8.cpu().numpy(), want)
+
+
+DECODE_SHAPES = [
+    # seq_lens, Hq, Hkv, bs
+    ([1, 15, 16, 17, 31, 32, 33, 100], 8, 8, 16),      # group 1
+    ([5, 64, 200, 1], 8, 4, 16),                       # group 2
+    ([129, 77, 3, 256, 40], 16, 4, 8),                 # group 4, block 8
+    ([300, 2, 63, 97], 64, 8, 32),                     # group 8, block 32
+    ([513, 1000, 17], 24, 8, 16),                      # group 3
+]
+
+
+@pytest.mark.parametrize("case", range(len(DECODE_SHAPES)))
+def test_fp8_decode_small_shapes(case):
+    lens, Hq, Hkv, bs = DECODE_SHAPES[case]
+    b = make_batch(name=f"d8{case}", seq_lens=lens, q_lens=[1] * len(lens), num_heads=Hq,
+                   num_kv_heads=Hkv, head_size=128, block_size=bs, scale=128 ** -0.5,
+                   seed=820 + case, device=DEV)
+    pool8 = fp8_pool_of(b)
+    codes = _write(b, pool8, FP8_K_SCALE, FP8_V_SCALE)
+    compare(_decode(b, pool8, FP8_K_SCALE, FP8_V_SCALE),
+            _oracle(b, codes, FP8_K_SCALE, FP8_V_SCALE), f"fp8 decode case {case}")
+
+
+@pytest.mark.parametrize("ks,vs", [(0.25, 0.003), (0.0123, 0.9)])
+def test_fp8_decode_other_scales(ks, vs):
+    b = make_batch(name="d8s", seq_lens=[400, 90, 1, 777], q_lens=[1] * 4, num_heads=32,
+                   num_kv_heads=8, head_size=128, block_size=16, scale=-0.07, seed=830,
+                   device=DEV)
+    pool8 = fp8_pool_of(b, ks, vs)
+    codes = _write(b, pool8, ks, vs)
+    compare(_decode(b, pool8, ks, vs), _oracle(b, codes, ks, vs), f"fp8 decode scales {ks} {vs}")
+
+
+def test_fp8_decode_empty_sequences_give_zeros():
+    b = make_batch(name="d8e", seq_lens=[0, 20, 0, 5], q_lens=[1] * 4, num_heads=8,
+                   num_kv_heads=2, head_size=128, block_size=16, scale=0.1, seed=840,
+                   device=DEV)
+    pool8 = fp8_pool_of(b)
+    codes = _write(b, pool8, FP8_K_SCALE, FP8_V_SCALE)
+    out = _decode(b, pool8, FP8_K_SCALE, FP8_V_SCALE)
+    compare(out, _oracle(b, codes, FP8_K_SCALE, FP8_V_SCALE), "fp8 decode, empty sequences")
+    assert (out[0] == 0).all() and (out[2] == 0).all()
+
+
+def test_fp8_decode_large_queries_stay_in_range():
+    """Queries far outside f16 range are scaled per head by a power of two."""
+    b = make_batch(name="d8q", seq_lens=[50, 300], q_lens=[1, 1], num_heads=16, num_kv_heads=4,
+                   head_size=128, block_size=16, scale=1e-6, seed=850, q_scale=1e6,
+                   device=DEV)
+    pool8 = fp8_pool_of(b)
+    codes = _write(b, pool8, FP8_K_SCALE, FP8_V_SCALE)
+    compare(_decode(b, pool8, FP8_K_SCALE, FP8_V_SCALE),
+            _oracle(b, codes, FP8_K_SCALE, FP8_V_SCALE), "fp8 decode, large queries")
+
+
+def test_fp8_decode_workload_full_size():
+    b = make_config(2, device=DEV)
+    pool8 = fp8_pool_of(b)
+    codes = _write(b, pool8, FP8_K_SCALE, FP8_V_SCALE)
+    assert np.array_equal(pool8.cpu().numpy(), codes), "fp8 cache write"
+    out = _decode(b, pool8, FP8_K_SCALE, FP8_V_SCALE)
+    rows = np.arange(0, b.num_seqs, 5, dtype=np.int32)
+    compare(out[torch.as_tensor(rows, device=DEV).long()],
+            _oracle(b, codes, FP8_K_SCALE, FP8_V_SCALE, rows), "fp8 workload 2 (sampled)")
+
+
+def test_fp8_decode_rejects_head_size_64():
+    b = make_batch(name="d8r", seq_lens=[10], q_lens=[1], num_heads=4, num_kv_heads=4,
+                   head_size=64, block_size=16, scale=0.1, seed=860, device=DEV)
+    pool8 = fp8_pool_of(b)
+    with pytest.raises(binding.PaError) as e:
+        _decode(b, pool8, 1.0, 1.0)
+    assert e.value.status == 2
