@@ -557,6 +557,29 @@ def run_mixed(args, world, rank, local):
         torch.cuda.synchronize(dev)
     binding.pa_error_check(stream)
     ms = [sum(e[j].elapsed_time(e[j + 1]) for e in evs) / args.steps for j in range(3)]
+
+    # The same step through the one unified call (write, chunks, decode tokens).
+    out_all = torch.empty_like(b.q)
+    ws_all = torch.empty(binding.pa_attention_varlen_workspace_bytes(
+        b.num_seqs, n_pre, b.num_heads, b.num_kv_heads, b.head_size), dtype=torch.uint8,
+        device=dev)
+
+    def unified():
+        binding.pa_attention_varlen(out_all, b.q, b.k_new, b.v_new, b.slot_mapping, cu_pre, n_pre,
+                                    r_pre, max_q, b.kv_cache, b.block_tables, b.seq_lens, max_dec,
+                                    b.scale, ws_all, stream)
+
+    for _ in range(max(args.warmup, 3)):
+        unified()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(args.steps):
+        unified()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    binding.pa_error_check(stream)
+    unified_ms = e0.elapsed_time(e1) / args.steps
     if rank != 0:
         return
     flops = prefill_flops(b, 0, n_pre)
@@ -568,6 +591,7 @@ def run_mixed(args, world, rank, local):
             "warmup": args.warmup, "dtype": "bf16", "data": "synthetic",
             "config": workload_config(4),
             "kernels_ms": {"pa_cache_write": ms[0], "pa_prefill_chunk": ms[1], "pa_decode": ms[2]},
+            "unified_call_ms": unified_ms,
             "prefill": {"tflops": flops / (ms[1] / 1e3) / 1e12, "flops_per_launch": flops,
                         "peak_tflops": pk["bf16_tflops"],
                         "frac": flops / (ms[1] / 1e3) / 1e12 / pk["bf16_tflops"]},

@@ -246,6 +246,48 @@ pa_status pa_prefill_chunk(void *out, const void *q, const int32_t *cu_q_lens, i
                            const int32_t *seq_lens, float scale, pa_stream_t stream);
 
 /*
+ * Workspace pa_attention_varlen needs: pa_decode's for the batch's
+ * num_seqs - num_prefills decode sequences.  Returns 0 for invalid arguments.
+ */
+size_t pa_attention_varlen_workspace_bytes(int num_seqs, int num_prefills, int num_heads,
+                                           int num_kv_heads, int head_size);
+
+/*
+ * pa_attention_varlen - one step of attention over a flattened mixed batch.
+ *
+ * The forward pass "flattens the batch into a single sequence"
+ * (§Generate function) mixing prompt chunks (chunked prefill) with decode
+ * tokens.  The batch lists its num_prefills chunk sequences first (query rows
+ * [0, num_prefill_tokens), cu_q_lens[0..num_prefills] their row offsets, so
+ * cu_q_lens[num_prefills] == num_prefill_tokens) and then its decode
+ * sequences, one query row each, in order.  The call
+ *   1. writes the step's new K/V rows into their slots (pa_cache_write), one
+ *      per query row, unless slot_mapping is NULL;
+ *   2. attends every chunk row causally to its sequence (pa_prefill_chunk);
+ *   3. attends every decode row to its whole sequence (pa_decode).
+ *   out, q        [num_prefill_tokens + num_decodes][num_heads][head_size] bf16
+ *   k_new, v_new  [same rows][num_kv_heads][head_size] bf16 (read only if
+ *                 slot_mapping != NULL)
+ *   slot_mapping  [same rows] int32 slots, or NULL
+ *   cu_q_lens     [num_prefills + 1] int32 (read only if num_prefills > 0)
+ *   max_prefill_q_len  host bound of the chunks' query lengths
+ *   block_tables, seq_lens  for all num_seqs sequences, chunks first
+ *   max_seq_len   host bound of the decode sequences' lengths
+ *   workspace     >= pa_attention_varlen_workspace_bytes(...) bytes, 256-byte
+ *                 aligned
+ * Launches on `stream` in that order; arguments are checked as by the three
+ * calls, and the first failure is returned (earlier launches stand).
+ */
+pa_status pa_attention_varlen(void *out, const void *q, const void *k_new, const void *v_new,
+                              const int32_t *slot_mapping, const int32_t *cu_q_lens,
+                              int num_seqs, int num_prefills, int num_prefill_tokens,
+                              int max_prefill_q_len, void *kv_cache, int num_blocks,
+                              int block_size, int num_heads, int num_kv_heads, int head_size,
+                              const int32_t *block_tables, int max_blocks_per_seq,
+                              const int32_t *seq_lens, int max_seq_len, float scale,
+                              void *workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/*
  * Synchronise `stream`, then read and clear the device error word the kernels
  * of this library set on the current device.  Returns PA_OK, PA_ERR_OOB,
  * PA_ERR_TIMEOUT, or PA_ERR_CUDA if the synchronisation itself failed.

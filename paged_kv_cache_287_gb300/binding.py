@@ -26,7 +26,7 @@ EXPORTS = ("pa_status_string", "pa_kv_block_bytes", "pa_kv_block_bytes_dtype", "
            "pa_cache_write_fp8", "pa_decode_fp8",
            "pa_decode_workspace_bytes", "pa_decode", "pa_decode_noalloc",
            "pa_decode_cascade_workspace_bytes", "pa_decode_cascade", "pa_prefill_chunk",
-           "pa_error_check")
+           "pa_attention_varlen_workspace_bytes", "pa_attention_varlen", "pa_error_check")
 
 
 class PaError(RuntimeError):
@@ -76,6 +76,11 @@ def lib(path: Optional[str] = None):
                                     sz, P]
     L.pa_prefill_chunk.restype = i
     L.pa_prefill_chunk.argtypes = [P, P, P, i, i, P, i, i, i, i, i, P, i, P, ctypes.c_float, P]
+    L.pa_attention_varlen_workspace_bytes.restype = sz
+    L.pa_attention_varlen_workspace_bytes.argtypes = [i, i, i, i, i]
+    L.pa_attention_varlen.restype = i
+    L.pa_attention_varlen.argtypes = [P, P, P, P, P, P, i, i, i, i, P, i, i, i, i, i, P, i, P, i,
+                                      ctypes.c_float, P, sz, P]
     L.pa_error_check.restype = i
     L.pa_error_check.argtypes = [P]
     if path is None:
@@ -275,6 +280,51 @@ def pa_prefill_chunk(out: torch.Tensor, q: torch.Tensor, cu_q_lens: torch.Tensor
                                   block_tables.data_ptr(), block_tables.shape[1],
                                   seq_lens.data_ptr(), float(scale), _stream(stream)),
            "pa_prefill_chunk")
+
+
+def pa_attention_varlen_workspace_bytes(num_seqs: int, num_prefills: int, num_heads: int,
+                                        num_kv_heads: int, head_size: int) -> int:
+    return int(lib().pa_attention_varlen_workspace_bytes(num_seqs, num_prefills, num_heads,
+                                                         num_kv_heads, head_size))
+
+
+def pa_attention_varlen(out: torch.Tensor, q: torch.Tensor, k_new: Optional[torch.Tensor],
+                        v_new: Optional[torch.Tensor], slot_mapping: Optional[torch.Tensor],
+                        cu_q_lens: torch.Tensor, num_prefills: int, num_prefill_tokens: int,
+                        max_prefill_q_len: int, kv_cache: torch.Tensor,
+                        block_tables: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                        scale: float, workspace: torch.Tensor, stream=None) -> None:
+    """One step over a flattened mixed batch (chunks first, then decode tokens):
+    optional cache write, chunked prefill, decode."""
+    NB, bs, Hkv, D = _pool_geom(kv_cache)
+    _need(q, "q", torch.bfloat16, 3)
+    _need(out, "out", torch.bfloat16, 3)
+    _need(cu_q_lens, "cu_q_lens", torch.int32, 1)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(workspace, "workspace", torch.uint8, 1)
+    B = seq_lens.shape[0]
+    rows, Hq, Dq = q.shape
+    if Dq != D or out.shape != q.shape or block_tables.shape[0] != B or \
+            rows != num_prefill_tokens + B - num_prefills:
+        raise ValueError("inconsistent varlen shapes")
+    kp = vp = sp = None
+    if slot_mapping is not None:
+        _need(k_new, "k_new", torch.bfloat16, 3)
+        _need(v_new, "v_new", torch.bfloat16, 3)
+        _need(slot_mapping, "slot_mapping", torch.int32, 1)
+        if k_new.shape != (rows, Hkv, D) or v_new.shape != (rows, Hkv, D) or \
+                slot_mapping.shape[0] != rows:
+            raise ValueError("k_new/v_new/slot_mapping must have one row per query row")
+        kp, vp, sp = k_new.data_ptr(), v_new.data_ptr(), slot_mapping.data_ptr()
+    _check(lib().pa_attention_varlen(out.data_ptr(), q.data_ptr(), kp, vp, sp,
+                                     cu_q_lens.data_ptr(), B, int(num_prefills),
+                                     int(num_prefill_tokens), int(max_prefill_q_len),
+                                     kv_cache.data_ptr(), NB, bs, Hq, Hkv, D,
+                                     block_tables.data_ptr(), block_tables.shape[1],
+                                     seq_lens.data_ptr(), int(max_seq_len), float(scale),
+                                     workspace.data_ptr(), workspace.numel(), _stream(stream)),
+           "pa_attention_varlen")
 
 
 def pa_error_check(stream=None) -> None:

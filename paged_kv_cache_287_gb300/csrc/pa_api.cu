@@ -304,6 +304,59 @@ pa_status pa_prefill_chunk(void *out, const void *q, const int32_t *cu_q_lens, i
                                         scale, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t pa_attention_varlen_workspace_bytes(int num_seqs, int num_prefills, int num_heads,
+                                           int num_kv_heads, int head_size) {
+    if (num_prefills < 0 || num_prefills > num_seqs) return 0;
+    return pa_decode_workspace_bytes(num_seqs - num_prefills, num_heads, num_kv_heads, head_size);
+}
+
+pa_status pa_attention_varlen(void *out, const void *q, const void *k_new, const void *v_new,
+                              const int32_t *slot_mapping, const int32_t *cu_q_lens,
+                              int num_seqs, int num_prefills, int num_prefill_tokens,
+                              int max_prefill_q_len, void *kv_cache, int num_blocks,
+                              int block_size, int num_heads, int num_kv_heads, int head_size,
+                              const int32_t *block_tables, int max_blocks_per_seq,
+                              const int32_t *seq_lens, int max_seq_len, float scale,
+                              void *workspace, size_t workspace_bytes, pa_stream_t stream) {
+    pa_status st = check_pool(kv_cache, num_blocks, block_size, num_kv_heads, head_size);
+    if (st != PA_OK) return st;
+    if ((st = check_heads(num_heads, num_kv_heads)) != PA_OK) return st;
+    if (num_seqs < 0 || num_prefills < 0 || num_prefills > num_seqs || num_prefill_tokens < 0 ||
+        max_prefill_q_len < 0 || max_seq_len < 0 || max_blocks_per_seq <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_prefills > 0 && num_prefill_tokens < num_prefills) return PA_ERR_INVALID_ARG;
+    if (num_prefills == 0 && num_prefill_tokens != 0) return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    const int num_decodes = num_seqs - num_prefills;
+    const int64_t rows = (int64_t)num_prefill_tokens + num_decodes;
+    const int64_t row_elems = (int64_t)num_heads * head_size;
+    // 1. The step's new K/V into their slots (one row per query row).
+    if (slot_mapping) {
+        st = pa_cache_write(kv_cache, num_blocks, block_size, num_kv_heads, head_size, k_new,
+                            v_new, (int64_t)num_kv_heads * head_size, slot_mapping, (int)rows,
+                            stream);
+        if (st != PA_OK) return st;
+    }
+    // 2. Prefill chunks: sequences [0, num_prefills), query rows [0, num_prefill_tokens).
+    if (num_prefills > 0) {
+        st = pa_prefill_chunk(out, q, cu_q_lens, num_prefills, max_prefill_q_len, kv_cache,
+                              num_blocks, block_size, num_heads, num_kv_heads, head_size,
+                              block_tables, max_blocks_per_seq, seq_lens, scale, stream);
+        if (st != PA_OK) return st;
+    }
+    // 3. Decode tokens: the remaining sequences, one query row each.
+    if (num_decodes > 0) {
+        const size_t off = (size_t)num_prefill_tokens * (size_t)row_elems * 2;
+        st = pa_decode(static_cast<uint8_t *>(out) + off, static_cast<const uint8_t *>(q) + off,
+                       kv_cache, num_blocks, block_size, num_heads, num_kv_heads, head_size,
+                       block_tables + (size_t)num_prefills * max_blocks_per_seq,
+                       max_blocks_per_seq, seq_lens + num_prefills, num_decodes, max_seq_len,
+                       scale, workspace, workspace_bytes, stream);
+        if (st != PA_OK) return st;
+    }
+    return PA_OK;
+}
+
 pa_status pa_error_check(pa_stream_t stream) {
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return PA_ERR_CUDA;

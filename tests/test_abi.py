@@ -135,3 +135,22 @@ def test_fp8_host_checks(lib):
     assert lib.pa_decode_fp8(*bad) == 0
     assert lib.pa_kv_block_bytes_dtype(16, 8, 128, 1) == 32768
     assert lib.pa_kv_block_bytes_dtype(16, 8, 128, 2) == lib.pa_kv_block_bytes(16, 8, 128)
+
+
+def test_varlen_host_checks(lib):
+    args = [FAKE, FAKE, None, None, None, FAKE, 4, 2, 100, 64, FAKE, 10, 16, 32, 8, 128, FAKE, 4,
+            FAKE, 64, 0.1, FAKE, 1 << 30, None]
+    bad = list(args)
+    bad[7] = 5                                  # more chunk sequences than sequences
+    assert lib.pa_attention_varlen(*bad) == 1
+    bad = list(args)
+    bad[8] = 1                                  # fewer chunk rows than chunk sequences
+    assert lib.pa_attention_varlen(*bad) == 1
+    bad = list(args)
+    bad[7], bad[8] = 0, 3                       # chunk rows without chunk sequences
+    assert lib.pa_attention_varlen(*bad) == 1
+    bad = list(args)
+    bad[6] = 0                                  # empty batch: no-op
+    bad[7] = bad[8] = 0
+    assert lib.pa_attention_varlen(*bad) == 0
+    assert lib.pa_attention_varlen_workspace_bytes(4, 5, 32, 8, 128) == 0

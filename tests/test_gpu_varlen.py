@@ -1,0 +1,88 @@
+"""The unified call over a flattened mixed batch (pa_attention_varlen): the
+step's cache write, its prefill chunks and its decode tokens in one call,
+checked against the oracle's write and attention of the same flattened batch."""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_cache_287_gb300 import binding
+from paged_kv_cache_287_gb300.workloads import make_batch, make_config
+from tests._gpu import bits, compare, gpu_decode, gpu_prefill, oracle_pool, oracle_rows
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(autouse=True)
+def _clean_errors():
+    binding.pa_error_check()
+    yield
+    binding.pa_error_check()
+
+
+def varlen(b, num_prefills: int, write: bool = True) -> torch.Tensor:
+    out = torch.full_like(b.q, float("nan"))
+    npt = int(b.cu_q_lens[num_prefills])
+    max_q = int(b.q_lens[:num_prefills].max()) if num_prefills else 0
+    dec_lens = b.seq_lens[num_prefills:]
+    max_len = int(dec_lens.max()) if dec_lens.numel() else 0
+    ws = torch.empty(binding.pa_attention_varlen_workspace_bytes(
+        b.num_seqs, num_prefills, b.num_heads, b.num_kv_heads, b.head_size) or 1,
+        dtype=torch.uint8, device=DEV)
+    binding.pa_attention_varlen(out, b.q, b.k_new if write else None,
+                                b.v_new if write else None, b.slot_mapping if write else None,
+                                b.cu_q_lens[:num_prefills + 1].contiguous(), num_prefills, npt,
+                                max_q, b.kv_cache, b.block_tables, b.seq_lens, max_len, b.scale,
+                                ws)
+    binding.pa_error_check()
+    return out
+
+
+@pytest.mark.parametrize("shape", [
+    # seq_lens, q_lens (chunks first), Hq, Hkv, D, bs
+    ([300, 40, 513, 90, 17, 1], [129, 40, 200, 1, 1, 1], 32, 8, 128, 16),
+    ([64, 700, 33], [64, 1, 1], 16, 4, 64, 8),
+    ([150, 260], [70, 129], 8, 2, 128, 32),      # chunks only
+    ([5, 99, 1000], [1, 1, 1], 24, 8, 128, 16),  # decode tokens only
+])
+def test_varlen_small_batches(shape):
+    lens, qls, Hq, Hkv, D, bs = shape
+    b = make_batch(name="v", seq_lens=lens, q_lens=qls, num_heads=Hq, num_kv_heads=Hkv,
+                   head_size=D, block_size=bs, scale=D ** -0.5, seed=900 + len(lens),
+                   device=DEV)
+    n_pre = sum(1 for q in qls if q > 1) if any(q > 1 for q in qls) else 0
+    pool = oracle_pool(b)
+    out = varlen(b, n_pre)
+    assert np.array_equal(bits(b.kv_cache), pool), "cache write"
+    compare(out, oracle_rows(b, pool), f"varlen {lens}")
+
+
+def test_varlen_mixed_workload_matches_separate_calls_bitwise():
+    b = make_config(4, device=DEV)
+    pool = oracle_pool(b)
+    out = varlen(b, 8)
+    assert np.array_equal(bits(b.kv_cache), pool), "cache write"
+    pre = gpu_prefill(b, 0, 8)
+    dec = gpu_decode(b, 8, b.num_seqs)
+    assert np.array_equal(bits(out[:4096]), bits(pre))
+    assert np.array_equal(bits(out[4096:]), bits(dec))
+    rows = np.concatenate([np.arange(0, 4096, 97), np.arange(4096, 4344, 7)]).astype(np.int32)
+    compare(out[torch.as_tensor(rows, device=DEV).long()], oracle_rows(b, pool, rows),
+            "mixed workload, unified call (sampled rows)")
+
+
+def test_varlen_without_slot_mapping_writes_nothing():
+    b = make_batch(name="vn", seq_lens=[40, 20], q_lens=[8, 1], num_heads=8, num_kv_heads=2,
+                   head_size=128, block_size=16, scale=0.1, seed=950, device=DEV)
+    binding.pa_cache_write(b.kv_cache, b.k_new, b.v_new, b.slot_mapping)
+    before = bits(b.kv_cache).copy()
+    b.k_new.fill_(7.0)
+    varlen(b, 1, write=False)
+    assert np.array_equal(bits(b.kv_cache), before)
