@@ -77,7 +77,7 @@ def measured_peaks():
 
 
 def profile_traffic(name: str):
-    """DRAM bytes per launch from a committed ncu summary, if its kernel source is unchanged."""
+    """DRAM bytes per launch from a committed ncu summary, if its kernel sources are unchanged."""
     path = os.path.join(ROOT, "profiles", name)
     if not os.path.exists(path):
         return None
@@ -87,13 +87,17 @@ def profile_traffic(name: str):
             if ":" in line and not line.startswith("#"):
                 k, v = line.split(":", 1)
                 fields[k.strip()] = v.strip()
-    src = os.path.join(ROOT, "paged_kv_cache_287_gb300", "csrc", fields.get("source", ""))
-    if not os.path.exists(src):
+    srcs = fields.get("source", "").split(",")
+    want = fields.get("source_sha256", "").split(",")
+    if len(srcs) != len(want):
         return None
-    with open(src, "rb") as f:
-        digest = hashlib.sha256(f.read()).hexdigest()
-    if digest != fields.get("source_sha256"):
-        return None
+    for name, sha in zip(srcs, want):
+        src = os.path.join(ROOT, "paged_kv_cache_287_gb300", "csrc", name.strip())
+        if not name.strip() or not os.path.exists(src):
+            return None
+        with open(src, "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != sha.strip():
+                return None
     try:
         return float(fields["dram_bytes_per_launch"])
     except (KeyError, ValueError):
