@@ -382,17 +382,24 @@ def run_ours(args, world, rank, local):
         step()
     binding.pa_error_check(stream)
     graph = None
+    per_graph = max(1, args.graph_steps) if args.graph else 1
+    if args.steps % per_graph:
+        raise SystemExit("--steps must be a multiple of --graph-steps")
     if args.graph:
-        # One captured step (cache write + decode kernels) replayed per timed step.
+        # per_graph captured steps (cache write + decode kernels each) per replay;
+        # several steps per replay take the host's launch of the graph off the
+        # per-step time of a launch-bound workload.
         graph = torch.cuda.CUDAGraph()
         cap = torch.cuda.Stream(dev)
         torch.cuda.synchronize(dev)
         with torch.cuda.graph(graph, stream=cap):
-            step(st=cap)
+            for _ in range(per_graph):
+                step(st=cap)
         torch.cuda.synchronize(dev)
 
     def timed():
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+        n_rep = args.steps // per_graph if graph is not None else args.steps
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_rep)]
         start = torch.cuda.Event(enable_timing=True)
         stop = torch.cuda.Event(enable_timing=True)
         barrier(world)
@@ -401,7 +408,7 @@ def run_ours(args, world, rank, local):
         if sampler:
             sampler.__enter__()
         start.record(stream)
-        for i in range(args.steps):
+        for i in range(n_rep):
             if graph is not None:
                 evs[i][0].record(stream)
                 graph.replay()
@@ -478,7 +485,8 @@ def run_ours(args, world, rank, local):
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16" if fp8 else "bf16",
         "data": "synthetic",
-        "config": dict(workload_config(n, args.seqs), launch="cuda-graph" if graph else "eager",
+        "config": dict(workload_config(n, args.seqs),
+                       launch=(f"cuda-graph, {per_graph} steps per replay" if graph else "eager"),
                        kv_cache="fp8-e4m3 (per-tensor k/v scale 1/64)" if fp8 else "bf16",
                        **({"cascade_shared_len": shared} if args.cascade else {})),
         "seqs_per_s": seqs_s,
@@ -616,6 +624,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph", action="store_true",
                     help="replay one CUDA-graph-captured step per timed step")
+    ap.add_argument("--graph-steps", type=int, default=1,
+                    help="with --graph: steps captured in one graph (replayed steps/N times)")
     ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
                     help="KV-cache element type of the decode workloads")
     ap.add_argument("--cascade", action="store_true",

@@ -259,3 +259,27 @@ def test_negative_and_zero_softmax_scale(scale):
     pool = oracle_pool(d)
     gpu_write(d)
     compare(gpu_decode(d), oracle_rows(d, pool), f"decode, scale {scale}")
+
+
+def test_decode_at_the_largest_batch_the_tables_hold():
+    """15 091 sequences (group 4, head size 128) fill the kernel's per-CTA length and
+    prefix tables; one more is refused on the host before anything is launched."""
+    B = 15091
+    g = torch.Generator().manual_seed(31)
+    lens = torch.randint(1, 40, (B,), generator=g).tolist()
+    b = make_batch(name="maxb", seq_lens=lens, q_lens=[1] * B, num_heads=4, num_kv_heads=1,
+                   head_size=128, block_size=16, scale=128 ** -0.5, seed=32, device=DEV)
+    pool = oracle_pool(b)
+    gpu_write(b)
+    out = gpu_decode(b)
+    binding.pa_error_check()
+    rows = np.arange(0, B, 37, dtype=np.int32)
+    compare(out[torch.as_tensor(rows, device=DEV).long()], oracle_rows(b, pool, rows),
+            "decode, largest batch (sampled rows)")
+    over = torch.cat([b.seq_lens, b.seq_lens[:1]])
+    tables = torch.cat([b.block_tables, b.block_tables[:1]])
+    q = torch.cat([b.q, b.q[:1]])
+    with pytest.raises(binding.PaError) as e:
+        binding.pa_decode(torch.empty_like(q), q, b.kv_cache, tables, over, int(over.max()),
+                          b.scale, workspace_for(b, B + 1))
+    assert e.value.status == 2
