@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpagedattn.so")
-SOURCES = ["pa_api.cu", "pa_cache_write.cu", "pa_decode.cu", "pa_prefill.cu",
+SOURCES = ["pa_api.cu", "pa_cache_write.cu", "pa_attention.cu",
            "pa_decode_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -197,17 +197,23 @@ size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, 
     return pa::decode_workspace_bytes(num_seqs, head_size, pa::device_sm_count());
 }
 
-pa_status pa_decode(void *out, const void *q, const void *kv_cache, int num_blocks,
-                    int block_size, int num_heads, int num_kv_heads, int head_size,
-                    const int32_t *block_tables, int max_blocks_per_seq,
-                    const int32_t *seq_lens, int num_seqs, int max_seq_len, float scale,
-                    void *workspace, size_t workspace_bytes, pa_stream_t stream) {
+// pa_decode's checks of everything but the workspace; PA_OK with
+// *nothing_to_do set for an empty batch.
+static pa_status decode_checks(const void *out, const void *q, const void *kv_cache, int num_blocks,
+                        int block_size, int num_heads, int num_kv_heads, int head_size,
+                        const int32_t *block_tables, int max_blocks_per_seq,
+                        const int32_t *seq_lens, int num_seqs, int max_seq_len, float scale,
+                        bool *nothing_to_do) {
+    *nothing_to_do = false;
     pa_status st = check_pool(kv_cache, num_blocks, block_size, num_kv_heads, head_size);
     if (st != PA_OK) return st;
     if ((st = check_heads(num_heads, num_kv_heads)) != PA_OK) return st;
     if (num_seqs < 0 || max_seq_len < 0 || max_blocks_per_seq <= 0) return PA_ERR_INVALID_ARG;
     if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f) return PA_ERR_INVALID_ARG;
-    if (num_seqs == 0) return PA_OK;
+    if (num_seqs == 0) {
+        *nothing_to_do = true;
+        return PA_OK;
+    }
     if (!out || !q || !block_tables || !seq_lens || !aligned(out, 16) || !aligned(q, 16) ||
         !aligned(block_tables, 4) || !aligned(seq_lens, 4))
         return PA_ERR_INVALID_ARG;
@@ -216,6 +222,43 @@ pa_status pa_decode(void *out, const void *q, const void *kv_cache, int num_bloc
         return PA_ERR_UNSUPPORTED;
     if ((long long)num_seqs * num_kv_heads * (((long long)max_seq_len + 15) / 16) >= (1LL << 31))
         return PA_ERR_UNSUPPORTED;
+    return PA_OK;
+}
+
+// pa_prefill_chunk's checks; PA_OK with *nothing_to_do set for an empty batch.
+static pa_status prefill_checks(const void *out, const void *q, const int32_t *cu_q_lens,
+                         int num_chunks, int max_q_len, const void *kv_cache, int num_blocks,
+                         int block_size, int num_heads, int num_kv_heads, int head_size,
+                         const int32_t *block_tables, int max_blocks_per_seq,
+                         const int32_t *seq_lens, float scale, bool *nothing_to_do) {
+    *nothing_to_do = false;
+    pa_status st = check_pool(kv_cache, num_blocks, block_size, num_kv_heads, head_size);
+    if (st != PA_OK) return st;
+    if ((st = check_heads(num_heads, num_kv_heads)) != PA_OK) return st;
+    if (num_chunks < 0 || max_q_len < 0 || max_blocks_per_seq <= 0) return PA_ERR_INVALID_ARG;
+    if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f) return PA_ERR_INVALID_ARG;
+    if (num_chunks == 0 || max_q_len == 0) {
+        *nothing_to_do = true;
+        return PA_OK;
+    }
+    if (!out || !q || !cu_q_lens || !block_tables || !seq_lens || !aligned(out, 16) ||
+        !aligned(q, 16) || !aligned(cu_q_lens, 4) || !aligned(block_tables, 4) ||
+        !aligned(seq_lens, 4))
+        return PA_ERR_INVALID_ARG;
+    if (num_chunks > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+    return PA_OK;
+}
+
+pa_status pa_decode(void *out, const void *q, const void *kv_cache, int num_blocks,
+                    int block_size, int num_heads, int num_kv_heads, int head_size,
+                    const int32_t *block_tables, int max_blocks_per_seq,
+                    const int32_t *seq_lens, int num_seqs, int max_seq_len, float scale,
+                    void *workspace, size_t workspace_bytes, pa_stream_t stream) {
+    bool none = false;
+    pa_status st = decode_checks(out, q, kv_cache, num_blocks, block_size, num_heads,
+                                 num_kv_heads, head_size, block_tables, max_blocks_per_seq,
+                                 seq_lens, num_seqs, max_seq_len, scale, &none);
+    if (st != PA_OK || none) return st;
     const size_t need = pa::decode_workspace_bytes(num_seqs, head_size, pa::device_sm_count());
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return PA_ERR_WORKSPACE;
     pa::KvGeom g{num_blocks, block_size, num_kv_heads, head_size};
@@ -287,17 +330,11 @@ pa_status pa_prefill_chunk(void *out, const void *q, const int32_t *cu_q_lens, i
                            int num_heads, int num_kv_heads, int head_size,
                            const int32_t *block_tables, int max_blocks_per_seq,
                            const int32_t *seq_lens, float scale, pa_stream_t stream) {
-    pa_status st = check_pool(kv_cache, num_blocks, block_size, num_kv_heads, head_size);
-    if (st != PA_OK) return st;
-    if ((st = check_heads(num_heads, num_kv_heads)) != PA_OK) return st;
-    if (num_chunks < 0 || max_q_len < 0 || max_blocks_per_seq <= 0) return PA_ERR_INVALID_ARG;
-    if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f) return PA_ERR_INVALID_ARG;
-    if (num_chunks == 0 || max_q_len == 0) return PA_OK;
-    if (!out || !q || !cu_q_lens || !block_tables || !seq_lens || !aligned(out, 16) ||
-        !aligned(q, 16) || !aligned(cu_q_lens, 4) || !aligned(block_tables, 4) ||
-        !aligned(seq_lens, 4))
-        return PA_ERR_INVALID_ARG;
-    if (num_chunks > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+    bool none = false;
+    pa_status st = prefill_checks(out, q, cu_q_lens, num_chunks, max_q_len, kv_cache, num_blocks,
+                                  block_size, num_heads, num_kv_heads, head_size, block_tables,
+                                  max_blocks_per_seq, seq_lens, scale, &none);
+    if (st != PA_OK || none) return st;
     pa::KvGeom g{num_blocks, block_size, num_kv_heads, head_size};
     return from_cuda(pa::launch_prefill(out, q, cu_q_lens, num_chunks, max_q_len, kv_cache, g,
                                         num_heads, block_tables, max_blocks_per_seq, seq_lens,
@@ -307,7 +344,10 @@ pa_status pa_prefill_chunk(void *out, const void *q, const int32_t *cu_q_lens, i
 size_t pa_attention_varlen_workspace_bytes(int num_seqs, int num_prefills, int num_heads,
                                            int num_kv_heads, int head_size) {
     if (num_prefills < 0 || num_prefills > num_seqs) return 0;
-    return pa_decode_workspace_bytes(num_seqs - num_prefills, num_heads, num_kv_heads, head_size);
+    const size_t dec =
+        pa_decode_workspace_bytes(num_seqs - num_prefills, num_heads, num_kv_heads, head_size);
+    if (dec == 0 || head_size <= 0) return dec;
+    return pa::mixed_workspace_bytes(num_seqs - num_prefills, head_size, pa::device_sm_count());
 }
 
 pa_status pa_attention_varlen(void *out, const void *q, const void *k_new, const void *v_new,
@@ -337,6 +377,36 @@ pa_status pa_attention_varlen(void *out, const void *q, const void *k_new, const
                             stream);
         if (st != PA_OK) return st;
     }
+    // 2+3 in one launch when both parts are present: decode and prefill side by
+    // side on disjoint SMs.
+    const size_t off = (size_t)num_prefill_tokens * (size_t)row_elems * 2;
+    pa::KvGeom g{num_blocks, block_size, num_kv_heads, head_size};
+    if (num_prefills > 0 && num_decodes > 0 && pa::mixed_supported(num_decodes, num_heads, g)) {
+        bool none_p = false, none_d = false;
+        st = prefill_checks(out, q, cu_q_lens, num_prefills, max_prefill_q_len, kv_cache,
+                            num_blocks, block_size, num_heads, num_kv_heads, head_size,
+                            block_tables, max_blocks_per_seq, seq_lens, scale, &none_p);
+        if (st != PA_OK) return st;
+        st = decode_checks(static_cast<uint8_t *>(out) + off,
+                           static_cast<const uint8_t *>(q) + off, kv_cache, num_blocks,
+                           block_size, num_heads, num_kv_heads, head_size,
+                           block_tables + (size_t)num_prefills * max_blocks_per_seq,
+                           max_blocks_per_seq, seq_lens + num_prefills, num_decodes, max_seq_len,
+                           scale, &none_d);
+        if (st != PA_OK) return st;
+        if (!none_p) {
+            const size_t need =
+                pa::mixed_workspace_bytes(num_decodes, head_size, pa::device_sm_count());
+            if (!workspace || !aligned(workspace, 256) || workspace_bytes < need)
+                return PA_ERR_WORKSPACE;
+            return from_cuda(pa::launch_mixed(out, q, cu_q_lens, num_prefills,
+                                              num_prefill_tokens, max_prefill_q_len, kv_cache, g,
+                                              num_heads, block_tables, max_blocks_per_seq,
+                                              seq_lens, num_seqs, scale, workspace,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+        }
+    }
+    // Otherwise one part at a time.
     // 2. Prefill chunks: sequences [0, num_prefills), query rows [0, num_prefill_tokens).
     if (num_prefills > 0) {
         st = pa_prefill_chunk(out, q, cu_q_lens, num_prefills, max_prefill_q_len, kv_cache,
@@ -346,7 +416,6 @@ pa_status pa_attention_varlen(void *out, const void *q, const void *k_new, const
     }
     // 3. Decode tokens: the remaining sequences, one query row each.
     if (num_decodes > 0) {
-        const size_t off = (size_t)num_prefill_tokens * (size_t)row_elems * 2;
         st = pa_decode(static_cast<uint8_t *>(out) + off, static_cast<const uint8_t *>(q) + off,
                        kv_cache, num_blocks, block_size, num_heads, num_kv_heads, head_size,
                        block_tables + (size_t)num_prefills * max_blocks_per_seq,

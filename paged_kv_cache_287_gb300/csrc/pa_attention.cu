@@ -1,0 +1,182 @@
+// pa_attention.cu - the attention kernels of libpagedattn in one translation unit:
+// decode (pa_decode.cuh), chunked prefill (pa_prefill.cuh), and the single-launch
+// kernel for a flattened mixed batch that runs both side by side.
+#include "pa_decode.cuh"
+#include "pa_prefill.cuh"
+
+// ----------------------------------------------------------------------------
+// One launch for a flattened mixed batch ("Inside vLLM: Anatomy of a
+// High-Throughput LLM Inference System", §Generate function: the forward pass
+// flattens the batch into a single sequence).  Decode is bound by HBM and the
+// chunked prefill by the tensor-core hand-over chain, so the two run side by
+// side on disjoint SMs: the grid's first `sms` CTAs are decode slots, of which
+// the first k stream the decode tiles (k chosen on the device, below) and the
+// rest exit at once; the remaining CTAs are the prefill's, dispatched onto every
+// SM the decode does not hold.  The decode's pieces are merged by the usual
+// merge kernel, launched after (not as a programmatic dependent: waiting merge
+// CTAs would occupy the SMs the prefill needs).
+namespace pa {
+namespace {
+
+// Decode CTAs of the mixed launch keep two stages per warp: on part of the GPU
+// each SM has to hold twice the bytes in flight.
+constexpr int kMixStages = 2;
+// Rates measured on GB300 for the split: decode with 12 warps x 2 stages streams
+// about 96 GB/s per SM, 7.0 TB/s at most in all; chunked prefill does about
+// 7.5 TFLOP/s per SM.
+constexpr float kMixDecodeSmGBs = 96.0f, kMixHbmGBs = 7000.0f, kMixPrefillSmTflops = 7.5f;
+
+struct MixPlanArgs {
+    const int32_t *seq_lens;   // all sequences, chunks first
+    const int32_t *cu_q_lens;  // chunk row offsets [num_prefills + 1]
+    int num_prefills, num_seqs, sms, max_len;
+    float dec_bytes_per_token;  // K+V bytes per decode token: 2 * Hkv * D * 2
+    float pre_flops_per_pair;   // flops per visible (query, key) pair: 4 * Hq * D
+    int *plan;                   // out: {decode CTAs, decode warps}
+};
+
+// Decode bytes and prefill flops of the batch, then the number of decode SMs k
+// that makes both parts finish together: min over k of
+// max(bytes / min(k * decode rate, HBM), flops / ((sms - k) * prefill rate)).
+// fp32 throughout (the choice needs no more; this GPU's fp64 rate is low), the
+// search spread over one warp.
+__global__ void __launch_bounds__(256) mix_plan_kernel(const MixPlanArgs a) {
+    __shared__ float s_dec[256], s_pre[256];
+    const int tid = threadIdx.x;
+    float dec = 0.f, pre = 0.f;
+    for (int s = tid; s < a.num_seqs; s += 256) {
+        const long long len = max(0, min(a.seq_lens[s], a.max_len));
+        if (s < a.num_prefills) {
+            const long long ql = a.cu_q_lens[s + 1] - a.cu_q_lens[s];
+            const long long ctx = max(0LL, len - ql);
+            pre += (float)(ql * ctx + ql * (ql + 1) / 2);
+        } else {
+            dec += (float)len;
+        }
+    }
+    s_dec[tid] = dec;
+    s_pre[tid] = pre;
+    __syncthreads();
+    for (int o = 128; o > 0; o >>= 1) {
+        if (tid < o) {
+            s_dec[tid] += s_dec[tid + o];
+            s_pre[tid] += s_pre[tid + o];
+        }
+        __syncthreads();
+    }
+    if (tid < 32) {
+        // times in microseconds: bytes / (GB/s * 1e3), flops / (TFLOP/s * 1e6)
+        const float bytes = s_dec[0] * a.dec_bytes_per_token;
+        const float flops = s_pre[0] * a.pre_flops_per_pair;
+        int best = 1;
+        float best_t = 3.0e38f;
+        for (int k = 1 + tid; k < a.sms; k += 32) {
+            const float td = bytes / (fminf(k * kMixDecodeSmGBs, kMixHbmGBs) * 1e3f);
+            const float tp = flops / ((a.sms - k) * kMixPrefillSmTflops * 1e6f);
+            const float t = fmaxf(td, tp);
+            if (t < best_t) {
+                best_t = t;
+                best = k;
+            }
+        }
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ot = __shfl_xor_sync(0xffffffffu, best_t, o);
+            const int ok = __shfl_xor_sync(0xffffffffu, best, o);
+            if (ot < best_t || (ot == best_t && ok < best)) {
+                best_t = ot;
+                best = ok;
+            }
+        }
+        if (tid == 0) {
+            a.plan[0] = best;
+            a.plan[1] = best * kDecodeWarps;
+        }
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kDecodeWarps * 32, 1)
+    mixed_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs da,
+                 const PrefillArgs pa, int dec_slots, uint3 pre_grid) {
+    if ((int)blockIdx.x < dec_slots) {
+        if ((int)blockIdx.x < da.plan[0])
+            decode_body<D, kDecodeWarps, kMixStages, false>(kv_map, da, blockIdx.x, da.plan[1]);
+        return;
+    }
+    const unsigned v = blockIdx.x - (unsigned)dec_slots;
+    const uint3 bid = make_uint3(v % pre_grid.x, (v / pre_grid.x) % pre_grid.y,
+                                 v / (pre_grid.x * pre_grid.y));
+    prefill_body<D>(kv_map, pa, bid, pre_grid);
+}
+
+template <int D>
+cudaError_t launch_mixed_d(const CUtensorMap &map, const DecodeArgs &da, const PrefillArgs &pa,
+                           dim3 pgrid, int sms, size_t smem, cudaStream_t stream) {
+    auto kern = mixed_kernel<D>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const unsigned n_pre = pgrid.x * pgrid.y * pgrid.z;
+    kern<<<(unsigned)sms + n_pre, kDecodeWarps * 32, smem, stream>>>(
+        map, da, pa, sms, make_uint3(pgrid.x, pgrid.y, pgrid.z));
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    decode_merge_kernel<D><<<(unsigned)(da.num_seqs * da.num_kv_heads),
+                             (unsigned)(da.group * D / 4), 0, stream>>>(da);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t mixed_workspace_bytes(int num_decodes, int head_size, int sm_count) {
+    return decode_workspace_bytes(num_decodes, head_size, sm_count) + 256;
+}
+
+bool mixed_supported(int num_decodes, int num_heads, const KvGeom &g) {
+    const int G = num_heads / g.num_kv_heads;
+    const size_t dec = g.head_size == 128 ? decode_smem_bytes<128, false, kMixStages>(num_decodes, G)
+                                          : decode_smem_bytes<64, false, kMixStages>(num_decodes, G);
+    const size_t pre = g.head_size == 128 ? TcLay<128>::kSmem : TcLay<64>::kSmem;
+    return dec <= pre;  // the prefill's shared memory is the launch's
+}
+
+cudaError_t launch_mixed(void *out, const void *q, const int32_t *cu_q_lens, int num_prefills,
+                         int num_prefill_tokens, int max_prefill_q_len, const void *kv_cache,
+                         const KvGeom &g, int num_heads, const int32_t *block_tables,
+                         int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs,
+                         float scale, void *workspace, cudaStream_t stream) {
+    const int sms = device_sm_count();
+    const int D = g.head_size, num_decodes = num_seqs - num_prefills;
+    CUtensorMap map;
+    if (!encode_kv_map(&map, kv_cache, g, g.block_size >= kTile ? kTile : g.block_size))
+        return cudaErrorInvalidValue;
+    int *plan = reinterpret_cast<int *>(static_cast<uint8_t *>(workspace) +
+                                        decode_workspace_bytes(num_decodes, D, sms));
+    MixPlanArgs pl;
+    pl.seq_lens = seq_lens;
+    pl.cu_q_lens = cu_q_lens;
+    pl.num_prefills = num_prefills;
+    pl.num_seqs = num_seqs;
+    pl.sms = sms;
+    pl.max_len = max_blocks_per_seq * g.block_size;
+    pl.dec_bytes_per_token = 2.0f * g.num_kv_heads * D * 2;
+    pl.pre_flops_per_pair = 4.0f * num_heads * D;
+    pl.plan = plan;
+    mix_plan_kernel<<<1, 256, 0, stream>>>(pl);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const size_t off = (size_t)num_prefill_tokens * num_heads * D * 2;
+    DecodeArgs da = make_decode_args(static_cast<uint8_t *>(out) + off,
+                                     static_cast<const uint8_t *>(q) + off, g, num_heads,
+                                     block_tables + (size_t)num_prefills * max_blocks_per_seq,
+                                     max_blocks_per_seq, seq_lens + num_prefills, num_decodes,
+                                     scale, workspace, false, sms);
+    da.plan = plan;
+    dim3 pgrid;
+    const PrefillArgs pa =
+        make_prefill_args(out, q, cu_q_lens, num_prefills, max_prefill_q_len, g, num_heads,
+                          block_tables, max_blocks_per_seq, seq_lens, scale, &pgrid);
+    if (D == 128) return launch_mixed_d<128>(map, da, pa, pgrid, sms, TcLay<128>::kSmem, stream);
+    return launch_mixed_d<64>(map, da, pa, pgrid, sms, TcLay<64>::kSmem, stream);
+}
+
+}  // namespace pa

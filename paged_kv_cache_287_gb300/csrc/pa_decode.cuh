@@ -91,6 +91,9 @@ struct DecodeArgs {
     int pre_splits;
     const float *pre_ml;   // [pre_splits][num_seqs][num_heads][2]
     const float *pre_acc;  // [pre_splits][num_seqs][num_heads][D]
+    // Mixed-batch launch: the number of decode CTAs and their total warps were
+    // chosen on the device; plan = {ctas, total_warps} (nullptr otherwise).
+    const int *plan;
 };
 
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -111,9 +114,12 @@ __device__ __forceinline__ int kv_row(int blk, int h, int off, const DecodeArgs 
     return ((blk * 2) * a.num_kv_heads + h) * a.block_size + off;
 }
 
+// The split-context decode of one CTA (index cta of a grid whose warps number
+// total_warps), W warps with an S-stage ring each; called by decode_kernel and by
+// the mixed-batch kernel.
 template <int D, int W, int S, bool KV8>
-__global__ void __launch_bounds__(W * 32, 1)
-    decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
+__device__ __forceinline__ void decode_body(const CUtensorMap &kv_map, const DecodeArgs &a,
+                                            int cta, int total_warps) {
     using L = Lay<D, KV8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(align_up(reinterpret_cast<size_t>(smem_raw), 1024));
@@ -161,15 +167,15 @@ __global__ void __launch_bounds__(W * 32, 1)
         fence_barrier_init();
     }
     __syncthreads();
-    if (blockIdx.x == 0)
+    if (cta == 0)
         for (int s = tid; s <= B; s += W * 32) a.prefix[s] = s_pre[s];
     // The merge kernel may be scheduled now; it waits for this grid to finish.
     asm volatile("griddepcontrol.launch_dependents;" :::);
 
     // This warp's equal share of the flattened tile list.
     const long long T = (long long)s_pre[B] * Hkv;
-    const long long NW = a.total_warps;
-    const long long g = (long long)blockIdx.x * W + warp;
+    const long long NW = total_warps;
+    const long long g = (long long)cta * W + warp;
     const int t_begin = (int)((g * T) / NW);
     const int t_end = (int)(((g + 1) * T) / NW);
     const int n = t_end - t_begin;
@@ -639,6 +645,12 @@ __global__ void __launch_bounds__(W * 32, 1)
     }
 }
 
+template <int D, int W, int S, bool KV8>
+__global__ void __launch_bounds__(W * 32, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
+    decode_body<D, W, S, KV8>(kv_map, a, blockIdx.x, a.total_warps);
+}
+
 // Merge the pieces of segments that were split across warps; zero empty sequences.
 // One CTA per (sequence, KV head); one thread per (query head, 4 dims).  Launched
 // as a programmatic dependent of the split kernel: it may start early and waits
@@ -662,7 +674,7 @@ __global__ void __launch_bounds__(kHeadsPad * D / 4) decode_merge_kernel(const D
         return;
     }
     // Pieces g0..g1 of this segment (none if the sequence has no tokens here).
-    const long long NW = a.total_warps;
+    const long long NW = a.plan ? a.plan[1] : a.total_warps;
     long long T = 1, S0 = 0, S1 = 0, g0 = 0, g1 = -1;
     if (nt > 0) {
         T = (long long)a.prefix[a.num_seqs] * Hkv;
@@ -786,6 +798,46 @@ cudaError_t take_error_decode(unsigned *bits) {
 
 namespace {
 
+// Arguments of a decode launch over ctas CTAs (workspace carved as
+// decode_workspace_bytes lays it out); no cascade, scales 1.
+DecodeArgs make_decode_args(void *out, const void *q, const KvGeom &g, int num_heads,
+                            const int32_t *block_tables, int max_blocks_per_seq,
+                            const int32_t *seq_lens, int num_seqs, float scale, void *workspace,
+                            bool kv8, int ctas) {
+    const int sms = device_sm_count();
+    const int D = g.head_size;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const size_t nw_max = (size_t)sms * kDecodeWarps;
+    DecodeArgs a;
+    a.out = static_cast<__nv_bfloat16 *>(out);
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.block_tables = block_tables;
+    a.seq_lens = seq_lens;
+    a.prefix = reinterpret_cast<int32_t *>(ws);
+    ws += align_up((size_t)(num_seqs + 1) * 4, 256);
+    a.part_ml = reinterpret_cast<float *>(ws);
+    ws += align_up(nw_max * 2 * kHeadsPad * 2 * 4, 256);
+    a.part_acc = reinterpret_cast<float *>(ws);
+    a.num_seqs = num_seqs;
+    a.num_heads = num_heads;
+    a.num_kv_heads = g.num_kv_heads;
+    a.group = num_heads / g.num_kv_heads;
+    a.block_size = g.block_size;
+    a.max_blocks = max_blocks_per_seq;
+    a.num_blocks = g.num_blocks;
+    a.total_warps = ctas * kDecodeWarps;
+    a.stage_bytes = 2 * (D * (kv8 ? 1 : 2) / 128) * kTile * 128 + q_slot_bytes(a.group, D);
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.k_scale = 1.f;
+    a.v_scale = 1.f;
+    a.shared_len = 0;
+    a.pre_splits = 0;
+    a.pre_ml = nullptr;
+    a.pre_acc = nullptr;
+    a.plan = nullptr;
+    return a;
+}
+
 cudaError_t launch_decode_impl(void *out, const void *q, const void *kv_cache, const KvGeom &g,
                                int num_heads, const int32_t *block_tables, int max_blocks_per_seq,
                                const int32_t *seq_lens, int num_seqs, int max_seq_len,
@@ -806,28 +858,8 @@ cudaError_t launch_decode_impl(void *out, const void *q, const void *kv_cache, c
                            ((std::max(max_seq_len - shared_len, 1) + kTile - 1) / kTile);
     long long ctas = (tmax + kDecodeWarps - 1) / kDecodeWarps;
     ctas = std::max(1LL, std::min<long long>(ctas, sms));
-    uint8_t *ws = static_cast<uint8_t *>(workspace);
-    const size_t nw_max = (size_t)sms * kDecodeWarps;
-    DecodeArgs a;
-    a.out = static_cast<__nv_bfloat16 *>(out);
-    a.q = static_cast<const __nv_bfloat16 *>(q);
-    a.block_tables = block_tables;
-    a.seq_lens = seq_lens;
-    a.prefix = reinterpret_cast<int32_t *>(ws);
-    ws += align_up((size_t)(num_seqs + 1) * 4, 256);
-    a.part_ml = reinterpret_cast<float *>(ws);
-    ws += align_up(nw_max * 2 * kHeadsPad * 2 * 4, 256);
-    a.part_acc = reinterpret_cast<float *>(ws);
-    a.num_seqs = num_seqs;
-    a.num_heads = num_heads;
-    a.num_kv_heads = g.num_kv_heads;
-    a.group = num_heads / g.num_kv_heads;
-    a.block_size = g.block_size;
-    a.max_blocks = max_blocks_per_seq;
-    a.num_blocks = g.num_blocks;
-    a.total_warps = (int)ctas * kDecodeWarps;
-    a.stage_bytes = 2 * (D * (kv8 ? 1 : 2) / 128) * kTile * 128 + q_slot_bytes(a.group, D);
-    a.scale_log2 = scale * 1.4426950408889634f;
+    DecodeArgs a = make_decode_args(out, q, g, num_heads, block_tables, max_blocks_per_seq,
+                                    seq_lens, num_seqs, scale, workspace, kv8, (int)ctas);
     a.k_scale = k_scale;
     a.v_scale = v_scale;
     a.shared_len = shared_len;
@@ -838,6 +870,8 @@ cudaError_t launch_decode_impl(void *out, const void *q, const void *kv_cache, c
     if (D == 128) return launch_decode_d<128, false>(a, map, (int)ctas, stream);
     return launch_decode_d<64, false>(a, map, (int)ctas, stream);
 }
+
+
 
 }  // namespace
 

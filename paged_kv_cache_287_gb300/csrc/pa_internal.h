@@ -74,6 +74,17 @@ cudaError_t launch_decode_suffix(void *out, const void *q, const void *kv_cache,
                                  const float *pre_ml, const float *pre_acc, int pre_splits,
                                  cudaStream_t stream);
 
+// One launch for a flattened mixed batch (chunks first, then decode sequences):
+// decode and chunked prefill side by side on disjoint SMs, split on the device.
+// mixed_supported: whether the decode part's shared memory fits the launch.
+size_t mixed_workspace_bytes(int num_decodes, int head_size, int sm_count);
+bool mixed_supported(int num_decodes, int num_heads, const KvGeom &g);
+cudaError_t launch_mixed(void *out, const void *q, const int32_t *cu_q_lens, int num_prefills,
+                         int num_prefill_tokens, int max_prefill_q_len, const void *kv_cache,
+                         const KvGeom &g, int num_heads, const int32_t *block_tables,
+                         int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs,
+                         float scale, void *workspace, cudaStream_t stream);
+
 cudaError_t launch_prefill(void *out, const void *q, const int32_t *cu_q_lens, int num_chunks,
                            int max_q_len, const void *kv_cache, const KvGeom &g, int num_heads,
                            const int32_t *block_tables, int max_blocks_per_seq,

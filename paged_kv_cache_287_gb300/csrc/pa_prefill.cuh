@@ -39,7 +39,7 @@ __device__ unsigned g_err_prefill;
 
 // The softmax reference max is raised only when a row max exceeds it by more
 // than this (log2 units): P stays <= 2^8 and O is rescaled rarely.
-constexpr float kRescaleSlack = 8.0f;
+constexpr float kTcRescaleSlack = 8.0f;
 
 constexpr int kTcRows = 128;    // query rows per tile (the MMA's M)
 constexpr int kTcTiles = 2;     // query tiles per CTA
@@ -104,9 +104,12 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity) {
     return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity));
 }
 
+// One prefill CTA at (virtual) block index bid of a grid of size grid; called by
+// prefill_tc_kernel and by the mixed-batch kernel (whose CTAs may have more warps
+// than kTcWarps: the extra warps only take part in the CTA-wide barriers).
 template <int D>
-__global__ void __launch_bounds__(kTcThreads, 1)
-    prefill_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const PrefillArgs a) {
+__device__ __forceinline__ void prefill_body(const CUtensorMap &kv_map, const PrefillArgs &a,
+                                             const uint3 bid, const uint3 grid) {
     using L = TcLay<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -129,8 +132,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __shared__ int s_ctx[kRankMax];
     __shared__ int s_pick;
     const bool prefix = a.part_ml != nullptr;
-    int s = prefix ? 0 : blockIdx.z;
-    const int nchunks = gridDim.z;
+    int s = prefix ? 0 : (int)bid.z;
+    const int nchunks = grid.z;
     if (!prefix && nchunks <= kRankMax) {
         for (int i = threadIdx.x; i < nchunks; i += blockDim.x)
             s_ctx[i] = a.seq_lens[i] - (a.cu_q_lens[i + 1] - a.cu_q_lens[i]);
@@ -142,13 +145,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int ck = s_ctx[k];
                 rank += (ck > ci) || (ck == ci && k < i);
             }
-            if (rank == (int)blockIdx.z) s_pick = i;
+            if (rank == (int)bid.z) s_pick = i;
         }
         __syncthreads();
         s = s_pick;
     }
-    const int h = blockIdx.y;
-    const int qt = gridDim.x - 1 - blockIdx.x;  // latest query tiles first
+    const int h = bid.y;
+    const int qt = grid.x - 1 - bid.x;  // latest query tiles first
     const int q0 = prefix ? 0 : a.cu_q_lens[s];
     const int q_len = prefix ? a.prefix_rows : a.cu_q_lens[s + 1] - q0;
     const int QT = a.q_tile, G = a.group;
@@ -169,7 +172,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int t_last = std::min(t0 + kTcTiles * QT, q_len) - 1;
         n_kt = (ctx + t_last + 1 + kTcKeys - 1) / kTcKeys;
     } else {
-        key0 = (int)blockIdx.z * a.split_tiles * kTcKeys;
+        key0 = (int)bid.z * a.split_tiles * kTcKeys;
         len = std::min(a.shared_len - key0, a.split_tiles * kTcKeys);
         ctx = len;  // no causal limit: every row sees the whole range
         n_kt = (len + kTcKeys - 1) / kTcKeys;
@@ -411,7 +414,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     r1m = fmax3(r1m, x[c + 2], x[c + 3]);
                 }
                 const float mx = fmaxf(r0m, r1m) * sl2;
-                const bool grow = mx > m + kRescaleSlack;
+                const bool grow = mx > m + kTcRescaleSlack;
                 if (__any_sync(0xffffffffu, grow)) {
                     const float mn = grow ? fmaxf(m, mx) : m;
                     const float cr = fast_exp2(m - mn);
@@ -494,7 +497,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (prefix) {
                 // Unnormalised partial of this (split, sequence, query head).
                 const size_t rec =
-                    ((size_t)blockIdx.z * q_len + (t0 + tok)) * a.num_heads + (size_t)h * G + gq;
+                    ((size_t)bid.z * q_len + (t0 + tok)) * a.num_heads + (size_t)h * G + gq;
                 float4 *pacc = reinterpret_cast<float4 *>(a.part_acc + rec * D);
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
@@ -540,6 +543,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 }
 
 template <int D>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const PrefillArgs a) {
+    prefill_body<D>(kv_map, a, blockIdx, gridDim);
+}
+
+template <int D>
 cudaError_t launch_prefill_tc(const PrefillArgs &a, const CUtensorMap &map, dim3 grid,
                               cudaStream_t stream) {
     const size_t smem = TcLay<D>::kSmem;
@@ -560,13 +569,13 @@ cudaError_t take_error_prefill(unsigned *bits) {
     return e;
 }
 
-cudaError_t launch_prefill(void *out, const void *q, const int32_t *cu_q_lens, int num_chunks,
-                           int max_q_len, const void *kv_cache, const KvGeom &g, int num_heads,
-                           const int32_t *block_tables, int max_blocks_per_seq,
-                           const int32_t *seq_lens, float scale, cudaStream_t stream) {
-    CUtensorMap map;
-    if (!encode_kv_map(&map, kv_cache, g, g.block_size >= 16 ? 16 : g.block_size))
-        return cudaErrorInvalidValue;
+namespace {
+
+// Arguments and grid of a chunked-prefill launch.
+PrefillArgs make_prefill_args(void *out, const void *q, const int32_t *cu_q_lens, int num_chunks,
+                              int max_q_len, const KvGeom &g, int num_heads,
+                              const int32_t *block_tables, int max_blocks_per_seq,
+                              const int32_t *seq_lens, float scale, dim3 *grid) {
     PrefillArgs a;
     a.out = static_cast<__nv_bfloat16 *>(out);
     a.q = static_cast<const __nv_bfloat16 *>(q);
@@ -589,8 +598,24 @@ cudaError_t launch_prefill(void *out, const void *q, const int32_t *cu_q_lens, i
     a.part_acc = nullptr;
     a.shared_len = a.split_tiles = a.prefix_rows = 0;
     const int per_cta = kTcTiles * a.q_tile;
-    dim3 grid((unsigned)((max_q_len + per_cta - 1) / per_cta), (unsigned)g.num_kv_heads,
-              (unsigned)num_chunks);
+    *grid = dim3((unsigned)((max_q_len + per_cta - 1) / per_cta), (unsigned)g.num_kv_heads,
+                 (unsigned)num_chunks);
+    return a;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(void *out, const void *q, const int32_t *cu_q_lens, int num_chunks,
+                           int max_q_len, const void *kv_cache, const KvGeom &g, int num_heads,
+                           const int32_t *block_tables, int max_blocks_per_seq,
+                           const int32_t *seq_lens, float scale, cudaStream_t stream) {
+    CUtensorMap map;
+    if (!encode_kv_map(&map, kv_cache, g, g.block_size >= 16 ? 16 : g.block_size))
+        return cudaErrorInvalidValue;
+    dim3 grid;
+    const PrefillArgs a = make_prefill_args(out, q, cu_q_lens, num_chunks, max_q_len, g,
+                                            num_heads, block_tables, max_blocks_per_seq,
+                                            seq_lens, scale, &grid);
     if (g.head_size == 128) return launch_prefill_tc<128>(a, map, grid, stream);
     return launch_prefill_tc<64>(a, map, grid, stream);
 }
