@@ -286,7 +286,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap &kv_map, const Dec
     const int tr0 = lane >> 2;             // tokens whose scores this lane holds: tr0, tr0+8
     // Output dim of accumulator row tr0 (+8 if hi) of MMA tile mt.
     auto dim_of = [&](int mt, int hi) {
-        if constexpr (KV8) return 32 * (mt >> 1) + 4 * tr0 + 2 * (mt & 1) + hi;
+        if constexpr (KV8) return 16 * mt + 2 * tr0 + hi;
         return mt * 16 + tr0 + 8 * hi;
     };
 
@@ -490,31 +490,23 @@ __device__ __forceinline__ void decode_body(const CUtensorMap &kv_map, const Dec
                 mma_bf16(acc[mt], af, b0, b1);
             }
         } else {
-            // V^T fragments from e4m3 codes.  MMA row m of tile mt stands for dim
-            // 32*(mt/2) + 4*(m%8) + 2*(mt%2) + m/8, so a lane (m%8 = g) needs dims
-            // 32*q + 4g .. 4g+3 of its four tokens 2t, 2t+1, 2t+8, 2t+9 (the
-            // k-slots of P^T): four 32-bit loads per 32 dims, a 4x4 byte
-            // transpose, and each (dim, token pair) becomes one f16 pair.
-            const int t2 = 2 * (lane & 3), g = lane >> 2;
+            // V^T fragments from e4m3 codes.  ldmatrix.trans on 16-bit units gives a
+            // lane, for tokens 2t, 2t+1 (or 2t+8, 2t+9) and dims 2g, 2g+1 of a 16-dim
+            // chunk, the four codes (t0,d0) (t0,d1) (t1,d0) (t1,d1); one byte permute
+            // makes them the token pairs of dim 2g and of dim 2g+1, and each pair is
+            // one f16x2.  MMA row g of tile mt stands for dim 16 mt + 2g, row g+8 for
+            // dim 16 mt + 2g + 1.
+            const int mi = lane >> 3;
+            const int row = (lane & 7) + (mi & 1) * 8;
 #pragma unroll
             for (int q = 0; q < D / 32; ++q) {
-                const uint32_t off = (uint32_t)(g & 3) << 2;
-                const int chunk = 2 * q + (g >> 2);
-                uint32_t w0, w1, w2, w3;
-                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w0) : "r"(swz128(vbase, t2, chunk) + off));
-                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w1) : "r"(swz128(vbase, t2 + 1, chunk) + off));
-                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w2) : "r"(swz128(vbase, t2 + 8, chunk) + off));
-                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w3) : "r"(swz128(vbase, t2 + 9, chunk) + off));
-                const uint32_t u0 = prmt(w0, w1, 0x5140u), u1 = prmt(w0, w1, 0x7362u);
-                const uint32_t u2 = prmt(w2, w3, 0x5140u), u3 = prmt(w2, w3, 0x7362u);
-                // d_j = codes of dim 32q + 4g + j for tokens (2t, 2t+1, 2t+8, 2t+9)
-                const uint32_t d0 = prmt(u0, u2, 0x5410u), d1 = prmt(u0, u2, 0x7632u);
-                const uint32_t d2 = prmt(u1, u3, 0x5410u), d3 = prmt(u1, u3, 0x7632u);
+                uint32_t w[4];
+                ldsm_x4_t(w, swz128(vbase, row, 2 * q + (mi >> 1)));
                 uint32_t af[4], ag[4];
-                e4m3x4_to_f16x4(d0, af[0], af[2]);  // row g: dim 4g + 0
-                e4m3x4_to_f16x4(d1, af[1], af[3]);  // row g + 8: dim 4g + 1
-                e4m3x4_to_f16x4(d2, ag[0], ag[2]);  // tile 2q + 1, row g: dim 4g + 2
-                e4m3x4_to_f16x4(d3, ag[1], ag[3]);  // tile 2q + 1, row g + 8: dim 4g + 3
+                e4m3x4_to_f16x4(prmt(w[0], 0u, 0x3120u), af[0], af[1]);  // tokens 2t, 2t+1
+                e4m3x4_to_f16x4(prmt(w[1], 0u, 0x3120u), af[2], af[3]);  // tokens 2t+8, 2t+9
+                e4m3x4_to_f16x4(prmt(w[2], 0u, 0x3120u), ag[0], ag[1]);
+                e4m3x4_to_f16x4(prmt(w[3], 0u, 0x3120u), ag[2], ag[3]);
                 mma_f16(acc[2 * q], af, b0, b1);
                 mma_f16(acc[2 * q + 1], ag, b0, b1);
             }
