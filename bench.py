@@ -590,14 +590,32 @@ def run_mixed(args, world, rank, local):
                                                        b.num_kv_heads, b.head_size),
                      dtype=torch.uint8, device=dev)
 
+    fp8 = args.kv == "fp8"
+    if fp8:
+        from paged_kv_cache_287_gb300.workloads import FP8_K_SCALE, FP8_V_SCALE, fp8_pool_of
+        pool8 = fp8_pool_of(b)
+
     def step(ev=None):
         if ev: ev[0].record(stream)
-        binding.pa_cache_write(b.kv_cache, b.k_new, b.v_new, b.slot_mapping, stream)
+        if fp8:
+            binding.pa_cache_write_fp8(pool8, b.k_new, b.v_new, b.slot_mapping, FP8_K_SCALE,
+                                       FP8_V_SCALE, stream)
+        else:
+            binding.pa_cache_write(b.kv_cache, b.k_new, b.v_new, b.slot_mapping, stream)
         if ev: ev[1].record(stream)
-        binding.pa_prefill_chunk(out_pre, q_pre, cu_pre, max_q, b.kv_cache, bt_pre, sl_pre,
-                                 b.scale, stream)
+        if fp8:
+            binding.pa_prefill_chunk_fp8(out_pre, q_pre, cu_pre, max_q, pool8, bt_pre, sl_pre,
+                                         b.scale, FP8_K_SCALE, FP8_V_SCALE, stream)
+        else:
+            binding.pa_prefill_chunk(out_pre, q_pre, cu_pre, max_q, b.kv_cache, bt_pre, sl_pre,
+                                     b.scale, stream)
         if ev: ev[2].record(stream)
-        binding.pa_decode(out_dec, q_dec, b.kv_cache, bt_dec, sl_dec, max_dec, b.scale, ws, stream)
+        if fp8:
+            binding.pa_decode_fp8(out_dec, q_dec, pool8, bt_dec, sl_dec, max_dec, b.scale,
+                                  FP8_K_SCALE, FP8_V_SCALE, ws, stream)
+        else:
+            binding.pa_decode(out_dec, q_dec, b.kv_cache, bt_dec, sl_dec, max_dec, b.scale, ws,
+                              stream)
         if ev: ev[3].record(stream)
 
     for _ in range(max(args.warmup, 3)):
@@ -623,36 +641,42 @@ def run_mixed(args, world, rank, local):
                                     r_pre, max_q, b.kv_cache, b.block_tables, b.seq_lens, max_dec,
                                     b.scale, ws_all, stream)
 
-    for _ in range(max(args.warmup, 3)):
-        unified()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize(dev)
-    e0.record(stream)
-    for _ in range(args.steps):
-        unified()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    binding.pa_error_check(stream)
-    unified_ms = e0.elapsed_time(e1) / args.steps
+    unified_ms = None
+    if not fp8:  # the one-launch mixed step reads a bf16 pool
+        for _ in range(max(args.warmup, 3)):
+            unified()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(args.steps):
+            unified()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        binding.pa_error_check(stream)
+        unified_ms = e0.elapsed_time(e1) / args.steps
     if rank != 0:
         return
     flops = prefill_flops(b, 0, n_pre)
     kv_dec = kv_read_bytes(sl_dec.tolist(), b.num_kv_heads, b.head_size)
     with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
         pk = json.load(f)
-    line = {"metric": "mixed chunked-prefill + decode step", "value": unified_ms, "unit": "ms",
+    line = {"metric": "mixed chunked-prefill + decode step",
+            "value": unified_ms if unified_ms is not None else sum(ms), "unit": "ms",
             "higher_is_better": False, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "dtype": "bf16", "data": "synthetic",
-            "config": workload_config(4),
-            "step": "pa_attention_varlen: cache write, then chunked prefill and decode side by "
-                    "side in one launch (decode SMs chosen on the device)",
+            "warmup": args.warmup, "dtype": "f16" if fp8 else "bf16", "data": "synthetic",
+            "config": dict(workload_config(4),
+                           kv_cache="fp8-e4m3 (per-tensor k/v scale 1/64)" if fp8 else "bf16"),
+            "step": ("pa_attention_varlen: cache write, then chunked prefill and decode side "
+                     "by side in one launch (decode SMs chosen on the device)")
+            if unified_ms is not None else
+            "FP8 pool: pa_cache_write_fp8, pa_prefill_chunk_fp8, pa_decode_fp8 in turn",
             "kernels_ms": {"pa_cache_write": ms[0], "pa_prefill_chunk": ms[1], "pa_decode": ms[2]},
             "sequential_step_ms": sum(ms),
             "prefill": {"tflops": flops / (ms[1] / 1e3) / 1e12, "flops_per_launch": flops,
                         "peak_tflops": pk["bf16_tflops"],
                         "frac": flops / (ms[1] / 1e3) / 1e12 / pk["bf16_tflops"]},
-            "decode": {"kv_gbs": kv_dec / (ms[2] / 1e3) / 1e9,
-                       "frac": kv_dec / (ms[2] / 1e3) / 1e9 / pk["hbm_gbs"]},
+            "decode": {"kv_gbs": kv_dec / (2 if fp8 else 1) / (ms[2] / 1e3) / 1e9,
+                       "frac": kv_dec / (2 if fp8 else 1) / (ms[2] / 1e3) / 1e9 / pk["hbm_gbs"]},
             "cache_write": {"gbs": 2 * b.k_new.numel() * 2 * 2 / (ms[0] / 1e3) / 1e9},
             "clocks": sampler.summary(), "gpu_launches": 4 * args.steps,
             "unified_gpu_launches_per_step": 4}

@@ -127,6 +127,21 @@ pa_status pa_decode_fp8(void *out, const void *q, const void *kv_cache, int num_
                         pa_stream_t stream);
 
 /*
+ * pa_prefill_chunk_fp8 - pa_prefill_chunk over an FP8 pool: K = code value *
+ * k_scale, V = code value * v_scale.  head_size must be 128 (else
+ * PA_ERR_UNSUPPORTED).  Each K/V tile is converted to f16 in shared memory
+ * (exactly) and the products run as f16 tcgen05 MMAs with fp32 accumulation;
+ * each query row is scaled by a power of two into f16 range first (exact), P
+ * is rounded to f16.  Other arguments, results and errors as pa_prefill_chunk.
+ */
+pa_status pa_prefill_chunk_fp8(void *out, const void *q, const int32_t *cu_q_lens,
+                               int num_chunks, int max_q_len, const void *kv_cache,
+                               int num_blocks, int block_size, int num_heads, int num_kv_heads,
+                               int head_size, const int32_t *block_tables,
+                               int max_blocks_per_seq, const int32_t *seq_lens, float scale,
+                               float k_scale, float v_scale, pa_stream_t stream);
+
+/*
  * Workspace pa_decode needs on the current device for this shape, in bytes
  * (partial softmax states of split contexts plus a small table).  Depends on
  * the device's SM count.  Returns 0 for invalid arguments.

@@ -23,7 +23,7 @@ STATUS = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_E
 
 # Every symbol include/pa.h declares.
 EXPORTS = ("pa_status_string", "pa_kv_block_bytes", "pa_kv_block_bytes_dtype", "pa_cache_write",
-           "pa_cache_write_fp8", "pa_decode_fp8",
+           "pa_cache_write_fp8", "pa_decode_fp8", "pa_prefill_chunk_fp8",
            "pa_decode_workspace_bytes", "pa_decode", "pa_decode_noalloc",
            "pa_decode_cascade_workspace_bytes", "pa_decode_cascade", "pa_prefill_chunk",
            "pa_attention_varlen_workspace_bytes", "pa_attention_varlen", "pa_error_check")
@@ -61,6 +61,9 @@ def lib(path: Optional[str] = None):
     L.pa_decode_fp8.restype = i
     L.pa_decode_fp8.argtypes = [P, P, P, i, i, i, i, i, P, i, P, i, i, ctypes.c_float,
                                 ctypes.c_float, ctypes.c_float, P, sz, P]
+    L.pa_prefill_chunk_fp8.restype = i
+    L.pa_prefill_chunk_fp8.argtypes = [P, P, P, i, i, P, i, i, i, i, i, P, i, P, ctypes.c_float,
+                                       ctypes.c_float, ctypes.c_float, P]
     L.pa_cache_write.restype = i
     L.pa_cache_write.argtypes = [P, i, i, i, i, P, P, i64, P, i, P]
     L.pa_decode_workspace_bytes.restype = sz
@@ -189,6 +192,29 @@ def pa_decode_fp8(out: torch.Tensor, q: torch.Tensor, kv_cache: torch.Tensor,
                                seq_lens.data_ptr(), B, int(max_seq_len), float(scale),
                                float(k_scale), float(v_scale), workspace.data_ptr(),
                                workspace.numel(), _stream(stream)), "pa_decode_fp8")
+
+
+def pa_prefill_chunk_fp8(out: torch.Tensor, q: torch.Tensor, cu_q_lens: torch.Tensor,
+                         max_q_len: int, kv_cache: torch.Tensor, block_tables: torch.Tensor,
+                         seq_lens: torch.Tensor, scale: float, k_scale: float, v_scale: float,
+                         stream=None) -> None:
+    """Chunked prefill over an FP8 pool (uint8 e4m3 codes times k_scale / v_scale)."""
+    NB, bs, Hkv, D = _pool8_geom(kv_cache)
+    _need(q, "q", torch.bfloat16, 3)
+    _need(out, "out", torch.bfloat16, 3)
+    _need(cu_q_lens, "cu_q_lens", torch.int32, 1)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    n = seq_lens.shape[0]
+    Hq = q.shape[1]
+    if q.shape[2] != D or out.shape != q.shape or cu_q_lens.shape[0] != n + 1 or \
+            block_tables.shape[0] != n:
+        raise ValueError("inconsistent prefill shapes")
+    _check(lib().pa_prefill_chunk_fp8(out.data_ptr(), q.data_ptr(), cu_q_lens.data_ptr(), n,
+                                      int(max_q_len), kv_cache.data_ptr(), NB, bs, Hq, Hkv, D,
+                                      block_tables.data_ptr(), block_tables.shape[1],
+                                      seq_lens.data_ptr(), float(scale), float(k_scale),
+                                      float(v_scale), _stream(stream)), "pa_prefill_chunk_fp8")
 
 
 def pa_decode_workspace_bytes(num_seqs: int, num_heads: int, num_kv_heads: int,

@@ -426,6 +426,27 @@ pa_status pa_attention_varlen(void *out, const void *q, const void *k_new, const
     return PA_OK;
 }
 
+pa_status pa_prefill_chunk_fp8(void *out, const void *q, const int32_t *cu_q_lens,
+                               int num_chunks, int max_q_len, const void *kv_cache,
+                               int num_blocks, int block_size, int num_heads, int num_kv_heads,
+                               int head_size, const int32_t *block_tables,
+                               int max_blocks_per_seq, const int32_t *seq_lens, float scale,
+                               float k_scale, float v_scale, pa_stream_t stream) {
+    bool none = false;
+    pa_status st = prefill_checks(out, q, cu_q_lens, num_chunks, max_q_len, kv_cache, num_blocks,
+                                  block_size, num_heads, num_kv_heads, head_size, block_tables,
+                                  max_blocks_per_seq, seq_lens, scale, &none);
+    if (st != PA_OK) return st;
+    if (head_size != 128) return PA_ERR_UNSUPPORTED;
+    if (!good_scale(k_scale) || !good_scale(v_scale)) return PA_ERR_INVALID_ARG;
+    if (none) return PA_OK;
+    pa::KvGeom g{num_blocks, block_size, num_kv_heads, head_size};
+    return from_cuda(pa::launch_prefill_fp8(out, q, cu_q_lens, num_chunks, max_q_len, kv_cache,
+                                            g, num_heads, block_tables, max_blocks_per_seq,
+                                            seq_lens, scale, k_scale, v_scale,
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
 pa_status pa_error_check(pa_stream_t stream) {
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return PA_ERR_CUDA;

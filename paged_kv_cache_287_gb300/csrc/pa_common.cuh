@@ -358,6 +358,12 @@ __device__ __forceinline__ uint64_t tc_desc_sw128(uint32_t smem_addr, uint32_t l
 
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 D, M x N, A K-major,
 // B K-major (b_mn_major = 0) or MN-major (1).
+// Same for f16 A and B (format fields 0).
+__host__ __device__ constexpr uint32_t tc_idesc_f16(int m, int n, int b_mn_major) {
+    return (1u << 4) | ((uint32_t)b_mn_major << 16) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(m >> 4) << 24);
+}
+
 __host__ __device__ constexpr uint32_t tc_idesc_bf16(int m, int n, int b_mn_major) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn_major << 16) |
            ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);

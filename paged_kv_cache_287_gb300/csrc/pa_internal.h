@@ -85,6 +85,13 @@ cudaError_t launch_mixed(void *out, const void *q, const int32_t *cu_q_lens, int
                          int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs,
                          float scale, void *workspace, cudaStream_t stream);
 
+// Chunked prefill over an FP8 pool (head_size 128).
+cudaError_t launch_prefill_fp8(void *out, const void *q, const int32_t *cu_q_lens,
+                               int num_chunks, int max_q_len, const void *kv_cache,
+                               const KvGeom &g, int num_heads, const int32_t *block_tables,
+                               int max_blocks_per_seq, const int32_t *seq_lens, float scale,
+                               float k_scale, float v_scale, cudaStream_t stream);
+
 cudaError_t launch_prefill(void *out, const void *q, const int32_t *cu_q_lens, int num_chunks,
                            int max_q_len, const void *kv_cache, const KvGeom &g, int num_heads,
                            const int32_t *block_tables, int max_blocks_per_seq,

@@ -76,6 +76,7 @@ struct PrefillArgs {
     float *part_ml;    // [splits][num_seqs][num_heads][2]: m (log2 units), l
     float *part_acc;   // [splits][num_seqs][num_heads][D]
     int shared_len, split_tiles, prefix_rows;  // prefix_rows: the batch's sequences
+    float k_scale, v_scale;  // FP8 pool: real K/V = e4m3 value * scale (1 for bf16)
 };
 
 template <int D>
@@ -107,7 +108,13 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity) {
 // One prefill CTA at (virtual) block index bid of a grid of size grid; called by
 // prefill_tc_kernel and by the mixed-batch kernel (whose CTAs may have more warps
 // than kTcWarps: the extra warps only take part in the CTA-wide barriers).
-template <int D>
+// KV8: an FP8 (e4m3) pool.  Each K/V tile then lands by TMA in the upper half of
+// its ring slot, and the extra warp kTcWarps converts it in place to f16 (every
+// e4m3 value is an f16 value), one row per lane: a row's f16 output overwrites
+// only that row's codes.  The products run as f16 MMAs; each query row is scaled
+// by a power of two into f16 range, and the scores are scaled back with k_scale;
+// P is f16, and v_scale multiplies the normalised output.
+template <int D, bool KV8 = false>
 __device__ __forceinline__ void prefill_body(const CUtensorMap &kv_map, const PrefillArgs &a,
                                              const uint3 bid, const uint3 grid) {
     using L = TcLay<D>;
@@ -124,6 +131,8 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &kv_map, const Pr
     uint64_t *q_full = bars + 22;  // [2]
     uint64_t *drain = bars + 24;   // [2], one per issuer
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 26);
+    // FP8 pool: a tile's codes have landed in its slot's upper half.
+    uint64_t *k_staged = bars + 27, *v_staged = bars + 30;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // Grid (query tile, head, chunk rank): CTAs are dispatched in that order, so
@@ -201,6 +210,10 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &kv_map, const Pr
             mbar_init(&q_full[i], 4);
             mbar_init(&drain[i], 1);
         }
+        if (KV8) {
+            for (int i = 0; i < kKSlots; ++i) mbar_init(&k_staged[i], 1);
+            for (int i = 0; i < kVSlots; ++i) mbar_init(&v_staged[i], 1);
+        }
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -229,13 +242,22 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &kv_map, const Pr
         int nxt = box_row(0);
         int issued = 0;
         auto load = [&](uint8_t *dst, uint64_t *bar, int row) {
-            if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)L::kKBytes);
-            __syncwarp();
-            if (lane < nbox) {
+            if constexpr (KV8) {
+                // The tile's codes (128 bytes per key) into the slot's upper half.
+                if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(kTcKeys * 128));
+                __syncwarp();
+                if (lane < nbox)
+                    tma_load_2d_hint(dst + L::kKBytes / 2 + lane * box_rows * 128, &kv_map, bar,
+                                     0, row, policy);
+            } else {
+                if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)L::kKBytes);
+                __syncwarp();
+                if (lane < nbox) {
 #pragma unroll
-                for (int p = 0; p < L::kPanels; ++p)
-                    tma_load_2d_hint(dst + p * L::kKvPanel + lane * box_rows * 128, &kv_map, bar,
-                                     64 * p, row, policy);
+                    for (int p = 0; p < L::kPanels; ++p)
+                        tma_load_2d_hint(dst + p * L::kKvPanel + lane * box_rows * 128, &kv_map,
+                                         bar, 64 * p, row, policy);
+                }
             }
         };
         for (int kt = 0; kt < n_kt; ++kt) {
@@ -247,24 +269,26 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &kv_map, const Pr
                 if (lane == 0) atomicOr(&g_err_prefill, kErrTimeout);
                 break;
             }
-            load(sK + ks * L::kKBytes, &k_full[ks], cur);
+            load(sK + ks * L::kKBytes, KV8 ? &k_staged[ks] : &k_full[ks], cur);
             if (kt >= kVSlots &&
                 !warp_wait(&v_empty[vs], (uint32_t)(kt / kVSlots - 1) & 1u)) {
                 if (lane == 0) atomicOr(&g_err_prefill, kErrTimeout);
                 issued = -(kt + 1);  // K of tile kt is in flight, V is not
                 break;
             }
-            load(sV + vs * L::kKBytes, &v_full[vs], cur < -(1 << 29) ? cur : cur + v_off);
+            load(sV + vs * L::kKBytes, KV8 ? &v_staged[vs] : &v_full[vs],
+                 cur < -(1 << 29) ? cur : cur + v_off);
             issued = kt + 1;
         }
         // Never leave with copies in flight into this CTA's shared memory.
         {
             const int last = issued < 0 ? -issued : issued;   // tiles whose K was issued
             const int vlast = issued < 0 ? last - 1 : last;    // tiles whose V was issued
+            uint64_t *kb = KV8 ? k_staged : k_full, *vb = KV8 ? v_staged : v_full;
             for (int kt = std::max(0, last - kKSlots); kt < last; ++kt)
-                mbar_wait_bounded(&k_full[kt % kKSlots], (uint32_t)(kt / kKSlots) & 1u);
+                mbar_wait_bounded(&kb[kt % kKSlots], (uint32_t)(kt / kKSlots) & 1u);
             for (int kt = std::max(0, vlast - kVSlots); kt < vlast; ++kt)
-                mbar_wait_bounded(&v_full[kt % kVSlots], (uint32_t)(kt / kVSlots) & 1u);
+                mbar_wait_bounded(&vb[kt % kVSlots], (uint32_t)(kt / kVSlots) & 1u);
         }
     } else if (warp == 1 || (warp == kTcWarps - 1 && has1)) {
         // ------------------------------------------------------------ MMA issuers
@@ -273,8 +297,9 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &kv_map, const Pr
         // hand-over, and while one issuer waits for its P.V to finish the other's
         // products keep the tensor cores busy.
         const int t = warp == 1 ? 0 : 1;
-        const uint32_t idesc_s = tc_idesc_bf16(kTcRows, kHalf, 0);
-        const uint32_t idesc_pv = tc_idesc_bf16(kTcRows, D, 1);
+        const uint32_t idesc_s =
+            KV8 ? tc_idesc_f16(kTcRows, kHalf, 0) : tc_idesc_bf16(kTcRows, kHalf, 0);
+        const uint32_t idesc_pv = KV8 ? tc_idesc_f16(kTcRows, D, 1) : tc_idesc_bf16(kTcRows, D, 1);
         const uint32_t q_base = smem_u32(sQ) + t * L::kQTile;
         const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV);
         // S_t,f = Q_t . K_j[64 f, 64 f + 64)^T into tensor-memory columns
@@ -351,6 +376,51 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &kv_map, const Pr
         if (lane == 0) tc_commit(&drain[t]);
         __syncwarp();
         mbar_wait_bounded(&drain[t], 0);
+    } else if (KV8 && warp == kTcWarps) {
+        // ------------------------------------------------------------ e4m3 -> f16
+        // A lane converts whole rows (keys) of the tile: reads the row's 128 codes
+        // (8 chunks, 128B-swizzled as TMA left them in the upper half), then writes
+        // its 128 f16 values into the two 64-dim panels.  Panel 1 is the upper
+        // half, and row r of it is exactly the bytes of code row r, which this lane
+        // has already read.
+        auto convert = [&](uint8_t *slot) {
+            const uint8_t *codes = slot + L::kKBytes / 2;
+#pragma unroll 1
+            for (int r = lane; r < kTcKeys; r += 32) {
+                uint4 in[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    in[c] = *reinterpret_cast<const uint4 *>(codes + r * 128 + ((c ^ (r & 7)) << 4));
+                asm volatile("" ::: "memory");
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t f[8];
+                    e4m3x4_to_f16x4(in[c].x, f[0], f[1]);
+                    e4m3x4_to_f16x4(in[c].y, f[2], f[3]);
+                    e4m3x4_to_f16x4(in[c].z, f[4], f[5]);
+                    e4m3x4_to_f16x4(in[c].w, f[6], f[7]);
+                    uint8_t *dst = slot + (c >> 2) * L::kKvPanel + r * 128;
+                    const int ch = 2 * (c & 3);
+                    *reinterpret_cast<uint4 *>(dst + ((ch ^ (r & 7)) << 4)) =
+                        make_uint4(f[0], f[1], f[2], f[3]);
+                    *reinterpret_cast<uint4 *>(dst + (((ch + 1) ^ (r & 7)) << 4)) =
+                        make_uint4(f[4], f[5], f[6], f[7]);
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+        };
+        bool ok = true;
+        for (int kt = 0; ok && kt < n_kt; ++kt) {
+            const int ks = kt % kKSlots, vs = kt % kVSlots;
+            if (!(ok = warp_wait(&k_staged[ks], (uint32_t)(kt / kKSlots) & 1u))) break;
+            convert(sK + ks * L::kKBytes);
+            if (lane == 0) mbar_arrive(&k_full[ks]);
+            if (!(ok = warp_wait(&v_staged[vs], (uint32_t)(kt / kVSlots) & 1u))) break;
+            convert(sV + vs * L::kKBytes);
+            if (lane == 0) mbar_arrive(&v_full[vs]);
+        }
+        if (!ok && lane == 0) atomicOr(&g_err_prefill, kErrTimeout);
     } else if (warp >= 2 && warp < 2 + 4 * kTcTiles && ((warp - 2) / 4 == 0 || has1)) {
         // ------------------------------------------------------------ softmax warpgroups
         const int t = (warp - 2) / 4;             // query tile of this warpgroup
@@ -362,29 +432,64 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &kv_map, const Pr
         const bool real = row < QT * G && t0 + tok < q_len;
         // Query row -> shared memory in the 128B-swizzled K-major layout.  Loads
         // are bounds-checked: the host does not know the total number of rows.
+        float sl2 = a.scale_log2;  // > 0: a negative scale was moved into Q
         {
             const uint4 *src = reinterpret_cast<const uint4 *>(
                 a.q + ((size_t)(q0 + t0 + tok) * a.num_heads + (size_t)h * G + gq) * D);
             const uint32_t flip = a.negate_q ? 0x80008000u : 0u;  // exact bf16 negation
             uint8_t *qt_smem = sQ + t * L::kQTile;
+            if constexpr (!KV8) {
 #pragma unroll
-            for (int p = 0; p < L::kPanels; ++p)
+                for (int p = 0; p < L::kPanels; ++p)
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    uint4 v = real ? src[p * 8 + c] : make_uint4(0, 0, 0, 0);
-                    v.x ^= flip;
-                    v.y ^= flip;
-                    v.z ^= flip;
-                    v.w ^= flip;
-                    *reinterpret_cast<uint4 *>(qt_smem + p * L::kQPanel + row * 128 +
-                                               ((c ^ (row & 7)) << 4)) = v;
+                    for (int c = 0; c < 8; ++c) {
+                        uint4 v = real ? src[p * 8 + c] : make_uint4(0, 0, 0, 0);
+                        v.x ^= flip;
+                        v.y ^= flip;
+                        v.z ^= flip;
+                        v.w ^= flip;
+                        *reinterpret_cast<uint4 *>(qt_smem + p * L::kQPanel + row * 128 +
+                                                   ((c ^ (row & 7)) << 4)) = v;
+                    }
+            } else {
+                // f16 query: the row times the power of two that puts its largest
+                // element in [1, 2) (exact: f16 keeps every bf16 significand); the
+                // scores are scaled back, together with k_scale, through sl2.
+                uint4 v[D / 8];
+                float mx = 0.f;
+#pragma unroll
+                for (int c = 0; c < D / 8; ++c) {
+                    v[c] = real ? src[c] : make_uint4(0, 0, 0, 0);
+                    v[c].x ^= flip;
+                    v[c].y ^= flip;
+                    v[c].z ^= flip;
+                    v[c].w ^= flip;
+                    mx = fmax3(mx, fabsf(bf16_lo(v[c].x)), fabsf(bf16_hi(v[c].x)));
+                    mx = fmax3(mx, fabsf(bf16_lo(v[c].y)), fabsf(bf16_hi(v[c].y)));
+                    mx = fmax3(mx, fabsf(bf16_lo(v[c].z)), fabsf(bf16_hi(v[c].z)));
+                    mx = fmax3(mx, fabsf(bf16_lo(v[c].w)), fabsf(bf16_hi(v[c].w)));
                 }
+                int ex = mx > 0.f ? (int)((__float_as_uint(mx) >> 23) & 0xffu) - 127 : 0;
+                ex = max(-126, min(126, ex));
+                const float down = __uint_as_float((uint32_t)(127 - ex) << 23);  // 2^-ex
+                sl2 *= a.k_scale * __uint_as_float((uint32_t)(127 + ex) << 23);
+#pragma unroll
+                for (int c = 0; c < D / 8; ++c) {
+                    const uint4 h4 = make_uint4(
+                        pack_f16(bf16_lo(v[c].x) * down, bf16_hi(v[c].x) * down),
+                        pack_f16(bf16_lo(v[c].y) * down, bf16_hi(v[c].y) * down),
+                        pack_f16(bf16_lo(v[c].z) * down, bf16_hi(v[c].z) * down),
+                        pack_f16(bf16_lo(v[c].w) * down, bf16_hi(v[c].w) * down));
+                    const int p = c / 8, ch = c % 8;
+                    *reinterpret_cast<uint4 *>(qt_smem + p * L::kQPanel + row * 128 +
+                                               ((ch ^ (row & 7)) << 4)) = h4;
+                }
+            }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&q_full[t]);
         }
         const int lim = real && !prefix ? std::min(ctx + t0 + tok, len - 1) : len - 1;
-        const float sl2 = a.scale_log2;  // > 0: a negative scale was moved into Q
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; ok && j < n_kt; ++j) {
@@ -459,8 +564,8 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &kv_map, const Pr
                         const float p2 = fast_exp2(t2), p3 = fast_exp2(t3);
                         add2(s0, s1, p0, p1);
                         add2(s2, s3, p2, p3);
-                        pk[c] = pack_bf16(p0, p1);
-                        pk[c + 1] = pack_bf16(p2, p3);
+                        pk[c] = KV8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
+                        pk[c + 1] = KV8 ? pack_f16(p2, p3) : pack_bf16(p2, p3);
                     }
                     tmem_st16(cf + 16 * qr, pk);
                 }
@@ -513,7 +618,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &kv_map, const Pr
                 }
                 if (real) reinterpret_cast<float2 *>(a.part_ml)[rec] = make_float2(m, l);
             } else {
-            const float inv = 1.f / l;
+            const float inv = (KV8 ? a.v_scale : 1.f) / l;
             uint4 *dst = reinterpret_cast<uint4 *>(
                 a.out + ((size_t)(q0 + t0 + tok) * a.num_heads + (size_t)h * G + gq) * D);
 #pragma unroll
@@ -542,21 +647,21 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &kv_map, const Pr
     }
 }
 
-template <int D>
-__global__ void __launch_bounds__(kTcThreads, 1)
+template <int D, bool KV8 = false>
+__global__ void __launch_bounds__((kTcWarps + (KV8 ? 1 : 0)) * 32, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const PrefillArgs a) {
-    prefill_body<D>(kv_map, a, blockIdx, gridDim);
+    prefill_body<D, KV8>(kv_map, a, blockIdx, gridDim);
 }
 
-template <int D>
+template <int D, bool KV8 = false>
 cudaError_t launch_prefill_tc(const PrefillArgs &a, const CUtensorMap &map, dim3 grid,
                               cudaStream_t stream) {
     const size_t smem = TcLay<D>::kSmem;
-    auto kern = prefill_tc_kernel<D>;
+    auto kern = prefill_tc_kernel<D, KV8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kTcThreads, smem, stream>>>(map, a);
+    kern<<<grid, (kTcWarps + (KV8 ? 1 : 0)) * 32, smem, stream>>>(map, a);
     return cudaGetLastError();
 }
 
@@ -597,6 +702,7 @@ PrefillArgs make_prefill_args(void *out, const void *q, const int32_t *cu_q_lens
     a.part_ml = nullptr;
     a.part_acc = nullptr;
     a.shared_len = a.split_tiles = a.prefix_rows = 0;
+    a.k_scale = a.v_scale = 1.f;
     const int per_cta = kTcTiles * a.q_tile;
     *grid = dim3((unsigned)((max_q_len + per_cta - 1) / per_cta), (unsigned)g.num_kv_heads,
                  (unsigned)num_chunks);
@@ -618,6 +724,23 @@ cudaError_t launch_prefill(void *out, const void *q, const int32_t *cu_q_lens, i
                                             seq_lens, scale, &grid);
     if (g.head_size == 128) return launch_prefill_tc<128>(a, map, grid, stream);
     return launch_prefill_tc<64>(a, map, grid, stream);
+}
+
+cudaError_t launch_prefill_fp8(void *out, const void *q, const int32_t *cu_q_lens,
+                               int num_chunks, int max_q_len, const void *kv_cache,
+                               const KvGeom &g, int num_heads, const int32_t *block_tables,
+                               int max_blocks_per_seq, const int32_t *seq_lens, float scale,
+                               float k_scale, float v_scale, cudaStream_t stream) {
+    CUtensorMap map;
+    if (g.head_size != 128 ||
+        !encode_kv_map_fp8(&map, kv_cache, g, g.block_size >= 16 ? 16 : g.block_size))
+        return cudaErrorInvalidValue;
+    dim3 grid;
+    PrefillArgs a = make_prefill_args(out, q, cu_q_lens, num_chunks, max_q_len, g, num_heads,
+                                      block_tables, max_blocks_per_seq, seq_lens, scale, &grid);
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    return launch_prefill_tc<128, true>(a, map, grid, stream);
 }
 
 int prefix_splits(int num_seqs, int num_heads, int num_kv_heads, int shared_len, int sm_count) {
@@ -662,6 +785,7 @@ cudaError_t launch_prefix_partials(const void *q, const void *kv_cache, const Kv
     const int tiles = (shared_len + kTcKeys - 1) / kTcKeys;
     a.split_tiles = (tiles + splits - 1) / splits;
     a.prefix_rows = num_seqs;
+    a.k_scale = a.v_scale = 1.f;
     const int per_cta = kTcTiles * a.q_tile;
     dim3 grid((unsigned)((num_seqs + per_cta - 1) / per_cta), (unsigned)g.num_kv_heads,
               (unsigned)splits);

@@ -158,3 +158,56 @@ def test_fp8_decode_rejects_head_size_64():
     with pytest.raises(binding.PaError) as e:
         _decode(b, pool8, 1.0, 1.0)
     assert e.value.status == 2
+
+
+PREFILL_SHAPES = [
+    # seq_lens, q_lens, Hq, Hkv, bs
+    ([300, 40, 513], [129, 40, 200], 32, 8, 16),   # group 4, several tiles, ragged
+    ([150, 260], [70, 129], 8, 8, 8),              # group 1, block 8
+    ([2000, 700], [1024, 333], 64, 8, 32),         # group 8, block 32, long
+    ([37, 5], [37, 1], 24, 8, 16),                 # group 3, tiny chunks
+]
+
+
+@pytest.mark.parametrize("case", range(len(PREFILL_SHAPES)))
+def test_fp8_prefill_small_shapes(case):
+    lens, qls, Hq, Hkv, bs = PREFILL_SHAPES[case]
+    b = make_batch(name=f"p8{case}", seq_lens=lens, q_lens=qls, num_heads=Hq, num_kv_heads=Hkv,
+                   head_size=128, block_size=bs, scale=128 ** -0.5, seed=870 + case, device=DEV)
+    pool8 = fp8_pool_of(b)
+    codes = _write(b, pool8, FP8_K_SCALE, FP8_V_SCALE)
+    out = torch.full_like(b.q, float("nan"))
+    binding.pa_prefill_chunk_fp8(out, b.q, b.cu_q_lens, max(qls), pool8, b.block_tables,
+                                 b.seq_lens, b.scale, FP8_K_SCALE, FP8_V_SCALE)
+    binding.pa_error_check()
+    compare(out, _oracle(b, codes, FP8_K_SCALE, FP8_V_SCALE), f"fp8 prefill case {case}")
+
+
+@pytest.mark.parametrize("scale", [-0.1, 0.0])
+def test_fp8_prefill_negative_and_zero_scale_and_other_kv_scales(scale):
+    b = make_batch(name="p8s", seq_lens=[400, 90], q_lens=[200, 90], num_heads=16,
+                   num_kv_heads=4, head_size=128, block_size=16, scale=scale, seed=880,
+                   q_scale=300.0, device=DEV)
+    ks, vs = 0.2, 0.0045
+    pool8 = fp8_pool_of(b, ks, vs)
+    codes = _write(b, pool8, ks, vs)
+    out = torch.full_like(b.q, float("nan"))
+    binding.pa_prefill_chunk_fp8(out, b.q, b.cu_q_lens, 200, pool8, b.block_tables, b.seq_lens,
+                                 b.scale, ks, vs)
+    binding.pa_error_check()
+    compare(out, _oracle(b, codes, ks, vs), f"fp8 prefill, scale {scale}")
+
+
+def test_fp8_prefill_mixed_workload_chunks():
+    b = make_config(4, device=DEV)
+    pool8 = fp8_pool_of(b)
+    codes = _write(b, pool8, FP8_K_SCALE, FP8_V_SCALE)
+    q = b.q[:4096]
+    out = torch.full_like(q, float("nan"))
+    binding.pa_prefill_chunk_fp8(out, q, b.cu_q_lens[:9].contiguous(), 512, pool8,
+                                 b.block_tables[:8], b.seq_lens[:8], b.scale, FP8_K_SCALE,
+                                 FP8_V_SCALE)
+    binding.pa_error_check()
+    rows = np.arange(0, 4096, 41, dtype=np.int32)
+    compare(out[torch.as_tensor(rows, device=DEV).long()],
+            _oracle(b, codes, FP8_K_SCALE, FP8_V_SCALE, rows), "fp8 prefill, mixed workload")
