@@ -637,23 +637,27 @@ def run_mixed(args, world, rank, local):
         device=dev)
 
     def unified():
-        binding.pa_attention_varlen(out_all, b.q, b.k_new, b.v_new, b.slot_mapping, cu_pre, n_pre,
-                                    r_pre, max_q, b.kv_cache, b.block_tables, b.seq_lens, max_dec,
-                                    b.scale, ws_all, stream)
+        if fp8:
+            binding.pa_attention_varlen(out_all, b.q, b.k_new, b.v_new, b.slot_mapping, cu_pre,
+                                        n_pre, r_pre, max_q, pool8, b.block_tables, b.seq_lens,
+                                        max_dec, b.scale, ws_all, stream,
+                                        kv_scales=(FP8_K_SCALE, FP8_V_SCALE))
+        else:
+            binding.pa_attention_varlen(out_all, b.q, b.k_new, b.v_new, b.slot_mapping, cu_pre,
+                                        n_pre, r_pre, max_q, b.kv_cache, b.block_tables,
+                                        b.seq_lens, max_dec, b.scale, ws_all, stream)
 
-    unified_ms = None
-    if not fp8:  # the one-launch mixed step reads a bf16 pool
-        for _ in range(max(args.warmup, 3)):
-            unified()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize(dev)
-        e0.record(stream)
-        for _ in range(args.steps):
-            unified()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        binding.pa_error_check(stream)
-        unified_ms = e0.elapsed_time(e1) / args.steps
+    for _ in range(max(args.warmup, 3)):
+        unified()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(args.steps):
+        unified()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    binding.pa_error_check(stream)
+    unified_ms = e0.elapsed_time(e1) / args.steps
     if rank != 0:
         return
     flops = prefill_flops(b, 0, n_pre)
@@ -661,15 +665,14 @@ def run_mixed(args, world, rank, local):
     with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
         pk = json.load(f)
     line = {"metric": "mixed chunked-prefill + decode step",
-            "value": unified_ms if unified_ms is not None else sum(ms), "unit": "ms",
+            "value": unified_ms, "unit": "ms",
             "higher_is_better": False, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "dtype": "f16" if fp8 else "bf16", "data": "synthetic",
             "config": dict(workload_config(4),
                            kv_cache="fp8-e4m3 (per-tensor k/v scale 1/64)" if fp8 else "bf16"),
-            "step": ("pa_attention_varlen: cache write, then chunked prefill and decode side "
-                     "by side in one launch (decode SMs chosen on the device)")
-            if unified_ms is not None else
-            "FP8 pool: pa_cache_write_fp8, pa_prefill_chunk_fp8, pa_decode_fp8 in turn",
+            "step": "pa_attention_varlen: cache write, then chunked prefill and decode side "
+                    "by side in one launch (decode SMs chosen on the device)"
+                    + ("; FP8 pool" if fp8 else ""),
             "kernels_ms": {"pa_cache_write": ms[0], "pa_prefill_chunk": ms[1], "pa_decode": ms[2]},
             "sequential_step_ms": sum(ms),
             "prefill": {"tflops": flops / (ms[1] / 1e3) / 1e12, "flops_per_launch": flops,

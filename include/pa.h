@@ -303,6 +303,22 @@ pa_status pa_attention_varlen(void *out, const void *q, const void *k_new, const
                               void *workspace, size_t workspace_bytes, pa_stream_t stream);
 
 /*
+ * pa_attention_varlen_fp8 - pa_attention_varlen over an FP8 pool: the writes
+ * quantise as pa_cache_write_fp8, the chunks and decode tokens read as
+ * pa_prefill_chunk_fp8 and pa_decode_fp8 (head_size 128), in one launch when
+ * both are present.  Workspace: pa_attention_varlen_workspace_bytes.
+ */
+pa_status pa_attention_varlen_fp8(void *out, const void *q, const void *k_new,
+                                  const void *v_new, const int32_t *slot_mapping,
+                                  const int32_t *cu_q_lens, int num_seqs, int num_prefills,
+                                  int num_prefill_tokens, int max_prefill_q_len, void *kv_cache,
+                                  int num_blocks, int block_size, int num_heads,
+                                  int num_kv_heads, int head_size, const int32_t *block_tables,
+                                  int max_blocks_per_seq, const int32_t *seq_lens,
+                                  int max_seq_len, float scale, float k_scale, float v_scale,
+                                  void *workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/*
  * Synchronise `stream`, then read and clear the device error word the kernels
  * of this library set on the current device.  Returns PA_OK, PA_ERR_OOB,
  * PA_ERR_TIMEOUT, or PA_ERR_CUDA if the synchronisation itself failed.

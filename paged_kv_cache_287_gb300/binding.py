@@ -26,7 +26,8 @@ EXPORTS = ("pa_status_string", "pa_kv_block_bytes", "pa_kv_block_bytes_dtype", "
            "pa_cache_write_fp8", "pa_decode_fp8", "pa_prefill_chunk_fp8",
            "pa_decode_workspace_bytes", "pa_decode", "pa_decode_noalloc",
            "pa_decode_cascade_workspace_bytes", "pa_decode_cascade", "pa_prefill_chunk",
-           "pa_attention_varlen_workspace_bytes", "pa_attention_varlen", "pa_error_check")
+           "pa_attention_varlen_workspace_bytes", "pa_attention_varlen",
+           "pa_attention_varlen_fp8", "pa_error_check")
 
 
 class PaError(RuntimeError):
@@ -84,6 +85,10 @@ def lib(path: Optional[str] = None):
     L.pa_attention_varlen.restype = i
     L.pa_attention_varlen.argtypes = [P, P, P, P, P, P, i, i, i, i, P, i, i, i, i, i, P, i, P, i,
                                       ctypes.c_float, P, sz, P]
+    L.pa_attention_varlen_fp8.restype = i
+    L.pa_attention_varlen_fp8.argtypes = [P, P, P, P, P, P, i, i, i, i, P, i, i, i, i, i, P, i, P,
+                                          i, ctypes.c_float, ctypes.c_float, ctypes.c_float, P,
+                                          sz, P]
     L.pa_error_check.restype = i
     L.pa_error_check.argtypes = [P]
     if path is None:
@@ -319,10 +324,18 @@ def pa_attention_varlen(out: torch.Tensor, q: torch.Tensor, k_new: Optional[torc
                         cu_q_lens: torch.Tensor, num_prefills: int, num_prefill_tokens: int,
                         max_prefill_q_len: int, kv_cache: torch.Tensor,
                         block_tables: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
-                        scale: float, workspace: torch.Tensor, stream=None) -> None:
+                        scale: float, workspace: torch.Tensor, stream=None,
+                        kv_scales: Optional[tuple] = None) -> None:
     """One step over a flattened mixed batch (chunks first, then decode tokens):
-    optional cache write, chunked prefill, decode."""
-    NB, bs, Hkv, D = _pool_geom(kv_cache)
+    optional cache write, chunked prefill, decode.  A uint8 kv_cache is an FP8
+    (e4m3) pool and needs kv_scales = (k_scale, v_scale)."""
+    fp8 = kv_cache.dtype == torch.uint8
+    if fp8:
+        if kv_scales is None:
+            raise ValueError("an FP8 pool needs kv_scales=(k_scale, v_scale)")
+        NB, bs, Hkv, D = _pool8_geom(kv_cache)
+    else:
+        NB, bs, Hkv, D = _pool_geom(kv_cache)
     _need(q, "q", torch.bfloat16, 3)
     _need(out, "out", torch.bfloat16, 3)
     _need(cu_q_lens, "cu_q_lens", torch.int32, 1)
@@ -343,14 +356,17 @@ def pa_attention_varlen(out: torch.Tensor, q: torch.Tensor, k_new: Optional[torc
                 slot_mapping.shape[0] != rows:
             raise ValueError("k_new/v_new/slot_mapping must have one row per query row")
         kp, vp, sp = k_new.data_ptr(), v_new.data_ptr(), slot_mapping.data_ptr()
-    _check(lib().pa_attention_varlen(out.data_ptr(), q.data_ptr(), kp, vp, sp,
-                                     cu_q_lens.data_ptr(), B, int(num_prefills),
-                                     int(num_prefill_tokens), int(max_prefill_q_len),
-                                     kv_cache.data_ptr(), NB, bs, Hq, Hkv, D,
-                                     block_tables.data_ptr(), block_tables.shape[1],
-                                     seq_lens.data_ptr(), int(max_seq_len), float(scale),
-                                     workspace.data_ptr(), workspace.numel(), _stream(stream)),
-           "pa_attention_varlen")
+    common = (out.data_ptr(), q.data_ptr(), kp, vp, sp, cu_q_lens.data_ptr(), B, int(num_prefills),
+              int(num_prefill_tokens), int(max_prefill_q_len), kv_cache.data_ptr(), NB, bs, Hq,
+              Hkv, D, block_tables.data_ptr(), block_tables.shape[1], seq_lens.data_ptr(),
+              int(max_seq_len), float(scale))
+    if fp8:
+        _check(lib().pa_attention_varlen_fp8(*common, float(kv_scales[0]), float(kv_scales[1]),
+                                             workspace.data_ptr(), workspace.numel(),
+                                             _stream(stream)), "pa_attention_varlen_fp8")
+    else:
+        _check(lib().pa_attention_varlen(*common, workspace.data_ptr(), workspace.numel(),
+                                         _stream(stream)), "pa_attention_varlen")
 
 
 def pa_error_check(stream=None) -> None:

@@ -350,14 +350,15 @@ size_t pa_attention_varlen_workspace_bytes(int num_seqs, int num_prefills, int n
     return pa::mixed_workspace_bytes(num_seqs - num_prefills, head_size, pa::device_sm_count());
 }
 
-pa_status pa_attention_varlen(void *out, const void *q, const void *k_new, const void *v_new,
-                              const int32_t *slot_mapping, const int32_t *cu_q_lens,
-                              int num_seqs, int num_prefills, int num_prefill_tokens,
-                              int max_prefill_q_len, void *kv_cache, int num_blocks,
-                              int block_size, int num_heads, int num_kv_heads, int head_size,
-                              const int32_t *block_tables, int max_blocks_per_seq,
-                              const int32_t *seq_lens, int max_seq_len, float scale,
-                              void *workspace, size_t workspace_bytes, pa_stream_t stream) {
+// pa_attention_varlen over a bf16 pool, or (kv8) pa_attention_varlen_fp8.
+static pa_status varlen_impl(void *out, const void *q, const void *k_new, const void *v_new,
+                             const int32_t *slot_mapping, const int32_t *cu_q_lens, int num_seqs,
+                             int num_prefills, int num_prefill_tokens, int max_prefill_q_len,
+                             void *kv_cache, int num_blocks, int block_size, int num_heads,
+                             int num_kv_heads, int head_size, const int32_t *block_tables,
+                             int max_blocks_per_seq, const int32_t *seq_lens, int max_seq_len,
+                             float scale, bool kv8, float k_scale, float v_scale,
+                             void *workspace, size_t workspace_bytes, pa_stream_t stream) {
     pa_status st = check_pool(kv_cache, num_blocks, block_size, num_kv_heads, head_size);
     if (st != PA_OK) return st;
     if ((st = check_heads(num_heads, num_kv_heads)) != PA_OK) return st;
@@ -366,22 +367,27 @@ pa_status pa_attention_varlen(void *out, const void *q, const void *k_new, const
         return PA_ERR_INVALID_ARG;
     if (num_prefills > 0 && num_prefill_tokens < num_prefills) return PA_ERR_INVALID_ARG;
     if (num_prefills == 0 && num_prefill_tokens != 0) return PA_ERR_INVALID_ARG;
+    if (kv8 && head_size != 128) return PA_ERR_UNSUPPORTED;
+    if (kv8 && (!good_scale(k_scale) || !good_scale(v_scale))) return PA_ERR_INVALID_ARG;
     if (num_seqs == 0) return PA_OK;
     const int num_decodes = num_seqs - num_prefills;
     const int64_t rows = (int64_t)num_prefill_tokens + num_decodes;
     const int64_t row_elems = (int64_t)num_heads * head_size;
     // 1. The step's new K/V into their slots (one row per query row).
     if (slot_mapping) {
-        st = pa_cache_write(kv_cache, num_blocks, block_size, num_kv_heads, head_size, k_new,
-                            v_new, (int64_t)num_kv_heads * head_size, slot_mapping, (int)rows,
-                            stream);
+        st = kv8 ? pa_cache_write_fp8(kv_cache, num_blocks, block_size, num_kv_heads, head_size,
+                                      k_new, v_new, (int64_t)num_kv_heads * head_size,
+                                      slot_mapping, (int)rows, k_scale, v_scale, stream)
+                 : pa_cache_write(kv_cache, num_blocks, block_size, num_kv_heads, head_size,
+                                  k_new, v_new, (int64_t)num_kv_heads * head_size, slot_mapping,
+                                  (int)rows, stream);
         if (st != PA_OK) return st;
     }
     // 2+3 in one launch when both parts are present: decode and prefill side by
     // side on disjoint SMs.
     const size_t off = (size_t)num_prefill_tokens * (size_t)row_elems * 2;
     pa::KvGeom g{num_blocks, block_size, num_kv_heads, head_size};
-    if (num_prefills > 0 && num_decodes > 0 && pa::mixed_supported(num_decodes, num_heads, g)) {
+    if (num_prefills > 0 && num_decodes > 0 && pa::mixed_supported(num_decodes, num_heads, g, kv8)) {
         bool none_p = false, none_d = false;
         st = prefill_checks(out, q, cu_q_lens, num_prefills, max_prefill_q_len, kv_cache,
                             num_blocks, block_size, num_heads, num_kv_heads, head_size,
@@ -402,28 +408,72 @@ pa_status pa_attention_varlen(void *out, const void *q, const void *k_new, const
             return from_cuda(pa::launch_mixed(out, q, cu_q_lens, num_prefills,
                                               num_prefill_tokens, max_prefill_q_len, kv_cache, g,
                                               num_heads, block_tables, max_blocks_per_seq,
-                                              seq_lens, num_seqs, scale, workspace,
+                                              seq_lens, num_seqs, scale, workspace, kv8,
+                                              k_scale, v_scale,
                                               reinterpret_cast<cudaStream_t>(stream)));
         }
     }
     // Otherwise one part at a time.
     // 2. Prefill chunks: sequences [0, num_prefills), query rows [0, num_prefill_tokens).
     if (num_prefills > 0) {
-        st = pa_prefill_chunk(out, q, cu_q_lens, num_prefills, max_prefill_q_len, kv_cache,
-                              num_blocks, block_size, num_heads, num_kv_heads, head_size,
-                              block_tables, max_blocks_per_seq, seq_lens, scale, stream);
+        st = kv8 ? pa_prefill_chunk_fp8(out, q, cu_q_lens, num_prefills, max_prefill_q_len,
+                                        kv_cache, num_blocks, block_size, num_heads,
+                                        num_kv_heads, head_size, block_tables,
+                                        max_blocks_per_seq, seq_lens, scale, k_scale, v_scale,
+                                        stream)
+                 : pa_prefill_chunk(out, q, cu_q_lens, num_prefills, max_prefill_q_len,
+                                    kv_cache, num_blocks, block_size, num_heads, num_kv_heads,
+                                    head_size, block_tables, max_blocks_per_seq, seq_lens,
+                                    scale, stream);
         if (st != PA_OK) return st;
     }
     // 3. Decode tokens: the remaining sequences, one query row each.
     if (num_decodes > 0) {
-        st = pa_decode(static_cast<uint8_t *>(out) + off, static_cast<const uint8_t *>(q) + off,
-                       kv_cache, num_blocks, block_size, num_heads, num_kv_heads, head_size,
-                       block_tables + (size_t)num_prefills * max_blocks_per_seq,
-                       max_blocks_per_seq, seq_lens + num_prefills, num_decodes, max_seq_len,
-                       scale, workspace, workspace_bytes, stream);
+        void *dout = static_cast<uint8_t *>(out) + off;
+        const void *dq = static_cast<const uint8_t *>(q) + off;
+        const int32_t *dbt = block_tables + (size_t)num_prefills * max_blocks_per_seq;
+        st = kv8 ? pa_decode_fp8(dout, dq, kv_cache, num_blocks, block_size, num_heads,
+                                 num_kv_heads, head_size, dbt, max_blocks_per_seq,
+                                 seq_lens + num_prefills, num_decodes, max_seq_len, scale,
+                                 k_scale, v_scale, workspace, workspace_bytes, stream)
+                 : pa_decode(dout, dq, kv_cache, num_blocks, block_size, num_heads,
+                             num_kv_heads, head_size, dbt, max_blocks_per_seq,
+                             seq_lens + num_prefills, num_decodes, max_seq_len, scale,
+                             workspace, workspace_bytes, stream);
         if (st != PA_OK) return st;
     }
     return PA_OK;
+}
+
+pa_status pa_attention_varlen(void *out, const void *q, const void *k_new, const void *v_new,
+                              const int32_t *slot_mapping, const int32_t *cu_q_lens,
+                              int num_seqs, int num_prefills, int num_prefill_tokens,
+                              int max_prefill_q_len, void *kv_cache, int num_blocks,
+                              int block_size, int num_heads, int num_kv_heads, int head_size,
+                              const int32_t *block_tables, int max_blocks_per_seq,
+                              const int32_t *seq_lens, int max_seq_len, float scale,
+                              void *workspace, size_t workspace_bytes, pa_stream_t stream) {
+    return varlen_impl(out, q, k_new, v_new, slot_mapping, cu_q_lens, num_seqs, num_prefills,
+                       num_prefill_tokens, max_prefill_q_len, kv_cache, num_blocks, block_size,
+                       num_heads, num_kv_heads, head_size, block_tables, max_blocks_per_seq,
+                       seq_lens, max_seq_len, scale, false, 1.f, 1.f, workspace, workspace_bytes,
+                       stream);
+}
+
+pa_status pa_attention_varlen_fp8(void *out, const void *q, const void *k_new,
+                                  const void *v_new, const int32_t *slot_mapping,
+                                  const int32_t *cu_q_lens, int num_seqs, int num_prefills,
+                                  int num_prefill_tokens, int max_prefill_q_len, void *kv_cache,
+                                  int num_blocks, int block_size, int num_heads,
+                                  int num_kv_heads, int head_size, const int32_t *block_tables,
+                                  int max_blocks_per_seq, const int32_t *seq_lens,
+                                  int max_seq_len, float scale, float k_scale, float v_scale,
+                                  void *workspace, size_t workspace_bytes, pa_stream_t stream) {
+    return varlen_impl(out, q, k_new, v_new, slot_mapping, cu_q_lens, num_seqs, num_prefills,
+                       num_prefill_tokens, max_prefill_q_len, kv_cache, num_blocks, block_size,
+                       num_heads, num_kv_heads, head_size, block_tables, max_blocks_per_seq,
+                       seq_lens, max_seq_len, scale, true, k_scale, v_scale, workspace,
+                       workspace_bytes, stream);
 }
 
 pa_status pa_prefill_chunk_fp8(void *out, const void *q, const int32_t *cu_q_lens,

@@ -21,10 +21,16 @@ namespace {
 // Decode CTAs of the mixed launch keep two stages per warp: on part of the GPU
 // each SM has to hold twice the bytes in flight.
 constexpr int kMixStages = 2;
-// Rates measured on GB300 for the split: decode with 12 warps x 2 stages streams
-// about 96 GB/s per SM, 7.0 TB/s at most in all; chunked prefill does about
-// 7.5 TFLOP/s per SM.
+// An FP8 tile is half the bytes: three stages per warp.
+constexpr int kMixStagesFp8 = 3;
+// Rates measured on GB300 for the split (bf16 pool): decode with 12 warps x 2
+// stages streams about 96 GB/s per SM, 7.0 TB/s at most in all; chunked prefill
+// does about 7.5 TFLOP/s per SM.  FP8 pool: see launch_mixed.
 constexpr float kMixDecodeSmGBs = 96.0f, kMixHbmGBs = 7000.0f, kMixPrefillSmTflops = 7.5f;
+// FP8 pool: the decode issues about 2.6 times the instructions per byte and
+// streams about 46 GB/s per SM on part of the GPU (measured: the mixed step is
+// within 1 % of its best for 52 to 70 decode SMs on the mixed workload).
+constexpr float kMixDecodeSmGBsFp8 = 46.0f;
 
 struct MixPlanArgs {
     const int32_t *seq_lens;   // all sequences, chunks first
@@ -32,6 +38,7 @@ struct MixPlanArgs {
     int num_prefills, num_seqs, sms, max_len;
     float dec_bytes_per_token;  // K+V bytes per decode token: 2 * Hkv * D * 2
     float pre_flops_per_pair;   // flops per visible (query, key) pair: 4 * Hq * D
+    float dec_sm_gbs, hbm_gbs, pre_sm_tflops;  // rates of the two parts
     int *plan;                   // out: {decode CTAs, decode warps}
 };
 
@@ -71,8 +78,8 @@ __global__ void __launch_bounds__(256) mix_plan_kernel(const MixPlanArgs a) {
         int best = 1;
         float best_t = 3.0e38f;
         for (int k = 1 + tid; k < a.sms; k += 32) {
-            const float td = bytes / (fminf(k * kMixDecodeSmGBs, kMixHbmGBs) * 1e3f);
-            const float tp = flops / ((a.sms - k) * kMixPrefillSmTflops * 1e6f);
+            const float td = bytes / (fminf(k * a.dec_sm_gbs, a.hbm_gbs) * 1e3f);
+            const float tp = flops / ((a.sms - k) * a.pre_sm_tflops * 1e6f);
             const float t = fmaxf(td, tp);
             if (t < best_t) {
                 best_t = t;
@@ -94,25 +101,27 @@ __global__ void __launch_bounds__(256) mix_plan_kernel(const MixPlanArgs a) {
     }
 }
 
-template <int D>
+// KV8: an FP8 pool for both roles (the prefill role's converter is warp 11).
+template <int D, bool KV8>
 __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     mixed_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs da,
                  const PrefillArgs pa, int dec_slots, uint3 pre_grid) {
     if ((int)blockIdx.x < dec_slots) {
         if ((int)blockIdx.x < da.plan[0])
-            decode_body<D, kDecodeWarps, kMixStages, false>(kv_map, da, blockIdx.x, da.plan[1]);
+            decode_body<D, kDecodeWarps, KV8 ? kMixStagesFp8 : kMixStages, KV8>(
+                kv_map, da, blockIdx.x, da.plan[1]);
         return;
     }
     const unsigned v = blockIdx.x - (unsigned)dec_slots;
     const uint3 bid = make_uint3(v % pre_grid.x, (v / pre_grid.x) % pre_grid.y,
                                  v / (pre_grid.x * pre_grid.y));
-    prefill_body<D>(kv_map, pa, bid, pre_grid);
+    prefill_body<D, KV8>(kv_map, pa, bid, pre_grid);
 }
 
-template <int D>
+template <int D, bool KV8>
 cudaError_t launch_mixed_d(const CUtensorMap &map, const DecodeArgs &da, const PrefillArgs &pa,
                            dim3 pgrid, int sms, size_t smem, cudaStream_t stream) {
-    auto kern = mixed_kernel<D>;
+    auto kern = mixed_kernel<D, KV8>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -131,10 +140,13 @@ size_t mixed_workspace_bytes(int num_decodes, int head_size, int sm_count) {
     return decode_workspace_bytes(num_decodes, head_size, sm_count) + 256;
 }
 
-bool mixed_supported(int num_decodes, int num_heads, const KvGeom &g) {
+bool mixed_supported(int num_decodes, int num_heads, const KvGeom &g, bool kv8) {
     const int G = num_heads / g.num_kv_heads;
-    const size_t dec = g.head_size == 128 ? decode_smem_bytes<128, false, kMixStages>(num_decodes, G)
-                                          : decode_smem_bytes<64, false, kMixStages>(num_decodes, G);
+    if (kv8 && g.head_size != 128) return false;
+    const size_t dec =
+        kv8 ? decode_smem_bytes<128, true, kMixStagesFp8>(num_decodes, G)
+        : g.head_size == 128 ? decode_smem_bytes<128, false, kMixStages>(num_decodes, G)
+                             : decode_smem_bytes<64, false, kMixStages>(num_decodes, G);
     const size_t pre = g.head_size == 128 ? TcLay<128>::kSmem : TcLay<64>::kSmem;
     return dec <= pre;  // the prefill's shared memory is the launch's
 }
@@ -143,11 +155,14 @@ cudaError_t launch_mixed(void *out, const void *q, const int32_t *cu_q_lens, int
                          int num_prefill_tokens, int max_prefill_q_len, const void *kv_cache,
                          const KvGeom &g, int num_heads, const int32_t *block_tables,
                          int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs,
-                         float scale, void *workspace, cudaStream_t stream) {
+                         float scale, void *workspace, bool kv8, float k_scale, float v_scale,
+                         cudaStream_t stream) {
     const int sms = device_sm_count();
     const int D = g.head_size, num_decodes = num_seqs - num_prefills;
     CUtensorMap map;
-    if (!encode_kv_map(&map, kv_cache, g, g.block_size >= kTile ? kTile : g.block_size))
+    const int box_rows = g.block_size >= kTile ? kTile : g.block_size;
+    if (!(kv8 ? encode_kv_map_fp8(&map, kv_cache, g, box_rows)
+              : encode_kv_map(&map, kv_cache, g, box_rows)))
         return cudaErrorInvalidValue;
     int *plan = reinterpret_cast<int *>(static_cast<uint8_t *>(workspace) +
                                         decode_workspace_bytes(num_decodes, D, sms));
@@ -158,8 +173,14 @@ cudaError_t launch_mixed(void *out, const void *q, const int32_t *cu_q_lens, int
     pl.num_seqs = num_seqs;
     pl.sms = sms;
     pl.max_len = max_blocks_per_seq * g.block_size;
-    pl.dec_bytes_per_token = 2.0f * g.num_kv_heads * D * 2;
+    pl.dec_bytes_per_token = 2.0f * g.num_kv_heads * D * (kv8 ? 1 : 2);
     pl.pre_flops_per_pair = 4.0f * num_heads * D;
+    // FP8 pool (measured on GB300): decode about kMixDecodeSmGBsFp8 per SM with 12
+    // warps x 3 stages, 6.3 TB/s at most; the prefill, with its conversion, about
+    // 7.1 TFLOP/s per SM.
+    pl.dec_sm_gbs = kv8 ? kMixDecodeSmGBsFp8 : kMixDecodeSmGBs;
+    pl.hbm_gbs = kv8 ? 6300.f : kMixHbmGBs;
+    pl.pre_sm_tflops = kv8 ? 7.1f : kMixPrefillSmTflops;
     pl.plan = plan;
     mix_plan_kernel<<<1, 256, 0, stream>>>(pl);
     cudaError_t e = cudaGetLastError();
@@ -169,14 +190,21 @@ cudaError_t launch_mixed(void *out, const void *q, const int32_t *cu_q_lens, int
                                      static_cast<const uint8_t *>(q) + off, g, num_heads,
                                      block_tables + (size_t)num_prefills * max_blocks_per_seq,
                                      max_blocks_per_seq, seq_lens + num_prefills, num_decodes,
-                                     scale, workspace, false, sms);
+                                     scale, workspace, kv8, sms);
     da.plan = plan;
+    da.k_scale = k_scale;
+    da.v_scale = v_scale;
     dim3 pgrid;
-    const PrefillArgs pa =
+    PrefillArgs pa =
         make_prefill_args(out, q, cu_q_lens, num_prefills, max_prefill_q_len, g, num_heads,
                           block_tables, max_blocks_per_seq, seq_lens, scale, &pgrid);
-    if (D == 128) return launch_mixed_d<128>(map, da, pa, pgrid, sms, TcLay<128>::kSmem, stream);
-    return launch_mixed_d<64>(map, da, pa, pgrid, sms, TcLay<64>::kSmem, stream);
+    pa.k_scale = k_scale;
+    pa.v_scale = v_scale;
+    if (kv8)
+        return launch_mixed_d<128, true>(map, da, pa, pgrid, sms, TcLay<128>::kSmem, stream);
+    if (D == 128)
+        return launch_mixed_d<128, false>(map, da, pa, pgrid, sms, TcLay<128>::kSmem, stream);
+    return launch_mixed_d<64, false>(map, da, pa, pgrid, sms, TcLay<64>::kSmem, stream);
 }
 
 }  // namespace pa

@@ -78,12 +78,13 @@ cudaError_t launch_decode_suffix(void *out, const void *q, const void *kv_cache,
 // decode and chunked prefill side by side on disjoint SMs, split on the device.
 // mixed_supported: whether the decode part's shared memory fits the launch.
 size_t mixed_workspace_bytes(int num_decodes, int head_size, int sm_count);
-bool mixed_supported(int num_decodes, int num_heads, const KvGeom &g);
+bool mixed_supported(int num_decodes, int num_heads, const KvGeom &g, bool kv8);
 cudaError_t launch_mixed(void *out, const void *q, const int32_t *cu_q_lens, int num_prefills,
                          int num_prefill_tokens, int max_prefill_q_len, const void *kv_cache,
                          const KvGeom &g, int num_heads, const int32_t *block_tables,
                          int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs,
-                         float scale, void *workspace, cudaStream_t stream);
+                         float scale, void *workspace, bool kv8, float k_scale, float v_scale,
+                         cudaStream_t stream);
 
 // Chunked prefill over an FP8 pool (head_size 128).
 cudaError_t launch_prefill_fp8(void *out, const void *q, const int32_t *cu_q_lens,

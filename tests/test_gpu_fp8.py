@@ -211,3 +211,55 @@ def test_fp8_prefill_mixed_workload_chunks():
     rows = np.arange(0, 4096, 41, dtype=np.int32)
     compare(out[torch.as_tensor(rows, device=DEV).long()],
             _oracle(b, codes, FP8_K_SCALE, FP8_V_SCALE, rows), "fp8 prefill, mixed workload")
+
+
+def _varlen_fp8(b, n_pre, ks, vs):
+    out = torch.full_like(b.q, float("nan"))
+    ws = torch.empty(binding.pa_attention_varlen_workspace_bytes(
+        b.num_seqs, n_pre, b.num_heads, b.num_kv_heads, b.head_size), dtype=torch.uint8,
+        device=DEV)
+    binding.pa_attention_varlen(out, b.q, b.k_new, b.v_new, b.slot_mapping,
+                                b.cu_q_lens[:n_pre + 1].contiguous(), n_pre,
+                                int(b.cu_q_lens[n_pre]), int(b.q_lens[:n_pre].max()), pool8_of[0],
+                                b.block_tables, b.seq_lens, int(b.seq_lens[n_pre:].max()),
+                                b.scale, ws, kv_scales=(ks, vs))
+    binding.pa_error_check()
+    return out
+
+
+pool8_of = [None]
+
+
+@pytest.mark.parametrize("shape", [
+    ([300, 40, 513, 90, 17, 1], [129, 40, 200, 1, 1, 1], 32, 8, 16),
+    ([64, 700, 33, 2000], [64, 1, 1, 1], 64, 8, 32),
+])
+def test_fp8_varlen_one_launch(shape):
+    lens, qls, Hq, Hkv, bs = shape
+    b = make_batch(name="v8", seq_lens=lens, q_lens=qls, num_heads=Hq, num_kv_heads=Hkv,
+                   head_size=128, block_size=bs, scale=128 ** -0.5, seed=890 + len(lens),
+                   device=DEV)
+    n_pre = sum(1 for q in qls if q > 1)
+    pool8_of[0] = fp8_pool_of(b)
+    codes = oracle.cache_write_fp8(pool8_of[0], b.k_new, b.v_new, b.slot_mapping, FP8_K_SCALE,
+                                   FP8_V_SCALE)
+    out = _varlen_fp8(b, n_pre, FP8_K_SCALE, FP8_V_SCALE)
+    assert np.array_equal(pool8_of[0].cpu().numpy(), codes), "fp8 cache write"
+    compare(out, _oracle(b, codes, FP8_K_SCALE, FP8_V_SCALE), f"fp8 varlen {lens}")
+
+
+def test_fp8_varlen_mixed_workload():
+    b = make_config(4, device=DEV)
+    pool8_of[0] = fp8_pool_of(b)
+    codes = oracle.cache_write_fp8(pool8_of[0], b.k_new, b.v_new, b.slot_mapping, FP8_K_SCALE,
+                                   FP8_V_SCALE)
+    out = _varlen_fp8(b, 8, FP8_K_SCALE, FP8_V_SCALE)
+    assert np.array_equal(pool8_of[0].cpu().numpy(), codes), "fp8 cache write"
+    pre = torch.empty_like(b.q[:4096])
+    binding.pa_prefill_chunk_fp8(pre, b.q[:4096], b.cu_q_lens[:9].contiguous(), 512,
+                                 pool8_of[0], b.block_tables[:8], b.seq_lens[:8], b.scale,
+                                 FP8_K_SCALE, FP8_V_SCALE)
+    assert torch.equal(pre.view(torch.int16), out[:4096].view(torch.int16)), "chunk rows"
+    rows = np.concatenate([np.arange(0, 4096, 97), np.arange(4096, 4344)]).astype(np.int32)
+    compare(out[torch.as_tensor(rows, device=DEV).long()],
+            _oracle(b, codes, FP8_K_SCALE, FP8_V_SCALE, rows), "fp8 mixed workload, one launch")
