@@ -1,4 +1,4 @@
-// pa_prefill.cu - chunked-prefill attention over a paged KV cache.
+// pa_prefill.cuh - chunked-prefill attention over a paged KV cache.
 //
 // Chunked prefill ("Inside vLLM: Anatomy of a High-Throughput LLM Inference
 // System", advanced features: a long prompt is split into chunks interleaved with
@@ -20,12 +20,19 @@
 //              softmax, P (bf16) written into tensor memory over its own
 //              scores, and the final normalisation of O.
 // Tensor memory (512 columns x 128 lanes): S_0/P_0 [0,128), S_1/P_1 [128,256),
-// O_0 [256,384), O_1 [384,512).  Each K/V tile is worked in two 64-key halves
-// with their own hand-overs: while the softmax runs on one half, the tensor
-// cores compute the other half's scores or its P.V.  P of a half overwrites its
-// own scores, so that half's next scores are issued only after its P.V is done.
-// Keys past a row's position are masked; tiles past the CTA's causal limit are
-// never fetched.
+// O_0 [256,384), O_1 [384,512).  Per K/V tile and query tile: S = Q.K^T as one
+// N = 128 product (a 64-key product costs nearly as much: each k step re-reads
+// the 128-row A operand), the softmax over all 128 keys (P overwrites the first
+// 64 columns of its own scores), and O += P.V in two 64-key parts, the first
+// issued while the softmax still works on keys 64-127.  A tile's next scores
+// are issued once its P.V is done (P sits where they are written), so each
+// tile is a chain scores -> softmax -> P.V -> scores whose length, set mostly
+// by the latency of a group of dependent MMAs, bounds the kernel; the other
+// tile's chain fills the tensor cores meanwhile.  The two tiles' softmaxes take
+// turns (a token passed between the warpgroups): one tile's softmax runs under
+// the other tile's products instead of sharing the exponential units with the
+// other softmax.  Keys past a row's position are masked; tiles past the CTA's
+// causal limit are never fetched.
 #include <algorithm>
 #include <cmath>
 
@@ -44,7 +51,6 @@ constexpr float kTcRescaleSlack = 8.0f;
 constexpr int kTcRows = 128;    // query rows per tile (the MMA's M)
 constexpr int kTcTiles = 2;     // query tiles per CTA
 constexpr int kTcKeys = 128;    // keys per K/V tile
-constexpr int kHalf = 64;       // keys per score half: S, softmax and P.V run per half
 constexpr int kKSlots = 3;      // K ring: a slot frees once both Q.K^T products are done
 constexpr int kVSlots = 2;      // V ring: a slot frees once both P.V products are done
 // warp 0: TMA producer; warps 2..9: softmax warpgroups; warps 1 and 10: one MMA
@@ -126,8 +132,10 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &kv_map, const Pr
     uint8_t *sV = sK + kKSlots * L::kKBytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kOperands);
     uint64_t *k_full = bars, *k_empty = bars + 3, *v_full = bars + 6, *v_empty = bars + 8;
-    // Per (query tile t, key half f), index 2 t + f: scores ready, P written, P.V done.
-    uint64_t *s_full = bars + 10, *p_full = bars + 14, *pv_done = bars + 18;
+    // Per query tile t: scores ready, P of keys 0-63 written, P.V done, softmax done (the
+    // turn token), P of keys 64-127 written.
+    uint64_t *s_full = bars + 10, *p_full = bars + 12, *pv_done = bars + 14, *sm_turn = bars + 16;
+    uint64_t *p_hi = bars + 18;
     uint64_t *q_full = bars + 22;  // [2]
     uint64_t *drain = bars + 24;   // [2], one per issuer
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 26);
@@ -201,10 +209,12 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &kv_map, const Pr
             mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], issuers);
         }
-        for (int i = 0; i < 2 * kTcTiles; ++i) {
+        for (int i = 0; i < kTcTiles; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], 4);
             mbar_init(&pv_done[i], 1);
+            mbar_init(&sm_turn[i], 4);
+            mbar_init(&p_hi[i], 4);
         }
         for (int i = 0; i < kTcTiles; ++i) {
             mbar_init(&q_full[i], 4);
@@ -298,77 +308,71 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &kv_map, const Pr
         // products keep the tensor cores busy.
         const int t = warp == 1 ? 0 : 1;
         const uint32_t idesc_s =
-            KV8 ? tc_idesc_f16(kTcRows, kHalf, 0) : tc_idesc_bf16(kTcRows, kHalf, 0);
+            KV8 ? tc_idesc_f16(kTcRows, kTcKeys, 0) : tc_idesc_bf16(kTcRows, kTcKeys, 0);
         const uint32_t idesc_pv = KV8 ? tc_idesc_f16(kTcRows, D, 1) : tc_idesc_bf16(kTcRows, D, 1);
         const uint32_t q_base = smem_u32(sQ) + t * L::kQTile;
         const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV);
-        // S_t,f = Q_t . K_j[64 f, 64 f + 64)^T into tensor-memory columns
-        // [128 t + 64 f, 128 t + 64 f + 64).
-        auto issue_s = [&](int j, int f) {
+        // S_t = Q_t . K_j^T into tensor-memory columns [128 t, 128 t + 128).
+        auto issue_s = [&](int j) {
             if (lane == 0) {
-                const uint32_t kb = k_base + (j % kKSlots) * L::kKBytes + f * kHalf * 128;
+                const uint32_t kb = k_base + (j % kKSlots) * L::kKBytes;
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint32_t off = (k >> 2) * L::kQPanel + (k & 3) * 32;
                     const uint64_t ad = tc_desc_sw128(q_base + off, 16, 1024);
                     const uint64_t bd = tc_desc_sw128(kb + (k >> 2) * L::kKvPanel + (k & 3) * 32,
                                                       16, 1024);
-                    tc_mma_ss(tmem + t * kTcRows + f * kHalf, ad, bd, idesc_s, k > 0 ? 1u : 0u);
+                    tc_mma_ss(tmem + t * kTcRows, ad, bd, idesc_s, k > 0 ? 1u : 0u);
                 }
-                tc_commit(&s_full[2 * t + f]);
-                if (f == 1) tc_commit(&k_empty[j % kKSlots]);
+                tc_commit(&s_full[t]);
+                tc_commit(&k_empty[j % kKSlots]);
             }
             __syncwarp();
         };
-        // O_t += P_t,f . V_j[64 f, 64 f + 64); P_t,f is packed bf16 in the first 32
-        // columns of its own score half.
-        auto issue_pv = [&](int j, int f) {
+        // O_t += P_t . V_j for keys [64 h, 64 h + 64) of the tile; P_t is packed two
+        // per column in the first 64 columns of its scores (16 keys per 8 columns).
+        auto issue_pv = [&](int j, int h) {
             if (lane == 0) {
-                const uint32_t vb = v_base + (j % kVSlots) * L::kKBytes + f * kHalf * 128;
+                const uint32_t vb = v_base + (j % kVSlots) * L::kKBytes;
 #pragma unroll
-                for (int kk = 0; kk < kHalf / 16; ++kk) {
+                for (int kk = 4 * h; kk < 4 * h + 4; ++kk) {
                     const uint64_t bd = tc_desc_sw128(vb + kk * 16 * 128, L::kKvPanel, 1024);
-                    tc_mma_ts(tmem + kColO + t * kTcRows, tmem + t * kTcRows + f * kHalf + kk * 8,
-                              bd, idesc_pv, (j > 0 || f > 0 || kk > 0) ? 1u : 0u);
+                    tc_mma_ts(tmem + kColO + t * kTcRows, tmem + t * kTcRows + kk * 8, bd,
+                              idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
                 }
-                tc_commit(&pv_done[2 * t + f]);
-                if (f == 1) tc_commit(&v_empty[j % kVSlots]);
+                if (h == 1) {
+                    tc_commit(&pv_done[t]);
+                    tc_commit(&v_empty[j % kVSlots]);
+                }
             }
             __syncwarp();
         };
         bool ok = warp_wait(&q_full[t], 0) && warp_wait(&k_full[0], 0);
-        // Tile 1 starts once tile 0's first softmax half is done, so the two
-        // softmax warpgroups start out of step.
-        if (ok && t == 1) ok = warp_wait(&p_full[0], 0);
         if (ok) {
             tc_fence_after();
-            issue_s(0, 0);
-            issue_s(0, 1);
+            issue_s(0);
         }
-        // Per half f: O_t += P_t,f.V_j as soon as P_t,f is ready, then, once that
-        // product is done (P_t,f sits where S_t,f is written), S_t,f for the next
-        // K tile.  The other half's softmax runs meanwhile, so the tensor cores
-        // work under the softmax instead of after it.
+        // O_t += P_t.V_j in two 64-key parts, each as soon as its P is written;
+        // once that product is done (P_t sits where S_t is written), S_t for the
+        // next K tile.  V_j is waited for before P (it normally arrives far
+        // ahead, so the hand-over is not delayed by the check); the next K tile
+        // after the P.V is issued (from an FP8 pool it arrives later, through the
+        // conversion warp).  The other tile's products run meanwhile.
         for (int j = 0; ok && j < n_kt; ++j) {
-            if (!(ok = warp_wait(&p_full[2 * t], (uint32_t)j & 1u))) break;
             if (!(ok = warp_wait(&v_full[j % kVSlots], (uint32_t)(j / kVSlots) & 1u))) break;
+            if (!(ok = warp_wait(&p_full[t], (uint32_t)j & 1u))) break;
             tc_fence_after();
             issue_pv(j, 0);
+            if (!(ok = warp_wait(&p_hi[t], (uint32_t)j & 1u))) break;
+            tc_fence_after();
+            issue_pv(j, 1);
             if (j + 1 < n_kt) {
                 if (!(ok = warp_wait(&k_full[(j + 1) % kKSlots],
                                      (uint32_t)((j + 1) / kKSlots) & 1u)))
                     break;
-                if (!(ok = warp_wait(&pv_done[2 * t], (uint32_t)j & 1u))) break;
+                if (!(ok = warp_wait(&pv_done[t], (uint32_t)j & 1u))) break;
                 tc_fence_after();
-                issue_s(j + 1, 0);
-            }
-            if (!(ok = warp_wait(&p_full[2 * t + 1], (uint32_t)j & 1u))) break;
-            tc_fence_after();
-            issue_pv(j, 1);
-            if (j + 1 < n_kt) {
-                if (!(ok = warp_wait(&pv_done[2 * t + 1], (uint32_t)j & 1u))) break;
-                tc_fence_after();
-                issue_s(j + 1, 1);
+                issue_s(j + 1);
             }
         }
         if (!ok && lane == 0) atomicOr(&g_err_prefill, kErrTimeout);
@@ -490,69 +494,59 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &kv_map, const Pr
             if (lane == 0) mbar_arrive(&q_full[t]);
         }
         const int lim = real && !prefix ? std::min(ctx + t0 + tok, len - 1) : len - 1;
+        const int other = has1 ? 1 - t : -1;  // the warpgroup this one takes turns with
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; ok && j < n_kt; ++j) {
-#pragma unroll 1
-            for (int f = 0; f < 2; ++f) {
-                const uint32_t cf = cs + f * kHalf;  // this half's score / P columns
-                if (!(ok = warp_wait(&s_full[2 * t + f], (uint32_t)j & 1u))) break;
-                tc_fence_after();
-                const int k0 = j * kTcKeys + f * kHalf;
-                float x[kHalf];
+            // Tile 0 goes first: tile 0's softmax of K tile j follows tile 1's of
+            // j - 1, and tile 1's follows tile 0's of j.
+            if (other >= 0 && (t == 1 || j > 0) &&
+                !(ok = warp_wait(&sm_turn[other], (uint32_t)(t == 1 ? j : j - 1) & 1u)))
+                break;
+            if (!(ok = warp_wait(&s_full[t], (uint32_t)j & 1u))) break;
+            tc_fence_after();
+            const int k0 = j * kTcKeys;
+            float x[kTcKeys];
 #pragma unroll
-                for (int c = 0; c < kHalf / 32; ++c)
-                    tmem_ld32(cf + 32 * c, *reinterpret_cast<float(*)[32]>(&x[32 * c]));
-                tc_wait_ld();
-                if (k0 + kHalf - 1 > lim) {
-                    // Diagonal / last keys: those past this row's limit get -inf.
+            for (int c = 0; c < kTcKeys / 32; ++c)
+                tmem_ld32(cs + 32 * c, *reinterpret_cast<float(*)[32]>(&x[32 * c]));
+            tc_wait_ld();
+            if (k0 + kTcKeys - 1 > lim) {
+                // Diagonal / last keys: those past this row's limit get -inf.
 #pragma unroll
-                    for (int c = 0; c < kHalf; ++c)
-                        if (k0 + c > lim) x[c] = -INFINITY;
-                }
-                // The scale is folded into the exponent below, so the max is taken
-                // over raw scores (three-input max, two independent chains).
-                float r0m = -INFINITY, r1m = -INFINITY;
+                for (int c = 0; c < kTcKeys; ++c)
+                    if (k0 + c > lim) x[c] = -INFINITY;
+            }
+            // The scale is folded into the exponent below, so the max is taken
+            // over raw scores (three-input max, four independent chains).
+            float r0m = -INFINITY, r1m = -INFINITY, r2m = -INFINITY, r3m = -INFINITY;
 #pragma unroll
-                for (int c = 0; c < kHalf; c += 4) {
-                    r0m = fmax3(r0m, x[c], x[c + 1]);
-                    r1m = fmax3(r1m, x[c + 2], x[c + 3]);
-                }
-                const float mx = fmaxf(r0m, r1m) * sl2;
-                const bool grow = mx > m + kTcRescaleSlack;
-                if (__any_sync(0xffffffffu, grow)) {
-                    const float mn = grow ? fmaxf(m, mx) : m;
-                    const float cr = fast_exp2(m - mn);
-                    l *= cr;
-                    if (j > 0 || f > 0) {
-                        // Every earlier P.V of this tile must be done before O is
-                        // rescaled.  The other half's previous product is the only
-                        // one not already implied by this half's scores being ready
-                        // (each half's S is issued after its own previous P.V).
-                        ok = f == 0 ? warp_wait(&pv_done[2 * t + 1], (uint32_t)(j - 1) & 1u)
-                                    : warp_wait(&pv_done[2 * t], (uint32_t)j & 1u);
-                        if (!ok) break;
-                        tc_fence_after();
-#pragma unroll 1
-                        for (int c = 0; c < D / 32; ++c) {
-                            float o[32];
-                            tmem_ld32(co + 32 * c, o);
-                            tc_wait_ld();
+            for (int c = 0; c < kTcKeys; c += 8) {
+                r0m = fmax3(r0m, x[c], x[c + 1]);
+                r1m = fmax3(r1m, x[c + 2], x[c + 3]);
+                r2m = fmax3(r2m, x[c + 4], x[c + 5]);
+                r3m = fmax3(r3m, x[c + 6], x[c + 7]);
+            }
+            const float mx = fmaxf(fmaxf(r0m, r1m), fmaxf(r2m, r3m)) * sl2;
+            const bool grow = mx > m + kTcRescaleSlack;
+            const bool rescale = __any_sync(0xffffffffu, grow);
+            float cr = 1.f;
+            if (rescale) {
+                const float mn = grow ? fmaxf(m, mx) : m;
+                cr = fast_exp2(m - mn);
+                l *= cr;
+                m = mn;
+            }
+            // P = 2^(x*scale - m) <= 2^8, packed two per column into the first 64
+            // columns (already read), keys 0-63 first: their P.V starts while keys
+            // 64-127 are worked.  Packed fp32 pairs: one FFMA for (x*scale - m) and
+            // one add for the row sums per two scores; the row sum is kept in fp32
+            // before the 16-bit rounding.
+            const float nm = -m;
+            float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+            auto p_part = [&](int h) {
 #pragma unroll
-                            for (int e = 0; e < 32; ++e) o[e] *= cr;
-                            tmem_st32(co + 32 * c, *reinterpret_cast<const uint32_t(*)[32]>(o));
-                        }
-                    }
-                    m = mn;
-                }
-                // P = 2^(x*scale - m) <= 2^8, packed to bf16 into the half's first 32
-                // columns (already read).  Packed fp32 pairs: one FFMA for
-                // (x*scale - m) and one add for the row sums per two scores; the row
-                // sum is kept in fp32 before the bf16 rounding.
-                const float nm = -m;
-                float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-                for (int qr = 0; qr < kHalf / 32; ++qr) {
+                for (int qr = 2 * h; qr < 2 * h + 2; ++qr) {
                     uint32_t pk[16];
 #pragma unroll
                     for (int c = 0; c < 16; c += 2) {
@@ -567,34 +561,57 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &kv_map, const Pr
                         pk[c] = KV8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
                         pk[c + 1] = KV8 ? pack_f16(p2, p3) : pack_bf16(p2, p3);
                     }
-                    tmem_st16(cf + 16 * qr, pk);
+                    tmem_st16(cs + 16 * qr, pk);
                 }
-                tc_wait_st();
-                l += (s0 + s1) + (s2 + s3);
-                if (f == 0 && j * kTcKeys + kTcKeys > len) {
-                    // Keys at or past the sequence end: zero their V rows so P=0 adds
-                    // exactly nothing whatever the stale data is.  Each tile's
-                    // warpgroup zeroes them before its first hand-over of the tile
-                    // (the two write the same zeros), since the two tiles' products
-                    // are issued independently.
-                    if (!(ok = warp_wait(&v_full[j % kVSlots], (uint32_t)(j / kVSlots) & 1u)))
-                        break;
-                    const int r0 = len - j * kTcKeys, nr = kTcKeys - r0;
-                    uint8_t *vs = sV + (size_t)(j % kVSlots) * L::kKBytes;
-                    for (int e = row; e < nr * 8 * L::kPanels; e += 128) {
-                        const int p = e / (nr * 8), rr = (e >> 3) % nr, ch = e & 7;
-                        *reinterpret_cast<uint4 *>(vs + p * L::kKvPanel + (r0 + rr) * 128 +
-                                                   ch * 16) = make_uint4(0, 0, 0, 0);
-                    }
-                    fence_proxy_async_smem();
+            };
+            p_part(0);
+            if (rescale && j > 0) {
+                // The scores being ready means every earlier P.V of this tile is
+                // done (the scores are issued after it), and the next one waits for
+                // this warpgroup: O is idle and is rescaled in place.
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    float o[32];
+                    tmem_ld32(co + 32 * c, o);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] *= cr;
+                    tmem_st32(co + 32 * c, *reinterpret_cast<const uint32_t(*)[32]>(o));
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&p_full[2 * t + f]);
+            }
+            tc_wait_st();
+            if (j * kTcKeys + kTcKeys > len) {
+                // Keys at or past the sequence end: zero their V rows so P=0 adds
+                // exactly nothing whatever the stale data is.  Each tile's
+                // warpgroup zeroes them before its hand-over of the tile (the two
+                // write the same zeros), since the two tiles' products are issued
+                // independently.
+                if (!(ok = warp_wait(&v_full[j % kVSlots], (uint32_t)(j / kVSlots) & 1u)))
+                    break;
+                const int r0 = len - j * kTcKeys, nr = kTcKeys - r0;
+                uint8_t *vs = sV + (size_t)(j % kVSlots) * L::kKBytes;
+                for (int e = row; e < nr * 8 * L::kPanels; e += 128) {
+                    const int p = e / (nr * 8), rr = (e >> 3) % nr, ch = e & 7;
+                    *reinterpret_cast<uint4 *>(vs + p * L::kKvPanel + (r0 + rr) * 128 +
+                                               ch * 16) = make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[t]);
+            p_part(1);
+            l += (s0 + s1) + (s2 + s3);
+            tc_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&p_hi[t]);
+                mbar_arrive(&sm_turn[t]);
             }
         }
-        // The last half's P.V completes after every earlier product of the tile.
-        if (ok) ok = warp_wait(&pv_done[2 * t + 1], (uint32_t)(n_kt - 1) & 1u);
+        // The last P.V completes after every earlier product of the tile.
+        if (ok) ok = warp_wait(&pv_done[t], (uint32_t)(n_kt - 1) & 1u);
         if (!ok) {
             if (lane == 0) atomicOr(&g_err_prefill, kErrTimeout);
         } else {
