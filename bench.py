@@ -438,9 +438,11 @@ def run_ours(args, world, rank, local):
     total_ms = max_over_ranks(total_ms, world, dev)
 
     # End to end: every step's inputs from pinned host memory, its output back to
-    # pinned host memory.  Two buffer sets and a copy stream: step i+1's inputs
-    # are copied in, and step i-1's output out, while step i computes (what a
-    # serving loop does with the copy engines).
+    # pinned host memory.  Two buffer sets and one stream per copy direction:
+    # step i+1's inputs are copied in, and step i-1's output out, while step i
+    # computes (what a serving loop does with the copy engines).  One stream for
+    # both directions would queue step i+1's inputs behind step i's output copy,
+    # which waits for step i's kernels.
     # A step's inputs travel as one staging buffer (typed views into it), so each
     # step issues one host-to-device copy.
     names = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "seq_lens")
@@ -467,28 +469,30 @@ def run_ours(args, world, rank, local):
     out_host = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(2)]
     h2d = sum(getattr(b, k).numel() * getattr(b, k).element_size() for k in names)
     d2h = out_host[0].numel() * out_host[0].element_size()
-    copy = torch.cuda.Stream(dev)
+    copy_in, copy_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     free = [torch.cuda.Event() for _ in range(2)]      # buffer set's last output copied out
     landed = [torch.cuda.Event() for _ in range(2)]    # buffer set's inputs copied in
     done = [torch.cuda.Event() for _ in range(2)]      # buffer set's step computed
     for e in free:
-        e.record(copy)
+        e.record(copy_out)
 
     def e2e_step(i):
         p = i % 2
-        copy.wait_event(free[p])
-        with torch.cuda.stream(copy):
+        # The buffer set is free once its previous output has been copied out
+        # (which also orders this copy after that step's kernels read it).
+        copy_in.wait_event(free[p])
+        with torch.cuda.stream(copy_in):
             dev_buf[p].copy_(host_buf, non_blocking=True)
-        landed[p].record(copy)
+        landed[p].record(copy_in)
         stream.wait_event(landed[p])
         write(dev_in[p]["k_new"], dev_in[p]["v_new"], dev_in[p]["slot_mapping"], stream)
         attend(dev_in[p]["q"], dev_in[p]["block_tables"], dev_in[p]["seq_lens"], stream,
                dst=dev_out[p])
         done[p].record(stream)
-        copy.wait_event(done[p])
-        with torch.cuda.stream(copy):
+        copy_out.wait_event(done[p])
+        with torch.cuda.stream(copy_out):
             out_host[p].copy_(dev_out[p], non_blocking=True)
-        free[p].record(copy)
+        free[p].record(copy_out)
 
     for i in range(max(args.warmup, 3)):
         e2e_step(i)
@@ -540,9 +544,9 @@ def run_ours(args, world, rank, local):
         "e2e": {"value": world * kv * args.steps / e2e_s / 1e9, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "KV pool resident in HBM (the cache); every step's inputs copied in "
-                        "from pinned host memory and its output copied out, on a copy stream "
-                        "overlapping the neighbouring steps' kernels (two buffer sets); host "
-                        "wall clock over all steps"},
+                        "from pinned host memory and its output copied out, on one stream per "
+                        "copy direction overlapping the neighbouring steps' kernels (two "
+                        "buffer sets); host wall clock over all steps"},
         "clocks": clocks,
         "gpu_launches": (4 if args.cascade else 3) * args.steps,
     }
