@@ -1,4 +1,4 @@
-// pa_decode.cu - paged decode attention: one query token per sequence.
+// pa_decode.cuh - paged decode attention: one query token per sequence.
 //
 // The method: "Inside vLLM: Anatomy of a High-Throughput LLM Inference System"
 // (§Engine core: a sequence's tokens are found through the blocks its block table
