@@ -210,12 +210,13 @@ def barrier(world: int):
         dist.barrier()
 
 
-def cpu_oracle_rate(n: int, budget_s: float = 12.0, seed=None, first: int = 64):
+def cpu_oracle_rate(n: int, budget_s: float = 12.0, seed=None, first: int = 64,
+                    threads: int = 0):
     """Time the oracle (cache write + attention) on the first sequences of workload n.
 
     Sequences are processed one at a time, cycling over the sample, until about
-    budget_s seconds of wall time are spent.  Returns (GB/s of KV read, seqs/s,
-    sequences timed, sample size, threads).
+    budget_s seconds of wall time are spent; threads = 0 uses every host core.
+    Returns (GB/s of KV read, seqs/s, sequences timed, sample size, threads).
     """
     import numpy as np
 
@@ -225,7 +226,7 @@ def cpu_oracle_rate(n: int, budget_s: float = 12.0, seed=None, first: int = 64):
     k = min(len(config_spec(n)["seq_lens"]), first)
     b = sample_of_config(n, k, device="cpu", seed=seed)
     lib = oracle.load()
-    threads = oracle.max_threads(lib)
+    threads = threads or oracle.max_threads(lib)
     lens = b.seq_lens.tolist()
     pool = oracle._u16(b.kv_cache).copy()
     done_bytes = 0
@@ -239,7 +240,8 @@ def cpu_oracle_rate(n: int, budget_s: float = 12.0, seed=None, first: int = 64):
         oracle.cache_write(pool, b.k_new[r0:r1], b.v_new[r0:r1], b.slot_mapping[r0:r1], lib=lib,
                            inplace=True)
         oracle.attention(b.q[r0:r1], np.array([0, r1 - r0], np.int32), pool,
-                         b.block_tables[one], b.seq_lens[one], b.num_heads, b.scale, lib=lib)
+                         b.block_tables[one], b.seq_lens[one], b.num_heads, b.scale,
+                         threads=threads, lib=lib)
         spent += time.perf_counter() - t
         done_bytes += kv_read_bytes(lens[s:s + 1], b.num_kv_heads, b.head_size)
         done += 1
@@ -552,11 +554,16 @@ def run_ours(args, world, rank, local):
     }
     if world == 1 and not args.no_cpu_baseline and not fp8:
         gbs, sps, done, k, threads = cpu_oracle_rate(n)
+        gbs1, sps1, done1, _, _ = cpu_oracle_rate(n, budget_s=4.0, threads=1)
         line["cpu_baseline"] = {"value": gbs, "unit": UNIT, "cores": threads, "kind": "oracle",
                                 "seqs_per_s": sps,
                                 "sample": f"{done} sequence-steps cycling over the first {k} "
                                           f"sequences of {b.name} (cache write + fp64 "
-                                          f"attention, all heads, one sequence per call)"}
+                                          f"attention, all heads, one sequence per call)",
+                                "single_thread": {"value": gbs1, "unit": UNIT, "cores": 1,
+                                                  "seqs_per_s": sps1,
+                                                  "sample": f"{done1} sequence-steps, same "
+                                                            f"sample, one thread"}}
     print(json.dumps(line), flush=True)
 
 
