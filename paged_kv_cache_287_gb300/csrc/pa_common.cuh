@@ -85,17 +85,8 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
 }
 
 // ------------------------------------------------------------------ TMA / bulk copies
-// 2-D tiled tensor load into shared memory, completing on an mbarrier.
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar,
-                                            int x, int y) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-        : "memory");
-}
-
-// Same, with an L2 eviction-priority hint (policy from createpolicy).
+// 2-D tiled tensor load into shared memory, completing on an mbarrier, with an
+// L2 eviction-priority hint (policy from createpolicy).
 __device__ __forceinline__ void tma_load_2d_hint(void *dst, const CUtensorMap *map,
                                                  uint64_t *bar, int x, int y, uint64_t policy) {
     asm volatile(
