@@ -183,6 +183,23 @@ def test_fp8_prefill_small_shapes(case):
     compare(out, _oracle(b, codes, FP8_K_SCALE, FP8_V_SCALE), f"fp8 prefill case {case}")
 
 
+def test_fp8_prefill_long_context_and_empty_chunk():
+    """The FP8 prefill (conversion warp in the loop) over a 40 000-token cached
+    context, with an empty chunk between two others."""
+    lens, qls = [40300, 5000, 3000], [300, 0, 257]
+    b = make_batch(name="p8long", seq_lens=lens, q_lens=qls, num_heads=32, num_kv_heads=8,
+                   head_size=128, block_size=16, scale=128 ** -0.5, seed=32, device=DEV)
+    pool8 = fp8_pool_of(b)
+    codes = _write(b, pool8, FP8_K_SCALE, FP8_V_SCALE)
+    out = torch.full_like(b.q, float("nan"))
+    binding.pa_prefill_chunk_fp8(out, b.q, b.cu_q_lens, max(qls), pool8, b.block_tables,
+                                 b.seq_lens, b.scale, FP8_K_SCALE, FP8_V_SCALE)
+    binding.pa_error_check()
+    rows = [0, 1, 31, 32, 63, 64, 150, 299, 300, 301, 430, 556]
+    compare(out[rows], _oracle(b, codes, FP8_K_SCALE, FP8_V_SCALE, rows=rows),
+            "fp8 long-context prefill")
+
+
 @pytest.mark.parametrize("scale", [-0.1, 0.0])
 def test_fp8_prefill_negative_and_zero_scale_and_other_kv_scales(scale):
     b = make_batch(name="p8s", seq_lens=[400, 90], q_lens=[200, 90], num_heads=16,

@@ -202,6 +202,20 @@ def test_prefill_of_single_token_chunks_matches_decode():
     compare(gpu_decode(b), oracle_rows(b, pool), "decode")
 
 
+def test_prefill_long_context_and_empty_chunk():
+    """A chunk after a 40 000-token cached context (316 K/V tiles through each
+    query tile's hand-over chain), an empty chunk between two others, and a
+    ragged last chunk; rows sampled across tile and chunk boundaries."""
+    lens, qls = [40300, 5000, 3000], [300, 0, 257]
+    b = make_batch(name="plong", seq_lens=lens, q_lens=qls, num_heads=32, num_kv_heads=8,
+                   head_size=128, block_size=16, scale=128 ** -0.5, seed=31, device=DEV)
+    pool = oracle_pool(b)
+    gpu_write(b)
+    out = gpu_prefill(b)
+    rows = [0, 1, 31, 32, 63, 64, 150, 298, 299, 300, 301, 332, 430, 555, 556]
+    compare(out[rows], oracle_rows(b, pool, rows=rows), "long-context prefill")
+
+
 # ----------------------------------------------------------------- full-size workloads
 
 def _sample_rows(b, per_chunk: int, seed: int):
