@@ -57,11 +57,12 @@ def decode_algorithmic_bytes(b, elem_bytes: int = 2) -> int:
     return kv + qo + nblk * 4 + b.num_seqs * 4
 
 
-def cascade_algorithmic_bytes(b, shared_len: int) -> int:
+def cascade_algorithmic_bytes(b, shared_len: int, kv_elem_bytes: int = 2) -> int:
     """Bytes a shared-prefix decode must move: the shared tokens' K+V once, each
-    sequence's own tokens, q, out and the tables; the prefix partials stay in L2."""
+    sequence's own tokens, q, out and the tables; the prefix partials stay in L2.
+    kv_elem_bytes: 2 for a bf16 pool, 1 for FP8."""
     own = [int(L) - shared_len for L in b.seq_lens.tolist()]
-    kv = kv_read_bytes([shared_len] + own, b.num_kv_heads, b.head_size)
+    kv = kv_read_bytes([shared_len] + own, b.num_kv_heads, b.head_size) * kv_elem_bytes // 2
     qo = 2 * b.q.numel() * 2
     nblk = shared_len // b.block_size + sum(-(-L // b.block_size) for L in own)
     return kv + qo + nblk * 4 + b.num_seqs * 4
@@ -333,8 +334,6 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.current_stream(dev)
     out = torch.empty_like(b.q)
     fp8 = args.kv == "fp8"
-    if fp8 and args.cascade:
-        raise SystemExit("--cascade reads a bf16 pool")
     pool = b.kv_cache
     if fp8:
         from paged_kv_cache_287_gb300.workloads import FP8_K_SCALE, FP8_V_SCALE, fp8_pool_of
@@ -355,7 +354,10 @@ def run_ours(args, world, rank, local):
 
     def attend(q, tables, lens, st, dst=None):
         dst = out if dst is None else dst
-        if args.cascade:
+        if args.cascade and fp8:
+            binding.pa_decode_cascade_fp8(dst, q, pool, tables, lens, max_len, shared, b.scale,
+                                          FP8_K_SCALE, FP8_V_SCALE, ws, st)
+        elif args.cascade:
             binding.pa_decode_cascade(dst, q, pool, tables, lens, max_len, shared, b.scale,
                                       ws, st)
         elif fp8:
@@ -513,12 +515,13 @@ def run_ours(args, world, rank, local):
     value = world * kv * args.steps / (total_ms / 1e3) / 1e9
     seqs_s = world * b.num_seqs * args.steps / (total_ms / 1e3)
     peak, peak_src = measured_peaks()
-    alg = cascade_algorithmic_bytes(b, shared) if args.cascade else \
+    alg = cascade_algorithmic_bytes(b, shared, 1 if fp8 else 2) if args.cascade else \
         decode_algorithmic_bytes(b, 1 if fp8 else 2)
     achieved = alg / (decode_ms / 1e3) / 1e9
     if args.cascade:
-        kernel = "pa_decode_cascade (prefix pass + suffix decode + merge kernel)"
-        traffic_file = f"cascade_{b.name}.traffic.txt"
+        kernel = (f"pa_decode_cascade{'_fp8' if fp8 else ''} (prefix pass + suffix decode + "
+                  f"merge kernel)")
+        traffic_file = f"cascade{'_fp8' if fp8 else ''}_{b.name}.traffic.txt"
     elif fp8:
         kernel = "pa_decode_fp8 (split-context kernel + merge kernel)"
         traffic_file = f"decode_fp8_{b.name}.traffic.txt"

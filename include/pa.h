@@ -238,6 +238,22 @@ pa_status pa_decode_cascade(void *out, const void *q, const void *kv_cache, int 
                             size_t workspace_bytes, pa_stream_t stream);
 
 /*
+ * pa_decode_cascade_fp8 - pa_decode_cascade over an FP8 pool: K = code value *
+ * k_scale, V = code value * v_scale (the pool pa_cache_write_fp8 fills).
+ * head_size must be 128 (else PA_ERR_UNSUPPORTED); k_scale and v_scale must be
+ * finite and > 0 (else PA_ERR_INVALID_ARG).  The prefix pass converts K/V to
+ * f16 as pa_prefill_chunk_fp8 does, the own tokens are read as in
+ * pa_decode_fp8.  Workspace: pa_decode_cascade_workspace_bytes.  Other
+ * arguments, results and errors as pa_decode_cascade.
+ */
+pa_status pa_decode_cascade_fp8(void *out, const void *q, const void *kv_cache, int num_blocks,
+                                int block_size, int num_heads, int num_kv_heads, int head_size,
+                                const int32_t *block_tables, int max_blocks_per_seq,
+                                const int32_t *seq_lens, int num_seqs, int max_seq_len,
+                                int shared_len, float scale, float k_scale, float v_scale,
+                                void *workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/*
  * pa_prefill_chunk - chunked-prefill attention of query chunks against their
  * cached context and themselves, causal.
  *

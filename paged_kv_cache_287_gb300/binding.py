@@ -25,7 +25,8 @@ STATUS = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_E
 EXPORTS = ("pa_status_string", "pa_kv_block_bytes", "pa_kv_block_bytes_dtype", "pa_cache_write",
            "pa_cache_write_fp8", "pa_decode_fp8", "pa_prefill_chunk_fp8",
            "pa_decode_workspace_bytes", "pa_decode", "pa_decode_noalloc",
-           "pa_decode_cascade_workspace_bytes", "pa_decode_cascade", "pa_prefill_chunk",
+           "pa_decode_cascade_workspace_bytes", "pa_decode_cascade", "pa_decode_cascade_fp8",
+           "pa_prefill_chunk",
            "pa_attention_varlen_workspace_bytes", "pa_attention_varlen",
            "pa_attention_varlen_fp8", "pa_error_check")
 
@@ -78,6 +79,9 @@ def lib(path: Optional[str] = None):
     L.pa_decode_cascade.restype = i
     L.pa_decode_cascade.argtypes = [P, P, P, i, i, i, i, i, P, i, P, i, i, i, ctypes.c_float, P,
                                     sz, P]
+    L.pa_decode_cascade_fp8.restype = i
+    L.pa_decode_cascade_fp8.argtypes = [P, P, P, i, i, i, i, i, P, i, P, i, i, i, ctypes.c_float,
+                                        ctypes.c_float, ctypes.c_float, P, sz, P]
     L.pa_prefill_chunk.restype = i
     L.pa_prefill_chunk.argtypes = [P, P, P, i, i, P, i, i, i, i, i, P, i, P, ctypes.c_float, P]
     L.pa_attention_varlen_workspace_bytes.restype = sz
@@ -273,8 +277,17 @@ def pa_decode_cascade_workspace_bytes(num_seqs: int, num_heads: int, num_kv_head
 def pa_decode_cascade(out: torch.Tensor, q: torch.Tensor, kv_cache: torch.Tensor,
                       block_tables: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
                       shared_len: int, scale: float, workspace: torch.Tensor,
-                      stream=None) -> None:
-    """pa_decode for a batch whose first shared_len tokens sit in the same blocks."""
+                      stream=None, kv_scales=None) -> None:
+    """pa_decode for a batch whose first shared_len tokens sit in the same blocks.
+
+    A uint8 (FP8 e4m3) pool goes to pa_decode_cascade_fp8 with
+    kv_scales = (k_scale, v_scale)."""
+    if kv_cache.dtype == torch.uint8:
+        if kv_scales is None:
+            raise ValueError("an FP8 pool needs kv_scales=(k_scale, v_scale)")
+        return pa_decode_cascade_fp8(out, q, kv_cache, block_tables, seq_lens, max_seq_len,
+                                     shared_len, scale, kv_scales[0], kv_scales[1], workspace,
+                                     stream)
     NB, bs, Hkv, D = _pool_geom(kv_cache)
     _need(q, "q", torch.bfloat16, 3)
     _need(out, "out", torch.bfloat16, 3)
@@ -289,6 +302,29 @@ def pa_decode_cascade(out: torch.Tensor, q: torch.Tensor, kv_cache: torch.Tensor
                                    seq_lens.data_ptr(), B, int(max_seq_len), int(shared_len),
                                    float(scale), workspace.data_ptr(), workspace.numel(),
                                    _stream(stream)), "pa_decode_cascade")
+
+
+def pa_decode_cascade_fp8(out: torch.Tensor, q: torch.Tensor, kv_cache: torch.Tensor,
+                          block_tables: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                          shared_len: int, scale: float, k_scale: float, v_scale: float,
+                          workspace: torch.Tensor, stream=None) -> None:
+    """pa_decode_cascade over an FP8 pool (uint8 e4m3 codes times k_scale / v_scale)."""
+    NB, bs, Hkv, D = _pool8_geom(kv_cache)
+    _need(q, "q", torch.bfloat16, 3)
+    _need(out, "out", torch.bfloat16, 3)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(workspace, "workspace", torch.uint8, 1)
+    B, Hq, Dq = q.shape
+    if Dq != D or out.shape != q.shape or seq_lens.shape[0] != B or block_tables.shape[0] != B:
+        raise ValueError("inconsistent decode shapes")
+    _check(lib().pa_decode_cascade_fp8(out.data_ptr(), q.data_ptr(), kv_cache.data_ptr(), NB, bs,
+                                       Hq, Hkv, D, block_tables.data_ptr(),
+                                       block_tables.shape[1], seq_lens.data_ptr(), B,
+                                       int(max_seq_len), int(shared_len), float(scale),
+                                       float(k_scale), float(v_scale), workspace.data_ptr(),
+                                       workspace.numel(), _stream(stream)),
+           "pa_decode_cascade_fp8")
 
 
 def pa_prefill_chunk(out: torch.Tensor, q: torch.Tensor, cu_q_lens: torch.Tensor,

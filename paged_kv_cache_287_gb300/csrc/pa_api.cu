@@ -277,25 +277,28 @@ size_t pa_decode_cascade_workspace_bytes(int num_seqs, int num_heads, int num_kv
            pa::prefix_partial_bytes(splits, num_seqs, num_heads, head_size);
 }
 
-pa_status pa_decode_cascade(void *out, const void *q, const void *kv_cache, int num_blocks,
-                            int block_size, int num_heads, int num_kv_heads, int head_size,
-                            const int32_t *block_tables, int max_blocks_per_seq,
-                            const int32_t *seq_lens, int num_seqs, int max_seq_len,
-                            int shared_len, float scale, void *workspace,
-                            size_t workspace_bytes, pa_stream_t stream) {
+// pa_decode_cascade and pa_decode_cascade_fp8 (kv8: an FP8 pool, head size 128).
+static pa_status cascade_impl(void *out, const void *q, const void *kv_cache, int num_blocks,
+                              int block_size, int num_heads, int num_kv_heads, int head_size,
+                              const int32_t *block_tables, int max_blocks_per_seq,
+                              const int32_t *seq_lens, int num_seqs, int max_seq_len,
+                              int shared_len, float scale, bool kv8, float k_scale, float v_scale,
+                              void *workspace, size_t workspace_bytes, pa_stream_t stream) {
     pa_status st = check_pool(kv_cache, num_blocks, block_size, num_kv_heads, head_size);
     if (st != PA_OK) return st;
     if ((st = check_heads(num_heads, num_kv_heads)) != PA_OK) return st;
+    if (kv8 && head_size != 128) return PA_ERR_UNSUPPORTED;
     if (num_seqs < 0 || max_seq_len < 0 || max_blocks_per_seq <= 0) return PA_ERR_INVALID_ARG;
     if (shared_len < 0 || shared_len > max_seq_len) return PA_ERR_INVALID_ARG;
     if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f) return PA_ERR_INVALID_ARG;
+    if (kv8 && (!good_scale(k_scale) || !good_scale(v_scale))) return PA_ERR_INVALID_ARG;
     if (shared_len % 16 != 0 || shared_len % block_size != 0) return PA_ERR_UNSUPPORTED;
     if (num_seqs == 0) return PA_OK;
     if (!out || !q || !block_tables || !seq_lens || !aligned(out, 16) || !aligned(q, 16) ||
         !aligned(block_tables, 4) || !aligned(seq_lens, 4))
         return PA_ERR_INVALID_ARG;
     if (max_seq_len > max_blocks_per_seq * block_size) return PA_ERR_INVALID_ARG;
-    if (num_seqs > pa::decode_max_seqs(head_size, num_heads / num_kv_heads))
+    if (num_seqs > pa::decode_max_seqs(head_size, num_heads / num_kv_heads, kv8))
         return PA_ERR_UNSUPPORTED;
     if ((long long)num_seqs * num_kv_heads * (((long long)max_seq_len + 15) / 16) >= (1LL << 31))
         return PA_ERR_UNSUPPORTED;
@@ -316,13 +319,38 @@ pa_status pa_decode_cascade(void *out, const void *q, const void *kv_cache, int 
         pre_acc = reinterpret_cast<float *>(base + (rows * 2 * 4 + 255) / 256 * 256);
         cudaError_t e = pa::launch_prefix_partials(q, kv_cache, g, num_heads, block_tables,
                                                    max_blocks_per_seq, num_seqs, shared_len,
-                                                   scale, splits, pre_ml, pre_acc, s);
+                                                   scale, splits, pre_ml, pre_acc, kv8, k_scale,
+                                                   v_scale, s);
         if (e != cudaSuccess) return from_cuda(e);
     }
     return from_cuda(pa::launch_decode_suffix(out, q, kv_cache, g, num_heads, block_tables,
                                               max_blocks_per_seq, seq_lens, num_seqs,
                                               max_seq_len, shared_len, scale, workspace, pre_ml,
-                                              pre_acc, splits, s));
+                                              pre_acc, splits, kv8, k_scale, v_scale, s));
+}
+
+pa_status pa_decode_cascade(void *out, const void *q, const void *kv_cache, int num_blocks,
+                            int block_size, int num_heads, int num_kv_heads, int head_size,
+                            const int32_t *block_tables, int max_blocks_per_seq,
+                            const int32_t *seq_lens, int num_seqs, int max_seq_len,
+                            int shared_len, float scale, void *workspace,
+                            size_t workspace_bytes, pa_stream_t stream) {
+    return cascade_impl(out, q, kv_cache, num_blocks, block_size, num_heads, num_kv_heads,
+                        head_size, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+                        max_seq_len, shared_len, scale, false, 1.f, 1.f, workspace,
+                        workspace_bytes, stream);
+}
+
+pa_status pa_decode_cascade_fp8(void *out, const void *q, const void *kv_cache, int num_blocks,
+                                int block_size, int num_heads, int num_kv_heads, int head_size,
+                                const int32_t *block_tables, int max_blocks_per_seq,
+                                const int32_t *seq_lens, int num_seqs, int max_seq_len,
+                                int shared_len, float scale, float k_scale, float v_scale,
+                                void *workspace, size_t workspace_bytes, pa_stream_t stream) {
+    return cascade_impl(out, q, kv_cache, num_blocks, block_size, num_heads, num_kv_heads,
+                        head_size, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+                        max_seq_len, shared_len, scale, true, k_scale, v_scale, workspace,
+                        workspace_bytes, stream);
 }
 
 pa_status pa_prefill_chunk(void *out, const void *q, const int32_t *cu_q_lens, int num_chunks,

@@ -890,10 +890,11 @@ cudaError_t launch_decode_suffix(void *out, const void *q, const void *kv_cache,
                                  int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs,
                                  int max_seq_len, int shared_len, float scale, void *workspace,
                                  const float *pre_ml, const float *pre_acc, int pre_splits,
-                                 cudaStream_t stream) {
+                                 bool kv8, float k_scale, float v_scale, cudaStream_t stream) {
     return launch_decode_impl(out, q, kv_cache, g, num_heads, block_tables, max_blocks_per_seq,
                               seq_lens, num_seqs, max_seq_len, shared_len, scale, workspace,
-                              pre_ml, pre_acc, pre_splits, false, 1.f, 1.f, stream);
+                              pre_ml, pre_acc, pre_splits, kv8, kv8 ? k_scale : 1.f,
+                              kv8 ? v_scale : 1.f, stream);
 }
 
 size_t prefix_partial_bytes(int splits, int num_seqs, int num_heads, int head_size) {

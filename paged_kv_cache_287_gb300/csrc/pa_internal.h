@@ -57,12 +57,13 @@ cudaError_t launch_decode(void *out, const void *q, const void *kv_cache, const 
 // Shared-prefix (cascade) decode.  The first shared_len tokens of every sequence
 // sit in sequence 0's first blocks.  The prefix pass computes, per key-range split,
 // the unnormalised (m, l, O) of every (sequence, query head) over those tokens.
+// kv8: an FP8 pool (head size 128), real K/V = code * k_scale / v_scale.
 int prefix_splits(int num_seqs, int num_heads, int num_kv_heads, int shared_len, int sm_count);
 cudaError_t launch_prefix_partials(const void *q, const void *kv_cache, const KvGeom &g,
                                    int num_heads, const int32_t *block_tables,
                                    int max_blocks_per_seq, int num_seqs, int shared_len,
                                    float scale, int splits, float *part_ml, float *part_acc,
-                                   cudaStream_t stream);
+                                   bool kv8, float k_scale, float v_scale, cudaStream_t stream);
 // Bytes of prefix partials for `splits` splits.
 size_t prefix_partial_bytes(int splits, int num_seqs, int num_heads, int head_size);
 // Decode over each sequence's tokens [shared_len, seq_len), folding in the prefix
@@ -72,7 +73,7 @@ cudaError_t launch_decode_suffix(void *out, const void *q, const void *kv_cache,
                                  int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs,
                                  int max_seq_len, int shared_len, float scale, void *workspace,
                                  const float *pre_ml, const float *pre_acc, int pre_splits,
-                                 cudaStream_t stream);
+                                 bool kv8, float k_scale, float v_scale, cudaStream_t stream);
 
 // One launch for a flattened mixed batch (chunks first, then decode sequences):
 // decode and chunked prefill side by side on disjoint SMs, split on the device.

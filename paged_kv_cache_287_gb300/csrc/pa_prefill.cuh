@@ -617,7 +617,10 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &kv_map, const Pr
         } else {
             tc_fence_after();
             if (prefix) {
-                // Unnormalised partial of this (split, sequence, query head).
+                // Unnormalised partial of this (split, sequence, query head); an
+                // FP8 pool's v_scale is applied here, as the decode applies it to
+                // the pieces it merges with.
+                const float vsc = KV8 ? a.v_scale : 1.f;
                 const size_t rec =
                     ((size_t)bid.z * q_len + (t0 + tok)) * a.num_heads + (size_t)h * G + gq;
                 float4 *pacc = reinterpret_cast<float4 *>(a.part_acc + rec * D);
@@ -629,8 +632,8 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &kv_map, const Pr
                     if (real) {
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
-                            pacc[c * 8 + e] =
-                                make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+                            pacc[c * 8 + e] = make_float4(o[4 * e] * vsc, o[4 * e + 1] * vsc,
+                                                          o[4 * e + 2] * vsc, o[4 * e + 3] * vsc);
                     }
                 }
                 if (real) reinterpret_cast<float2 *>(a.part_ml)[rec] = make_float2(m, l);
@@ -777,9 +780,11 @@ cudaError_t launch_prefix_partials(const void *q, const void *kv_cache, const Kv
                                    int num_heads, const int32_t *block_tables,
                                    int max_blocks_per_seq, int num_seqs, int shared_len,
                                    float scale, int splits, float *part_ml, float *part_acc,
-                                   cudaStream_t stream) {
+                                   bool kv8, float k_scale, float v_scale, cudaStream_t stream) {
     CUtensorMap map;
-    if (!encode_kv_map(&map, kv_cache, g, g.block_size >= 16 ? 16 : g.block_size))
+    const int box_rows = g.block_size >= 16 ? 16 : g.block_size;
+    if (kv8 ? (g.head_size != 128 || !encode_kv_map_fp8(&map, kv_cache, g, box_rows))
+            : !encode_kv_map(&map, kv_cache, g, box_rows))
         return cudaErrorInvalidValue;
     PrefillArgs a;
     a.out = nullptr;
@@ -802,10 +807,12 @@ cudaError_t launch_prefix_partials(const void *q, const void *kv_cache, const Kv
     const int tiles = (shared_len + kTcKeys - 1) / kTcKeys;
     a.split_tiles = (tiles + splits - 1) / splits;
     a.prefix_rows = num_seqs;
-    a.k_scale = a.v_scale = 1.f;
+    a.k_scale = kv8 ? k_scale : 1.f;
+    a.v_scale = kv8 ? v_scale : 1.f;
     const int per_cta = kTcTiles * a.q_tile;
     dim3 grid((unsigned)((num_seqs + per_cta - 1) / per_cta), (unsigned)g.num_kv_heads,
               (unsigned)splits);
+    if (kv8) return launch_prefill_tc<128, true>(a, map, grid, stream);
     if (g.head_size == 128) return launch_prefill_tc<128>(a, map, grid, stream);
     return launch_prefill_tc<64>(a, map, grid, stream);
 }

@@ -109,6 +109,23 @@ def test_cascade_host_checks(lib):
     bad[11] = 0                                 # no sequences: no-op
     assert lib.pa_decode_cascade(*bad) == 0
     assert lib.pa_decode_cascade_workspace_bytes(0, 32, 8, 128, 64) == 0
+    # The FP8 form: the same checks, plus head size 128 only and positive scales.
+    a8 = args[:15] + [0.5, 0.25] + args[15:]
+    bad = list(a8)
+    bad[13] = 8
+    assert lib.pa_decode_cascade_fp8(*bad) == 2
+    bad = list(a8)
+    bad[7] = 64                                 # head_size 64 is bf16-only
+    assert lib.pa_decode_cascade_fp8(*bad) == 2
+    bad = list(a8)
+    bad[16] = 0.0                               # v_scale must be > 0
+    assert lib.pa_decode_cascade_fp8(*bad) == 1
+    bad = list(a8)
+    bad[15] = float("inf")                      # k_scale must be finite
+    assert lib.pa_decode_cascade_fp8(*bad) == 1
+    bad = list(a8)
+    bad[11] = 0                                 # no sequences: no-op
+    assert lib.pa_decode_cascade_fp8(*bad) == 0
 
 
 def test_fp8_host_checks(lib):

@@ -12,8 +12,10 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from paged_kv_cache_287_gb300 import binding
-from paged_kv_cache_287_gb300.workloads import make_batch, make_config
+from paged_kv_cache_287_gb300.workloads import (FP8_K_SCALE, FP8_V_SCALE, fp8_pool_of,
+                                                make_batch, make_config)
 from tests._gpu import bits, compare, gpu_decode, gpu_write, oracle_pool, oracle_rows
 
 pytestmark = pytest.mark.gpu
@@ -121,3 +123,72 @@ def test_cascade_rejects_unaligned_shared_length():
     with pytest.raises(binding.PaError) as e:
         gpu_cascade(b, 24)  # three blocks of 8: not a multiple of 16
     assert e.value.status == 2
+
+
+# ----------------------------------------------------------------- FP8 pool
+
+def _fp8_case(b, shared_len, ks=FP8_K_SCALE, vs=FP8_V_SCALE, seq_lens=None):
+    """Quantise the batch's K/V into an FP8 pool (the new rows by the CUDA write,
+    checked bit-exact against the oracle's), run the FP8 cascade and return it
+    with the oracle's plain FP8 decode of the same codes."""
+    pool8 = fp8_pool_of(b, ks, vs)
+    codes = oracle.cache_write_fp8(pool8, b.k_new, b.v_new, b.slot_mapping, ks, vs)
+    binding.pa_cache_write_fp8(pool8, b.k_new, b.v_new, b.slot_mapping, ks, vs)
+    binding.pa_error_check()
+    assert np.array_equal(pool8.cpu().numpy(), codes)
+    lens = b.seq_lens if seq_lens is None else seq_lens
+    out = torch.full_like(b.q, float("nan"))
+    ws = torch.empty(binding.pa_decode_cascade_workspace_bytes(
+        b.num_seqs, b.num_heads, b.num_kv_heads, b.head_size, shared_len), dtype=torch.uint8,
+        device=DEV)
+    binding.pa_decode_cascade(out, b.q, pool8, b.block_tables, lens, int(lens.max()),
+                              shared_len, b.scale, ws, kv_scales=(ks, vs))
+    binding.pa_error_check()
+    want = oracle.attention_fp8(b.q, b.cu_q_lens, codes, ks, vs, b.block_tables, lens,
+                                b.num_heads, b.scale)
+    return out, want, pool8
+
+
+@pytest.mark.parametrize("case", [0, 1, 3, 4])
+def test_fp8_cascade_small_shapes(case):
+    B, pb, (lo, hi), Hq, Hkv, D, bs = CASCADE_SHAPES[case]  # head size 128 cases
+    g = torch.Generator().manual_seed(700 + case)
+    suffix = torch.randint(lo, hi + 1, (B,), generator=g).tolist()
+    lens = [pb * bs + x for x in suffix]
+    b = make_batch(name=f"c8{case}", seq_lens=lens, q_lens=[1] * B, num_heads=Hq,
+                   num_kv_heads=Hkv, head_size=D, block_size=bs, scale=D ** -0.5,
+                   seed=800 + case, shared_prefix_blocks=pb, device=DEV)
+    out, want, _ = _fp8_case(b, pb * bs)
+    compare(out, want, f"fp8 cascade case {case}")
+
+
+def test_fp8_cascade_other_scales_and_empty_suffixes():
+    pb, bs = 12, 16
+    b = make_batch(name="c8z", seq_lens=[pb * bs + x for x in (5, 70, 1, 33, 9)],
+                   q_lens=[1] * 5, num_heads=32, num_kv_heads=8, head_size=128, block_size=bs,
+                   scale=-0.07, seed=81, shared_prefix_blocks=pb, device=DEV)
+    lens = b.seq_lens.clone()
+    lens[1] = pb * bs
+    out, want, _ = _fp8_case(b, pb * bs, ks=0.2, vs=0.0045, seq_lens=lens)
+    compare(out, want, "fp8 cascade, other scales, empty suffixes")
+
+
+def test_fp8_cascade_matches_fp8_decode():
+    b = make_batch(name="c8d", seq_lens=[512 + x for x in (100, 3, 250, 64, 1, 77)],
+                   q_lens=[1] * 6, num_heads=64, num_kv_heads=8, head_size=128, block_size=16,
+                   scale=128 ** -0.5, seed=83, shared_prefix_blocks=32, device=DEV)
+    out, _, pool8 = _fp8_case(b, 512)
+    d = torch.full_like(b.q, float("nan"))
+    ws = torch.empty(binding.pa_decode_workspace_bytes(b.num_seqs, b.num_heads, b.num_kv_heads,
+                                                       b.head_size), dtype=torch.uint8,
+                     device=DEV)
+    binding.pa_decode_fp8(d, b.q, pool8, b.block_tables, b.seq_lens, int(b.seq_lens.max()),
+                          b.scale, FP8_K_SCALE, FP8_V_SCALE, ws)
+    binding.pa_error_check()
+    assert (out.float() - d.float()).abs().max().item() <= 1e-2
+
+
+def test_fp8_cascade_prefix_workload_full_size():
+    b = make_config(5, device=DEV)
+    out, want, _ = _fp8_case(b, b.shared_prefix_blocks * b.block_size)
+    compare(out, want, "prefix-shared workload, FP8 cascade")
