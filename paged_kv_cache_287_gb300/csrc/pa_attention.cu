@@ -1,6 +1,8 @@
 // pa_attention.cu - the attention kernels of libpagedattn in one translation unit:
 // decode (pa_decode.cuh), chunked prefill (pa_prefill.cuh), and the single-launch
 // kernel for a flattened mixed batch that runs both side by side.
+#include <type_traits>
+
 #include "pa_decode.cuh"
 #include "pa_prefill.cuh"
 
@@ -39,6 +41,7 @@ struct MixPlanArgs {
     float dec_bytes_per_token;  // K+V bytes per decode token: 2 * Hkv * D * 2
     float pre_flops_per_pair;   // flops per visible (query, key) pair: 4 * Hq * D
     float dec_sm_gbs, hbm_gbs, pre_sm_tflops;  // rates of the two parts
+    int dec_warps;               // decode warps per decode CTA
     int *plan;                   // out: {decode CTAs, decode warps}
 };
 
@@ -96,20 +99,22 @@ __global__ void __launch_bounds__(256) mix_plan_kernel(const MixPlanArgs a) {
         }
         if (tid == 0) {
             a.plan[0] = best;
-            a.plan[1] = best * kDecodeWarps;
+            a.plan[1] = best * a.dec_warps;
         }
     }
 }
 
 // KV8: an FP8 pool for both roles (the prefill role's converter is warp 11).
-template <int D, bool KV8>
+// DW: warps of the decode role (12, or 11 where 12 rings of the decode's stages
+// would not fit the prefill role's shared memory; the 12th then idles).
+template <int D, bool KV8, int DW>
 __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     mixed_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs da,
                  const PrefillArgs pa, int dec_slots, uint3 pre_grid) {
     if ((int)blockIdx.x < dec_slots) {
         if ((int)blockIdx.x < da.plan[0])
-            decode_body<D, kDecodeWarps, KV8 ? kMixStagesFp8 : kMixStages, KV8>(
-                kv_map, da, blockIdx.x, da.plan[1]);
+            decode_body<D, DW, KV8 ? kMixStagesFp8 : kMixStages, KV8>(kv_map, da, blockIdx.x,
+                                                                      da.plan[1]);
         return;
     }
     const unsigned v = blockIdx.x - (unsigned)dec_slots;
@@ -118,10 +123,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     prefill_body<D, KV8>(kv_map, pa, bid, pre_grid);
 }
 
-template <int D, bool KV8>
+template <int D, bool KV8, int DW = kDecodeWarps>
 cudaError_t launch_mixed_d(const CUtensorMap &map, const DecodeArgs &da, const PrefillArgs &pa,
                            dim3 pgrid, int sms, size_t smem, cudaStream_t stream) {
-    auto kern = mixed_kernel<D, KV8>;
+    auto kern = mixed_kernel<D, KV8, DW>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -140,15 +145,33 @@ size_t mixed_workspace_bytes(int num_decodes, int head_size, int sm_count) {
     return decode_workspace_bytes(num_decodes, head_size, sm_count) + 256;
 }
 
-bool mixed_supported(int num_decodes, int num_heads, const KvGeom &g, bool kv8) {
+namespace {
+
+// Warps of the mixed launch's decode role: 12 when their rings fit the prefill
+// role's shared memory (which is the launch's), else 11 for a bf16 pool of head
+// size 128 (the launch instantiated for that), else 0 (no one launch).
+int mixed_decode_warps(int num_decodes, int num_heads, const KvGeom &g, bool kv8) {
     const int G = num_heads / g.num_kv_heads;
-    if (kv8 && g.head_size != 128) return false;
-    const size_t dec =
-        kv8 ? decode_smem_bytes<128, true, kMixStagesFp8>(num_decodes, G)
-        : g.head_size == 128 ? decode_smem_bytes<128, false, kMixStages>(num_decodes, G)
-                             : decode_smem_bytes<64, false, kMixStages>(num_decodes, G);
+    if (kv8 && g.head_size != 128) return 0;
     const size_t pre = g.head_size == 128 ? TcLay<128>::kSmem : TcLay<64>::kSmem;
-    return dec <= pre;  // the prefill's shared memory is the launch's
+    auto fits = [&](auto w) {
+        constexpr int W = decltype(w)::value;
+        const size_t dec =
+            kv8 ? decode_smem_bytes<128, true, kMixStagesFp8, W>(num_decodes, G)
+            : g.head_size == 128 ? decode_smem_bytes<128, false, kMixStages, W>(num_decodes, G)
+                                 : decode_smem_bytes<64, false, kMixStages, W>(num_decodes, G);
+        return dec <= pre;
+    };
+    if (fits(std::integral_constant<int, kDecodeWarps>{})) return kDecodeWarps;
+    if (!kv8 && g.head_size == 128 && fits(std::integral_constant<int, kDecodeWarps - 1>{}))
+        return kDecodeWarps - 1;
+    return 0;
+}
+
+}  // namespace
+
+bool mixed_supported(int num_decodes, int num_heads, const KvGeom &g, bool kv8) {
+    return mixed_decode_warps(num_decodes, num_heads, g, kv8) > 0;
 }
 
 cudaError_t launch_mixed(void *out, const void *q, const int32_t *cu_q_lens, int num_prefills,
@@ -178,7 +201,12 @@ cudaError_t launch_mixed(void *out, const void *q, const int32_t *cu_q_lens, int
     // FP8 pool (measured on GB300): decode about kMixDecodeSmGBsFp8 per SM with 12
     // warps x 3 stages, 6.3 TB/s at most; the prefill, with its conversion, about
     // 7.1 TFLOP/s per SM.
-    pl.dec_sm_gbs = kv8 ? kMixDecodeSmGBsFp8 : kMixDecodeSmGBs;
+    // The decode's rate per SM scales with its warps (each holds the same bytes
+    // in flight).
+    const int dw = mixed_decode_warps(num_decodes, num_heads, g, kv8);
+    if (dw == 0) return cudaErrorInvalidValue;
+    pl.dec_warps = dw;
+    pl.dec_sm_gbs = (kv8 ? kMixDecodeSmGBsFp8 : kMixDecodeSmGBs) * dw / kDecodeWarps;
     pl.hbm_gbs = kv8 ? 6300.f : kMixHbmGBs;
     pl.pre_sm_tflops = kv8 ? 7.1f : kMixPrefillSmTflops;
     pl.plan = plan;
@@ -202,6 +230,9 @@ cudaError_t launch_mixed(void *out, const void *q, const int32_t *cu_q_lens, int
     pa.v_scale = v_scale;
     if (kv8)
         return launch_mixed_d<128, true>(map, da, pa, pgrid, sms, TcLay<128>::kSmem, stream);
+    if (D == 128 && dw < kDecodeWarps)
+        return launch_mixed_d<128, false, kDecodeWarps - 1>(map, da, pa, pgrid, sms,
+                                                            TcLay<128>::kSmem, stream);
     if (D == 128)
         return launch_mixed_d<128, false>(map, da, pa, pgrid, sms, TcLay<128>::kSmem, stream);
     return launch_mixed_d<64, false>(map, da, pa, pgrid, sms, TcLay<64>::kSmem, stream);

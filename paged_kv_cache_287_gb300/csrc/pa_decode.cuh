@@ -98,11 +98,11 @@ struct DecodeArgs {
 
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-template <int D, bool KV8 = false, int S = kDecodeStages>
+template <int D, bool KV8 = false, int S = kDecodeStages, int W = kDecodeWarps>
 __host__ __device__ constexpr size_t decode_smem_bytes(int num_seqs, int group) {
     return 1024 /* alignment slack */ +
-           (size_t)kDecodeWarps * S * (2 * Lay<D, KV8>::kKvBytes + q_slot_bytes(group, D)) +
-           (size_t)kDecodeWarps * S * 8 + (size_t)(2 * num_seqs + 1) * 4;
+           (size_t)W * S * (2 * Lay<D, KV8>::kKvBytes + q_slot_bytes(group, D)) +
+           (size_t)W * S * 8 + (size_t)(2 * num_seqs + 1) * 4;
 }
 
 // TMA row of (block, K, head, offset) in the pool viewed as rows of head_size.
@@ -116,7 +116,8 @@ __device__ __forceinline__ int kv_row(int blk, int h, int off, const DecodeArgs 
 
 // The split-context decode of one CTA (index cta of a grid whose warps number
 // total_warps), W warps with an S-stage ring each; called by decode_kernel and by
-// the mixed-batch kernel.
+// the mixed-batch kernel, whose CTAs may have more warps than W: those take part
+// in the set-up and its two CTA-wide barriers, then leave.
 template <int D, int W, int S, bool KV8>
 __device__ __forceinline__ void decode_body(const CUtensorMap &kv_map, const DecodeArgs &a,
                                             int cta, int total_warps) {
@@ -137,7 +138,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap &kv_map, const Dec
     const int max_len = a.max_blocks * bs;
     // s_len holds the tokens this kernel covers: those past the shared prefix.
     const int sh = a.shared_len;
-    for (int s = tid; s < B; s += W * 32) {
+    for (int s = tid; s < B; s += blockDim.x) {
         int len = a.seq_lens[s];
         if (len < sh || len > max_len) {
             atomicOr(&g_err_decode, kErrOob);
@@ -162,16 +163,17 @@ __device__ __forceinline__ void decode_body(const CUtensorMap &kv_map, const Dec
         }
         if (lane == 0) s_pre[B] = carry;
     }
-    if (lane == 0) {
+    if (lane == 0 && warp < W) {
         for (int st = 0; st < S; ++st) mbar_init(&bars[warp * S + st], 1);
         fence_barrier_init();
     }
     __syncthreads();
     if (cta == 0)
-        for (int s = tid; s <= B; s += W * 32) a.prefix[s] = s_pre[s];
+        for (int s = tid; s <= B; s += blockDim.x) a.prefix[s] = s_pre[s];
     // The merge kernel may be scheduled now; it waits for this grid to finish.
     asm volatile("griddepcontrol.launch_dependents;" :::);
 
+    if (warp >= W) return;
     // This warp's equal share of the flattened tile list.
     const long long T = (long long)s_pre[B] * Hkv;
     const long long NW = total_warps;

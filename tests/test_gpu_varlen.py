@@ -102,6 +102,38 @@ def test_varlen_one_launch_decode_counts(n_dec):
             f"one launch, {n_dec} decode sequences")
 
 
+@pytest.mark.parametrize("n_dec", [3, 240])
+def test_varlen_one_launch_group_8(n_dec):
+    """Eight query heads per KV head at head size 128: the decode role's twelve
+    two-stage rings do not fit the launch's shared memory, so it runs eleven
+    warps; the step is still one attention launch (the plan in the workspace is
+    written) and matches the oracle."""
+    g = torch.Generator().manual_seed(70 + n_dec)
+    dec = torch.randint(1, 2500, (n_dec,), generator=g).tolist()
+    lens = [900, 260] + dec
+    qls = [256, 129] + [1] * n_dec
+    b = make_batch(name=f"vg8_{n_dec}", seq_lens=lens, q_lens=qls, num_heads=64,
+                   num_kv_heads=8, head_size=128, block_size=16, scale=128 ** -0.5,
+                   seed=970 + n_dec, device=DEV)
+    pool = oracle_pool(b)
+    nb = binding.pa_attention_varlen_workspace_bytes(b.num_seqs, 2, 64, 8, 128)
+    ws = torch.full((nb,), 255, dtype=torch.uint8, device=DEV)  # plan slots read -1
+    out = torch.full_like(b.q, float("nan"))
+    npt = int(b.cu_q_lens[2])
+    binding.pa_attention_varlen(out, b.q, b.k_new, b.v_new, b.slot_mapping,
+                                b.cu_q_lens[:3].contiguous(), 2, npt, 256, b.kv_cache,
+                                b.block_tables, b.seq_lens, max(dec), b.scale, ws)
+    binding.pa_error_check()
+    plan = ws[nb - 256:nb - 248].view(torch.int32).tolist()
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    assert 1 <= plan[0] < sms and plan[1] == 11 * plan[0], plan
+    assert np.array_equal(bits(b.kv_cache), pool)
+    rows = np.concatenate([np.arange(0, npt, 7), npt + np.arange(0, n_dec, max(1, n_dec // 50))])
+    rows = rows.astype(np.int32)
+    compare(out[torch.as_tensor(rows, device=DEV).long()], oracle_rows(b, pool, rows),
+            f"one launch, group 8, {n_dec} decode sequences")
+
+
 def test_varlen_without_slot_mapping_writes_nothing():
     b = make_batch(name="vn", seq_lens=[40, 20], q_lens=[8, 1], num_heads=8, num_kv_heads=2,
                    head_size=128, block_size=16, scale=0.1, seed=950, device=DEV)
