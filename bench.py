@@ -249,6 +249,37 @@ def cpu_oracle_rate(n: int, budget_s: float = 12.0, seed=None, first: int = 64,
     return done_bytes / spent / 1e9, done / spent, done, k, threads
 
 
+def cpu_mixed_step_ms(b, stride: int = 8, threads: int = 0):
+    """The oracle's time for one step of a flattened mixed batch (cache write of
+    every new token + fp64 attention of every chunk row and decode token),
+    estimated from a timed sample: the whole cache write, then attention of every
+    stride-th row, scaled by causally visible (query, key) pairs.  Returns
+    (ms per step, sampled rows, all rows, threads)."""
+    import numpy as np
+
+    import oracle
+
+    lib = oracle.load()
+    threads = threads or oracle.max_threads(lib)
+    cu = b.cu_q_lens.tolist()
+    lens = b.seq_lens.tolist()
+    vis = []  # visible keys of every query row
+    for s in range(b.num_seqs):
+        ql = cu[s + 1] - cu[s]
+        vis += [lens[s] - ql + i + 1 for i in range(ql)]
+    rows = np.arange(0, len(vis), stride, dtype=np.int32)
+    pool = oracle._u16(b.kv_cache).copy()
+    t = time.perf_counter()
+    oracle.cache_write(pool, b.k_new, b.v_new, b.slot_mapping, lib=lib, inplace=True)
+    tw = time.perf_counter() - t
+    t = time.perf_counter()
+    oracle.attention(b.q, b.cu_q_lens, pool, b.block_tables, b.seq_lens, b.num_heads, b.scale,
+                     rows=rows, threads=threads, lib=lib)
+    ta = time.perf_counter() - t
+    work = sum(vis[r] for r in rows.tolist())
+    return (tw + ta * sum(vis) / work) * 1e3, len(rows), len(vis), threads
+
+
 # ----------------------------------------------------------------------------- arms
 
 def run_reference(args, world, rank):
@@ -262,6 +293,34 @@ def run_reference(args, world, rank):
 
     n = args.workload
     spec = config_spec(n)
+    if n == 4:
+        # The mixed step's own metric: the oracle's time per step, each timed
+        # step a sample of rows scaled to the whole step.
+        from paged_kv_cache_287_gb300.workloads import make_config
+        b = make_config(4, device="cpu")
+        for _ in range(args.warmup):
+            cpu_mixed_step_ms(b, stride=64)
+        est, t0 = [], time.perf_counter()
+        for _ in range(args.steps):
+            ms, nrows, allrows, threads = cpu_mixed_step_ms(b, stride=64)
+            est.append(ms)
+        el = time.perf_counter() - t0
+        value = sum(est) / len(est)
+        sample = (f"each step: the cache write of all {int(b.cu_q_lens[-1])} new tokens and "
+                  f"fp64 attention of every 64th of the {allrows} query rows ({nrows} rows), "
+                  f"scaled to the whole step by causally visible (query, key) pairs")
+        print(json.dumps({
+            "impl": "reference", "metric": "mixed chunked-prefill + decode step",
+            "value": value, "unit": "ms", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": value, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(4),
+            "cpu_baseline": {"value": value, "unit": "ms", "cores": threads, "kind": "oracle",
+                             "sample": sample, "wall_s": el},
+            "e2e": {"value": value, "unit": "ms", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}), flush=True)
+        return
     per_step = 2
     b = sample_of_config(n, per_step, device="cpu")
     lib = oracle.load()
@@ -672,15 +731,88 @@ def run_mixed(args, world, rank, local):
     torch.cuda.synchronize(dev)
     binding.pa_error_check(stream)
     unified_ms = e0.elapsed_time(e1) / args.steps
+
+    # End to end through the unified call: every step's inputs (q, new K/V, slots,
+    # chunk offsets, tables, lengths) from pinned host memory in one staging
+    # buffer, its output back, one stream per copy direction and two buffer sets,
+    # as the decode workloads' leg; the pool stays resident.
+    names = ("q", "k_new", "v_new", "slot_mapping", "cu_q_lens", "block_tables", "seq_lens")
+    offs, total = {}, 0
+    for k in names:
+        t = getattr(b, k)
+        offs[k] = total
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+
+    def views(buf):
+        v = {}
+        for k in names:
+            t = getattr(b, k)
+            v[k] = buf[offs[k]:offs[k] + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+        return v
+
+    host_buf = torch.empty(total, dtype=torch.uint8, pin_memory=True)
+    for k, v in views(host_buf).items():
+        v.copy_(getattr(b, k).to("cpu"))
+    dev_buf = [torch.empty(total, dtype=torch.uint8, device=dev) for _ in range(2)]
+    dev_in = [views(x) for x in dev_buf]
+    dev_out = [torch.empty_like(b.q) for _ in range(2)]
+    out_host = [torch.empty(b.q.shape, dtype=b.q.dtype, pin_memory=True) for _ in range(2)]
+    h2d = sum(getattr(b, k).numel() * getattr(b, k).element_size() for k in names)
+    d2h = out_host[0].numel() * out_host[0].element_size()
+    copy_in, copy_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    free = [torch.cuda.Event() for _ in range(2)]
+    landed = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
+    for e in free:
+        e.record(copy_out)
+
+    def e2e_step(i):
+        p = i % 2
+        x = dev_in[p]
+        copy_in.wait_event(free[p])
+        with torch.cuda.stream(copy_in):
+            dev_buf[p].copy_(host_buf, non_blocking=True)
+        landed[p].record(copy_in)
+        stream.wait_event(landed[p])
+        cu = x["cu_q_lens"][:n_pre + 1]
+        if fp8:
+            binding.pa_attention_varlen(dev_out[p], x["q"], x["k_new"], x["v_new"],
+                                        x["slot_mapping"], cu, n_pre, r_pre, max_q, pool8,
+                                        x["block_tables"], x["seq_lens"], max_dec, b.scale,
+                                        ws_all, stream, kv_scales=(FP8_K_SCALE, FP8_V_SCALE))
+        else:
+            binding.pa_attention_varlen(dev_out[p], x["q"], x["k_new"], x["v_new"],
+                                        x["slot_mapping"], cu, n_pre, r_pre, max_q, b.kv_cache,
+                                        x["block_tables"], x["seq_lens"], max_dec, b.scale,
+                                        ws_all, stream)
+        done[p].record(stream)
+        copy_out.wait_event(done[p])
+        with torch.cuda.stream(copy_out):
+            out_host[p].copy_(dev_out[p], non_blocking=True)
+        free[p].record(copy_out)
+
+    for i in range(max(args.warmup, 3)):
+        e2e_step(i)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        e2e_step(i)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(time.perf_counter() - t0, world, dev) * 1e3 / args.steps
+    binding.pa_error_check(stream)
+    barrier(world)
     if rank != 0:
         return
     flops = prefill_flops(b, 0, n_pre)
     kv_dec = kv_read_bytes(sl_dec.tolist(), b.num_kv_heads, b.head_size)
     with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
         pk = json.load(f)
+    pre_tflops = flops / (ms[1] / 1e3) / 1e12
     line = {"metric": "mixed chunked-prefill + decode step",
-            "value": unified_ms, "unit": "ms",
-            "higher_is_better": False, "n_gpus": world, "steps": args.steps,
+            "value": unified_ms, "unit": "ms", "ms_per_step": unified_ms,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+            "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "dtype": "f16" if fp8 else "bf16", "data": "synthetic",
             "config": dict(workload_config(4),
                            kv_cache="fp8-e4m3 (per-tensor k/v scale 1/64)" if fp8 else "bf16"),
@@ -695,8 +827,34 @@ def run_mixed(args, world, rank, local):
             "decode": {"kv_gbs": kv_dec / (2 if fp8 else 1) / (ms[2] / 1e3) / 1e9,
                        "frac": kv_dec / (2 if fp8 else 1) / (ms[2] / 1e3) / 1e9 / pk["hbm_gbs"]},
             "cache_write": {"gbs": 2 * b.k_new.numel() * 2 * 2 / (ms[0] / 1e3) / 1e9},
+            # The tensor-bound kernel of the step, timed alone in the separate calls
+            # (so against the burst bf16 peak; its f16 MMAs run at the same rate).
+            "roofline": {"bound": "tensor", "achieved": pre_tflops,
+                         "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": pre_tflops / pk["bf16_tflops"],
+                         "traffic": profile_traffic(
+                             f"prefill{'_fp8' if fp8 else ''}_{b.name}.traffic.txt"),
+                         "kernel": f"pa_prefill_chunk{'_fp8' if fp8 else ''}",
+                         "algorithmic_flops_per_launch": flops, "launch_ms": ms[1],
+                         "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops)"},
+            "e2e": {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h,
+                    "note": "the unified call with every step's inputs copied in from pinned "
+                            "host memory and its output copied out, one stream per copy "
+                            "direction, two buffer sets; the KV pool resident; host wall "
+                            "clock over all steps"},
             "clocks": sampler.summary(), "gpu_launches": 4 * args.steps,
             "unified_gpu_launches_per_step": 4}
+    if world == 1 and not args.no_cpu_baseline and not fp8:
+        est, nrows, allrows, threads = cpu_mixed_step_ms(
+            type(b)(**{**b.__dict__, **{k: getattr(b, k).cpu()
+                                          for k, v in b.__dict__.items()
+                                          if isinstance(v, torch.Tensor)}}), stride=16)
+        line["cpu_baseline"] = {"value": est, "unit": "ms", "cores": threads, "kind": "oracle",
+                                "sample": f"the cache write of all new tokens and fp64 "
+                                          f"attention of every 16th of the {allrows} query "
+                                          f"rows ({nrows} rows), scaled to the whole step by "
+                                          f"causally visible (query, key) pairs"}
     print(json.dumps(line), flush=True)
 
 
