@@ -826,7 +826,9 @@ def run_mixed(args, world, rank, local):
                         "frac": flops / (ms[1] / 1e3) / 1e12 / pk["bf16_tflops"]},
             "decode": {"kv_gbs": kv_dec / (2 if fp8 else 1) / (ms[2] / 1e3) / 1e9,
                        "frac": kv_dec / (2 if fp8 else 1) / (ms[2] / 1e3) / 1e9 / pk["hbm_gbs"]},
-            "cache_write": {"gbs": 2 * b.k_new.numel() * 2 * 2 / (ms[0] / 1e3) / 1e9},
+            # bf16 rows read, pool bytes written (one byte per element in an FP8 pool)
+            "cache_write": {"gbs": 2 * b.k_new.numel() * (2 + (1 if fp8 else 2)) /
+                                   (ms[0] / 1e3) / 1e9},
             # The tensor-bound kernel of the step, timed alone in the separate calls
             # (so against the burst bf16 peak; its f16 MMAs run at the same rate).
             "roofline": {"bound": "tensor", "achieved": pre_tflops,
