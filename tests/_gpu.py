@@ -61,11 +61,30 @@ def oracle_rows(b, pool_bits: np.ndarray, rows=None) -> np.ndarray:
                             b.num_heads, b.scale, rows=rows)
 
 
+# (what, max |d|, mean |d|, max |d| in bf16 ulps of the rounded oracle) of every
+# compare() in this process, reported at the end of the test session.
+ULP_LOG: list = []
+
+
+def bf16_ulps(got: np.ndarray, want: np.ndarray) -> np.ndarray:
+    """|got - bf16(want)| in units in the last place of bf16(want) (2^(e-7) for a
+    value in [2^e, 2^(e+1)); the smallest normal's ulp for zero)."""
+    w = torch.from_numpy(np.ascontiguousarray(want)).to(torch.bfloat16).double().numpy()
+    aw = np.abs(w)
+    e = np.floor(np.log2(np.where(aw > 0, aw, 2.0 ** -126)))
+    ulp = np.exp2(np.maximum(e, -126.0) - 7.0)
+    return np.abs(got - w) / ulp
+
+
 def compare(got: torch.Tensor, want: np.ndarray, what: str = ""):
     g = got.detach().float().cpu().double().numpy()
     assert g.shape == want.shape, (g.shape, want.shape)
     assert np.isfinite(g).all(), f"{what}: non-finite output"
     d = np.abs(g - want)
     mx, mean = float(d.max()) if d.size else 0.0, float(d.mean()) if d.size else 0.0
-    assert mx <= MAX_ABS and mean <= MEAN_ABS, f"{what}: max|d| {mx:.3e} mean|d| {mean:.3e}"
+    ulps = float(bf16_ulps(g, want).max()) if d.size else 0.0
+    ULP_LOG.append((what, mx, mean, ulps))
+    note = " (within one bf16 ulp of the rounded oracle: output rounding only)" if ulps <= 1 else ""
+    assert mx <= MAX_ABS and mean <= MEAN_ABS, \
+        f"{what}: max|d| {mx:.3e} mean|d| {mean:.3e}, {ulps:.1f} bf16 ulps{note}"
     return mx, mean
