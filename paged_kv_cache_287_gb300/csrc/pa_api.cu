@@ -274,7 +274,8 @@ size_t pa_decode_cascade_workspace_bytes(int num_seqs, int num_heads, int num_kv
     const int sms = pa::device_sm_count();
     const int splits = pa::prefix_splits(num_seqs, num_heads, num_kv_heads, shared_len, sms);
     return pa::decode_workspace_bytes(num_seqs, head_size, sms) +
-           pa::prefix_partial_bytes(splits, num_seqs, num_heads, head_size);
+           pa::prefix_partial_bytes(splits, num_seqs, num_heads, head_size) +
+           (splits > 0 ? pa::cascade_whole_bytes(num_seqs, num_kv_heads, head_size) : 0);
 }
 
 // pa_decode_cascade and pa_decode_cascade_fp8 (kv8: an FP8 pool, head size 128).
@@ -306,12 +307,16 @@ static pa_status cascade_impl(void *out, const void *q, const void *kv_cache, in
     const int sms = pa::device_sm_count();
     const int splits = pa::prefix_splits(num_seqs, num_heads, num_kv_heads, shared_len, sms);
     const size_t dec = pa::decode_workspace_bytes(num_seqs, head_size, sms);
-    const size_t need = dec + pa::prefix_partial_bytes(splits, num_seqs, num_heads, head_size);
+    const size_t pre = pa::prefix_partial_bytes(splits, num_seqs, num_heads, head_size);
+    const size_t need =
+        dec + pre + (splits > 0 ? pa::cascade_whole_bytes(num_seqs, num_kv_heads, head_size) : 0);
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return PA_ERR_WORKSPACE;
     pa::KvGeom g{num_blocks, block_size, num_kv_heads, head_size};
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     float *pre_ml = nullptr, *pre_acc = nullptr;
+    void *whole = nullptr;  // after the prefix partials
     if (splits > 0) {
+        whole = static_cast<uint8_t *>(workspace) + dec + pre;
         // Prefix partials after the decode workspace: (m, l) records, then O rows.
         uint8_t *base = static_cast<uint8_t *>(workspace) + dec;
         const size_t rows = (size_t)splits * num_seqs * num_heads;
@@ -326,7 +331,7 @@ static pa_status cascade_impl(void *out, const void *q, const void *kv_cache, in
     return from_cuda(pa::launch_decode_suffix(out, q, kv_cache, g, num_heads, block_tables,
                                               max_blocks_per_seq, seq_lens, num_seqs,
                                               max_seq_len, shared_len, scale, workspace, pre_ml,
-                                              pre_acc, splits, kv8, k_scale, v_scale, s));
+                                              pre_acc, splits, whole, kv8, k_scale, v_scale, s));
 }
 
 pa_status pa_decode_cascade(void *out, const void *q, const void *kv_cache, int num_blocks,

@@ -11,6 +11,8 @@
 //     (152 SMs x W warps), so skewed lengths cost nothing in balance.  A
 //     (sequence, head) segment that falls across ranges is finished in pieces whose
 //     (max, sum, acc) states are merged by log-sum-exp in a second small kernel.
+//     For a shared-prefix batch that kernel also folds the prefix pass's partials
+//     into every (sequence, head), so no decode warp waits on them.
 //   * Every warp runs its own pipeline: lane 0 issues 128B-swizzled 2-D TMA
 //     copies of the K and V tiles named by the block table into an S-stage ring in
 //     shared memory (plus the segment's G query rows with a bulk copy); the warp
@@ -85,12 +87,16 @@ struct DecodeArgs {
     float scale_log2;  // scale * log2(e)
     float k_scale, v_scale;  // FP8 pool: real K/V = e4m3 value * scale (1 for bf16)
     // Cascade: each sequence's tokens [0, shared_len) were attended by the prefix
-    // pass, whose pre_splits unnormalised partials per (sequence, query head) are
-    // folded in here; this kernel covers tokens [shared_len, seq_len).
+    // pass, whose pre_splits unnormalised partials per (sequence, query head) the
+    // merge kernel folds in; this kernel covers tokens [shared_len, seq_len).  A
+    // segment that one warp finishes whole then leaves its (m, l, acc) in the
+    // segment's own record instead of writing the output.
     int shared_len;
     int pre_splits;
     const float *pre_ml;   // [pre_splits][num_seqs][num_heads][2]
     const float *pre_acc;  // [pre_splits][num_seqs][num_heads][D]
+    float *whole_ml;       // [num_seqs * num_kv_heads][8][2]
+    float *whole_acc;      // [num_seqs * num_kv_heads][8][D]
     // Mixed-batch launch: the number of decode CTAs and their total warps were
     // chosen on the device; plan = {ctas, total_warps} (nullptr otherwise).
     const int *plan;
@@ -527,54 +533,8 @@ __device__ __forceinline__ void decode_body(const CUtensorMap &kv_map, const Dec
                     for (int e = 0; e < 4; ++e) acc[mt][e] *= a.v_scale;
             }
             const int nt = s_pre[s + 1] - s_pre[s];
-            if (first_j == 0 && j == nt - 1) {
-                if (a.pre_splits > 0) {
-                    // Fold in the shared prefix's partials of this lane's two heads.
-                    const bool w0 = hh0 < G, w1 = hh0 + 1 < G;
-                    const size_t r0 = (size_t)s * a.num_heads + (size_t)h * G + hh0;
-                    const size_t rstride = (size_t)B * a.num_heads;
-                    const float2 *pml = reinterpret_cast<const float2 *>(a.pre_ml);
-                    float M0 = m0, M1 = m1;
-                    for (int k = 0; k < a.pre_splits; ++k) {
-                        if (w0) M0 = fmaxf(M0, pml[k * rstride + r0].x);
-                        if (w1) M1 = fmaxf(M1, pml[k * rstride + r0 + 1].x);
-                    }
-                    const float c0 = fast_exp2(m0 - M0), c1 = fast_exp2(m1 - M1);
-                    l0 *= c0;
-                    l1 *= c1;
-#pragma unroll
-                    for (int mt = 0; mt < D / 16; ++mt) {
-                        acc[mt][0] *= c0;
-                        acc[mt][2] *= c0;
-                        acc[mt][1] *= c1;
-                        acc[mt][3] *= c1;
-                    }
-                    for (int k = 0; k < a.pre_splits; ++k) {
-                        const size_t r = k * rstride + r0;
-                        if (w0) {
-                            const float2 ml = pml[r];
-                            const float wk = fast_exp2(ml.x - M0);
-                            const float *pa = a.pre_acc + r * D;
-                            l0 += wk * ml.y;
-#pragma unroll
-                            for (int mt = 0; mt < D / 16; ++mt) {
-                                acc[mt][0] += wk * pa[dim_of(mt, 0)];
-                                acc[mt][2] += wk * pa[dim_of(mt, 1)];
-                            }
-                        }
-                        if (w1) {
-                            const float2 ml = pml[r + 1];
-                            const float wk = fast_exp2(ml.x - M1);
-                            const float *pa = a.pre_acc + (r + 1) * D;
-                            l1 += wk * ml.y;
-#pragma unroll
-                            for (int mt = 0; mt < D / 16; ++mt) {
-                                acc[mt][1] += wk * pa[dim_of(mt, 0)];
-                                acc[mt][3] += wk * pa[dim_of(mt, 1)];
-                            }
-                        }
-                    }
-                }
+            const bool whole = first_j == 0 && j == nt - 1;
+            if (whole && a.pre_splits == 0) {
                 // Whole segment in this warp: normalise and write bf16 rows, staged in
                 // the stage's query slot (G rows) for 16-byte stores.  Only the G real
                 // heads are staged: the slot holds no room for the padding heads.
@@ -601,8 +561,12 @@ __device__ __forceinline__ void decode_body(const CUtensorMap &kv_map, const Dec
                 for (int v = lane; v < G * D / 8; v += 32) dst[v] = srcv[v];
                 wrote_smem = true;
             } else {
+                // A piece of a split segment, or (cascade) a whole one: unnormalised
+                // (m, l, acc) for the merge kernel.
                 const size_t rec = (size_t)g * 2 + (first_piece ? 0 : 1);
-                float *pacc = a.part_acc + rec * kHeadsPad * D;
+                const size_t wrec = (size_t)s * Hkv + h;
+                float *pacc = whole ? a.whole_acc + wrec * kHeadsPad * D
+                                    : a.part_acc + rec * kHeadsPad * D;
 #pragma unroll
                 for (int mt = 0; mt < D / 16; ++mt) {
                     const int d0 = dim_of(mt, 0), d1 = dim_of(mt, 1);
@@ -612,7 +576,8 @@ __device__ __forceinline__ void decode_body(const CUtensorMap &kv_map, const Dec
                     pacc[(hh0 + 1) * D + d1] = acc[mt][3];
                 }
                 if (lane < 4) {
-                    float *pml = a.part_ml + rec * kHeadsPad * 2;
+                    float *pml = whole ? a.whole_ml + wrec * kHeadsPad * 2
+                                       : a.part_ml + rec * kHeadsPad * 2;
                     pml[hh0 * 2 + 0] = m0;
                     pml[hh0 * 2 + 1] = l0;
                     pml[(hh0 + 1) * 2 + 0] = m1;
@@ -646,7 +611,9 @@ __global__ void __launch_bounds__(W * 32, 1)
 }
 
 // Merge the pieces of segments that were split across warps; zero empty sequences.
-// One CTA per (sequence, KV head); one thread per (query head, 4 dims).  Launched
+// Cascade: also fold the shared prefix's partials into every segment (split,
+// whole or empty).  One CTA per (sequence, KV head); one thread per (query head,
+// 4 dims).  Launched
 // as a programmatic dependent of the split kernel: it may start early and waits
 // for that grid's completion before reading anything it wrote.
 template <int D>
@@ -670,13 +637,18 @@ __global__ void __launch_bounds__(kHeadsPad * D / 4) decode_merge_kernel(const D
     // Pieces g0..g1 of this segment (none if the sequence has no tokens here).
     const long long NW = a.plan ? a.plan[1] : a.total_warps;
     long long T = 1, S0 = 0, S1 = 0, g0 = 0, g1 = -1;
+    bool whole = false;  // one warp's record holds the whole segment
     if (nt > 0) {
         T = (long long)a.prefix[a.num_seqs] * Hkv;
         S0 = (long long)Hkv * pre + (long long)h * nt;
         S1 = S0 + nt;
         g0 = ((S0 + 1) * NW - 1) / T;
         g1 = (S1 * NW - 1) / T;
-        if (g0 == g1) return;  // written whole by one warp (prefix folded in there)
+        if (g0 == g1) {
+            if (P == 0) return;  // written by that warp
+            whole = true;
+            g1 = g0 - 1;         // no pieces
+        }
     }
     // Shared-prefix partials of this query head.
     const size_t pr0 = (size_t)s * a.num_heads + (size_t)h * G + hh;
@@ -688,6 +660,8 @@ __global__ void __launch_bounds__(kHeadsPad * D / 4) decode_merge_kernel(const D
     const long long b0 = g0 * tq + (g0 * tr) / NW, f0 = (g0 * tr) % NW;
     float M = -INFINITY;
     for (int sp = 0; sp < P; ++sp) M = fmaxf(M, pml[sp * prs + pr0].x);
+    const size_t wrec = (size_t)k * kHeadsPad + hh;  // segment k's record, this head
+    if (whole) M = fmaxf(M, a.whole_ml[wrec * 2]);
     long long b = b0, f = f0;
     for (long long gw = g0; gw <= g1; ++gw) {
         long long e = b + tq;
@@ -726,6 +700,16 @@ __global__ void __launch_bounds__(kHeadsPad * D / 4) decode_merge_kernel(const D
             den += w * ml.y;
         }
         b = e;
+    }
+    if (whole) {
+        const float2 ml = reinterpret_cast<const float2 *>(a.whole_ml)[wrec];
+        const float4 v = reinterpret_cast<const float4 *>(a.whole_acc + wrec * D)[d4];
+        const float w = exp2f(ml.x - M);
+        num.x += w * v.x;
+        num.y += w * v.y;
+        num.z += w * v.z;
+        num.w += w * v.w;
+        den += w * ml.y;
     }
     for (int sp = 0; sp < P; ++sp) {
         const size_t r = sp * prs + pr0;
@@ -828,6 +812,8 @@ DecodeArgs make_decode_args(void *out, const void *q, const KvGeom &g, int num_h
     a.pre_splits = 0;
     a.pre_ml = nullptr;
     a.pre_acc = nullptr;
+    a.whole_ml = nullptr;
+    a.whole_acc = nullptr;
     a.plan = nullptr;
     return a;
 }
@@ -836,8 +822,8 @@ cudaError_t launch_decode_impl(void *out, const void *q, const void *kv_cache, c
                                int num_heads, const int32_t *block_tables, int max_blocks_per_seq,
                                const int32_t *seq_lens, int num_seqs, int max_seq_len,
                                int shared_len, float scale, void *workspace, const float *pre_ml,
-                               const float *pre_acc, int pre_splits, bool kv8, float k_scale,
-                               float v_scale, cudaStream_t stream) {
+                               const float *pre_acc, int pre_splits, void *whole, bool kv8,
+                               float k_scale, float v_scale, cudaStream_t stream) {
     const int sms = device_sm_count();
     const int D = g.head_size;
     CUtensorMap map;
@@ -860,6 +846,13 @@ cudaError_t launch_decode_impl(void *out, const void *q, const void *kv_cache, c
     a.pre_splits = pre_splits;
     a.pre_ml = pre_ml;
     a.pre_acc = pre_acc;
+    if (whole) {
+        // (m, l) records, then the acc rows, as cascade_whole_bytes lays them out.
+        const size_t segs = (size_t)num_seqs * g.num_kv_heads;
+        a.whole_ml = static_cast<float *>(whole);
+        a.whole_acc = reinterpret_cast<float *>(static_cast<uint8_t *>(whole) +
+                                                align_up(segs * kHeadsPad * 2 * 4, 256));
+    }
     if (kv8) return launch_decode_d<128, true>(a, map, (int)ctas, stream);
     if (D == 128) return launch_decode_d<128, false>(a, map, (int)ctas, stream);
     return launch_decode_d<64, false>(a, map, (int)ctas, stream);
@@ -875,7 +868,7 @@ cudaError_t launch_decode(void *out, const void *q, const void *kv_cache, const 
                           void *workspace, cudaStream_t stream) {
     return launch_decode_impl(out, q, kv_cache, g, num_heads, block_tables, max_blocks_per_seq,
                               seq_lens, num_seqs, max_seq_len, 0, scale, workspace, nullptr,
-                              nullptr, 0, false, 1.f, 1.f, stream);
+                              nullptr, 0, nullptr, false, 1.f, 1.f, stream);
 }
 
 cudaError_t launch_decode_fp8(void *out, const void *q, const void *kv_cache, const KvGeom &g,
@@ -884,7 +877,7 @@ cudaError_t launch_decode_fp8(void *out, const void *q, const void *kv_cache, co
                               float k_scale, float v_scale, void *workspace, cudaStream_t stream) {
     return launch_decode_impl(out, q, kv_cache, g, num_heads, block_tables, max_blocks_per_seq,
                               seq_lens, num_seqs, max_seq_len, 0, scale, workspace, nullptr,
-                              nullptr, 0, true, k_scale, v_scale, stream);
+                              nullptr, 0, nullptr, true, k_scale, v_scale, stream);
 }
 
 cudaError_t launch_decode_suffix(void *out, const void *q, const void *kv_cache, const KvGeom &g,
@@ -892,16 +885,23 @@ cudaError_t launch_decode_suffix(void *out, const void *q, const void *kv_cache,
                                  int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs,
                                  int max_seq_len, int shared_len, float scale, void *workspace,
                                  const float *pre_ml, const float *pre_acc, int pre_splits,
-                                 bool kv8, float k_scale, float v_scale, cudaStream_t stream) {
+                                 void *whole, bool kv8, float k_scale, float v_scale,
+                                 cudaStream_t stream) {
     return launch_decode_impl(out, q, kv_cache, g, num_heads, block_tables, max_blocks_per_seq,
                               seq_lens, num_seqs, max_seq_len, shared_len, scale, workspace,
-                              pre_ml, pre_acc, pre_splits, kv8, kv8 ? k_scale : 1.f,
-                              kv8 ? v_scale : 1.f, stream);
+                              pre_ml, pre_acc, pre_splits, pre_splits > 0 ? whole : nullptr, kv8,
+                              kv8 ? k_scale : 1.f, kv8 ? v_scale : 1.f, stream);
 }
 
 size_t prefix_partial_bytes(int splits, int num_seqs, int num_heads, int head_size) {
     const size_t rows = (size_t)splits * num_seqs * num_heads;
     return align_up(rows * 2 * 4, 256) + align_up(rows * (size_t)head_size * 4, 256);
+}
+
+size_t cascade_whole_bytes(int num_seqs, int num_kv_heads, int head_size) {
+    const size_t segs = (size_t)num_seqs * num_kv_heads;
+    return align_up(segs * kHeadsPad * 2 * 4, 256) +
+           align_up(segs * kHeadsPad * (size_t)head_size * 4, 256);
 }
 
 }  // namespace pa

@@ -66,14 +66,18 @@ cudaError_t launch_prefix_partials(const void *q, const void *kv_cache, const Kv
                                    bool kv8, float k_scale, float v_scale, cudaStream_t stream);
 // Bytes of prefix partials for `splits` splits.
 size_t prefix_partial_bytes(int splits, int num_seqs, int num_heads, int head_size);
-// Decode over each sequence's tokens [shared_len, seq_len), folding in the prefix
-// partials (pre_splits of them at pre_ml / pre_acc) before normalising.
+// Bytes of the per-segment records of segments one warp finishes whole.
+size_t cascade_whole_bytes(int num_seqs, int num_kv_heads, int head_size);
+// Decode over each sequence's tokens [shared_len, seq_len); its merge kernel folds
+// in the prefix partials (pre_splits of them at pre_ml / pre_acc) before
+// normalising.  whole: cascade_whole_bytes of workspace for the whole segments.
 cudaError_t launch_decode_suffix(void *out, const void *q, const void *kv_cache, const KvGeom &g,
                                  int num_heads, const int32_t *block_tables,
                                  int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs,
                                  int max_seq_len, int shared_len, float scale, void *workspace,
                                  const float *pre_ml, const float *pre_acc, int pre_splits,
-                                 bool kv8, float k_scale, float v_scale, cudaStream_t stream);
+                                 void *whole, bool kv8, float k_scale, float v_scale,
+                                 cudaStream_t stream);
 
 // One launch for a flattened mixed batch (chunks first, then decode sequences):
 // decode and chunked prefill side by side on disjoint SMs, split on the device.
