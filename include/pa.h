@@ -203,7 +203,8 @@ pa_status pa_decode_noalloc(void *out, const void *q, const void *kv_cache, int 
 
 /*
  * Workspace pa_decode_cascade needs on the current device, in bytes: that of
- * pa_decode plus the shared prefix's partial softmax states.  Depends on the
+ * pa_decode plus the shared prefix's partial softmax states and one partial
+ * state per (sequence, KV head) for the sequences' own tokens.  Depends on the
  * device's SM count.  Returns 0 for invalid arguments.
  */
 size_t pa_decode_cascade_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads,

@@ -116,6 +116,32 @@ def test_cascade_prefix_workload_full_size():
     compare(out, oracle_rows(b, pool), "prefix-shared workload, cascade")
 
 
+@pytest.mark.parametrize("fp8", [False, True])
+def test_cascade_segments_finished_whole(fp8):
+    """Own suffixes of at most 16 tokens: one tile per (sequence, KV head), one tile
+    per warp of the small grid, so every segment is finished whole by one warp and
+    reaches the output only through its segment record and the merge kernel's fold
+    of the prefix partials; two sequences have no own tokens at all."""
+    pb, bs = 16, 16
+    suffix = [16, 1, 7, 16, 3, 12, 9]
+    b = make_batch(name=f"cw{int(fp8)}", seq_lens=[pb * bs + x for x in suffix],
+                   q_lens=[1] * len(suffix), num_heads=32, num_kv_heads=8, head_size=128,
+                   block_size=bs, scale=128 ** -0.5, seed=75 + fp8, shared_prefix_blocks=pb,
+                   device=DEV)
+    lens = b.seq_lens.clone()
+    lens[2] = pb * bs
+    lens[5] = pb * bs
+    if fp8:
+        out, want, _ = _fp8_case(b, pb * bs, seq_lens=lens)
+    else:
+        pool = oracle_pool(b)
+        gpu_write(b)
+        out = gpu_cascade(b, pb * bs, lens)
+        binding.pa_error_check()
+        want = oracle_rows(type(b)(**{**b.__dict__, "seq_lens": lens}), pool)
+    compare(out, want, f"cascade, whole segments{' (FP8)' if fp8 else ''}")
+
+
 def test_cascade_rejects_unaligned_shared_length():
     b = make_batch(name="cu", seq_lens=[40, 50], q_lens=[1, 1], num_heads=8, num_kv_heads=8,
                    head_size=64, block_size=8, scale=0.1, seed=74, shared_prefix_blocks=3,
