@@ -577,9 +577,15 @@ def run_ours(args, world, rank, local):
     alg = cascade_algorithmic_bytes(b, shared, 1 if fp8 else 2) if args.cascade else \
         decode_algorithmic_bytes(b, 1 if fp8 else 2)
     achieved = alg / (decode_ms / 1e3) / 1e9
+    # Kernels of one attention call (the cache write is one more per step).
+    attn_kernels = 2
     if args.cascade:
-        kernel = (f"pa_decode_cascade{'_fp8' if fp8 else ''} (prefix pass + suffix decode + "
-                  f"merge kernel)")
+        attn_kernels = binding.pa_decode_cascade_kernels(b.num_seqs, b.num_heads, b.num_kv_heads,
+                                                         b.head_size, b.block_size, max_len,
+                                                         shared, fp8)
+        kernel = (f"pa_decode_cascade{'_fp8' if fp8 else ''} ("
+                  + ("prefix pass beside the suffix decode in one launch, then the merge kernel"
+                     if attn_kernels == 2 else "prefix pass, suffix decode, merge kernel") + ")")
         traffic_file = f"cascade{'_fp8' if fp8 else ''}_{b.name}.traffic.txt"
     elif fp8:
         kernel = "pa_decode_fp8 (split-context kernel + merge kernel)"
@@ -612,7 +618,7 @@ def run_ours(args, world, rank, local):
                         "copy direction overlapping the neighbouring steps' kernels (two "
                         "buffer sets); host wall clock over all steps"},
         "clocks": clocks,
-        "gpu_launches": (4 if args.cascade else 3) * args.steps,
+        "gpu_launches": (1 + attn_kernels) * args.steps,
     }
     if world == 1 and not args.no_cpu_baseline and not fp8:
         gbs, sps, done, k, threads = cpu_oracle_rate(n)

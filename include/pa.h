@@ -211,6 +211,19 @@ size_t pa_decode_cascade_workspace_bytes(int num_seqs, int num_heads, int num_kv
                                          int head_size, int shared_len);
 
 /*
+ * Kernels one pa_decode_cascade call (pa_decode_cascade_fp8 when kv8 != 0) with
+ * these shapes launches on the current device: 3 when the shared prefix is
+ * attended by its own launch before the sequences' own tokens and the merge; 2
+ * when the prefix and the own tokens are attended side by side in one launch on
+ * disjoint SMs (chosen from the shapes for a bf16 pool), or when shared_len is 0
+ * (pa_decode); 0 when num_seqs is 0; -1 for invalid shapes.  For planning only
+ * (e.g. counting a CUDA graph's nodes): the results are the same either way, up
+ * to floating-point summation order.
+ */
+int pa_decode_cascade_kernels(int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                              int block_size, int max_seq_len, int shared_len, int kv8);
+
+/*
  * pa_decode_cascade - pa_decode for a batch whose sequences share a prefix.
  *
  * Prefix caching ("Inside vLLM: Anatomy of a High-Throughput LLM Inference

@@ -25,7 +25,8 @@ STATUS = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_E
 EXPORTS = ("pa_status_string", "pa_kv_block_bytes", "pa_kv_block_bytes_dtype", "pa_cache_write",
            "pa_cache_write_fp8", "pa_decode_fp8", "pa_prefill_chunk_fp8",
            "pa_decode_workspace_bytes", "pa_decode", "pa_decode_noalloc",
-           "pa_decode_cascade_workspace_bytes", "pa_decode_cascade", "pa_decode_cascade_fp8",
+           "pa_decode_cascade_workspace_bytes", "pa_decode_cascade_kernels", "pa_decode_cascade",
+           "pa_decode_cascade_fp8",
            "pa_prefill_chunk",
            "pa_attention_varlen_workspace_bytes", "pa_attention_varlen",
            "pa_attention_varlen_fp8", "pa_error_check")
@@ -76,6 +77,8 @@ def lib(path: Optional[str] = None):
     L.pa_decode_noalloc.argtypes = [P, P, P, i, i, i, i, i, P, i, P, i, i, ctypes.c_float, P]
     L.pa_decode_cascade_workspace_bytes.restype = sz
     L.pa_decode_cascade_workspace_bytes.argtypes = [i, i, i, i, i]
+    L.pa_decode_cascade_kernels.restype = i
+    L.pa_decode_cascade_kernels.argtypes = [i, i, i, i, i, i, i, i]
     L.pa_decode_cascade.restype = i
     L.pa_decode_cascade.argtypes = [P, P, P, i, i, i, i, i, P, i, P, i, i, i, ctypes.c_float, P,
                                     sz, P]
@@ -272,6 +275,14 @@ def pa_decode_cascade_workspace_bytes(num_seqs: int, num_heads: int, num_kv_head
                                       head_size: int, shared_len: int) -> int:
     return int(lib().pa_decode_cascade_workspace_bytes(num_seqs, num_heads, num_kv_heads,
                                                        head_size, shared_len))
+
+
+def pa_decode_cascade_kernels(num_seqs: int, num_heads: int, num_kv_heads: int, head_size: int,
+                              block_size: int, max_seq_len: int, shared_len: int,
+                              fp8: bool = False) -> int:
+    """Kernels one pa_decode_cascade (fp8: pa_decode_cascade_fp8) call launches."""
+    return int(lib().pa_decode_cascade_kernels(num_seqs, num_heads, num_kv_heads, head_size,
+                                               block_size, max_seq_len, shared_len, int(fp8)))
 
 
 def pa_decode_cascade(out: torch.Tensor, q: torch.Tensor, kv_cache: torch.Tensor,

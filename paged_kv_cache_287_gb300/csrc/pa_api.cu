@@ -278,6 +278,21 @@ size_t pa_decode_cascade_workspace_bytes(int num_seqs, int num_heads, int num_kv
            (splits > 0 ? pa::cascade_whole_bytes(num_seqs, num_kv_heads, head_size) : 0);
 }
 
+int pa_decode_cascade_kernels(int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                              int block_size, int max_seq_len, int shared_len, int kv8) {
+    if (num_seqs < 0 || max_seq_len < 0 || shared_len < 0 || shared_len > max_seq_len) return -1;
+    if (check_heads(num_heads, num_kv_heads) != PA_OK || num_kv_heads > 255) return -1;
+    if (head_size != 64 && head_size != 128) return -1;
+    if (block_size != 8 && block_size != 16 && block_size != 32) return -1;
+    if (num_seqs == 0) return 0;
+    if (shared_len == 0) return 2;  // pa_decode: split kernel and merge kernel
+    const pa::KvGeom g{1, block_size, num_kv_heads, head_size};
+    return pa::cascade_one_launch_ctas(num_seqs, num_heads, g, max_seq_len, shared_len, kv8 != 0,
+                                       pa::device_sm_count()) > 0
+               ? 2
+               : 3;
+}
+
 // pa_decode_cascade and pa_decode_cascade_fp8 (kv8: an FP8 pool, head size 128).
 static pa_status cascade_impl(void *out, const void *q, const void *kv_cache, int num_blocks,
                               int block_size, int num_heads, int num_kv_heads, int head_size,
@@ -317,11 +332,16 @@ static pa_status cascade_impl(void *out, const void *q, const void *kv_cache, in
     void *whole = nullptr;  // after the prefix partials
     if (splits > 0) {
         whole = static_cast<uint8_t *>(workspace) + dec + pre;
-        // Prefix partials after the decode workspace: (m, l) records, then O rows.
+        // Prefix partials: (m, l) records, then O rows (room for `splits` splits).
         uint8_t *base = static_cast<uint8_t *>(workspace) + dec;
         const size_t rows = (size_t)splits * num_seqs * num_heads;
         pre_ml = reinterpret_cast<float *>(base);
         pre_acc = reinterpret_cast<float *>(base + (rows * 2 * 4 + 255) / 256 * 256);
+        const cudaError_t one = pa::launch_cascade_one(
+            out, q, kv_cache, g, num_heads, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+            max_seq_len, shared_len, scale, workspace, pre_ml, pre_acc, whole, kv8, k_scale,
+            v_scale, s);
+        if (one != cudaErrorNotSupported) return from_cuda(one);
         cudaError_t e = pa::launch_prefix_partials(q, kv_cache, g, num_heads, block_tables,
                                                    max_blocks_per_seq, num_seqs, shared_len,
                                                    scale, splits, pre_ml, pre_acc, kv8, k_scale,

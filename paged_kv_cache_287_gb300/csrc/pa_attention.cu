@@ -112,9 +112,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     mixed_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs da,
                  const PrefillArgs pa, int dec_slots, uint3 pre_grid) {
     if ((int)blockIdx.x < dec_slots) {
-        if ((int)blockIdx.x < da.plan[0])
-            decode_body<D, DW, KV8 ? kMixStagesFp8 : kMixStages, KV8>(kv_map, da, blockIdx.x,
-                                                                      da.plan[1]);
+        // Without a device plan every decode slot streams (da.total_warps warps).
+        const int dec_ctas = da.plan ? da.plan[0] : dec_slots;
+        if ((int)blockIdx.x < dec_ctas)
+            decode_body<D, DW, KV8 ? kMixStagesFp8 : kMixStages, KV8>(
+                kv_map, da, blockIdx.x, da.plan ? da.plan[1] : da.total_warps);
         return;
     }
     const unsigned v = blockIdx.x - (unsigned)dec_slots;
@@ -123,16 +125,18 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     prefill_body<D, KV8>(kv_map, pa, bid, pre_grid);
 }
 
+// dec_slots: the grid's leading decode CTAs (with a device plan, the first
+// plan[0] of them stream and the rest exit).
 template <int D, bool KV8, int DW = kDecodeWarps>
 cudaError_t launch_mixed_d(const CUtensorMap &map, const DecodeArgs &da, const PrefillArgs &pa,
-                           dim3 pgrid, int sms, size_t smem, cudaStream_t stream) {
+                           dim3 pgrid, int dec_slots, size_t smem, cudaStream_t stream) {
     auto kern = mixed_kernel<D, KV8, DW>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const unsigned n_pre = pgrid.x * pgrid.y * pgrid.z;
-    kern<<<(unsigned)sms + n_pre, kDecodeWarps * 32, smem, stream>>>(
-        map, da, pa, sms, make_uint3(pgrid.x, pgrid.y, pgrid.z));
+    kern<<<(unsigned)dec_slots + n_pre, kDecodeWarps * 32, smem, stream>>>(
+        map, da, pa, dec_slots, make_uint3(pgrid.x, pgrid.y, pgrid.z));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     decode_merge_kernel<D><<<(unsigned)(da.num_seqs * da.num_kv_heads),
                              (unsigned)(da.group * D / 4), 0, stream>>>(da);
@@ -236,6 +240,105 @@ cudaError_t launch_mixed(void *out, const void *q, const int32_t *cu_q_lens, int
     if (D == 128)
         return launch_mixed_d<128, false>(map, da, pa, pgrid, sms, TcLay<128>::kSmem, stream);
     return launch_mixed_d<64, false>(map, da, pa, pgrid, sms, TcLay<64>::kSmem, stream);
+}
+
+// ----------------------------------------------------------------------------
+// Shared-prefix decode in one launch of the same kernel.  Once the prefix
+// partials are folded in by the merge kernel, the prefix pass and the own
+// tokens' decode are independent, so they run side by side: the prefix pass
+// with one key split on P SMs (its CTAs the grid's tail), the decode on the
+// other sms - P as the leading CTAs; then the merge.  Taken for a bf16 pool
+// when the prefix pass's CTAs fit in a quarter of the SMs and, by the rates
+// below, it ends before the decode would; otherwise the separate launches (the
+// prefix pass first, split over the whole GPU) are as fast or faster.  (An FP8
+// pool measured the same either way on the prefix-sharing workload: its decode
+// issues more instructions per byte and gains little from the SMs it keeps.)
+namespace {
+// Rates for the choice (measured on GB300, prefix-sharing workload): a prefix
+// CTA takes about 1.8 us per 128-key tile plus 4 us to start and finish; the
+// own tokens' decode streams about 36 GB/s per SM.
+constexpr float kCascadeTileUs = 1.8f, kCascadeStartUs = 4.0f, kCascadeDecSmGBs = 36.0f;
+}  // namespace
+
+int cascade_one_launch_ctas(int num_seqs, int num_heads, const KvGeom &g, int max_seq_len,
+                            int shared_len, bool kv8, int sms) {
+    if (kv8 || shared_len <= 0 || num_seqs <= 0) return 0;
+    const int G = num_heads / g.num_kv_heads;
+    const int per_cta = kTcTiles * (kTcRows / G);
+    const long long n_pre = (long long)((num_seqs + per_cta - 1) / per_cta) * g.num_kv_heads;
+    if (mixed_decode_warps(num_seqs, num_heads, g, false) == 0 || n_pre > sms / 4) return 0;
+    const int dec_ctas = sms - (int)n_pre;
+    const int tiles = (shared_len + kTcKeys - 1) / kTcKeys;
+    // Own tokens: about half the longest suffix per sequence on average.
+    const double own_bytes = (double)num_seqs * g.num_kv_heads *
+                             (0.5 * std::max(max_seq_len - shared_len, 0)) * 2.0 *
+                             g.head_size * 2;
+    const double dec_us = own_bytes / (dec_ctas * (double)kCascadeDecSmGBs * 1e3);
+    return tiles * kCascadeTileUs + kCascadeStartUs <= dec_us ? dec_ctas : 0;
+}
+
+cudaError_t launch_cascade_one(void *out, const void *q, const void *kv_cache, const KvGeom &g,
+                               int num_heads, const int32_t *block_tables,
+                               int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs,
+                               int max_seq_len, int shared_len, float scale, void *workspace,
+                               float *pre_ml, float *pre_acc, void *whole, bool kv8,
+                               float k_scale, float v_scale, cudaStream_t stream) {
+    const int sms = device_sm_count();
+    const int D = g.head_size, G = num_heads / g.num_kv_heads;
+    const int dec_ctas =
+        cascade_one_launch_ctas(num_seqs, num_heads, g, max_seq_len, shared_len, kv8, sms);
+    if (dec_ctas == 0) return cudaErrorNotSupported;
+    const int dw = mixed_decode_warps(num_seqs, num_heads, g, false);
+    const int q_tile = kTcRows / G, per_cta = kTcTiles * q_tile;
+    const int tiles = (shared_len + kTcKeys - 1) / kTcKeys;
+
+    (void)k_scale;
+    (void)v_scale;
+    CUtensorMap map;
+    const int box_rows = g.block_size >= kTile ? kTile : g.block_size;
+    if (!encode_kv_map(&map, kv_cache, g, box_rows)) return cudaErrorInvalidValue;
+    DecodeArgs da = make_decode_args(out, q, g, num_heads, block_tables, max_blocks_per_seq,
+                                     seq_lens, num_seqs, scale, workspace, false, dec_ctas);
+    da.total_warps = dec_ctas * dw;
+    da.shared_len = shared_len;
+    da.pre_splits = 1;
+    da.pre_ml = pre_ml;
+    da.pre_acc = pre_acc;
+    const size_t segs = (size_t)num_seqs * g.num_kv_heads;
+    da.whole_ml = static_cast<float *>(whole);
+    da.whole_acc = reinterpret_cast<float *>(static_cast<uint8_t *>(whole) +
+                                             align_up(segs * kHeadsPad * 2 * 4, 256));
+    // The prefix pass: every sequence's query rows against keys [0, shared_len)
+    // of sequence 0's blocks, one split.
+    PrefillArgs pa;
+    pa.out = nullptr;
+    pa.q = static_cast<const __nv_bfloat16 *>(q);
+    pa.cu_q_lens = nullptr;
+    pa.block_tables = block_tables;
+    pa.seq_lens = nullptr;
+    pa.num_heads = num_heads;
+    pa.num_kv_heads = g.num_kv_heads;
+    pa.group = G;
+    pa.block_size = g.block_size;
+    pa.max_blocks = max_blocks_per_seq;
+    pa.num_blocks = g.num_blocks;
+    pa.negate_q = scale < 0.f ? 1 : 0;
+    pa.scale_log2 = std::max(std::fabs(scale) * 1.4426950408889634f, 1e-30f);
+    pa.q_tile = q_tile;
+    pa.part_ml = pre_ml;
+    pa.part_acc = pre_acc;
+    pa.shared_len = shared_len;
+    pa.split_tiles = tiles;
+    pa.prefix_rows = num_seqs;
+    pa.k_scale = da.k_scale;
+    pa.v_scale = da.v_scale;
+    const dim3 pgrid((unsigned)((num_seqs + per_cta - 1) / per_cta), (unsigned)g.num_kv_heads, 1);
+    if (D == 128 && dw < kDecodeWarps)
+        return launch_mixed_d<128, false, kDecodeWarps - 1>(map, da, pa, pgrid, dec_ctas,
+                                                            TcLay<128>::kSmem, stream);
+    if (D == 128)
+        return launch_mixed_d<128, false>(map, da, pa, pgrid, dec_ctas, TcLay<128>::kSmem, stream);
+    return launch_mixed_d<64, false>(map, da, pa, pgrid, dec_ctas, TcLay<64>::kSmem, stream);
 }
 
 }  // namespace pa

@@ -66,6 +66,20 @@ cudaError_t launch_prefix_partials(const void *q, const void *kv_cache, const Kv
                                    bool kv8, float k_scale, float v_scale, cudaStream_t stream);
 // Bytes of prefix partials for `splits` splits.
 size_t prefix_partial_bytes(int splits, int num_seqs, int num_heads, int head_size);
+// The shared-prefix decode as one launch (prefix pass and own tokens side by side
+// on disjoint SMs, one key split) plus the merge; cudaErrorNotSupported (nothing
+// launched) when the separate launches suit the shape better.  pre_ml / pre_acc:
+// room for one split's partials; whole: cascade_whole_bytes.
+cudaError_t launch_cascade_one(void *out, const void *q, const void *kv_cache, const KvGeom &g,
+                               int num_heads, const int32_t *block_tables,
+                               int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs,
+                               int max_seq_len, int shared_len, float scale, void *workspace,
+                               float *pre_ml, float *pre_acc, void *whole, bool kv8,
+                               float k_scale, float v_scale, cudaStream_t stream);
+// Decode CTAs of that one launch for these shapes on `sms` SMs, or 0 when the
+// separate launches are used.
+int cascade_one_launch_ctas(int num_seqs, int num_heads, const KvGeom &g, int max_seq_len,
+                            int shared_len, bool kv8, int sms);
 // Bytes of the per-segment records of segments one warp finishes whole.
 size_t cascade_whole_bytes(int num_seqs, int num_kv_heads, int head_size);
 // Decode over each sequence's tokens [shared_len, seq_len); its merge kernel folds

@@ -128,6 +128,19 @@ def test_cascade_host_checks(lib):
     assert lib.pa_decode_cascade_fp8(*bad) == 0
 
 
+def test_cascade_kernel_count_query(lib):
+    q = lib.pa_decode_cascade_kernels
+    assert q(0, 32, 8, 128, 16, 64, 32, 0) == 0            # no sequences: nothing launched
+    assert q(5, 32, 8, 128, 16, 64, 0, 0) == 2             # no shared tokens: pa_decode
+    assert q(5, 32, 8, 128, 16, 64, 32, 0) in (2, 3)       # depends on the device's SMs
+    assert q(5, 32, 8, 128, 16, 64, 32, 1) == 3            # FP8 pool: separate launches
+    assert q(5, 32, 8, 128, 16, 64, 65, 0) == -1           # shared_len beyond max_seq_len
+    assert q(5, 30, 8, 128, 16, 64, 32, 0) == -1           # heads not a multiple
+    assert q(5, 32, 8, 96, 16, 64, 32, 0) == -1            # head size
+    assert q(5, 32, 8, 128, 12, 64, 32, 0) == -1           # block size
+    assert q(-1, 32, 8, 128, 16, 64, 32, 0) == -1
+
+
 def test_fp8_host_checks(lib):
     wr = [FAKE, 10, 16, 8, 128, FAKE, FAKE, 8 * 128, FAKE, 4, 0.5, 0.25, None]
     bad = list(wr)

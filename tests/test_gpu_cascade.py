@@ -142,6 +142,29 @@ def test_cascade_segments_finished_whole(fp8):
     compare(out, want, f"cascade, whole segments{' (FP8)' if fp8 else ''}")
 
 
+@pytest.mark.parametrize("fp8", [False, True])
+def test_cascade_long_own_suffixes(fp8):
+    """A short shared prefix and long own suffixes: the shape that runs the prefix
+    pass beside the own tokens' decode in one launch (the full prefix-sharing
+    workload does too)."""
+    pb, bs = 32, 16
+    g = torch.Generator().manual_seed(90 + fp8)
+    suffix = torch.randint(1, 4097, (48,), generator=g).tolist()
+    b = make_batch(name=f"cl{int(fp8)}", seq_lens=[pb * bs + x for x in suffix],
+                   q_lens=[1] * len(suffix), num_heads=32, num_kv_heads=8, head_size=128,
+                   block_size=bs, scale=128 ** -0.5, seed=91 + fp8, shared_prefix_blocks=pb,
+                   device=DEV)
+    if fp8:
+        out, want, _ = _fp8_case(b, pb * bs)
+    else:
+        pool = oracle_pool(b)
+        gpu_write(b)
+        out = gpu_cascade(b, pb * bs)
+        binding.pa_error_check()
+        want = oracle_rows(b, pool)
+    compare(out, want, f"cascade, long own suffixes{' (FP8)' if fp8 else ''}")
+
+
 def test_cascade_rejects_unaligned_shared_length():
     b = make_batch(name="cu", seq_lens=[40, 50], q_lens=[1, 1], num_heads=8, num_kv_heads=8,
                    head_size=64, block_size=8, scale=0.1, seed=74, shared_prefix_blocks=3,
