@@ -126,10 +126,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
 }
 
 // dec_slots: the grid's leading decode CTAs (with a device plan, the first
-// plan[0] of them stream and the rest exit).
+// plan[0] of them stream and the rest exit).  merge_early: launch the merge
+// kernel as a programmatic dependent (its CTAs may start once every CTA of this
+// grid has started and wait for its end), for grids that fit the GPU at once.
 template <int D, bool KV8, int DW = kDecodeWarps>
 cudaError_t launch_mixed_d(const CUtensorMap &map, const DecodeArgs &da, const PrefillArgs &pa,
-                           dim3 pgrid, int dec_slots, size_t smem, cudaStream_t stream) {
+                           dim3 pgrid, int dec_slots, size_t smem, cudaStream_t stream,
+                           bool merge_early = false) {
     auto kern = mixed_kernel<D, KV8, DW>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -138,9 +141,16 @@ cudaError_t launch_mixed_d(const CUtensorMap &map, const DecodeArgs &da, const P
     kern<<<(unsigned)dec_slots + n_pre, kDecodeWarps * 32, smem, stream>>>(
         map, da, pa, dec_slots, make_uint3(pgrid.x, pgrid.y, pgrid.z));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    decode_merge_kernel<D><<<(unsigned)(da.num_seqs * da.num_kv_heads),
-                             (unsigned)(da.group * D / 4), 0, stream>>>(da);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(da.num_seqs * da.num_kv_heads));
+    cfg.blockDim = dim3((unsigned)(da.group * D / 4));
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = merge_early ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, decode_merge_kernel<D>, da);
 }
 
 }  // namespace
@@ -333,12 +343,15 @@ cudaError_t launch_cascade_one(void *out, const void *q, const void *kv_cache, c
     pa.k_scale = da.k_scale;
     pa.v_scale = da.v_scale;
     const dim3 pgrid((unsigned)((num_seqs + per_cta - 1) / per_cta), (unsigned)g.num_kv_heads, 1);
+    // The grid (one CTA per SM) is resident at once, so the merge may launch early.
     if (D == 128 && dw < kDecodeWarps)
         return launch_mixed_d<128, false, kDecodeWarps - 1>(map, da, pa, pgrid, dec_ctas,
-                                                            TcLay<128>::kSmem, stream);
+                                                            TcLay<128>::kSmem, stream, true);
     if (D == 128)
-        return launch_mixed_d<128, false>(map, da, pa, pgrid, dec_ctas, TcLay<128>::kSmem, stream);
-    return launch_mixed_d<64, false>(map, da, pa, pgrid, dec_ctas, TcLay<64>::kSmem, stream);
+        return launch_mixed_d<128, false>(map, da, pa, pgrid, dec_ctas, TcLay<128>::kSmem, stream,
+                                          true);
+    return launch_mixed_d<64, false>(map, da, pa, pgrid, dec_ctas, TcLay<64>::kSmem, stream,
+                                     true);
 }
 
 }  // namespace pa
