@@ -215,7 +215,7 @@ size_t pa_decode_cascade_workspace_bytes(int num_seqs, int num_heads, int num_kv
  * these shapes launches on the current device: 3 when the shared prefix is
  * attended by its own launch before the sequences' own tokens and the merge; 2
  * when the prefix and the own tokens are attended side by side in one launch on
- * disjoint SMs (chosen from the shapes for a bf16 pool), or when shared_len is 0
+ * disjoint SMs (chosen from the shapes and the pool's type), or when shared_len is 0
  * (pa_decode); 0 when num_seqs is 0; -1 for invalid shapes.  For planning only
  * (e.g. counting a CUDA graph's nodes): the results are the same either way, up
  * to floating-point summation order.

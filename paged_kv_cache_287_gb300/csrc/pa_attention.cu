@@ -257,34 +257,38 @@ cudaError_t launch_mixed(void *out, const void *q, const int32_t *cu_q_lens, int
 // partials are folded in by the merge kernel, the prefix pass and the own
 // tokens' decode are independent, so they run side by side: the prefix pass
 // with one key split on P SMs (its CTAs the grid's tail), the decode on the
-// other sms - P as the leading CTAs; then the merge.  Taken for a bf16 pool
-// when the prefix pass's CTAs fit in a quarter of the SMs and, by the rates
-// below, it ends before the decode would; otherwise the separate launches (the
-// prefix pass first, split over the whole GPU) are as fast or faster.  (An FP8
-// pool measured the same either way on the prefix-sharing workload: its decode
-// issues more instructions per byte and gains little from the SMs it keeps.)
+// other sms - P as the leading CTAs; then the merge.  Taken when the prefix
+// pass's CTAs fit in a quarter of the SMs and, by the rates below, it ends
+// before the decode would; otherwise the separate launches (the prefix pass
+// first, split over the whole GPU) are faster.
 namespace {
 // Rates for the choice (measured on GB300, prefix-sharing workload): a prefix
 // CTA takes about 1.8 us per 128-key tile plus 4 us to start and finish; the
 // own tokens' decode streams about 36 GB/s per SM.
 constexpr float kCascadeTileUs = 1.8f, kCascadeStartUs = 4.0f, kCascadeDecSmGBs = 36.0f;
+// FP8 pool: the prefix pass converts each tile (about 1.9 us), the decode streams
+// about 29 GB/s per SM.
+constexpr float kCascadeTileUsFp8 = 1.9f, kCascadeDecSmGBsFp8 = 29.0f;
 }  // namespace
 
 int cascade_one_launch_ctas(int num_seqs, int num_heads, const KvGeom &g, int max_seq_len,
                             int shared_len, bool kv8, int sms) {
-    if (kv8 || shared_len <= 0 || num_seqs <= 0) return 0;
+    if (shared_len <= 0 || num_seqs <= 0) return 0;
     const int G = num_heads / g.num_kv_heads;
     const int per_cta = kTcTiles * (kTcRows / G);
     const long long n_pre = (long long)((num_seqs + per_cta - 1) / per_cta) * g.num_kv_heads;
-    if (mixed_decode_warps(num_seqs, num_heads, g, false) == 0 || n_pre > sms / 4) return 0;
+    if (mixed_decode_warps(num_seqs, num_heads, g, kv8) == 0 || n_pre > sms / 4) return 0;
     const int dec_ctas = sms - (int)n_pre;
     const int tiles = (shared_len + kTcKeys - 1) / kTcKeys;
     // Own tokens: about half the longest suffix per sequence on average.
     const double own_bytes = (double)num_seqs * g.num_kv_heads *
                              (0.5 * std::max(max_seq_len - shared_len, 0)) * 2.0 *
-                             g.head_size * 2;
-    const double dec_us = own_bytes / (dec_ctas * (double)kCascadeDecSmGBs * 1e3);
-    return tiles * kCascadeTileUs + kCascadeStartUs <= dec_us ? dec_ctas : 0;
+                             g.head_size * (kv8 ? 1 : 2);
+    const double dec_us =
+        own_bytes / (dec_ctas * (double)(kv8 ? kCascadeDecSmGBsFp8 : kCascadeDecSmGBs) * 1e3);
+    return tiles * (kv8 ? kCascadeTileUsFp8 : kCascadeTileUs) + kCascadeStartUs <= dec_us
+               ? dec_ctas
+               : 0;
 }
 
 cudaError_t launch_cascade_one(void *out, const void *q, const void *kv_cache, const KvGeom &g,
@@ -298,18 +302,20 @@ cudaError_t launch_cascade_one(void *out, const void *q, const void *kv_cache, c
     const int dec_ctas =
         cascade_one_launch_ctas(num_seqs, num_heads, g, max_seq_len, shared_len, kv8, sms);
     if (dec_ctas == 0) return cudaErrorNotSupported;
-    const int dw = mixed_decode_warps(num_seqs, num_heads, g, false);
+    const int dw = mixed_decode_warps(num_seqs, num_heads, g, kv8);
     const int q_tile = kTcRows / G, per_cta = kTcTiles * q_tile;
     const int tiles = (shared_len + kTcKeys - 1) / kTcKeys;
 
-    (void)k_scale;
-    (void)v_scale;
     CUtensorMap map;
     const int box_rows = g.block_size >= kTile ? kTile : g.block_size;
-    if (!encode_kv_map(&map, kv_cache, g, box_rows)) return cudaErrorInvalidValue;
+    if (!(kv8 ? encode_kv_map_fp8(&map, kv_cache, g, box_rows)
+              : encode_kv_map(&map, kv_cache, g, box_rows)))
+        return cudaErrorInvalidValue;
     DecodeArgs da = make_decode_args(out, q, g, num_heads, block_tables, max_blocks_per_seq,
-                                     seq_lens, num_seqs, scale, workspace, false, dec_ctas);
+                                     seq_lens, num_seqs, scale, workspace, kv8, dec_ctas);
     da.total_warps = dec_ctas * dw;
+    da.k_scale = kv8 ? k_scale : 1.f;
+    da.v_scale = kv8 ? v_scale : 1.f;
     da.shared_len = shared_len;
     da.pre_splits = 1;
     da.pre_ml = pre_ml;
@@ -344,6 +350,9 @@ cudaError_t launch_cascade_one(void *out, const void *q, const void *kv_cache, c
     pa.v_scale = da.v_scale;
     const dim3 pgrid((unsigned)((num_seqs + per_cta - 1) / per_cta), (unsigned)g.num_kv_heads, 1);
     // The grid (one CTA per SM) is resident at once, so the merge may launch early.
+    if (kv8)
+        return launch_mixed_d<128, true>(map, da, pa, pgrid, dec_ctas, TcLay<128>::kSmem, stream,
+                                         true);
     if (D == 128 && dw < kDecodeWarps)
         return launch_mixed_d<128, false, kDecodeWarps - 1>(map, da, pa, pgrid, dec_ctas,
                                                             TcLay<128>::kSmem, stream, true);
