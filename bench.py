@@ -182,6 +182,23 @@ def rejected_clocks(c) -> bool:
     return False
 
 
+def median_launch_ms(fn, stream, runs: int = 50, flush=None) -> float:
+    """Median device time of `runs` calls of fn(), each bracketed by its own pair
+    of CUDA events on `stream` (the stream fn launches on); flush(), untimed, runs
+    before each call when given (an L2 flush between runs)."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(runs)]
+    torch.cuda.synchronize()
+    for e0, e1 in evs:
+        if flush is not None:
+            flush()
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -372,6 +389,194 @@ def workload_config(n: int, first: int = 0):
             "parallelism": "replicas (one independent batch per GPU)"}
 
 
+def by_workload(args, dev, stream) -> dict:
+    """The other workloads of the set, measured in the same run as the headline.
+
+    Each figure is the median of at least 50 individually event-timed calls
+    (after warm-up) with the SM clocks sampled over those calls; pools larger
+    than L2 need no flush, and the prefix-sharing workload (whose shared prefix
+    and part of the own tokens fit in L2) is timed both cold (L2 flushed by
+    writing 512 MB before every call, untimed) and warm (back to back).
+    Workload 1 is launch-bound, so its figure is per step, eager and replayed
+    from a CUDA graph of 20 steps.  Key "_launches": this library's kernels
+    launched in these timed calls."""
+    from paged_kv_cache_287_gb300 import binding
+    from paged_kv_cache_287_gb300.workloads import (CONFIG_NAMES, FP8_K_SCALE, FP8_V_SCALE,
+                                                    fp8_pool_of, make_config)
+    with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+        pk = json.load(f)
+    hbm, tfl = float(pk["hbm_gbs"]), float(pk["bf16_tflops"])
+    runs = max(50, args.median_runs)
+    flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    launches = 0
+    sc = (FP8_K_SCALE, FP8_V_SCALE)
+
+    def timed(fn, kernels, flushed=False, warm=5):
+        nonlocal launches
+        for _ in range(warm):
+            fn()
+        with ClockSampler(dev) as clk:
+            ms = median_launch_ms(fn, stream, runs, (lambda: flush_buf.zero_()) if flushed else None)
+        binding.pa_error_check(stream)
+        launches += kernels * runs
+        return ms, clk.summary()
+
+    def hbm_roof(alg, ms):
+        a = alg / (ms / 1e3) / 1e9
+        return {"bound": "hbm", "achieved": a, "peak": hbm, "unit": "GB/s", "frac": a / hbm,
+                "algorithmic_bytes_per_launch": alg, "launch_ms": ms,
+                "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)"}
+
+    def ws_for(b, n=None):
+        return torch.empty(binding.pa_decode_workspace_bytes(
+            b.num_seqs if n is None else n, b.num_heads, b.num_kv_heads, b.head_size),
+            dtype=torch.uint8, device=dev)
+
+    res = {}
+    # 1: launch-bound tiny decode step (cache write + decode), eager and graphed.
+    b = make_config(1, device=dev)
+    out, ws = torch.empty_like(b.q), ws_for(b)
+
+    def step1(st=stream):
+        binding.pa_cache_write(b.kv_cache, b.k_new, b.v_new, b.slot_mapping, st)
+        binding.pa_decode(out, b.q, b.kv_cache, b.block_tables, b.seq_lens, b.max_seq_len,
+                          b.scale, ws, st)
+
+    eager, clk = timed(step1, 3)
+    graph, cap = torch.cuda.CUDAGraph(), torch.cuda.Stream(dev)
+    torch.cuda.synchronize(dev)
+    with torch.cuda.graph(graph, stream=cap):
+        for _ in range(20):
+            step1(cap)
+    torch.cuda.synchronize(dev)
+    replay, clk_g = timed(graph.replay, 60)
+    res[1] = {"workload": CONFIG_NAMES[1], "value": b.num_seqs / (eager / 1e3),
+              "unit": "seqs/s", "ms_per_step": eager, "step": "pa_cache_write + pa_decode, eager",
+              "graph": {"value": b.num_seqs / (replay / 20 / 1e3), "unit": "seqs/s",
+                        "ms_per_step": replay / 20, "steps_per_replay": 20, "clocks": clk_g},
+              "roofline": {"bound": "launch", "frac": None,
+                           "note": "264 KB of KV: launch latency, not HBM, bounds the step"},
+              "clocks": clk}
+    del b, out, ws, graph
+
+    # 2 (FP8 pool) and 3: decode of the Llama-3-8B batch and of the long skewed one.
+    for n in (2, 3):
+        b = make_config(n, device=dev)
+        out, ws = torch.empty_like(b.q), ws_for(b)
+        entry = {"workload": CONFIG_NAMES[n]}
+        if n == 3:
+            binding.pa_cache_write(b.kv_cache, b.k_new, b.v_new, b.slot_mapping, stream)
+            ms, clk = timed(lambda: binding.pa_decode(out, b.q, b.kv_cache, b.block_tables,
+                                                      b.seq_lens, b.max_seq_len, b.scale, ws,
+                                                      stream), 2)
+            entry.update({"value": kv_read_bytes(b.seq_lens.tolist(), b.num_kv_heads,
+                                                 b.head_size) / (ms / 1e3) / 1e9,
+                          "unit": "GB/s", "ms_per_step": ms,
+                          "seqs_per_s": b.num_seqs / (ms / 1e3), "kernel": "pa_decode",
+                          "roofline": hbm_roof(decode_algorithmic_bytes(b), ms), "clocks": clk})
+        pool8 = fp8_pool_of(b)
+        b.kv_cache = torch.empty(0, device=dev)
+        torch.cuda.empty_cache()
+        binding.pa_cache_write_fp8(pool8, b.k_new, b.v_new, b.slot_mapping, *sc, stream)
+        ms, clk = timed(lambda: binding.pa_decode_fp8(out, b.q, pool8, b.block_tables,
+                                                      b.seq_lens, b.max_seq_len, b.scale, *sc,
+                                                      ws, stream), 2)
+        entry["fp8"] = {"value": kv_read_bytes(b.seq_lens.tolist(), b.num_kv_heads,
+                                               b.head_size) / 2 / (ms / 1e3) / 1e9,
+                        "unit": "GB/s", "ms_per_step": ms, "seqs_per_s": b.num_seqs / (ms / 1e3),
+                        "kernel": "pa_decode_fp8",
+                        "roofline": hbm_roof(decode_algorithmic_bytes(b, 1), ms), "clocks": clk}
+        res[n] = entry
+        del b, out, ws, pool8
+        torch.cuda.empty_cache()
+
+    # 4: the mixed step through the one call, and its prefill alone.
+    b = make_config(4, device=dev)
+    n_pre = int((b.q_lens > 1).sum())
+    r_pre = int(b.cu_q_lens[n_pre])
+    cu_pre = b.cu_q_lens[:n_pre + 1].contiguous()
+    max_q, max_dec = int(b.q_lens[:n_pre].max()), int(b.seq_lens[n_pre:].max())
+    out_all = torch.empty_like(b.q)
+    out_pre = torch.empty_like(b.q[:r_pre])
+    ws = torch.empty(binding.pa_attention_varlen_workspace_bytes(
+        b.num_seqs, n_pre, b.num_heads, b.num_kv_heads, b.head_size), dtype=torch.uint8,
+        device=dev)
+    flops = prefill_flops(b, 0, n_pre)
+    entry = {"workload": CONFIG_NAMES[4]}
+    for kind in ("bf16", "fp8"):
+        pool = fp8_pool_of(b) if kind == "fp8" else b.kv_cache
+        kw = {"kv_scales": sc} if kind == "fp8" else {}
+        step_ms, clk = timed(lambda: binding.pa_attention_varlen(
+            out_all, b.q, b.k_new, b.v_new, b.slot_mapping, cu_pre, n_pre, r_pre, max_q, pool,
+            b.block_tables, b.seq_lens, max_dec, b.scale, ws, stream, **kw), 4)
+        if kind == "fp8":
+            pre = lambda: binding.pa_prefill_chunk_fp8(out_pre, b.q[:r_pre], cu_pre, max_q, pool,
+                                                       b.block_tables[:n_pre],
+                                                       b.seq_lens[:n_pre], b.scale, *sc, stream)
+        else:
+            pre = lambda: binding.pa_prefill_chunk(out_pre, b.q[:r_pre], cu_pre, max_q, pool,
+                                                   b.block_tables[:n_pre], b.seq_lens[:n_pre],
+                                                   b.scale, stream)
+        pre_ms, clk_p = timed(pre, 1)
+        tf = flops / (pre_ms / 1e3) / 1e12
+        e = {"value": step_ms, "unit": "ms", "higher_is_better": False, "ms_per_step": step_ms,
+             "step": "pa_attention_varlen" + ("_fp8" if kind == "fp8" else "") +
+                     ": cache write, then chunked prefill and decode side by side in one launch",
+             "prefill": {"tflops": tf, "launch_ms": pre_ms, "flops_per_launch": flops,
+                         "clocks": clk_p},
+             "roofline": {"bound": "tensor", "achieved": tf, "peak": tfl, "unit": "TFLOP/s",
+                          "frac": tf / tfl, "kernel": "pa_prefill_chunk" +
+                          ("_fp8" if kind == "fp8" else ""),
+                          "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops)"},
+             "clocks": clk}
+        if kind == "fp8":
+            entry["fp8"] = e
+        else:
+            entry.update(e)
+        del pool
+    res[4] = entry
+    del b, out_all, out_pre, ws
+    torch.cuda.empty_cache()
+
+    # 5: prefix-shared decode, plain and cascade (bf16 and FP8 pools), cold and warm.
+    b = make_config(5, device=dev)
+    shared = b.shared_prefix_blocks * b.block_size
+    out = torch.empty_like(b.q)
+    ws = torch.empty(binding.pa_decode_cascade_workspace_bytes(
+        b.num_seqs, b.num_heads, b.num_kv_heads, b.head_size, shared), dtype=torch.uint8,
+        device=dev)
+    binding.pa_cache_write(b.kv_cache, b.k_new, b.v_new, b.slot_mapping, stream)
+    plain_ms, clk = timed(lambda: binding.pa_decode(out, b.q, b.kv_cache, b.block_tables,
+                                                    b.seq_lens, b.max_seq_len, b.scale, ws,
+                                                    stream), 2, flushed=True)
+    logical = kv_read_bytes(b.seq_lens.tolist(), b.num_kv_heads, b.head_size)
+    entry = {"workload": CONFIG_NAMES[5],
+             "plain_decode": {"value": logical / (plain_ms / 1e3) / 1e9, "unit": "GB/s (logical)",
+                              "ms_per_step": plain_ms, "seqs_per_s": b.num_seqs / (plain_ms / 1e3),
+                              "timing": "cold (L2 flushed before each call)", "clocks": clk}}
+    pool8 = fp8_pool_of(b)
+    binding.pa_cache_write_fp8(pool8, b.k_new, b.v_new, b.slot_mapping, *sc, stream)
+    for kind, pool in (("bf16", b.kv_cache), ("fp8", pool8)):
+        kw = {"kv_scales": sc} if kind == "fp8" else {}
+        call = lambda: binding.pa_decode_cascade(out, b.q, pool, b.block_tables, b.seq_lens,
+                                                 b.max_seq_len, shared, b.scale, ws, stream, **kw)
+        alg = cascade_algorithmic_bytes(b, shared, 1 if kind == "fp8" else 2)
+        e = {}
+        for timing in ("cold", "warm"):
+            ms, clk = timed(call, 2, flushed=timing == "cold")
+            e[timing] = {"value": alg / (ms / 1e3) / 1e9, "unit": "GB/s (unique bytes)",
+                         "ms_per_step": ms, "seqs_per_s": b.num_seqs / (ms / 1e3),
+                         "roofline": hbm_roof(alg, ms), "clocks": clk}
+        c = dict(e["cold"], kernel="pa_decode_cascade" + ("_fp8" if kind == "fp8" else ""),
+                 timing="cold (L2 flushed by writing 512 MB before each call)", warm=e["warm"])
+        entry["cascade" if kind == "bf16" else "cascade_fp8"] = c
+    entry.update({k: entry["cascade"][k] for k in ("value", "unit", "ms_per_step", "roofline",
+                                                   "clocks")})
+    res[5] = entry
+    res["_launches"] = launches
+    return res
+
+
 def run_ours(args, world, rank, local):
     from paged_kv_cache_287_gb300 import binding
     from paged_kv_cache_287_gb300.workloads import make_config
@@ -499,6 +704,11 @@ def run_ours(args, world, rank, local):
         clocks["remeasured"] = True
     binding.pa_error_check(stream)
     total_ms = max_over_ranks(total_ms, world, dev)
+    # The attention call alone: the median of individually event-timed launches
+    # (the roofline's duration), after the timed steps.
+    runs = max(50, args.median_runs)
+    decode_med_ms = decode_ms if graph is not None else median_launch_ms(
+        lambda: attend(b.q, b.block_tables, b.seq_lens, stream), stream, runs)
 
     # End to end: every step's inputs from pinned host memory, its output back to
     # pinned host memory.  Two buffer sets and one stream per copy direction:
@@ -561,8 +771,9 @@ def run_ours(args, world, rank, local):
         e2e_step(i)
     barrier(world)
     torch.cuda.synchronize(dev)
+    n_e2e = max(args.steps, args.e2e_steps)
     t0 = time.perf_counter()
-    for i in range(args.steps):
+    for i in range(n_e2e):
         e2e_step(i)
     torch.cuda.synchronize(dev)
     e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
@@ -576,16 +787,16 @@ def run_ours(args, world, rank, local):
     peak, peak_src = measured_peaks()
     alg = cascade_algorithmic_bytes(b, shared, 1 if fp8 else 2) if args.cascade else \
         decode_algorithmic_bytes(b, 1 if fp8 else 2)
-    achieved = alg / (decode_ms / 1e3) / 1e9
+    achieved = alg / (decode_med_ms / 1e3) / 1e9
     # Kernels of one attention call (the cache write is one more per step).
     attn_kernels = 2
     if args.cascade:
         attn_kernels = binding.pa_decode_cascade_kernels(b.num_seqs, b.num_heads, b.num_kv_heads,
                                                          b.head_size, b.block_size, max_len,
                                                          shared, fp8)
-        kernel = (f"pa_decode_cascade{'_fp8' if fp8 else ''} ("
-                  + ("prefix pass beside the suffix decode in one launch, then the merge kernel"
-                     if attn_kernels == 2 else "prefix pass, suffix decode, merge kernel") + ")")
+        kernel = (f"pa_decode_cascade{'_fp8' if fp8 else ''} (counter clear, then the "
+                  "prefix pass beside the own tokens' decode in one launch, merged by the last "
+                  "arrivals)")
         traffic_file = f"cascade{'_fp8' if fp8 else ''}_{b.name}.traffic.txt"
     elif fp8:
         kernel = "pa_decode_fp8 (split-context kernel + merge kernel)"
@@ -607,12 +818,15 @@ def run_ours(args, world, rank, local):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": profile_traffic(traffic_file),
                      "kernel": kernel,
-                     "algorithmic_bytes_per_launch": alg, "launch_ms": decode_ms,
+                     "algorithmic_bytes_per_launch": alg, "launch_ms": decode_med_ms,
+                     "launch_ms_how": (f"median of {runs} individually event-timed launches"
+                                       if graph is None else "mean over the graph replays"),
+                     "launch_ms_mean_in_steps": decode_ms,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s"},
         "kernels_ms": {"pa_cache_write": write_ms, "pa_decode": decode_ms},
-        "e2e": {"value": world * kv * args.steps / e2e_s / 1e9, "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+        "e2e": {"value": world * kv * n_e2e / e2e_s / 1e9, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
                 "note": "KV pool resident in HBM (the cache); every step's inputs copied in "
                         "from pinned host memory and its output copied out, on one stream per "
                         "copy direction overlapping the neighbouring steps' kernels (two "
@@ -632,6 +846,11 @@ def run_ours(args, world, rank, local):
                                                   "seqs_per_s": sps1,
                                                   "sample": f"{done1} sequence-steps, same "
                                                             f"sample, one thread"}}
+    if (world == 1 and n == DEFAULT_WORKLOAD and not args.seqs and not args.graph
+            and not args.cascade and not fp8 and not args.no_by_workload):
+        # Every other workload of the set, measured in the same run on the same GPU.
+        line["by_workload"] = by_workload(args, dev, stream)
+        line["gpu_launches_by_workload"] = line["by_workload"].pop("_launches")
     print(json.dumps(line), flush=True)
 
 
@@ -709,6 +928,19 @@ def run_mixed(args, world, rank, local):
     binding.pa_error_check(stream)
     ms = [sum(e[j].elapsed_time(e[j + 1]) for e in evs) / args.steps for j in range(3)]
 
+    def prefill_only():
+        if fp8:
+            binding.pa_prefill_chunk_fp8(out_pre, q_pre, cu_pre, max_q, pool8, bt_pre, sl_pre,
+                                         b.scale, FP8_K_SCALE, FP8_V_SCALE, stream)
+        else:
+            binding.pa_prefill_chunk(out_pre, q_pre, cu_pre, max_q, b.kv_cache, bt_pre, sl_pre,
+                                     b.scale, stream)
+
+    # The tensor-bound kernel's roofline duration: the median of individually
+    # event-timed launches.
+    runs = max(50, args.median_runs)
+    pre_med_ms = median_launch_ms(prefill_only, stream, runs)
+
     # The same step through the one unified call (write, chunks, decode tokens).
     out_all = torch.empty_like(b.q)
     ws_all = torch.empty(binding.pa_attention_varlen_workspace_bytes(
@@ -737,6 +969,7 @@ def run_mixed(args, world, rank, local):
     torch.cuda.synchronize(dev)
     binding.pa_error_check(stream)
     unified_ms = e0.elapsed_time(e1) / args.steps
+    unified_med_ms = median_launch_ms(unified, stream, runs)
 
     # End to end through the unified call: every step's inputs (q, new K/V, slots,
     # chunk offsets, tables, lengths) from pinned host memory in one staging
@@ -801,11 +1034,12 @@ def run_mixed(args, world, rank, local):
         e2e_step(i)
     barrier(world)
     torch.cuda.synchronize(dev)
+    n_e2e = max(args.steps, args.e2e_steps)
     t0 = time.perf_counter()
-    for i in range(args.steps):
+    for i in range(n_e2e):
         e2e_step(i)
     torch.cuda.synchronize(dev)
-    e2e_ms = max_over_ranks(time.perf_counter() - t0, world, dev) * 1e3 / args.steps
+    e2e_ms = max_over_ranks(time.perf_counter() - t0, world, dev) * 1e3 / n_e2e
     binding.pa_error_check(stream)
     barrier(world)
     if rank != 0:
@@ -814,7 +1048,7 @@ def run_mixed(args, world, rank, local):
     kv_dec = kv_read_bytes(sl_dec.tolist(), b.num_kv_heads, b.head_size)
     with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
         pk = json.load(f)
-    pre_tflops = flops / (ms[1] / 1e3) / 1e12
+    pre_tflops = flops / (pre_med_ms / 1e3) / 1e12
     line = {"metric": "mixed chunked-prefill + decode step",
             "value": unified_ms, "unit": "ms", "ms_per_step": unified_ms,
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
@@ -827,7 +1061,9 @@ def run_mixed(args, world, rank, local):
                     + ("; FP8 pool" if fp8 else ""),
             "kernels_ms": {"pa_cache_write": ms[0], "pa_prefill_chunk": ms[1], "pa_decode": ms[2]},
             "sequential_step_ms": sum(ms),
-            "prefill": {"tflops": flops / (ms[1] / 1e3) / 1e12, "flops_per_launch": flops,
+            "unified_ms_median": unified_med_ms,
+            "prefill": {"tflops": pre_tflops, "flops_per_launch": flops,
+                        "launch_ms_median": pre_med_ms,
                         "peak_tflops": pk["bf16_tflops"],
                         "frac": flops / (ms[1] / 1e3) / 1e12 / pk["bf16_tflops"]},
             "decode": {"kv_gbs": kv_dec / (2 if fp8 else 1) / (ms[2] / 1e3) / 1e9,
@@ -843,10 +1079,11 @@ def run_mixed(args, world, rank, local):
                          "traffic": profile_traffic(
                              f"prefill{'_fp8' if fp8 else ''}_{b.name}.traffic.txt"),
                          "kernel": f"pa_prefill_chunk{'_fp8' if fp8 else ''}",
-                         "algorithmic_flops_per_launch": flops, "launch_ms": ms[1],
+                         "algorithmic_flops_per_launch": flops, "launch_ms": pre_med_ms,
+                         "launch_ms_how": f"median of {runs} individually event-timed launches",
                          "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops)"},
             "e2e": {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h,
+                    "d2h_bytes_per_step": d2h, "steps": n_e2e,
                     "note": "the unified call with every step's inputs copied in from pinned "
                             "host memory and its output copied out, one stream per copy "
                             "direction, two buffer sets; the KV pool resident; host wall "
@@ -884,6 +1121,12 @@ def main(argv=None):
                     help="shared-prefix decode (pa_decode_cascade) on a prefix-sharing workload")
     ap.add_argument("--seqs", type=int, default=0,
                     help="profile only the first N sequences of the workload (not a bench line)")
+    ap.add_argument("--median-runs", type=int, default=50,
+                    help="individually timed launches behind each median (at least 50)")
+    ap.add_argument("--e2e-steps", type=int, default=300,
+                    help="steps of the end-to-end leg (at least --steps)")
+    ap.add_argument("--no-by-workload", action="store_true",
+                    help="default workload only: skip the other workloads' figures")
     args = ap.parse_args(argv)
     world, rank, local = dist_setup()
     try:

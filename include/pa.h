@@ -53,7 +53,9 @@ typedef enum {
     PA_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed            */
     PA_ERR_OOB = 4,         /* a kernel met a block id or slot outside the pool       */
     PA_ERR_TIMEOUT = 5,     /* a kernel's bounded wait on its own copies gave up      */
-    PA_ERR_WORKSPACE = 6    /* workspace pointer null/misaligned or smaller than asked */
+    PA_ERR_WORKSPACE = 6,   /* workspace pointer null/misaligned or smaller than asked */
+    PA_ERR_PRECONDITION = 7 /* a kernel found a stated device-side precondition broken
+                               (pa_decode_cascade: a sequence's shared blocks differ) */
 } pa_status;
 
 /* Human-readable name of a status; never NULL. */
@@ -144,13 +146,19 @@ pa_status pa_prefill_chunk_fp8(void *out, const void *q, const int32_t *cu_q_len
 /*
  * Workspace pa_decode needs on the current device for this shape, in bytes
  * (partial softmax states of split contexts plus a small table).  Depends on
- * the device's SM count.  Returns 0 for invalid arguments.
+ * the device's SM count and the batch size, not on sequence lengths: every
+ * context is split over the whole GPU, so the partial states are per warp of
+ * the persistent grid.  Returns 0 for invalid arguments.
  */
 size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, int head_size);
 
 /*
  * pa_decode - one query token per sequence against its paged context.
  *
+ * Follows §Engine core (a sequence's tokens are found through the blocks its
+ * block table names: the blocks are the index from tokens to their KV) and
+ * §Generate function (the batch's decode tokens are rows of one flattened
+ * forward pass, each attending to its own sequence's cached KV).
  * Sequence s attends to its tokens 0 .. seq_lens[s]-1, found through
  * block_tables[s][t / block_size] at offset t % block_size; the new token's own
  * K/V must already be written (pa_cache_write), so seq_lens[s] counts it.
@@ -188,9 +196,12 @@ pa_status pa_decode(void *out, const void *q, const void *kv_cache, int num_bloc
  *   Scratch comes from a 16 MiB array in this library's device image, held by
  *   every GPU that loads the library until the process exits.  A shape whose
  *   pa_decode_workspace_bytes() exceeds 16 MiB returns PA_ERR_UNSUPPORTED.
- *   The call allocates nothing.  Its first call on a device (with that device
- *   current) looks up the array's device address; make that first call before
- *   any stream capture.
+ *   The call allocates nothing.  Its first call in a CUDA context (the device's
+ *   primary context, or another one made current) looks up the array's device
+ *   address in that context and keeps it for that context's later calls; make
+ *   that first call before any stream capture.  The 16 MiB hold every shape
+ *   pa_decode accepts on a 152-SM GB300 (the largest, 15 091 sequences of head
+ *   size 128, needs 15.1 MB).
  *   All calls share the one array: calls that overlap on the GPU (other
  *   streams, other threads) race and must be serialised by the caller.  No
  *   byte of the array needs to start at zero: each call writes before it reads.
@@ -212,13 +223,12 @@ size_t pa_decode_cascade_workspace_bytes(int num_seqs, int num_heads, int num_kv
 
 /*
  * Kernels one pa_decode_cascade call (pa_decode_cascade_fp8 when kv8 != 0) with
- * these shapes launches on the current device: 3 when the shared prefix is
- * attended by its own launch before the sequences' own tokens and the merge; 2
- * when the prefix and the own tokens are attended side by side in one launch on
- * disjoint SMs (chosen from the shapes and the pool's type), or when shared_len is 0
- * (pa_decode); 0 when num_seqs is 0; -1 for invalid shapes.  For planning only
- * (e.g. counting a CUDA graph's nodes): the results are the same either way, up
- * to floating-point summation order.
+ * these shapes launches on the current device: 2 (a kernel that clears the
+ * per-segment arrival counters, then the prefix pass and the own tokens' decode
+ * side by side in one launch on disjoint SMs; or the prefix pass, then the own
+ * tokens' decode: chosen from the shapes and the pool's type; or, when
+ * shared_len is 0, pa_decode's two); 0 when num_seqs is 0; -1 for invalid shapes.
+ * For planning only (e.g. counting a CUDA graph's nodes).
  */
 int pa_decode_cascade_kernels(int num_seqs, int num_heads, int num_kv_heads, int head_size,
                               int block_size, int max_seq_len, int shared_len, int kv8);
@@ -231,11 +241,14 @@ int pa_decode_cascade_kernels(int num_seqs, int num_heads, int num_kv_heads, int
  * prompt start hold the same physical KV blocks.  Here the first shared_len
  * tokens of every sequence are those blocks: block_tables[s][i] equals
  * block_tables[0][i] for i < shared_len / block_size (a precondition; the
- * prefix is read through sequence 0's table).  The prefix is attended once per
+ * prefix is read through sequence 0's table; the kernels compare the entries,
+ * and a mismatch makes pa_error_check() return PA_ERR_PRECONDITION).  The prefix is attended once per
  * KV head for all queries of the batch on the tensor cores, each sequence's own
- * tokens [shared_len, seq_lens[s]) as in pa_decode, and the two softmax states
- * are merged by log-sum-exp.  The result is pa_decode's up to floating-point
- * summation order.
+ * tokens [shared_len, seq_lens[s]) as in pa_decode, and the softmax states
+ * are merged by log-sum-exp, per (sequence, KV head), by whichever part of the
+ * work finishes that segment last (no separate merge launch).  The result is
+ * pa_decode's up to floating-point summation order, and the same bits on every
+ * call.
  *   Arguments are those of pa_decode, plus:
  *   shared_len    tokens shared by every sequence, 0 <= shared_len <= max_seq_len,
  *                 a multiple of 16 and of block_size (else PA_ERR_UNSUPPORTED);
@@ -320,8 +333,9 @@ size_t pa_attention_varlen_workspace_bytes(int num_seqs, int num_prefills, int n
  *   max_seq_len   host bound of the decode sequences' lengths
  *   workspace     >= pa_attention_varlen_workspace_bytes(...) bytes, 256-byte
  *                 aligned
- * Launches on `stream` in that order; arguments are checked as by the three
- * calls, and the first failure is returned (earlier launches stand).
+ * Launches on `stream` in that order.  Every argument is checked (as by the
+ * three calls, and the workspace) before anything is enqueued: a host-checkable
+ * fault returns its status with the pool untouched.
  */
 pa_status pa_attention_varlen(void *out, const void *q, const void *k_new, const void *v_new,
                               const int32_t *slot_mapping, const int32_t *cu_q_lens,
@@ -350,8 +364,9 @@ pa_status pa_attention_varlen_fp8(void *out, const void *q, const void *k_new,
 
 /*
  * Synchronise `stream`, then read and clear the device error word the kernels
- * of this library set on the current device.  Returns PA_OK, PA_ERR_OOB,
- * PA_ERR_TIMEOUT, or PA_ERR_CUDA if the synchronisation itself failed.
+ * of this library set on the current device.  Returns PA_OK, PA_ERR_TIMEOUT,
+ * PA_ERR_OOB or PA_ERR_PRECONDITION (the first of these that was set, in this
+ * order), or PA_ERR_CUDA if the synchronisation itself failed.
  */
 pa_status pa_error_check(pa_stream_t stream);
 

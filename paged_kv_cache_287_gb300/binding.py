@@ -19,7 +19,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libpagedattn.so")
 
 STATUS = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_CUDA",
-          4: "PA_ERR_OOB", 5: "PA_ERR_TIMEOUT", 6: "PA_ERR_WORKSPACE"}
+          4: "PA_ERR_OOB", 5: "PA_ERR_TIMEOUT", 6: "PA_ERR_WORKSPACE",
+          7: "PA_ERR_PRECONDITION"}
 
 # Every symbol include/pa.h declares.
 EXPORTS = ("pa_status_string", "pa_kv_block_bytes", "pa_kv_block_bytes_dtype", "pa_cache_write",

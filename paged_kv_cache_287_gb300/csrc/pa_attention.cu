@@ -126,31 +126,37 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
 }
 
 // dec_slots: the grid's leading decode CTAs (with a device plan, the first
-// plan[0] of them stream and the rest exit).  merge_early: launch the merge
-// kernel as a programmatic dependent (its CTAs may start once every CTA of this
-// grid has started and wait for its end), for grids that fit the GPU at once.
+// plan[0] of them stream and the rest exit).  cascade: a shared-prefix decode,
+// merged by the last arrivals (no merge kernel), launched as a programmatic
+// dependent of the kernel before it (which clears the arrival counters): its
+// CTAs start at once and wait for that grid only where they count.  Otherwise
+// the merge kernel follows as a plain launch.
 template <int D, bool KV8, int DW = kDecodeWarps>
 cudaError_t launch_mixed_d(const CUtensorMap &map, const DecodeArgs &da, const PrefillArgs &pa,
                            dim3 pgrid, int dec_slots, size_t smem, cudaStream_t stream,
-                           bool merge_early = false) {
+                           bool cascade = false) {
     auto kern = mixed_kernel<D, KV8, DW>;
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = ensure_smem<mixed_kernel<D, KV8, DW>>(smem);
     if (e != cudaSuccess) return e;
     const unsigned n_pre = pgrid.x * pgrid.y * pgrid.z;
-    kern<<<(unsigned)dec_slots + n_pre, kDecodeWarps * 32, smem, stream>>>(
-        map, da, pa, dec_slots, make_uint3(pgrid.x, pgrid.y, pgrid.z));
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(da.num_seqs * da.num_kv_heads));
-    cfg.blockDim = dim3((unsigned)(da.group * D / 4));
-    cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)dec_slots + n_pre);
+    cfg.blockDim = dim3(kDecodeWarps * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = merge_early ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, decode_merge_kernel<D>, da);
+    cfg.numAttrs = cascade ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, kern, map, da, pa, dec_slots,
+                           make_uint3(pgrid.x, pgrid.y, pgrid.z));
+    if (e != cudaSuccess || cascade) return e;
+    cudaLaunchConfig_t mcfg = {};
+    mcfg.gridDim = dim3((unsigned)(da.num_seqs * da.num_kv_heads));
+    mcfg.blockDim = dim3((unsigned)(da.group * D / 4));
+    mcfg.stream = stream;
+    return cudaLaunchKernelEx(&mcfg, decode_merge_kernel<D>, da);
 }
 
 }  // namespace
@@ -269,6 +275,10 @@ constexpr float kCascadeTileUs = 1.8f, kCascadeStartUs = 4.0f, kCascadeDecSmGBs 
 // FP8 pool: the prefix pass converts each tile (about 1.9 us), the decode streams
 // about 29 GB/s per SM.
 constexpr float kCascadeTileUsFp8 = 1.9f, kCascadeDecSmGBsFp8 = 29.0f;
+#ifndef PA_CASCADE_DEPTH
+#define PA_CASCADE_DEPTH 1
+#endif
+constexpr int kCascadeDepth = PA_CASCADE_DEPTH;
 }  // namespace
 
 int cascade_one_launch_ctas(int num_seqs, int num_heads, const KvGeom &g, int max_seq_len,
@@ -317,13 +327,12 @@ cudaError_t launch_cascade_one(void *out, const void *q, const void *kv_cache, c
     da.k_scale = kv8 ? k_scale : 1.f;
     da.v_scale = kv8 ? v_scale : 1.f;
     da.shared_len = shared_len;
-    da.pre_splits = 1;
-    da.pre_ml = pre_ml;
-    da.pre_acc = pre_acc;
-    const size_t segs = (size_t)num_seqs * g.num_kv_heads;
-    da.whole_ml = static_cast<float *>(whole);
-    da.whole_acc = reinterpret_cast<float *>(static_cast<uint8_t *>(whole) +
-                                             align_up(segs * kHeadsPad * 2 * 4, 256));
+    // One prefix split, which counts as an arrival (it runs in this launch).
+    set_cascade(da, D, whole, pre_ml, pre_acc, 1, 1);
+    // Most SMs stream the own tokens, so one tile in flight per warp (two from an
+    // FP8 pool, half the bytes) saturates HBM; more only lengthens the queueing
+    // of the prefix pass's loads beside them.
+    da.depth = kCascadeDepth + (kv8 ? 1 : 0);
     // The prefix pass: every sequence's query rows against keys [0, shared_len)
     // of sequence 0's blocks, one split.
     PrefillArgs pa;
@@ -348,8 +357,18 @@ cudaError_t launch_cascade_one(void *out, const void *q, const void *kv_cache, c
     pa.prefix_rows = num_seqs;
     pa.k_scale = da.k_scale;
     pa.v_scale = da.v_scale;
+    pa.cs = da.cs;
+    pa.seq_lens = seq_lens;  // rows of sequences with no own tokens are written directly
+    pa.clear_cnt = nullptr;
+    pa.clear_n = 0;
     const dim3 pgrid((unsigned)((num_seqs + per_cta - 1) / per_cta), (unsigned)g.num_kv_heads, 1);
-    // The grid (one CTA per SM) is resident at once, so the merge may launch early.
+    // The arrival counters start at zero: cleared by a one-CTA kernel, of which the
+    // attention launch is a programmatic dependent.
+    const int segs = num_seqs * g.num_kv_heads;
+    cascade_clear_kernel<<<std::min((segs + 255) / 256, 8), 256, 0, stream>>>(da.cs.seg_cnt,
+                                                                             segs);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
     if (kv8)
         return launch_mixed_d<128, true>(map, da, pa, pgrid, dec_ctas, TcLay<128>::kSmem, stream,
                                          true);

@@ -18,6 +18,7 @@ namespace pa {
 enum : unsigned {
     kErrOob = 1u,      // block id / slot outside the pool, or length beyond the table
     kErrTimeout = 2u,  // a bounded wait on the kernel's own copies gave up
+    kErrPrecondition = 4u,  // a caller's stated precondition does not hold (shared blocks)
 };
 
 // A wait on the kernel's own TMA copies gives up after this many nanoseconds.

@@ -11,8 +11,9 @@
 //     (152 SMs x W warps), so skewed lengths cost nothing in balance.  A
 //     (sequence, head) segment that falls across ranges is finished in pieces whose
 //     (max, sum, acc) states are merged by log-sum-exp in a second small kernel.
-//     For a shared-prefix batch that kernel also folds the prefix pass's partials
-//     into every (sequence, head), so no decode warp waits on them.
+//     For a shared-prefix batch every piece instead counts its arrival, and the
+//     contributor that completes a segment merges it with the prefix pass's
+//     partials (pa_merge.cuh): no second kernel, and no warp waits on another.
 //   * Every warp runs its own pipeline: lane 0 issues 128B-swizzled 2-D TMA
 //     copies of the K and V tiles named by the block table into an S-stage ring in
 //     shared memory (plus the segment's G query rows with a bulk copy); the warp
@@ -28,6 +29,7 @@
 
 #include "pa_common.cuh"
 #include "pa_internal.h"
+#include "pa_merge.cuh"
 
 namespace pa {
 namespace {
@@ -86,20 +88,21 @@ struct DecodeArgs {
     int stage_bytes;   // 2 * K/V tile bytes + query slot
     float scale_log2;  // scale * log2(e)
     float k_scale, v_scale;  // FP8 pool: real K/V = e4m3 value * scale (1 for bf16)
-    // Cascade: each sequence's tokens [0, shared_len) were attended by the prefix
-    // pass, whose pre_splits unnormalised partials per (sequence, query head) the
-    // merge kernel folds in; this kernel covers tokens [shared_len, seq_len).  A
-    // segment that one warp finishes whole then leaves its (m, l, acc) in the
-    // segment's own record instead of writing the output.
+    // Cascade (cs.pre_splits > 0): each sequence's tokens [0, shared_len) are
+    // attended by the prefix pass; this kernel covers tokens [shared_len,
+    // seq_len).  Every piece of a segment (a segment one warp finishes whole
+    // included) leaves its (m, l, acc) record and counts its arrival; the last
+    // contributor merges (pa_merge.cuh).
     int shared_len;
-    int pre_splits;
-    const float *pre_ml;   // [pre_splits][num_seqs][num_heads][2]
-    const float *pre_acc;  // [pre_splits][num_seqs][num_heads][D]
-    float *whole_ml;       // [num_seqs * num_kv_heads][8][2]
-    float *whole_acc;      // [num_seqs * num_kv_heads][8][D]
+    CascadeState cs;
     // Mixed-batch launch: the number of decode CTAs and their total warps were
     // chosen on the device; plan = {ctas, total_warps} (nullptr otherwise).
     const int *plan;
+    // Tiles a warp keeps in flight, at most the ring's stages (0: all of them).
+    // Fewer than the ring holds when enough SMs stream that HBM is saturated
+    // anyway: the bytes in flight then only lengthen every request's queueing,
+    // the loads of the kernel's other role included.
+    int depth;
 };
 
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -180,14 +183,99 @@ __device__ __forceinline__ void decode_body(const CUtensorMap &kv_map, const Dec
     asm volatile("griddepcontrol.launch_dependents;" :::);
 
     if (warp >= W) return;
-    // This warp's equal share of the flattened tile list.
+    // This warp's equal share of the flattened tile list.  With fewer tiles than
+    // warps only the first T warps take one each, so no warp's range is empty
+    // and a segment's pieces are the consecutive warps g0..g1.
     const long long T = (long long)s_pre[B] * Hkv;
     const long long NW = total_warps;
+    const long long NWe = NW < T ? NW : (T > 0 ? T : 1);
     const long long g = (long long)cta * W + warp;
-    const int t_begin = (int)((g * T) / NW);
-    const int t_end = (int)(((g + 1) * T) / NW);
+    const int t_begin = g < NWe ? (int)((g * T) / NWe) : 0;
+    const int t_end = g < NWe ? (int)(((g + 1) * T) / NWe) : 0;
     const int n = t_end - t_begin;
-    if (n <= 0) return;
+    // Cascade: the prefix pass reads the shared blocks through sequence 0's table,
+    // so every other sequence's first shared_len / block_size entries must equal
+    // sequence 0's.  The decode warps compare them, a strided share each, and flag
+    // a mismatch (the result is then not that of the caller's tables).
+    auto check_shared_tables = [&]() {
+        if (sh == 0) return;
+        const int nsh = sh / bs;
+        const long long total = (long long)(B - 1) * nsh;
+        for (long long x = g * 32 + lane; x < total; x += NW * 32) {
+            const int s = 1 + (int)(x / nsh), i = (int)(x - (long long)(s - 1) * nsh);
+            if (a.block_tables[(size_t)s * a.max_blocks + i] != a.block_tables[i])
+                atomicOr(&g_err_decode, kErrPrecondition);
+        }
+    };
+    // (sequence, KV head) segment of flattened tile x.
+    auto seg_of = [&](int x) {
+        int lo = 0, hi = B - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (Hkv * s_pre[mid] <= x) lo = mid; else hi = mid - 1;
+        }
+        const int nt = s_pre[lo + 1] - s_pre[lo];
+        return lo * Hkv + (x - Hkv * s_pre[lo]) / nt;
+    };
+    // Cascade, after this warp's last tile (its records are written; nothing of
+    // the streaming loop is live any more).  Its tiles cover the segments sf..sl;
+    // one lane per segment counts this warp's arrival there (the warp holding a
+    // segment's first tile also publishes where its first record is and how many
+    // pieces there are), and the warp merges every segment its arrival completed.
+    // With the prefix partials complete before this launch, the segments of
+    // sequences with no own tokens get no decode piece: the warps merge those from
+    // the prefix partials alone, one sequence each in turn.  (When the prefix pass
+    // runs in the same launch, it writes those rows itself.)
+    auto finish = [&]() {
+        if (a.cs.pre_splits == 0) return;
+        if (n > 0) {
+            const int sf = seg_of(t_begin), sl = seg_of(t_end - 1);
+            for (int base = sf; base <= sl; base += 32) {
+                const int sx = base + lane;
+                unsigned add = 0;
+                int s_ = 0, h_ = 0;
+                if (sx <= sl) {
+                    s_ = sx / Hkv;
+                    h_ = sx - s_ * Hkv;
+                    const int nt = s_pre[s_ + 1] - s_pre[s_];
+                    if (nt > 0) {
+                        const long long S0 = (long long)Hkv * s_pre[s_] + (long long)h_ * nt;
+                        const long long g0 = ((S0 + 1) * NWe - 1) / T;
+                        const long long g1 = ((S0 + nt) * NWe - 1) / T;
+                        const int n_dec = (int)(g1 - g0 + 1);
+                        if (g0 == g) {
+                            const int rec = n_dec == 1 ? -1 : (int)(g * 2 + (sx == sf ? 0 : 1));
+                            a.cs.seg_info[sx] = make_int2(rec, n_dec);
+                            add = kArrivalsDone - (unsigned)n_dec -
+                                  (unsigned)a.cs.prefix_arrives + 1u;
+                        } else {
+                            add = 1u;
+                        }
+                    }
+                }
+                __syncwarp();
+                const bool last = add != 0u && arrive(a.cs.seg_cnt + sx, add);
+                unsigned todo = __ballot_sync(0xffffffffu, last);
+                while (todo) {
+                    const int k = __ffs(todo) - 1;
+                    todo &= todo - 1;
+                    const int sk = __shfl_sync(0xffffffffu, s_, k);
+                    const int hk = __shfl_sync(0xffffffffu, h_, k);
+                    const int2 info = __ldcg(a.cs.seg_info + (size_t)sk * Hkv + hk);
+                    merge_segment<D>(a.cs, sk, hk, info.y, info.x);
+                }
+            }
+        }
+        if (!a.cs.prefix_arrives)
+            for (long long x = g; x < B; x += NW)
+                if (s_len[x] == 0)
+                    for (int hh = 0; hh < Hkv; ++hh) merge_segment<D>(a.cs, (int)x, hh, 0, 0);
+    };
+    if (n <= 0) {
+        check_shared_tables();
+        finish();
+        return;
+    }
 
     uint8_t *wring = ring + (size_t)warp * S * stage_bytes;
     uint64_t *wbar = bars + warp * S;
@@ -276,9 +364,12 @@ __device__ __forceinline__ void decode_body(const CUtensorMap &kv_map, const Dec
         }
     };
 
-    const int first_issue = n < S ? n : S;
+    const int ahead = a.depth > 0 && a.depth < S ? a.depth : S;
+    const int first_issue = n < ahead ? n : ahead;
     for (int i = 0; i < first_issue; ++i) issue(i);
     int issued = first_issue;
+    // While the first tiles are in flight.
+    check_shared_tables();
 
     float acc[D / 16][4];
     uint32_t qf[D / 16][2];
@@ -459,20 +550,15 @@ __device__ __forceinline__ void decode_body(const CUtensorMap &kv_map, const Dec
             m0 = mn0;
             m1 = mn1;
         }
-        // Per-lane partial sums of the rounded P actually multiplied; the head's 8
-        // lanes are summed once, at the end of the segment.
-        uint32_t plo, phi;
-        if constexpr (!KV8) {
-            plo = pack_bf16(fast_exp2(x0 - m0), fast_exp2(x1 - m1));
-            phi = pack_bf16(fast_exp2(x2 - m0), fast_exp2(x3 - m1));
-            l0 = l0 * cr0 + (bf16_lo(plo) + bf16_lo(phi));
-            l1 = l1 * cr1 + (bf16_hi(plo) + bf16_hi(phi));
-        } else {
-            plo = pack_f16(fast_exp2(x0 - m0), fast_exp2(x1 - m1));
-            phi = pack_f16(fast_exp2(x2 - m0), fast_exp2(x3 - m1));
-            l0 = l0 * cr0 + (f16_lo(plo) + f16_lo(phi));
-            l1 = l1 * cr1 + (f16_hi(plo) + f16_hi(phi));
-        }
+        // Per-lane partial sums of P in fp32, before its rounding to 16 bits for
+        // the P.V product (the rule of every kernel here); the head's 8 lanes are
+        // summed once, at the end of the segment.
+        const float p0 = fast_exp2(x0 - m0), p1 = fast_exp2(x1 - m1);
+        const float p2 = fast_exp2(x2 - m0), p3 = fast_exp2(x3 - m1);
+        l0 = l0 * cr0 + (p0 + p2);
+        l1 = l1 * cr1 + (p1 + p3);
+        const uint32_t plo = KV8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
+        const uint32_t phi = KV8 ? pack_f16(p2, p3) : pack_bf16(p2, p3);
         const uint32_t b0 = movmatrix_t(plo), b1 = movmatrix_t(phi);
 
         // O^T[dim][head] += V^T . P^T
@@ -534,7 +620,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap &kv_map, const Dec
             }
             const int nt = s_pre[s + 1] - s_pre[s];
             const bool whole = first_j == 0 && j == nt - 1;
-            if (whole && a.pre_splits == 0) {
+            if (whole && a.cs.pre_splits == 0) {
                 // Whole segment in this warp: normalise and write bf16 rows, staged in
                 // the stage's query slot (G rows) for 16-byte stores.  Only the G real
                 // heads are staged: the slot holds no room for the padding heads.
@@ -565,7 +651,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap &kv_map, const Dec
                 // (m, l, acc) for the merge kernel.
                 const size_t rec = (size_t)g * 2 + (first_piece ? 0 : 1);
                 const size_t wrec = (size_t)s * Hkv + h;
-                float *pacc = whole ? a.whole_acc + wrec * kHeadsPad * D
+                float *pacc = whole ? a.cs.whole_acc + wrec * kHeadsPad * D
                                     : a.part_acc + rec * kHeadsPad * D;
 #pragma unroll
                 for (int mt = 0; mt < D / 16; ++mt) {
@@ -576,7 +662,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap &kv_map, const Dec
                     pacc[(hh0 + 1) * D + d1] = acc[mt][3];
                 }
                 if (lane < 4) {
-                    float *pml = whole ? a.whole_ml + wrec * kHeadsPad * 2
+                    float *pml = whole ? a.cs.whole_ml + wrec * kHeadsPad * 2
                                        : a.part_ml + rec * kHeadsPad * 2;
                     pml[hh0 * 2 + 0] = m0;
                     pml[hh0 * 2 + 1] = l0;
@@ -589,9 +675,9 @@ __device__ __forceinline__ void decode_body(const CUtensorMap &kv_map, const Dec
         prev_seg = seg;
         if (wrote_smem) fence_proxy_async_smem();
         __syncwarp();
-        if (c + S < n) {
-            issue(c + S);
-            issued = c + S + 1;
+        if (c + ahead < n) {
+            issue(c + ahead);
+            issued = c + ahead + 1;
         }
         if ((c & 31) == 31) {
             dA0 = dB0;
@@ -602,6 +688,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap &kv_map, const Dec
             make_desc(cur_batch + 1, dB0, dB1, dB2, dB3);
         }
     }
+    finish();
 }
 
 template <int D, int W, int S, bool KV8>
@@ -610,12 +697,10 @@ __global__ void __launch_bounds__(W * 32, 1)
     decode_body<D, W, S, KV8>(kv_map, a, blockIdx.x, a.total_warps);
 }
 
-// Merge the pieces of segments that were split across warps; zero empty sequences.
-// Cascade: also fold the shared prefix's partials into every segment (split,
-// whole or empty).  One CTA per (sequence, KV head); one thread per (query head,
-// 4 dims).  Launched
-// as a programmatic dependent of the split kernel: it may start early and waits
-// for that grid's completion before reading anything it wrote.
+// Merge the pieces of segments that were split across warps; zero empty
+// sequences.  One CTA per (sequence, KV head); one thread per (query head, 4
+// dims).  Launched as a programmatic dependent of the split kernel: it may start
+// early and waits for that grid's completion before reading anything it wrote.
 template <int D>
 __global__ void __launch_bounds__(kHeadsPad * D / 4) decode_merge_kernel(const DecodeArgs a) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -629,92 +714,34 @@ __global__ void __launch_bounds__(kHeadsPad * D / 4) decode_merge_kernel(const D
     const int hh = i / (D / 4), d4 = i - hh * (D / 4);
     uint2 *orow =
         reinterpret_cast<uint2 *>(a.out + ((size_t)s * a.num_heads + (size_t)h * G + hh) * D);
-    const int P = a.pre_splits;
-    if (nt == 0 && P == 0) {
+    if (nt == 0) {
         orow[d4] = make_uint2(0u, 0u);
         return;
     }
-    // Pieces g0..g1 of this segment (none if the sequence has no tokens here).
+    // Pieces g0..g1 of this segment, under the split kernel's partition (the
+    // first min(NW, T) warps, equal shares).
     const long long NW = a.plan ? a.plan[1] : a.total_warps;
-    long long T = 1, S0 = 0, S1 = 0, g0 = 0, g1 = -1;
-    bool whole = false;  // one warp's record holds the whole segment
-    if (nt > 0) {
-        T = (long long)a.prefix[a.num_seqs] * Hkv;
-        S0 = (long long)Hkv * pre + (long long)h * nt;
-        S1 = S0 + nt;
-        g0 = ((S0 + 1) * NW - 1) / T;
-        g1 = (S1 * NW - 1) / T;
-        if (g0 == g1) {
-            if (P == 0) return;  // written by that warp
-            whole = true;
-            g1 = g0 - 1;         // no pieces
-        }
-    }
-    // Shared-prefix partials of this query head.
-    const size_t pr0 = (size_t)s * a.num_heads + (size_t)h * G + hh;
-    const size_t prs = (size_t)a.num_seqs * a.num_heads;
-    const float2 *pml = reinterpret_cast<const float2 *>(a.pre_ml);
-    // Warp gw covers tiles [floor(gw*T/NW), floor((gw+1)*T/NW)); the bounds are
-    // stepped incrementally (T = q*NW + r) instead of divided per warp.
-    const long long tq = T / NW, tr = T % NW;
-    const long long b0 = g0 * tq + (g0 * tr) / NW, f0 = (g0 * tr) % NW;
+    const long long T = (long long)a.prefix[a.num_seqs] * Hkv;
+    const long long NWe = NW < T ? NW : T;
+    const long long S0 = (long long)Hkv * pre + (long long)h * nt;
+    const long long S1 = S0 + nt;
+    const long long g0 = ((S0 + 1) * NWe - 1) / T;
+    const long long g1 = (S1 * NWe - 1) / T;
+    if (g0 == g1) return;  // written whole by that warp
+    // Warp gw covers tiles [floor(gw*T/NWe), floor((gw+1)*T/NWe)); its record of
+    // this segment is its first (slot 0) unless it began in an earlier segment.
     float M = -INFINITY;
-    for (int sp = 0; sp < P; ++sp) M = fmaxf(M, pml[sp * prs + pr0].x);
-    const size_t wrec = (size_t)k * kHeadsPad + hh;  // segment k's record, this head
-    if (whole) M = fmaxf(M, a.whole_ml[wrec * 2]);
-    long long b = b0, f = f0;
     for (long long gw = g0; gw <= g1; ++gw) {
-        long long e = b + tq;
-        f += tr;
-        if (f >= NW) {
-            f -= NW;
-            ++e;
-        }
-        if (max(b, S0) < min(e, S1)) {
-            const size_t rec = (size_t)gw * 2 + (b >= S0 ? 0 : 1);
-            M = fmaxf(M, a.part_ml[(rec * kHeadsPad + hh) * 2]);
-        }
-        b = e;
+        const size_t rec = (size_t)gw * 2 + (gw == g0 && (g0 * T) / NWe < S0 ? 1 : 0);
+        M = fmaxf(M, a.part_ml[(rec * kHeadsPad + hh) * 2]);
     }
     float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
     float den = 0.f;
-    b = b0;
-    f = f0;
     for (long long gw = g0; gw <= g1; ++gw) {
-        long long e = b + tq;
-        f += tr;
-        if (f >= NW) {
-            f -= NW;
-            ++e;
-        }
-        if (max(b, S0) < min(e, S1)) {
-            const size_t rec = (size_t)gw * 2 + (b >= S0 ? 0 : 1);
-            const float2 ml = reinterpret_cast<const float2 *>(a.part_ml)[rec * kHeadsPad + hh];
-            const float4 v =
-                reinterpret_cast<const float4 *>(a.part_acc + (rec * kHeadsPad + hh) * D)[d4];
-            const float w = exp2f(ml.x - M);
-            num.x += w * v.x;
-            num.y += w * v.y;
-            num.z += w * v.z;
-            num.w += w * v.w;
-            den += w * ml.y;
-        }
-        b = e;
-    }
-    if (whole) {
-        const float2 ml = reinterpret_cast<const float2 *>(a.whole_ml)[wrec];
-        const float4 v = reinterpret_cast<const float4 *>(a.whole_acc + wrec * D)[d4];
-        const float w = exp2f(ml.x - M);
-        num.x += w * v.x;
-        num.y += w * v.y;
-        num.z += w * v.z;
-        num.w += w * v.w;
-        den += w * ml.y;
-    }
-    for (int sp = 0; sp < P; ++sp) {
-        const size_t r = sp * prs + pr0;
-        const float2 ml = pml[r];
-        const float4 v = reinterpret_cast<const float4 *>(a.pre_acc + r * D)[d4];
+        const size_t rec = (size_t)gw * 2 + (gw == g0 && (g0 * T) / NWe < S0 ? 1 : 0);
+        const float2 ml = reinterpret_cast<const float2 *>(a.part_ml)[rec * kHeadsPad + hh];
+        const float4 v =
+            reinterpret_cast<const float4 *>(a.part_acc + (rec * kHeadsPad + hh) * D)[d4];
         const float w = exp2f(ml.x - M);
         num.x += w * v.x;
         num.y += w * v.y;
@@ -732,12 +759,12 @@ cudaError_t launch_decode_d(const DecodeArgs &a0, const CUtensorMap &map, int gr
     constexpr int S = KV8 ? kDecodeStagesFp8 : kDecodeStages;
     const size_t smem = decode_smem_bytes<D, KV8, S>(a0.num_seqs, a0.group);
     auto kern = decode_kernel<D, kDecodeWarps, S, KV8>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    cudaError_t e = ensure_smem<decode_kernel<D, kDecodeWarps, S, KV8>>(smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, kDecodeWarps * 32, smem, stream>>>(map, a0);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if (a0.cs.pre_splits > 0) return cudaSuccess;  // cascade: merged by the last arrivals
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(a0.num_seqs * a0.num_kv_heads));
     cfg.blockDim = dim3((unsigned)(a0.group * D / 4));
@@ -809,13 +836,37 @@ DecodeArgs make_decode_args(void *out, const void *q, const KvGeom &g, int num_h
     a.k_scale = 1.f;
     a.v_scale = 1.f;
     a.shared_len = 0;
-    a.pre_splits = 0;
-    a.pre_ml = nullptr;
-    a.pre_acc = nullptr;
-    a.whole_ml = nullptr;
-    a.whole_acc = nullptr;
+    a.cs = CascadeState{};
+    a.cs.out = a.out;
+    a.cs.part_ml = a.part_ml;
+    a.cs.part_acc = a.part_acc;
+    a.cs.num_seqs = num_seqs;
+    a.cs.num_heads = num_heads;
+    a.cs.num_kv_heads = g.num_kv_heads;
+    a.cs.group = a.group;
     a.plan = nullptr;
+    a.depth = 0;
     return a;
+}
+
+// Point a's cascade state at the per-segment records, segment table and
+// counters laid out as cascade_whole_bytes lays them out, and at the prefix
+// partials.
+void set_cascade(DecodeArgs &a, int head_size, void *whole, const float *pre_ml,
+                 const float *pre_acc, int pre_splits, int prefix_arrives) {
+    const size_t segs = (size_t)a.num_seqs * a.num_kv_heads;
+    uint8_t *w = static_cast<uint8_t *>(whole);
+    a.cs.whole_ml = reinterpret_cast<float *>(w);
+    w += align_up(segs * kHeadsPad * 2 * 4, 256);
+    a.cs.whole_acc = reinterpret_cast<float *>(w);
+    w += align_up(segs * kHeadsPad * (size_t)head_size * 4, 256);
+    a.cs.seg_info = reinterpret_cast<int2 *>(w);
+    w += align_up(segs * sizeof(int2), 256);
+    a.cs.seg_cnt = reinterpret_cast<unsigned *>(w);
+    a.cs.pre_ml = pre_ml;
+    a.cs.pre_acc = pre_acc;
+    a.cs.pre_splits = pre_splits;
+    a.cs.prefix_arrives = prefix_arrives;
 }
 
 cudaError_t launch_decode_impl(void *out, const void *q, const void *kv_cache, const KvGeom &g,
@@ -843,16 +894,9 @@ cudaError_t launch_decode_impl(void *out, const void *q, const void *kv_cache, c
     a.k_scale = k_scale;
     a.v_scale = v_scale;
     a.shared_len = shared_len;
-    a.pre_splits = pre_splits;
-    a.pre_ml = pre_ml;
-    a.pre_acc = pre_acc;
-    if (whole) {
-        // (m, l) records, then the acc rows, as cascade_whole_bytes lays them out.
-        const size_t segs = (size_t)num_seqs * g.num_kv_heads;
-        a.whole_ml = static_cast<float *>(whole);
-        a.whole_acc = reinterpret_cast<float *>(static_cast<uint8_t *>(whole) +
-                                                align_up(segs * kHeadsPad * 2 * 4, 256));
-    }
+    // Cascade: the prefix partials are complete before this launch (the prefix
+    // pass ran first and cleared the arrival counters).
+    if (whole) set_cascade(a, D, whole, pre_ml, pre_acc, pre_splits, 0);
     if (kv8) return launch_decode_d<128, true>(a, map, (int)ctas, stream);
     if (D == 128) return launch_decode_d<128, false>(a, map, (int)ctas, stream);
     return launch_decode_d<64, false>(a, map, (int)ctas, stream);
@@ -901,7 +945,16 @@ size_t prefix_partial_bytes(int splits, int num_seqs, int num_heads, int head_si
 size_t cascade_whole_bytes(int num_seqs, int num_kv_heads, int head_size) {
     const size_t segs = (size_t)num_seqs * num_kv_heads;
     return align_up(segs * kHeadsPad * 2 * 4, 256) +
-           align_up(segs * kHeadsPad * (size_t)head_size * 4, 256);
+           align_up(segs * kHeadsPad * (size_t)head_size * 4, 256) +
+           align_up(segs * sizeof(int2), 256) + align_up(segs * sizeof(unsigned), 256);
+}
+
+unsigned *cascade_counters(void *whole, int num_seqs, int num_kv_heads, int head_size) {
+    const size_t segs = (size_t)num_seqs * num_kv_heads;
+    return reinterpret_cast<unsigned *>(
+        static_cast<uint8_t *>(whole) + align_up(segs * kHeadsPad * 2 * 4, 256) +
+        align_up(segs * kHeadsPad * (size_t)head_size * 4, 256) +
+        align_up(segs * sizeof(int2), 256));
 }
 
 }  // namespace pa

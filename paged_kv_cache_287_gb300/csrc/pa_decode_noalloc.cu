@@ -11,8 +11,13 @@
 // The scratch is one file-scope __device__ array of kNoAllocScratchBytes.  Every
 // GPU that loads the library holds it until the process exits.  Host code only
 // sees a host-side stand-in for the array's name, so its device address is
-// looked up once per device (with that device current) by cudaGetSymbolAddress
-// and cached.  Every call on a device shares the array.
+// looked up by cudaGetSymbolAddress with the device current, and cached per CUDA
+// context (by the context's unique id): a context created later on the same
+// device (after cudaDeviceReset, or one made through the driver API and made
+// current) gets its own lookup, so no call uses an address of a context that is
+// gone.  Every call within one context shares the array.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "pa.h"
@@ -21,25 +26,63 @@
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = 16u << 20;  // 16 MiB
-constexpr int kMaxDevices = 64;
+constexpr int kMaxContexts = 64;
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 std::mutex g_scratch_mu;
-void *g_scratch_ptr[kMaxDevices] = {};
+struct Entry {
+    unsigned long long ctx_id;
+    void *ptr;
+};
+Entry g_scratch[kMaxContexts] = {};
+int g_scratch_n = 0;
 
-// Device address of the scratch array on the current device (looked up once).
-pa_status scratch_on_current_device(void **out) {
+using CtxGetCurrent = CUresult (*)(CUcontext *);
+using CtxGetId = CUresult (*)(CUcontext, unsigned long long *);
+
+template <typename F>
+F driver_fn(const char *name) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<F>(p);
+}
+
+// Unique id of the context current on this thread (0 if there is none or it
+// cannot be read).
+unsigned long long current_context_id() {
+    static CtxGetCurrent get_current = driver_fn<CtxGetCurrent>("cuCtxGetCurrent");
+    static CtxGetId get_id = driver_fn<CtxGetId>("cuCtxGetId");
+    if (!get_current || !get_id) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+    if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+// Device address of the scratch array in the current context.
+pa_status scratch_in_current_context(void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return PA_ERR_UNSUPPORTED;
+    unsigned long long id = current_context_id();
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return PA_ERR_CUDA;
-        g_scratch_ptr[dev] = p;
-    }
-    *out = g_scratch_ptr[dev];
+    if (id != 0)
+        for (int i = 0; i < g_scratch_n; ++i)
+            if (g_scratch[i].ctx_id == id) {
+                *out = g_scratch[i].ptr;
+                return PA_OK;
+            }
+    // Not seen yet (or no context bound yet: the lookup binds the device's primary
+    // context, whose id is read again afterwards).
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return PA_ERR_CUDA;
+    if (id == 0) id = current_context_id();
+    if (id != 0 && g_scratch_n < kMaxContexts) g_scratch[g_scratch_n++] = Entry{id, p};
+    *out = p;
     return PA_OK;
 }
 
@@ -58,7 +101,7 @@ pa_status pa_decode_noalloc(void *out, const void *q, const void *kv_cache, int 
         return PA_ERR_UNSUPPORTED;
     void *scratch = nullptr;
     if (num_seqs > 0) {
-        pa_status st = scratch_on_current_device(&scratch);
+        pa_status st = scratch_in_current_context(&scratch);
         if (st != PA_OK) return st;
     }
     return pa_decode(out, q, kv_cache, num_blocks, block_size, num_heads, num_kv_heads,

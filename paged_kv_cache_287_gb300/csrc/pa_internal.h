@@ -7,7 +7,30 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace pa {
+
+// Raise kernel Kern's dynamic shared-memory limit to at least `bytes` on the
+// current device.  The attribute call is made only when this (kernel, device)
+// has not yet been given that much: a launch path's per-call host cost is then
+// the launch itself.
+template <auto Kern>
+cudaError_t ensure_smem(size_t bytes) {
+    static std::atomic<int> granted[64];  // per device; zero at start
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    const bool tracked = dev >= 0 && dev < 64;
+    if (tracked && granted[dev].load(std::memory_order_acquire) >= (int)bytes) return cudaSuccess;
+    const cudaError_t e =
+        cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess && tracked) {
+        int cur = granted[dev].load(std::memory_order_relaxed);
+        while (cur < (int)bytes && !granted[dev].compare_exchange_weak(cur, (int)bytes)) {
+        }
+    }
+    return e;
+}
 
 // Geometry of the KV pool [num_blocks][2][num_kv_heads][block_size][head_size].
 struct KvGeom {
@@ -23,7 +46,9 @@ cudaError_t take_error_decode(unsigned *bits);
 cudaError_t take_error_prefill(unsigned *bits);
 
 // Encode a 2-D TMA map over the pool viewed as rows of head_size bf16 elements,
-// box = 64 elements x box_rows rows, 128-byte swizzle.  False on failure.
+// box = 64 elements x box_rows rows, 128-byte swizzle.  False on failure.  Maps
+// are kept in a small cache keyed by (pool address, geometry, element type, box),
+// so a pool used call after call is encoded once.
 bool encode_kv_map(CUtensorMap *map, const void *kv_cache, const KvGeom &g, int box_rows);
 // The same over an FP8 pool (rows of head_size bytes), box = 128 bytes x box_rows.
 bool encode_kv_map_fp8(CUtensorMap *map, const void *kv_cache, const KvGeom &g, int box_rows);
@@ -59,17 +84,21 @@ cudaError_t launch_decode(void *out, const void *q, const void *kv_cache, const 
 // the unnormalised (m, l, O) of every (sequence, query head) over those tokens.
 // kv8: an FP8 pool (head size 128), real K/V = code * k_scale / v_scale.
 int prefix_splits(int num_seqs, int num_heads, int num_kv_heads, int shared_len, int sm_count);
+// clear_cnt: the arrival counters (num_seqs * num_kv_heads) the decode launch
+// after it counts in; the prefix pass zeroes them.
 cudaError_t launch_prefix_partials(const void *q, const void *kv_cache, const KvGeom &g,
                                    int num_heads, const int32_t *block_tables,
                                    int max_blocks_per_seq, int num_seqs, int shared_len,
                                    float scale, int splits, float *part_ml, float *part_acc,
-                                   bool kv8, float k_scale, float v_scale, cudaStream_t stream);
+                                   unsigned *clear_cnt, bool kv8, float k_scale, float v_scale,
+                                   cudaStream_t stream);
 // Bytes of prefix partials for `splits` splits.
 size_t prefix_partial_bytes(int splits, int num_seqs, int num_heads, int head_size);
 // The shared-prefix decode as one launch (prefix pass and own tokens side by side
-// on disjoint SMs, one key split) plus the merge; cudaErrorNotSupported (nothing
-// launched) when the separate launches suit the shape better.  pre_ml / pre_acc:
-// room for one split's partials; whole: cascade_whole_bytes.
+// on disjoint SMs, one key split, merged by the last arrivals) after a kernel that
+// clears the arrival counters; cudaErrorNotSupported (nothing launched) when the
+// separate launches suit the shape better.  pre_ml / pre_acc: room for one
+// split's partials; whole: cascade_whole_bytes.
 cudaError_t launch_cascade_one(void *out, const void *q, const void *kv_cache, const KvGeom &g,
                                int num_heads, const int32_t *block_tables,
                                int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs,
@@ -80,11 +109,15 @@ cudaError_t launch_cascade_one(void *out, const void *q, const void *kv_cache, c
 // separate launches are used.
 int cascade_one_launch_ctas(int num_seqs, int num_heads, const KvGeom &g, int max_seq_len,
                             int shared_len, bool kv8, int sms);
-// Bytes of the per-segment records of segments one warp finishes whole.
+// Bytes of the per-segment state of a cascade: records of segments one warp
+// finishes whole, the segment table and the arrival counters (pa_merge.cuh);
+// cascade_counters: where the counters sit in it.
 size_t cascade_whole_bytes(int num_seqs, int num_kv_heads, int head_size);
-// Decode over each sequence's tokens [shared_len, seq_len); its merge kernel folds
-// in the prefix partials (pre_splits of them at pre_ml / pre_acc) before
-// normalising.  whole: cascade_whole_bytes of workspace for the whole segments.
+unsigned *cascade_counters(void *whole, int num_seqs, int num_kv_heads, int head_size);
+// Decode over each sequence's tokens [shared_len, seq_len); the contributor that
+// completes a segment merges it with the prefix partials (pre_splits of them at
+// pre_ml / pre_acc, complete before this launch).  whole: cascade_whole_bytes of
+// workspace (counters zeroed by the prefix pass).
 cudaError_t launch_decode_suffix(void *out, const void *q, const void *kv_cache, const KvGeom &g,
                                  int num_heads, const int32_t *block_tables,
                                  int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs,

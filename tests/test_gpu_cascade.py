@@ -241,3 +241,73 @@ def test_fp8_cascade_prefix_workload_full_size():
     b = make_config(5, device=DEV)
     out, want, _ = _fp8_case(b, b.shared_prefix_blocks * b.block_size)
     compare(out, want, "prefix-shared workload, FP8 cascade")
+
+
+@pytest.mark.parametrize("shape", ["whole", "one_launch"])
+@pytest.mark.parametrize("fp8", [False, True])
+def test_cascade_flags_a_diverging_shared_table(shape, fp8):
+    """The shared blocks are read through sequence 0's table; a sequence whose
+    shared entries name another block breaks the stated precondition.  The
+    kernels compare the entries and pa_error_check reports PA_ERR_PRECONDITION
+    (no fault: the other block is a valid pool block)."""
+    pb, bs = (16, 16) if shape == "whole" else (32, 16)
+    suffix = [16, 1, 7, 16, 3, 12, 9] if shape == "whole" else \
+        torch.randint(1, 4097, (48,), generator=torch.Generator().manual_seed(95)).tolist()
+    b = make_batch(name=f"cp{shape}{int(fp8)}", seq_lens=[pb * bs + x for x in suffix],
+                   q_lens=[1] * len(suffix), num_heads=32, num_kv_heads=8, head_size=128,
+                   block_size=bs, scale=128 ** -0.5, seed=96 + fp8, shared_prefix_blocks=pb,
+                   device=DEV)
+    s = len(suffix) - 2
+    b.block_tables[s, pb // 2] = b.block_tables[s, pb]   # one of its own blocks instead
+    pool = fp8_pool_of(b) if fp8 else b.kv_cache
+    out = torch.empty_like(b.q)
+    ws = torch.empty(binding.pa_decode_cascade_workspace_bytes(
+        b.num_seqs, b.num_heads, b.num_kv_heads, b.head_size, pb * bs), dtype=torch.uint8,
+        device=DEV)
+    binding.pa_decode_cascade(out, b.q, pool, b.block_tables, b.seq_lens, b.max_seq_len,
+                              pb * bs, b.scale, ws,
+                              kv_scales=(FP8_K_SCALE, FP8_V_SCALE) if fp8 else None)
+    with pytest.raises(binding.PaError) as e:
+        binding.pa_error_check()
+    assert binding.STATUS[e.value.status] == "PA_ERR_PRECONDITION"
+    # The same call on the intact tables reports nothing.
+    b.block_tables[s, pb // 2] = b.block_tables[0, pb // 2]
+    binding.pa_decode_cascade(out, b.q, pool, b.block_tables, b.seq_lens, b.max_seq_len,
+                              pb * bs, b.scale, ws,
+                              kv_scales=(FP8_K_SCALE, FP8_V_SCALE) if fp8 else None)
+    binding.pa_error_check()
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_cascade_where_the_prefix_pass_arrives_last(fp8):
+    """One long own suffix makes the host run the prefix pass beside the own
+    tokens' decode in one launch; the other 63 sequences own 1-16 tokens, which
+    the decode finishes within microseconds, long before the prefix pass over
+    2048 shared tokens ends.  So the prefix pass's arrival completes almost every
+    segment, and its CTAs do those merges (the long sequence's segments, split
+    over many decode warps, included); deterministic and equal to the oracle."""
+    pb, bs = 128, 16
+    g = torch.Generator().manual_seed(97)
+    suffix = [8192] + torch.randint(1, 17, (63,), generator=g).tolist()
+    b = make_batch(name=f"cpl{int(fp8)}", seq_lens=[pb * bs + x for x in suffix],
+                   q_lens=[1] * len(suffix), num_heads=32, num_kv_heads=8, head_size=128,
+                   block_size=bs, scale=128 ** -0.5, seed=98 + fp8, shared_prefix_blocks=pb,
+                   device=DEV)
+    if fp8:
+        out, want, pool8 = _fp8_case(b, pb * bs)
+        again = torch.full_like(b.q, float("nan"))
+        ws = torch.empty(binding.pa_decode_cascade_workspace_bytes(
+            b.num_seqs, b.num_heads, b.num_kv_heads, b.head_size, pb * bs), dtype=torch.uint8,
+            device=DEV)
+        binding.pa_decode_cascade(again, b.q, pool8, b.block_tables, b.seq_lens, b.max_seq_len,
+                                  pb * bs, b.scale, ws, kv_scales=(FP8_K_SCALE, FP8_V_SCALE))
+        binding.pa_error_check()
+    else:
+        pool = oracle_pool(b)
+        gpu_write(b)
+        out = gpu_cascade(b, pb * bs)
+        again = gpu_cascade(b, pb * bs)
+        binding.pa_error_check()
+        want = oracle_rows(b, pool)
+    assert np.array_equal(bits(out), bits(again))
+    compare(out, want, f"cascade, prefix pass last{' (FP8)' if fp8 else ''}")

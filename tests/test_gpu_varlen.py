@@ -142,3 +142,36 @@ def test_varlen_without_slot_mapping_writes_nothing():
     b.k_new.fill_(7.0)
     varlen(b, 1, write=False)
     assert np.array_equal(bits(b.kv_cache), before)
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_varlen_host_fault_leaves_the_pool_untouched(fp8):
+    """Every host check runs before the step's cache write is enqueued: with valid
+    write arguments and a misaligned cu_q_lens pointer, the call returns
+    PA_ERR_INVALID_ARG and the pool keeps every byte it had."""
+    import ctypes
+    b = make_batch(name="vs", seq_lens=[300, 40, 513, 90], q_lens=[129, 40, 1, 1],
+                   num_heads=32, num_kv_heads=8, head_size=128, block_size=16,
+                   scale=128 ** -0.5, seed=977, device=DEV)
+    pool = torch.full((b.num_blocks, 2, 8, 16, 128), 0x5A, dtype=torch.uint8, device=DEV) \
+        if fp8 else torch.full_like(b.kv_cache, 3.25)
+    before = pool.clone()
+    out = torch.zeros_like(b.q)
+    cu = b.cu_q_lens[:3].contiguous()
+    ws = torch.empty(binding.pa_attention_varlen_workspace_bytes(
+        b.num_seqs, 2, b.num_heads, b.num_kv_heads, b.head_size), dtype=torch.uint8, device=DEV)
+    L = binding.lib()
+    args = [out.data_ptr(), b.q.data_ptr(), b.k_new.data_ptr(), b.v_new.data_ptr(),
+            b.slot_mapping.data_ptr(), cu.data_ptr() + 2, b.num_seqs, 2, int(b.cu_q_lens[2]),
+            129, pool.data_ptr(), b.num_blocks, 16, 32, 8, 128, b.block_tables.data_ptr(),
+            b.block_tables.shape[1], b.seq_lens.data_ptr(), int(b.seq_lens.max()),
+            ctypes.c_float(b.scale)]
+    tail = [ws.data_ptr(), ws.numel(), torch.cuda.current_stream().cuda_stream]
+    if fp8:
+        status = L.pa_attention_varlen_fp8(*args, ctypes.c_float(1 / 64), ctypes.c_float(1 / 64),
+                                           *tail)
+    else:
+        status = L.pa_attention_varlen(*args, *tail)
+    torch.cuda.synchronize()
+    assert binding.STATUS[status] == "PA_ERR_INVALID_ARG"
+    assert torch.equal(pool.view(torch.uint8), before.view(torch.uint8))

@@ -4,20 +4,21 @@ Such callers (an engine whose KV-cache pool already holds nearly all of HBM, a
 host program that only receives device pointers, a decode loop that cannot
 afford an allocation that may synchronise the device) get the same decode with
 scratch from a fixed array inside the library.  These tests call it through the
-C ABI and check it against pa_decode with a caller-provided workspace, on two
-calls in a row, since every call reuses the same array.
+C ABI and check it against pa_decode with a caller-provided workspace, bit for
+bit, on two calls in a row, since every call reuses the same array.
 """
 
 from __future__ import annotations
 
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
 from paged_kv_cache_287_gb300 import binding
 from paged_kv_cache_287_gb300.workloads import make_batch, make_config
-from tests._gpu import compare, gpu_write, workspace_for
+from tests._gpu import bits, gpu_write, workspace_for
 
 pytestmark = pytest.mark.gpu
 
@@ -50,12 +51,36 @@ def test_noalloc_matches_workspace_decode_twice(workload):
     binding.pa_decode(ref, b.q, b.kv_cache, b.block_tables, b.seq_lens, b.max_seq_len, b.scale,
                       workspace_for(b))
     torch.cuda.synchronize()
-    ref_bits = ref.double().cpu().numpy()
+    ref_bits = bits(ref)
     for _ in range(2):
         out = torch.full_like(b.q, float("nan"))
         assert _noalloc(b, out) == 0
         binding.pa_error_check()
-        compare(out, ref_bits, "pa_decode_noalloc vs pa_decode")
+        # The same kernel, the same split of the contexts over the grid, the same
+        # inputs: only the scratch differs, so the outputs agree bit for bit (a
+        # scratch region carved one record off would not).
+        assert np.array_equal(bits(out), ref_bits), "pa_decode_noalloc differs from pa_decode"
+
+
+def test_noalloc_holds_the_largest_batch_pa_decode_accepts():
+    """The largest batch of head size 128 that pa_decode's tables hold (15 091
+    sequences, group 4): its workspace fits the 16 MiB scratch on this GPU, and the
+    call runs and agrees bit for bit with pa_decode."""
+    L = binding.lib()
+    B = 15091
+    assert L.pa_decode_workspace_bytes(B, 4, 1, 128) <= 16 << 20
+    g = torch.Generator().manual_seed(33)
+    lens = torch.randint(1, 40, (B,), generator=g).tolist()
+    b = make_batch(name="nmax", seq_lens=lens, q_lens=[1] * B, num_heads=4, num_kv_heads=1,
+                   head_size=128, block_size=16, scale=128 ** -0.5, seed=34, device=DEV)
+    gpu_write(b)
+    ref = torch.empty_like(b.q)
+    binding.pa_decode(ref, b.q, b.kv_cache, b.block_tables, b.seq_lens, b.max_seq_len, b.scale,
+                      workspace_for(b))
+    out = torch.full_like(b.q, float("nan"))
+    assert _noalloc(b, out) == 0
+    binding.pa_error_check()
+    assert np.array_equal(bits(out), bits(ref))
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
