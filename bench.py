@@ -436,10 +436,11 @@ def by_workload(args, dev, stream) -> dict:
     # 1: launch-bound tiny decode step (cache write + decode), eager and graphed.
     b = make_config(1, device=dev)
     out, ws = torch.empty_like(b.q), ws_for(b)
+    max_len = b.max_seq_len  # a host value, read once (the property syncs the device)
 
     def step1(st=stream):
         binding.pa_cache_write(b.kv_cache, b.k_new, b.v_new, b.slot_mapping, st)
-        binding.pa_decode(out, b.q, b.kv_cache, b.block_tables, b.seq_lens, b.max_seq_len,
+        binding.pa_decode(out, b.q, b.kv_cache, b.block_tables, b.seq_lens, max_len,
                           b.scale, ws, st)
 
     eager, clk = timed(step1, 3)
@@ -463,11 +464,12 @@ def by_workload(args, dev, stream) -> dict:
     for n in (2, 3):
         b = make_config(n, device=dev)
         out, ws = torch.empty_like(b.q), ws_for(b)
+        max_len = b.max_seq_len
         entry = {"workload": CONFIG_NAMES[n]}
         if n == 3:
             binding.pa_cache_write(b.kv_cache, b.k_new, b.v_new, b.slot_mapping, stream)
             ms, clk = timed(lambda: binding.pa_decode(out, b.q, b.kv_cache, b.block_tables,
-                                                      b.seq_lens, b.max_seq_len, b.scale, ws,
+                                                      b.seq_lens, max_len, b.scale, ws,
                                                       stream), 2)
             entry.update({"value": kv_read_bytes(b.seq_lens.tolist(), b.num_kv_heads,
                                                  b.head_size) / (ms / 1e3) / 1e9,
@@ -479,7 +481,7 @@ def by_workload(args, dev, stream) -> dict:
         torch.cuda.empty_cache()
         binding.pa_cache_write_fp8(pool8, b.k_new, b.v_new, b.slot_mapping, *sc, stream)
         ms, clk = timed(lambda: binding.pa_decode_fp8(out, b.q, pool8, b.block_tables,
-                                                      b.seq_lens, b.max_seq_len, b.scale, *sc,
+                                                      b.seq_lens, max_len, b.scale, *sc,
                                                       ws, stream), 2)
         entry["fp8"] = {"value": kv_read_bytes(b.seq_lens.tolist(), b.num_kv_heads,
                                                b.head_size) / 2 / (ms / 1e3) / 1e9,
@@ -541,13 +543,14 @@ def by_workload(args, dev, stream) -> dict:
     # 5: prefix-shared decode, plain and cascade (bf16 and FP8 pools), cold and warm.
     b = make_config(5, device=dev)
     shared = b.shared_prefix_blocks * b.block_size
+    max_len = b.max_seq_len
     out = torch.empty_like(b.q)
     ws = torch.empty(binding.pa_decode_cascade_workspace_bytes(
         b.num_seqs, b.num_heads, b.num_kv_heads, b.head_size, shared), dtype=torch.uint8,
         device=dev)
     binding.pa_cache_write(b.kv_cache, b.k_new, b.v_new, b.slot_mapping, stream)
     plain_ms, clk = timed(lambda: binding.pa_decode(out, b.q, b.kv_cache, b.block_tables,
-                                                    b.seq_lens, b.max_seq_len, b.scale, ws,
+                                                    b.seq_lens, max_len, b.scale, ws,
                                                     stream), 2, flushed=True)
     logical = kv_read_bytes(b.seq_lens.tolist(), b.num_kv_heads, b.head_size)
     entry = {"workload": CONFIG_NAMES[5],
@@ -559,7 +562,7 @@ def by_workload(args, dev, stream) -> dict:
     for kind, pool in (("bf16", b.kv_cache), ("fp8", pool8)):
         kw = {"kv_scales": sc} if kind == "fp8" else {}
         call = lambda: binding.pa_decode_cascade(out, b.q, pool, b.block_tables, b.seq_lens,
-                                                 b.max_seq_len, shared, b.scale, ws, stream, **kw)
+                                                 max_len, shared, b.scale, ws, stream, **kw)
         alg = cascade_algorithmic_bytes(b, shared, 1 if kind == "fp8" else 2)
         e = {}
         for timing in ("cold", "warm"):
@@ -794,9 +797,10 @@ def run_ours(args, world, rank, local):
         attn_kernels = binding.pa_decode_cascade_kernels(b.num_seqs, b.num_heads, b.num_kv_heads,
                                                          b.head_size, b.block_size, max_len,
                                                          shared, fp8)
-        kernel = (f"pa_decode_cascade{'_fp8' if fp8 else ''} (counter clear, then the "
-                  "prefix pass beside the own tokens' decode in one launch, merged by the last "
-                  "arrivals)")
+        kernel = (f"pa_decode_cascade{'_fp8' if fp8 else ''} ("
+                  + ("prefix pass beside the own tokens' decode in one launch, then the merge "
+                     "kernel" if attn_kernels == 2 else
+                     "prefix pass, own tokens' decode, merge kernel") + ")")
         traffic_file = f"cascade{'_fp8' if fp8 else ''}_{b.name}.traffic.txt"
     elif fp8:
         kernel = "pa_decode_fp8 (split-context kernel + merge kernel)"

@@ -223,12 +223,13 @@ size_t pa_decode_cascade_workspace_bytes(int num_seqs, int num_heads, int num_kv
 
 /*
  * Kernels one pa_decode_cascade call (pa_decode_cascade_fp8 when kv8 != 0) with
- * these shapes launches on the current device: 2 (a kernel that clears the
- * per-segment arrival counters, then the prefix pass and the own tokens' decode
- * side by side in one launch on disjoint SMs; or the prefix pass, then the own
- * tokens' decode: chosen from the shapes and the pool's type; or, when
- * shared_len is 0, pa_decode's two); 0 when num_seqs is 0; -1 for invalid shapes.
- * For planning only (e.g. counting a CUDA graph's nodes).
+ * these shapes launches on the current device: 2 when the shared prefix and the
+ * sequences' own tokens are attended side by side in one launch on disjoint
+ * SMs, then merged (chosen from the shapes and the pool's type), or when
+ * shared_len is 0 (pa_decode); 3 when the prefix is attended by its own launch
+ * before the own tokens and the merge; 0 when num_seqs is 0; -1 for invalid
+ * shapes.  For planning only (e.g. counting a CUDA graph's nodes): the results
+ * are the same either way, up to floating-point summation order.
  */
 int pa_decode_cascade_kernels(int num_seqs, int num_heads, int num_kv_heads, int head_size,
                               int block_size, int max_seq_len, int shared_len, int kv8);
@@ -245,8 +246,7 @@ int pa_decode_cascade_kernels(int num_seqs, int num_heads, int num_kv_heads, int
  * and a mismatch makes pa_error_check() return PA_ERR_PRECONDITION).  The prefix is attended once per
  * KV head for all queries of the batch on the tensor cores, each sequence's own
  * tokens [shared_len, seq_lens[s]) as in pa_decode, and the softmax states
- * are merged by log-sum-exp, per (sequence, KV head), by whichever part of the
- * work finishes that segment last (no separate merge launch).  The result is
+ * are merged by log-sum-exp, one warp per (sequence, KV head).  The result is
  * pa_decode's up to floating-point summation order, and the same bits on every
  * call.
  *   Arguments are those of pa_decode, plus:

@@ -357,13 +357,13 @@ int pa_decode_cascade_kernels(int num_seqs, int num_heads, int num_kv_heads, int
     if (check_heads(num_heads, num_kv_heads) != PA_OK || num_kv_heads > 255) return -1;
     if (head_size != 64 && head_size != 128) return -1;
     if (block_size != 8 && block_size != 16 && block_size != 32) return -1;
-    (void)kv8;
     if (num_seqs == 0) return 0;
-    // shared_len 0: pa_decode (split kernel, merge kernel).  Otherwise either the
-    // counter-clearing kernel and the one launch (prefix pass beside the own
-    // tokens' decode), or the prefix pass and the own tokens' decode: two either
-    // way, the merge being done by the last arrivals.
-    return 2;
+    if (shared_len == 0) return 2;  // pa_decode: split kernel and merge kernel
+    const pa::KvGeom g{1, block_size, num_kv_heads, head_size};
+    return pa::cascade_one_launch_ctas(num_seqs, num_heads, g, max_seq_len, shared_len, kv8 != 0,
+                                       pa::device_sm_count()) > 0
+               ? 2
+               : 3;
 }
 
 // pa_decode_cascade and pa_decode_cascade_fp8 (kv8: an FP8 pool, head size 128).
@@ -415,11 +415,10 @@ static pa_status cascade_impl(void *out, const void *q, const void *kv_cache, in
             max_seq_len, shared_len, scale, workspace, pre_ml, pre_acc, whole, kv8, k_scale,
             v_scale, s);
         if (one != cudaErrorNotSupported) return from_cuda(one);
-        cudaError_t e = pa::launch_prefix_partials(
-            q, kv_cache, g, num_heads, block_tables, max_blocks_per_seq, num_seqs, shared_len,
-            scale, splits, pre_ml, pre_acc,
-            pa::cascade_counters(whole, num_seqs, num_kv_heads, head_size), kv8, k_scale,
-            v_scale, s);
+        cudaError_t e = pa::launch_prefix_partials(q, kv_cache, g, num_heads, block_tables,
+                                                   max_blocks_per_seq, num_seqs, shared_len,
+                                                   scale, splits, pre_ml, pre_acc, kv8, k_scale,
+                                                   v_scale, s);
         if (e != cudaSuccess) return from_cuda(e);
     }
     return from_cuda(pa::launch_decode_suffix(out, q, kv_cache, g, num_heads, block_tables,

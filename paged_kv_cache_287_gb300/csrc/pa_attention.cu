@@ -117,22 +117,53 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
         if ((int)blockIdx.x < dec_ctas)
             decode_body<D, DW, KV8 ? kMixStagesFp8 : kMixStages, KV8>(
                 kv_map, da, blockIdx.x, da.plan ? da.plan[1] : da.total_warps);
-        return;
+    } else {
+        const unsigned v = blockIdx.x - (unsigned)dec_slots;
+        const uint3 bid = make_uint3(v % pre_grid.x, (v / pre_grid.x) % pre_grid.y,
+                                     v / (pre_grid.x * pre_grid.y));
+        prefill_body<D, KV8>(kv_map, pa, bid, pre_grid);
     }
-    const unsigned v = blockIdx.x - (unsigned)dec_slots;
-    const uint3 bid = make_uint3(v % pre_grid.x, (v / pre_grid.x) % pre_grid.y,
-                                 v / (pre_grid.x * pre_grid.y));
-    prefill_body<D, KV8>(kv_map, pa, bid, pre_grid);
+    if (da.grid_bar) {
+        // Cascade in one cooperative launch: once every CTA's records are written,
+        // every warp of the grid merges segments, one at a time.
+        if (!grid_barrier(da.grid_bar, gridDim.x) && threadIdx.x == 0)
+            atomicOr(&g_err_decode, kErrTimeout);
+        const int wpc = blockDim.x >> 5;
+        const int segs = da.num_seqs * da.num_kv_heads;
+        for (int k = blockIdx.x * wpc + (threadIdx.x >> 5); k < segs; k += gridDim.x * wpc)
+            cascade_merge_one<D, 2>(da, k);
+    }
 }
 
 // dec_slots: the grid's leading decode CTAs (with a device plan, the first
 // plan[0] of them stream and the rest exit).  cascade: a shared-prefix decode,
-// merged by the last arrivals (no merge kernel), launched as a programmatic
-// dependent of the kernel before it (which clears the arrival counters): its
-// CTAs start at once and wait for that grid only where they count.  Otherwise
-// the merge kernel follows as a plain launch.
+// whose merge kernel (a warp per segment) follows as a programmatic dependent:
+// the grid (one CTA per SM) is resident at once, and the merge CTAs take SMs as
+// this grid's CTAs leave them.  Otherwise the plain merge kernel follows as a
+// plain launch (the prefill CTAs come in waves, and early merge CTAs would hold
+// SMs they need).
+// Whether a cooperative launch of Kern with `grid` CTAs fits the current device
+// (every CTA resident at once); known once per (kernel, device).
+template <auto Kern>
+bool cooperative_fits(int grid, int threads, size_t smem) {
+    static std::atomic<int> cap_plus1[64];  // per device: CTAs that fit, plus one
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    int cap = cap_plus1[dev].load(std::memory_order_relaxed) - 1;
+    if (cap < 0) {
+        int coop = 0, per_sm = 0;
+        if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, Kern, threads, smem) !=
+                cudaSuccess)
+            return false;
+        cap = coop ? per_sm * device_sm_count() : 0;
+        cap_plus1[dev].store(cap + 1, std::memory_order_relaxed);
+    }
+    return grid <= cap;
+}
+
 template <int D, bool KV8, int DW = kDecodeWarps>
-cudaError_t launch_mixed_d(const CUtensorMap &map, const DecodeArgs &da, const PrefillArgs &pa,
+cudaError_t launch_mixed_d(const CUtensorMap &map, const DecodeArgs &da0, const PrefillArgs &pa,
                            dim3 pgrid, int dec_slots, size_t smem, cudaStream_t stream,
                            bool cascade = false) {
     auto kern = mixed_kernel<D, KV8, DW>;
@@ -140,22 +171,46 @@ cudaError_t launch_mixed_d(const CUtensorMap &map, const DecodeArgs &da, const P
     if (e != cudaSuccess) return e;
     const unsigned n_pre = pgrid.x * pgrid.y * pgrid.z;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)dec_slots + n_pre);
     cfg.blockDim = dim3(kDecodeWarps * 32);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = cascade ? 1 : 0;
+    cfg.numAttrs = 0;
+    DecodeArgs da = da0;
+    if (cascade && da.grid_bar &&
+        cooperative_fits<mixed_kernel<D, KV8, DW>>((int)cfg.gridDim.x, kDecodeWarps * 32, smem)) {
+        // The merge in the same launch, after a grid barrier on a word zeroed here.
+        e = cudaMemsetAsync(da.grid_bar, 0, sizeof(unsigned), stream);
+        if (e != cudaSuccess) return e;
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kern, map, da, pa, dec_slots,
+                               make_uint3(pgrid.x, pgrid.y, pgrid.z));
+        if (e == cudaSuccess) return e;
+        // Not placeable now (another context holds SMs): the merge as its own launch.
+        (void)cudaGetLastError();
+        cfg.numAttrs = 0;
+    }
+    da.grid_bar = nullptr;
     e = cudaLaunchKernelEx(&cfg, kern, map, da, pa, dec_slots,
                            make_uint3(pgrid.x, pgrid.y, pgrid.z));
-    if (e != cudaSuccess || cascade) return e;
+    if (e != cudaSuccess) return e;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t mcfg = {};
+    mcfg.stream = stream;
+    mcfg.attrs = attr;
+    if (cascade) {
+        mcfg.gridDim = dim3((unsigned)((da.num_seqs * da.num_kv_heads + 7) / 8));
+        mcfg.blockDim = dim3(256);
+        mcfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&mcfg, cascade_merge_kernel<D>, da);
+    }
     mcfg.gridDim = dim3((unsigned)(da.num_seqs * da.num_kv_heads));
     mcfg.blockDim = dim3((unsigned)(da.group * D / 4));
-    mcfg.stream = stream;
     return cudaLaunchKernelEx(&mcfg, decode_merge_kernel<D>, da);
 }
 
@@ -260,21 +315,23 @@ cudaError_t launch_mixed(void *out, const void *q, const int32_t *cu_q_lens, int
 
 // ----------------------------------------------------------------------------
 // Shared-prefix decode in one launch of the same kernel.  Once the prefix
-// partials are folded in by the merge kernel, the prefix pass and the own
-// tokens' decode are independent, so they run side by side: the prefix pass
-// with one key split on P SMs (its CTAs the grid's tail), the decode on the
-// other sms - P as the leading CTAs; then the merge.  Taken when the prefix
-// pass's CTAs fit in a quarter of the SMs and, by the rates below, it ends
-// before the decode would; otherwise the separate launches (the prefix pass
-// first, split over the whole GPU) are faster.
+// partials are merged by the merge kernel, the prefix pass and the own tokens'
+// decode are independent, so they run side by side: the prefix pass on P SMs
+// (its CTAs the grid's tail: row groups x KV heads x key splits), the decode on
+// the other sms - P as the leading CTAs; then the merge.  The key splits (1 to
+// 4) balance the two by the rates below; the one launch is taken when the
+// prefix CTAs fit in half the SMs and the prefix pass, so split, does not
+// outlast the decode by more than a sixth.  Otherwise the separate launches
+// (the prefix pass first, split over the whole GPU) are faster.
 namespace {
-// Rates for the choice (measured on GB300, prefix-sharing workload): a prefix
-// CTA takes about 1.8 us per 128-key tile plus 4 us to start and finish; the
-// own tokens' decode streams about 36 GB/s per SM.
-constexpr float kCascadeTileUs = 1.8f, kCascadeStartUs = 4.0f, kCascadeDecSmGBs = 36.0f;
-// FP8 pool: the prefix pass converts each tile (about 1.9 us), the decode streams
-// about 29 GB/s per SM.
-constexpr float kCascadeTileUsFp8 = 1.9f, kCascadeDecSmGBsFp8 = 29.0f;
+// Rates for the choice (measured on GB300, prefix-sharing workload, one launch
+// with the decode role keeping one tile in flight per warp): a prefix CTA takes
+// about 2.5 us per 128-key tile plus 4 us to start and finish, beside a decode
+// that keeps HBM busy; the own tokens' decode streams about 50 GB/s per SM.
+constexpr float kCascadeTileUs = 2.5f, kCascadeStartUs = 4.0f, kCascadeDecSmGBs = 50.0f;
+// FP8 pool: the prefix pass converts each tile (about 2.5 us with it), the
+// decode streams about 44 GB/s per SM.
+constexpr float kCascadeTileUsFp8 = 2.5f, kCascadeDecSmGBsFp8 = 44.0f;
 #ifndef PA_CASCADE_DEPTH
 #define PA_CASCADE_DEPTH 1
 #endif
@@ -282,23 +339,41 @@ constexpr int kCascadeDepth = PA_CASCADE_DEPTH;
 }  // namespace
 
 int cascade_one_launch_ctas(int num_seqs, int num_heads, const KvGeom &g, int max_seq_len,
-                            int shared_len, bool kv8, int sms) {
+                            int shared_len, bool kv8, int sms, int *splits) {
     if (shared_len <= 0 || num_seqs <= 0) return 0;
     const int G = num_heads / g.num_kv_heads;
     const int per_cta = kTcTiles * (kTcRows / G);
-    const long long n_pre = (long long)((num_seqs + per_cta - 1) / per_cta) * g.num_kv_heads;
-    if (mixed_decode_warps(num_seqs, num_heads, g, kv8) == 0 || n_pre > sms / 4) return 0;
-    const int dec_ctas = sms - (int)n_pre;
+    const long long groups = (long long)((num_seqs + per_cta - 1) / per_cta) * g.num_kv_heads;
+    if (mixed_decode_warps(num_seqs, num_heads, g, kv8) == 0) return 0;
     const int tiles = (shared_len + kTcKeys - 1) / kTcKeys;
+    // At most as many splits as the workspace holds prefix partials for.
+    const int room = prefix_splits(num_seqs, num_heads, g.num_kv_heads, shared_len, sms);
     // Own tokens: about half the longest suffix per sequence on average.
     const double own_bytes = (double)num_seqs * g.num_kv_heads *
                              (0.5 * std::max(max_seq_len - shared_len, 0)) * 2.0 *
                              g.head_size * (kv8 ? 1 : 2);
-    const double dec_us =
-        own_bytes / (dec_ctas * (double)(kv8 ? kCascadeDecSmGBsFp8 : kCascadeDecSmGBs) * 1e3);
-    return tiles * (kv8 ? kCascadeTileUsFp8 : kCascadeTileUs) + kCascadeStartUs <= dec_us
-               ? dec_ctas
-               : 0;
+    const double tile_us = kv8 ? kCascadeTileUsFp8 : kCascadeTileUs;
+    const double sm_gbs = kv8 ? kCascadeDecSmGBsFp8 : kCascadeDecSmGBs;
+    int best_p = 0;
+    double best_t = 0.0, best_pre = 0.0, best_dec = 0.0;
+    for (int p = 1; p <= std::min(4, std::min(room, tiles)); ++p) {
+        // Every split must hold keys (the merge reads one partial per split).
+        if ((tiles + (tiles + p - 1) / p - 1) / ((tiles + p - 1) / p) != p) continue;
+        const long long n_pre = groups * p;
+        if (n_pre > sms / 2) break;
+        const double pre_us = (double)((tiles + p - 1) / p) * tile_us + kCascadeStartUs;
+        const double dec_us = own_bytes / ((double)(sms - n_pre) * sm_gbs * 1e3);
+        const double t = std::max(pre_us, dec_us);
+        if (best_p == 0 || t < best_t) {
+            best_p = p;
+            best_t = t;
+            best_pre = pre_us;
+            best_dec = dec_us;
+        }
+    }
+    if (best_p == 0 || best_pre > best_dec * 7.0 / 6.0) return 0;
+    if (splits) *splits = best_p;
+    return sms - (int)(groups * best_p);
 }
 
 cudaError_t launch_cascade_one(void *out, const void *q, const void *kv_cache, const KvGeom &g,
@@ -309,8 +384,9 @@ cudaError_t launch_cascade_one(void *out, const void *q, const void *kv_cache, c
                                float k_scale, float v_scale, cudaStream_t stream) {
     const int sms = device_sm_count();
     const int D = g.head_size, G = num_heads / g.num_kv_heads;
-    const int dec_ctas =
-        cascade_one_launch_ctas(num_seqs, num_heads, g, max_seq_len, shared_len, kv8, sms);
+    int splits = 1;
+    const int dec_ctas = cascade_one_launch_ctas(num_seqs, num_heads, g, max_seq_len, shared_len,
+                                                 kv8, sms, &splits);
     if (dec_ctas == 0) return cudaErrorNotSupported;
     const int dw = mixed_decode_warps(num_seqs, num_heads, g, kv8);
     const int q_tile = kTcRows / G, per_cta = kTcTiles * q_tile;
@@ -327,8 +403,12 @@ cudaError_t launch_cascade_one(void *out, const void *q, const void *kv_cache, c
     da.k_scale = kv8 ? k_scale : 1.f;
     da.v_scale = kv8 ? v_scale : 1.f;
     da.shared_len = shared_len;
-    // One prefix split, which counts as an arrival (it runs in this launch).
-    set_cascade(da, D, whole, pre_ml, pre_acc, 1, 1);
+    set_cascade(da, whole, pre_ml, pre_acc, splits);
+    // The grid barrier's word: after the per-segment records.
+    const size_t segs = (size_t)num_seqs * g.num_kv_heads;
+    da.grid_bar = reinterpret_cast<unsigned *>(static_cast<uint8_t *>(whole) +
+                                               align_up(segs * kHeadsPad * 2 * 4, 256) +
+                                               align_up(segs * kHeadsPad * (size_t)D * 4, 256));
     // Most SMs stream the own tokens, so one tile in flight per warp (two from an
     // FP8 pool, half the bytes) saturates HBM; more only lengthens the queueing
     // of the prefix pass's loads beside them.
@@ -353,22 +433,12 @@ cudaError_t launch_cascade_one(void *out, const void *q, const void *kv_cache, c
     pa.part_ml = pre_ml;
     pa.part_acc = pre_acc;
     pa.shared_len = shared_len;
-    pa.split_tiles = tiles;
+    pa.split_tiles = (tiles + splits - 1) / splits;
     pa.prefix_rows = num_seqs;
     pa.k_scale = da.k_scale;
     pa.v_scale = da.v_scale;
-    pa.cs = da.cs;
-    pa.seq_lens = seq_lens;  // rows of sequences with no own tokens are written directly
-    pa.clear_cnt = nullptr;
-    pa.clear_n = 0;
-    const dim3 pgrid((unsigned)((num_seqs + per_cta - 1) / per_cta), (unsigned)g.num_kv_heads, 1);
-    // The arrival counters start at zero: cleared by a one-CTA kernel, of which the
-    // attention launch is a programmatic dependent.
-    const int segs = num_seqs * g.num_kv_heads;
-    cascade_clear_kernel<<<std::min((segs + 255) / 256, 8), 256, 0, stream>>>(da.cs.seg_cnt,
-                                                                             segs);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    const dim3 pgrid((unsigned)((num_seqs + per_cta - 1) / per_cta), (unsigned)g.num_kv_heads,
+                     (unsigned)splits);
     if (kv8)
         return launch_mixed_d<128, true>(map, da, pa, pgrid, dec_ctas, TcLay<128>::kSmem, stream,
                                          true);

@@ -10,10 +10,9 @@
 //     list is cut into equal contiguous ranges, one per warp of a persistent grid
 //     (152 SMs x W warps), so skewed lengths cost nothing in balance.  A
 //     (sequence, head) segment that falls across ranges is finished in pieces whose
-//     (max, sum, acc) states are merged by log-sum-exp in a second small kernel.
-//     For a shared-prefix batch every piece instead counts its arrival, and the
-//     contributor that completes a segment merges it with the prefix pass's
-//     partials (pa_merge.cuh): no second kernel, and no warp waits on another.
+//     (max, sum, acc) states are merged by log-sum-exp in a second small kernel;
+//     for a shared-prefix batch that kernel merges every segment with the prefix
+//     pass's partials, one warp per segment (pa_merge.cuh).
 //   * Every warp runs its own pipeline: lane 0 issues 128B-swizzled 2-D TMA
 //     copies of the K and V tiles named by the block table into an S-stage ring in
 //     shared memory (plus the segment's G query rows with a bulk copy); the warp
@@ -91,13 +90,15 @@ struct DecodeArgs {
     // Cascade (cs.pre_splits > 0): each sequence's tokens [0, shared_len) are
     // attended by the prefix pass; this kernel covers tokens [shared_len,
     // seq_len).  Every piece of a segment (a segment one warp finishes whole
-    // included) leaves its (m, l, acc) record and counts its arrival; the last
-    // contributor merges (pa_merge.cuh).
+    // included) leaves its (m, l, acc) record for the cascade merge kernel.
     int shared_len;
     CascadeState cs;
     // Mixed-batch launch: the number of decode CTAs and their total warps were
     // chosen on the device; plan = {ctas, total_warps} (nullptr otherwise).
     const int *plan;
+    // Cascade in one cooperative launch: a zeroed word for the grid barrier after
+    // which every warp of the grid merges segments (nullptr: the merge kernel).
+    unsigned *grid_bar;
     // Tiles a warp keeps in flight, at most the ring's stages (0: all of them).
     // Fewer than the ring holds when enough SMs stream that HBM is saturated
     // anyway: the bytes in flight then only lengthen every request's queueing,
@@ -207,73 +208,8 @@ __device__ __forceinline__ void decode_body(const CUtensorMap &kv_map, const Dec
                 atomicOr(&g_err_decode, kErrPrecondition);
         }
     };
-    // (sequence, KV head) segment of flattened tile x.
-    auto seg_of = [&](int x) {
-        int lo = 0, hi = B - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (Hkv * s_pre[mid] <= x) lo = mid; else hi = mid - 1;
-        }
-        const int nt = s_pre[lo + 1] - s_pre[lo];
-        return lo * Hkv + (x - Hkv * s_pre[lo]) / nt;
-    };
-    // Cascade, after this warp's last tile (its records are written; nothing of
-    // the streaming loop is live any more).  Its tiles cover the segments sf..sl;
-    // one lane per segment counts this warp's arrival there (the warp holding a
-    // segment's first tile also publishes where its first record is and how many
-    // pieces there are), and the warp merges every segment its arrival completed.
-    // With the prefix partials complete before this launch, the segments of
-    // sequences with no own tokens get no decode piece: the warps merge those from
-    // the prefix partials alone, one sequence each in turn.  (When the prefix pass
-    // runs in the same launch, it writes those rows itself.)
-    auto finish = [&]() {
-        if (a.cs.pre_splits == 0) return;
-        if (n > 0) {
-            const int sf = seg_of(t_begin), sl = seg_of(t_end - 1);
-            for (int base = sf; base <= sl; base += 32) {
-                const int sx = base + lane;
-                unsigned add = 0;
-                int s_ = 0, h_ = 0;
-                if (sx <= sl) {
-                    s_ = sx / Hkv;
-                    h_ = sx - s_ * Hkv;
-                    const int nt = s_pre[s_ + 1] - s_pre[s_];
-                    if (nt > 0) {
-                        const long long S0 = (long long)Hkv * s_pre[s_] + (long long)h_ * nt;
-                        const long long g0 = ((S0 + 1) * NWe - 1) / T;
-                        const long long g1 = ((S0 + nt) * NWe - 1) / T;
-                        const int n_dec = (int)(g1 - g0 + 1);
-                        if (g0 == g) {
-                            const int rec = n_dec == 1 ? -1 : (int)(g * 2 + (sx == sf ? 0 : 1));
-                            a.cs.seg_info[sx] = make_int2(rec, n_dec);
-                            add = kArrivalsDone - (unsigned)n_dec -
-                                  (unsigned)a.cs.prefix_arrives + 1u;
-                        } else {
-                            add = 1u;
-                        }
-                    }
-                }
-                __syncwarp();
-                const bool last = add != 0u && arrive(a.cs.seg_cnt + sx, add);
-                unsigned todo = __ballot_sync(0xffffffffu, last);
-                while (todo) {
-                    const int k = __ffs(todo) - 1;
-                    todo &= todo - 1;
-                    const int sk = __shfl_sync(0xffffffffu, s_, k);
-                    const int hk = __shfl_sync(0xffffffffu, h_, k);
-                    const int2 info = __ldcg(a.cs.seg_info + (size_t)sk * Hkv + hk);
-                    merge_segment<D>(a.cs, sk, hk, info.y, info.x);
-                }
-            }
-        }
-        if (!a.cs.prefix_arrives)
-            for (long long x = g; x < B; x += NW)
-                if (s_len[x] == 0)
-                    for (int hh = 0; hh < Hkv; ++hh) merge_segment<D>(a.cs, (int)x, hh, 0, 0);
-    };
     if (n <= 0) {
         check_shared_tables();
-        finish();
         return;
     }
 
@@ -688,7 +624,6 @@ __device__ __forceinline__ void decode_body(const CUtensorMap &kv_map, const Dec
             make_desc(cur_batch + 1, dB0, dB1, dB2, dB3);
         }
     }
-    finish();
 }
 
 template <int D, int W, int S, bool KV8>
@@ -725,20 +660,21 @@ __global__ void __launch_bounds__(kHeadsPad * D / 4) decode_merge_kernel(const D
     const long long NWe = NW < T ? NW : T;
     const long long S0 = (long long)Hkv * pre + (long long)h * nt;
     const long long S1 = S0 + nt;
-    const long long g0 = ((S0 + 1) * NWe - 1) / T;
-    const long long g1 = (S1 * NWe - 1) / T;
+    const long long g0 = div_floor_small((S0 + 1) * NWe - 1, T);
+    const long long g1 = div_floor_small(S1 * NWe - 1, T);
     if (g0 == g1) return;  // written whole by that warp
     // Warp gw covers tiles [floor(gw*T/NWe), floor((gw+1)*T/NWe)); its record of
     // this segment is its first (slot 0) unless it began in an earlier segment.
+    const int slot0 = g0 * T < S0 * NWe ? 1 : 0;  // floor(g0 T / NWe) < S0
     float M = -INFINITY;
     for (long long gw = g0; gw <= g1; ++gw) {
-        const size_t rec = (size_t)gw * 2 + (gw == g0 && (g0 * T) / NWe < S0 ? 1 : 0);
+        const size_t rec = (size_t)gw * 2 + (gw == g0 ? slot0 : 0);
         M = fmaxf(M, a.part_ml[(rec * kHeadsPad + hh) * 2]);
     }
     float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
     float den = 0.f;
     for (long long gw = g0; gw <= g1; ++gw) {
-        const size_t rec = (size_t)gw * 2 + (gw == g0 && (g0 * T) / NWe < S0 ? 1 : 0);
+        const size_t rec = (size_t)gw * 2 + (gw == g0 ? slot0 : 0);
         const float2 ml = reinterpret_cast<const float2 *>(a.part_ml)[rec * kHeadsPad + hh];
         const float4 v =
             reinterpret_cast<const float4 *>(a.part_acc + (rec * kHeadsPad + hh) * D)[d4];
@@ -753,6 +689,42 @@ __global__ void __launch_bounds__(kHeadsPad * D / 4) decode_merge_kernel(const D
     orow[d4] = make_uint2(pack_bf16(num.x * inv, num.y * inv), pack_bf16(num.z * inv, num.w * inv));
 }
 
+// Cascade: merge segment k (sequence, KV head) from its decode records and the
+// prefix pass's partials (pa_merge.cuh); a whole warp.  Segments of sequences
+// with no own tokens have no decode record.
+template <int D, int RG>
+__device__ __forceinline__ void cascade_merge_one(const DecodeArgs &a, int k) {
+    const int Hkv = a.num_kv_heads;
+    const int s = k / Hkv, h = k - s * Hkv;
+    const int pre = a.prefix[s];
+    const int nt = a.prefix[s + 1] - pre;
+    int n_dec = 0, rec0 = -1;
+    if (nt > 0) {
+        // Pieces g0..g1 under the split kernel's partition (the first min(NW, T)
+        // warps, equal shares); warp g0's record of this segment is its first
+        // unless the warp began in an earlier segment.
+        const long long NW = a.plan ? a.plan[1] : a.total_warps;
+        const long long T = (long long)a.prefix[a.num_seqs] * Hkv;
+        const long long NWe = NW < T ? NW : T;
+        const long long S0 = (long long)Hkv * pre + (long long)h * nt;
+        const long long g0 = div_floor_small((S0 + 1) * NWe - 1, T);
+        const long long g1 = div_floor_small((S0 + nt) * NWe - 1, T);
+        n_dec = (int)(g1 - g0 + 1);
+        rec0 = (int)(g0 * 2 + (g0 * T < S0 * NWe ? 1 : 0));  // floor(g0 T / NWe) < S0
+    }
+    merge_segment<D, RG>(a.cs, s, h, n_dec, rec0);
+}
+
+// The cascade's merge as its own launch, one warp per segment; launched as a
+// programmatic dependent of the kernel that wrote the records: it waits for that
+// grid's completion before reading anything.
+template <int D>
+__global__ void __launch_bounds__(256) cascade_merge_kernel(const DecodeArgs a) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int k = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (k < a.num_seqs * a.num_kv_heads) cascade_merge_one<D, 4>(a, k);
+}
+
 template <int D, bool KV8>
 cudaError_t launch_decode_d(const DecodeArgs &a0, const CUtensorMap &map, int grid,
                             cudaStream_t stream) {
@@ -764,7 +736,6 @@ cudaError_t launch_decode_d(const DecodeArgs &a0, const CUtensorMap &map, int gr
     kern<<<grid, kDecodeWarps * 32, smem, stream>>>(map, a0);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    if (a0.cs.pre_splits > 0) return cudaSuccess;  // cascade: merged by the last arrivals
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(a0.num_seqs * a0.num_kv_heads));
     cfg.blockDim = dim3((unsigned)(a0.group * D / 4));
@@ -775,6 +746,11 @@ cudaError_t launch_decode_d(const DecodeArgs &a0, const CUtensorMap &map, int gr
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (a0.cs.pre_splits > 0) {
+        cfg.gridDim = dim3((unsigned)((a0.num_seqs * a0.num_kv_heads + 7) / 8));
+        cfg.blockDim = dim3(256);
+        return cudaLaunchKernelEx(&cfg, cascade_merge_kernel<D>, a0);
+    }
     return cudaLaunchKernelEx(&cfg, decode_merge_kernel<D>, a0);
 }
 
@@ -846,27 +822,21 @@ DecodeArgs make_decode_args(void *out, const void *q, const KvGeom &g, int num_h
     a.cs.group = a.group;
     a.plan = nullptr;
     a.depth = 0;
+    a.grid_bar = nullptr;
     return a;
 }
 
-// Point a's cascade state at the per-segment records, segment table and
-// counters laid out as cascade_whole_bytes lays them out, and at the prefix
-// partials.
-void set_cascade(DecodeArgs &a, int head_size, void *whole, const float *pre_ml,
-                 const float *pre_acc, int pre_splits, int prefix_arrives) {
+// Point a's cascade state at the per-segment records (as cascade_whole_bytes
+// lays them out) and at the prefix partials.
+void set_cascade(DecodeArgs &a, void *whole, const float *pre_ml, const float *pre_acc,
+                 int pre_splits) {
     const size_t segs = (size_t)a.num_seqs * a.num_kv_heads;
     uint8_t *w = static_cast<uint8_t *>(whole);
     a.cs.whole_ml = reinterpret_cast<float *>(w);
-    w += align_up(segs * kHeadsPad * 2 * 4, 256);
-    a.cs.whole_acc = reinterpret_cast<float *>(w);
-    w += align_up(segs * kHeadsPad * (size_t)head_size * 4, 256);
-    a.cs.seg_info = reinterpret_cast<int2 *>(w);
-    w += align_up(segs * sizeof(int2), 256);
-    a.cs.seg_cnt = reinterpret_cast<unsigned *>(w);
+    a.cs.whole_acc = reinterpret_cast<float *>(w + align_up(segs * kHeadsPad * 2 * 4, 256));
     a.cs.pre_ml = pre_ml;
     a.cs.pre_acc = pre_acc;
     a.cs.pre_splits = pre_splits;
-    a.cs.prefix_arrives = prefix_arrives;
 }
 
 cudaError_t launch_decode_impl(void *out, const void *q, const void *kv_cache, const KvGeom &g,
@@ -894,9 +864,7 @@ cudaError_t launch_decode_impl(void *out, const void *q, const void *kv_cache, c
     a.k_scale = k_scale;
     a.v_scale = v_scale;
     a.shared_len = shared_len;
-    // Cascade: the prefix partials are complete before this launch (the prefix
-    // pass ran first and cleared the arrival counters).
-    if (whole) set_cascade(a, D, whole, pre_ml, pre_acc, pre_splits, 0);
+    if (whole) set_cascade(a, whole, pre_ml, pre_acc, pre_splits);
     if (kv8) return launch_decode_d<128, true>(a, map, (int)ctas, stream);
     if (D == 128) return launch_decode_d<128, false>(a, map, (int)ctas, stream);
     return launch_decode_d<64, false>(a, map, (int)ctas, stream);
@@ -945,16 +913,7 @@ size_t prefix_partial_bytes(int splits, int num_seqs, int num_heads, int head_si
 size_t cascade_whole_bytes(int num_seqs, int num_kv_heads, int head_size) {
     const size_t segs = (size_t)num_seqs * num_kv_heads;
     return align_up(segs * kHeadsPad * 2 * 4, 256) +
-           align_up(segs * kHeadsPad * (size_t)head_size * 4, 256) +
-           align_up(segs * sizeof(int2), 256) + align_up(segs * sizeof(unsigned), 256);
-}
-
-unsigned *cascade_counters(void *whole, int num_seqs, int num_kv_heads, int head_size) {
-    const size_t segs = (size_t)num_seqs * num_kv_heads;
-    return reinterpret_cast<unsigned *>(
-        static_cast<uint8_t *>(whole) + align_up(segs * kHeadsPad * 2 * 4, 256) +
-        align_up(segs * kHeadsPad * (size_t)head_size * 4, 256) +
-        align_up(segs * sizeof(int2), 256));
+           align_up(segs * kHeadsPad * (size_t)head_size * 4, 256) + 256;  // + barrier word
 }
 
 }  // namespace pa

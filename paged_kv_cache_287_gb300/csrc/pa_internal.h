@@ -84,21 +84,18 @@ cudaError_t launch_decode(void *out, const void *q, const void *kv_cache, const 
 // the unnormalised (m, l, O) of every (sequence, query head) over those tokens.
 // kv8: an FP8 pool (head size 128), real K/V = code * k_scale / v_scale.
 int prefix_splits(int num_seqs, int num_heads, int num_kv_heads, int shared_len, int sm_count);
-// clear_cnt: the arrival counters (num_seqs * num_kv_heads) the decode launch
-// after it counts in; the prefix pass zeroes them.
 cudaError_t launch_prefix_partials(const void *q, const void *kv_cache, const KvGeom &g,
                                    int num_heads, const int32_t *block_tables,
                                    int max_blocks_per_seq, int num_seqs, int shared_len,
                                    float scale, int splits, float *part_ml, float *part_acc,
-                                   unsigned *clear_cnt, bool kv8, float k_scale, float v_scale,
-                                   cudaStream_t stream);
+                                   bool kv8, float k_scale, float v_scale, cudaStream_t stream);
 // Bytes of prefix partials for `splits` splits.
 size_t prefix_partial_bytes(int splits, int num_seqs, int num_heads, int head_size);
 // The shared-prefix decode as one launch (prefix pass and own tokens side by side
-// on disjoint SMs, one key split, merged by the last arrivals) after a kernel that
-// clears the arrival counters; cudaErrorNotSupported (nothing launched) when the
-// separate launches suit the shape better.  pre_ml / pre_acc: room for one
-// split's partials; whole: cascade_whole_bytes.
+// on disjoint SMs, one key split) plus the cascade merge kernel;
+// cudaErrorNotSupported (nothing launched) when the separate launches suit the
+// shape better.  pre_ml / pre_acc: room for one split's partials; whole:
+// cascade_whole_bytes.
 cudaError_t launch_cascade_one(void *out, const void *q, const void *kv_cache, const KvGeom &g,
                                int num_heads, const int32_t *block_tables,
                                int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs,
@@ -106,18 +103,14 @@ cudaError_t launch_cascade_one(void *out, const void *q, const void *kv_cache, c
                                float *pre_ml, float *pre_acc, void *whole, bool kv8,
                                float k_scale, float v_scale, cudaStream_t stream);
 // Decode CTAs of that one launch for these shapes on `sms` SMs, or 0 when the
-// separate launches are used.
+// separate launches are used; *splits (if given): its prefix key splits.
 int cascade_one_launch_ctas(int num_seqs, int num_heads, const KvGeom &g, int max_seq_len,
-                            int shared_len, bool kv8, int sms);
-// Bytes of the per-segment state of a cascade: records of segments one warp
-// finishes whole, the segment table and the arrival counters (pa_merge.cuh);
-// cascade_counters: where the counters sit in it.
+                            int shared_len, bool kv8, int sms, int *splits = nullptr);
+// Bytes of the per-segment records of segments one decode warp finishes whole.
 size_t cascade_whole_bytes(int num_seqs, int num_kv_heads, int head_size);
-unsigned *cascade_counters(void *whole, int num_seqs, int num_kv_heads, int head_size);
-// Decode over each sequence's tokens [shared_len, seq_len); the contributor that
-// completes a segment merges it with the prefix partials (pre_splits of them at
-// pre_ml / pre_acc, complete before this launch).  whole: cascade_whole_bytes of
-// workspace (counters zeroed by the prefix pass).
+// Decode over each sequence's tokens [shared_len, seq_len), then the cascade
+// merge kernel, which merges every segment with the prefix partials (pre_splits
+// of them at pre_ml / pre_acc).  whole: cascade_whole_bytes of workspace.
 cudaError_t launch_decode_suffix(void *out, const void *q, const void *kv_cache, const KvGeom &g,
                                  int num_heads, const int32_t *block_tables,
                                  int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs,

@@ -38,7 +38,6 @@
 
 #include "pa_common.cuh"
 #include "pa_internal.h"
-#include "pa_merge.cuh"
 
 namespace pa {
 namespace {
@@ -84,15 +83,6 @@ struct PrefillArgs {
     float *part_acc;   // [splits][num_seqs][num_heads][D]
     int shared_len, split_tiles, prefix_rows;  // prefix_rows: the batch's sequences
     float k_scale, v_scale;  // FP8 pool: real K/V = e4m3 value * scale (1 for bf16)
-    // Shared-prefix mode beside the decode in one launch (cs.prefix_arrives): each
-    // (sequence, KV head) counts its arrival after its partials are written, and
-    // the merge is done here when that completes the segment; a sequence with no
-    // own tokens gets its output rows written directly (seq_lens then holds the
-    // batch's lengths).  clear_cnt: arrival counters this grid's first CTA zeroes
-    // (prefix pass before the decode launch), or nullptr.
-    CascadeState cs;
-    unsigned *clear_cnt;
-    int clear_n;
 };
 
 template <int D>
@@ -159,8 +149,6 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &kv_map, const Pr
     __shared__ int s_ctx[kRankMax];
     __shared__ int s_pick;
     const bool prefix = a.part_ml != nullptr;
-    if (prefix && a.clear_cnt && bid.x == 0 && bid.y == 0 && bid.z == 0)
-        for (int i = threadIdx.x; i < a.clear_n; i += blockDim.x) a.clear_cnt[i] = 0u;
     int s = prefix ? 0 : (int)bid.z;
     const int nchunks = grid.z;
     if (!prefix && nchunks <= kRankMax) {
@@ -630,15 +618,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &kv_map, const Pr
             if (lane == 0) atomicOr(&g_err_prefill, kErrTimeout);
         } else {
             tc_fence_after();
-            // Shared-prefix mode in one launch: a sequence with no own tokens has
-            // no other contributor, so its rows are final here.
-            bool direct = false;
-            if (prefix && a.cs.prefix_arrives && real) {
-                const int max_len = a.max_blocks * a.block_size;
-                const int ls = a.seq_lens[t0 + tok];
-                direct = ls <= a.shared_len || a.shared_len >= max_len;
-            }
-            if (prefix && !direct) {
+            if (prefix) {
                 // Unnormalised partial of this (split, sequence, query head); an
                 // FP8 pool's v_scale is applied here, as the decode applies it to
                 // the pieces it merges with.
@@ -661,9 +641,8 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &kv_map, const Pr
                 if (real) reinterpret_cast<float2 *>(a.part_ml)[rec] = make_float2(m, l);
             } else {
             const float inv = (KV8 ? a.v_scale : 1.f) / l;
-            __nv_bfloat16 *obase = prefix ? a.cs.out : a.out;
             uint4 *dst = reinterpret_cast<uint4 *>(
-                obase + ((size_t)(q0 + t0 + tok) * a.num_heads + (size_t)h * G + gq) * D);
+                a.out + ((size_t)(q0 + t0 + tok) * a.num_heads + (size_t)h * G + gq) * D);
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 float o[32];
@@ -679,34 +658,6 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &kv_map, const Pr
                             pack_bf16(o[8 * e + 6] * inv, o[8 * e + 7] * inv));
                 }
             }
-            }
-        }
-        if (prefix && a.cs.prefix_arrives) {
-            // Count this tile's segments with own tokens: once the warpgroup's rows
-            // are all written (named barrier), the thread of each segment's first
-            // query head arrives; segments this completes are merged by the
-            // warpgroup's warps, one segment per warp in turn.
-            __shared__ uint8_t s_last[kTcTiles][kTcRows];
-            const int wg_bar = 1 + t;
-            asm volatile("bar.sync %0, 128;" ::"r"(wg_bar) : "memory");
-            const int lt = row / G;  // this row's token (sequence) in the tile
-            if (row < QT * G && gq == 0) {
-                bool last = false;
-                if (ok && real) {
-                    const int max_len = a.max_blocks * a.block_size;
-                    const int ls = a.seq_lens[t0 + tok];
-                    if (ls > a.shared_len && a.shared_len < max_len)
-                        last = arrive(a.cs.seg_cnt + (size_t)(t0 + tok) * a.num_kv_heads + h, 1u);
-                }
-                s_last[t][lt] = last ? 1 : 0;
-            }
-            asm volatile("bar.sync %0, 128;" ::"r"(wg_bar) : "memory");
-            for (int k = warp & 3; k < QT; k += 4) {
-                if (!s_last[t][k]) continue;
-                const int sq = t0 + t * QT + k;
-                const size_t seg = (size_t)sq * a.num_kv_heads + h;
-                const int2 info = __ldcg(a.cs.seg_info + seg);
-                merge_segment<D>(a.cs, sq, h, info.y, info.x);
             }
         }
     }
@@ -773,9 +724,6 @@ PrefillArgs make_prefill_args(void *out, const void *q, const int32_t *cu_q_lens
     a.part_acc = nullptr;
     a.shared_len = a.split_tiles = a.prefix_rows = 0;
     a.k_scale = a.v_scale = 1.f;
-    a.cs = CascadeState{};
-    a.clear_cnt = nullptr;
-    a.clear_n = 0;
     const int per_cta = kTcTiles * a.q_tile;
     *grid = dim3((unsigned)((max_q_len + per_cta - 1) / per_cta), (unsigned)g.num_kv_heads,
                  (unsigned)num_chunks);
@@ -833,8 +781,7 @@ cudaError_t launch_prefix_partials(const void *q, const void *kv_cache, const Kv
                                    int num_heads, const int32_t *block_tables,
                                    int max_blocks_per_seq, int num_seqs, int shared_len,
                                    float scale, int splits, float *part_ml, float *part_acc,
-                                   unsigned *clear_cnt, bool kv8, float k_scale, float v_scale,
-                                   cudaStream_t stream) {
+                                   bool kv8, float k_scale, float v_scale, cudaStream_t stream) {
     CUtensorMap map;
     const int box_rows = g.block_size >= 16 ? 16 : g.block_size;
     if (kv8 ? (g.head_size != 128 || !encode_kv_map_fp8(&map, kv_cache, g, box_rows))
@@ -863,10 +810,6 @@ cudaError_t launch_prefix_partials(const void *q, const void *kv_cache, const Kv
     a.prefix_rows = num_seqs;
     a.k_scale = kv8 ? k_scale : 1.f;
     a.v_scale = kv8 ? v_scale : 1.f;
-    a.cs = CascadeState{};
-    // The decode launch that follows counts arrivals per (sequence, KV head).
-    a.clear_cnt = clear_cnt;
-    a.clear_n = num_seqs * g.num_kv_heads;
     const int per_cta = kTcTiles * a.q_tile;
     dim3 grid((unsigned)((num_seqs + per_cta - 1) / per_cta), (unsigned)g.num_kv_heads,
               (unsigned)splits);

@@ -132,8 +132,8 @@ def test_cascade_kernel_count_query(lib):
     q = lib.pa_decode_cascade_kernels
     assert q(0, 32, 8, 128, 16, 64, 32, 0) == 0            # no sequences: nothing launched
     assert q(5, 32, 8, 128, 16, 64, 0, 0) == 2             # no shared tokens: pa_decode
-    assert q(5, 32, 8, 128, 16, 64, 32, 0) == 2            # either path: two kernels
-    assert q(5, 32, 8, 128, 16, 64, 32, 1) == 2            # FP8 pool: the same
+    assert q(5, 32, 8, 128, 16, 64, 32, 0) in (2, 3)       # depends on the device's SMs
+    assert q(5, 32, 8, 128, 16, 64, 32, 1) in (2, 3)       # FP8 pool: the same choice
     assert q(5, 32, 8, 128, 16, 64, 65, 0) == -1           # shared_len beyond max_seq_len
     assert q(5, 30, 8, 128, 16, 64, 32, 0) == -1           # heads not a multiple
     assert q(5, 32, 8, 96, 16, 64, 32, 0) == -1            # head size

@@ -311,3 +311,30 @@ def test_cascade_where_the_prefix_pass_arrives_last(fp8):
         want = oracle_rows(b, pool)
     assert np.array_equal(bits(out), bits(again))
     compare(out, want, f"cascade, prefix pass last{' (FP8)' if fp8 else ''}")
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_cascade_with_the_prefix_keys_split_in_the_one_launch(fp8):
+    """A 4096-token shared prefix and own suffixes of up to 1024 tokens (2048 from
+    an FP8 pool, whose decode streams half the bytes), Llama-3-70B heads: the host
+    balances the long prefix pass against the own tokens' decode by splitting the
+    prefix keys over two CTAs per row group in the one launch, so every segment
+    merges two prefix partials with its decode pieces."""
+    pb, bs = 256, 16
+    g = torch.Generator().manual_seed(99)
+    suffix = torch.randint(64, 2049 if fp8 else 1025, (128,), generator=g).tolist()
+    b = make_batch(name=f"cs{int(fp8)}", seq_lens=[pb * bs + x for x in suffix],
+                   q_lens=[1] * len(suffix), num_heads=64, num_kv_heads=8, head_size=128,
+                   block_size=bs, scale=128 ** -0.5, seed=100 + fp8, shared_prefix_blocks=pb,
+                   device=DEV)
+    assert binding.lib().pa_decode_cascade_kernels(b.num_seqs, 64, 8, 128, bs, b.max_seq_len,
+                                                   pb * bs, int(fp8)) == 2
+    if fp8:
+        out, want, _ = _fp8_case(b, pb * bs)
+    else:
+        pool = oracle_pool(b)
+        gpu_write(b)
+        out = gpu_cascade(b, pb * bs)
+        binding.pa_error_check()
+        want = oracle_rows(b, pool)
+    compare(out, want, f"cascade, split prefix keys{' (FP8)' if fp8 else ''}")
