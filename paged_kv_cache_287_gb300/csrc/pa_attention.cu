@@ -123,16 +123,6 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
                                      v / (pre_grid.x * pre_grid.y));
         prefill_body<D, KV8>(kv_map, pa, bid, pre_grid);
     }
-    if (da.grid_bar) {
-        // Cascade in one cooperative launch: once every CTA's records are written,
-        // every warp of the grid merges segments, one at a time.
-        if (!grid_barrier(da.grid_bar, gridDim.x) && threadIdx.x == 0)
-            atomicOr(&g_err_decode, kErrTimeout);
-        const int wpc = blockDim.x >> 5;
-        const int segs = da.num_seqs * da.num_kv_heads;
-        for (int k = blockIdx.x * wpc + (threadIdx.x >> 5); k < segs; k += gridDim.x * wpc)
-            cascade_merge_one<D, 2>(da, k);
-    }
 }
 
 // dec_slots: the grid's leading decode CTAs (with a device plan, the first
@@ -142,28 +132,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
 // this grid's CTAs leave them.  Otherwise the plain merge kernel follows as a
 // plain launch (the prefill CTAs come in waves, and early merge CTAs would hold
 // SMs they need).
-// Whether a cooperative launch of Kern with `grid` CTAs fits the current device
-// (every CTA resident at once); known once per (kernel, device).
-template <auto Kern>
-bool cooperative_fits(int grid, int threads, size_t smem) {
-    static std::atomic<int> cap_plus1[64];  // per device: CTAs that fit, plus one
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
-    int cap = cap_plus1[dev].load(std::memory_order_relaxed) - 1;
-    if (cap < 0) {
-        int coop = 0, per_sm = 0;
-        if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, Kern, threads, smem) !=
-                cudaSuccess)
-            return false;
-        cap = coop ? per_sm * device_sm_count() : 0;
-        cap_plus1[dev].store(cap + 1, std::memory_order_relaxed);
-    }
-    return grid <= cap;
-}
-
 template <int D, bool KV8, int DW = kDecodeWarps>
-cudaError_t launch_mixed_d(const CUtensorMap &map, const DecodeArgs &da0, const PrefillArgs &pa,
+cudaError_t launch_mixed_d(const CUtensorMap &map, const DecodeArgs &da, const PrefillArgs &pa,
                            dim3 pgrid, int dec_slots, size_t smem, cudaStream_t stream,
                            bool cascade = false) {
     auto kern = mixed_kernel<D, KV8, DW>;
@@ -178,23 +148,6 @@ cudaError_t launch_mixed_d(const CUtensorMap &map, const DecodeArgs &da0, const 
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 0;
-    DecodeArgs da = da0;
-    if (cascade && da.grid_bar &&
-        cooperative_fits<mixed_kernel<D, KV8, DW>>((int)cfg.gridDim.x, kDecodeWarps * 32, smem)) {
-        // The merge in the same launch, after a grid barrier on a word zeroed here.
-        e = cudaMemsetAsync(da.grid_bar, 0, sizeof(unsigned), stream);
-        if (e != cudaSuccess) return e;
-        attr[0].id = cudaLaunchAttributeCooperative;
-        attr[0].val.cooperative = 1;
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, kern, map, da, pa, dec_slots,
-                               make_uint3(pgrid.x, pgrid.y, pgrid.z));
-        if (e == cudaSuccess) return e;
-        // Not placeable now (another context holds SMs): the merge as its own launch.
-        (void)cudaGetLastError();
-        cfg.numAttrs = 0;
-    }
-    da.grid_bar = nullptr;
     e = cudaLaunchKernelEx(&cfg, kern, map, da, pa, dec_slots,
                            make_uint3(pgrid.x, pgrid.y, pgrid.z));
     if (e != cudaSuccess) return e;
@@ -404,11 +357,6 @@ cudaError_t launch_cascade_one(void *out, const void *q, const void *kv_cache, c
     da.v_scale = kv8 ? v_scale : 1.f;
     da.shared_len = shared_len;
     set_cascade(da, whole, pre_ml, pre_acc, splits);
-    // The grid barrier's word: after the per-segment records.
-    const size_t segs = (size_t)num_seqs * g.num_kv_heads;
-    da.grid_bar = reinterpret_cast<unsigned *>(static_cast<uint8_t *>(whole) +
-                                               align_up(segs * kHeadsPad * 2 * 4, 256) +
-                                               align_up(segs * kHeadsPad * (size_t)D * 4, 256));
     // Most SMs stream the own tokens, so one tile in flight per warp (two from an
     // FP8 pool, half the bytes) saturates HBM; more only lengthens the queueing
     // of the prefix pass's loads beside them.

@@ -103,6 +103,30 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     return p;
 }
 
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// Global stores with an L2 eviction-priority hint (policy from createpolicy):
+// partial softmax states that a merge reads back soon are kept in L2 ahead of
+// streamed K/V.
+__device__ __forceinline__ void st_hint(float *p, float v, uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(policy)
+                 : "memory");
+}
+__device__ __forceinline__ void st_hint(float2 *p, float2 v, uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.v2.f32 [%0], {%1, %2}, %3;" ::"l"(p), "f"(v.x),
+                 "f"(v.y), "l"(policy)
+                 : "memory");
+}
+__device__ __forceinline__ void st_hint(float4 *p, float4 v, uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p),
+                 "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "l"(policy)
+                 : "memory");
+}
+
 // Contiguous global -> shared copy (16-byte aligned addresses, size multiple of 16).
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes,
                                           uint64_t *bar) {

@@ -96,9 +96,6 @@ struct DecodeArgs {
     // Mixed-batch launch: the number of decode CTAs and their total warps were
     // chosen on the device; plan = {ctas, total_warps} (nullptr otherwise).
     const int *plan;
-    // Cascade in one cooperative launch: a zeroed word for the grid barrier after
-    // which every warp of the grid merges segments (nullptr: the merge kernel).
-    unsigned *grid_bar;
     // Tiles a warp keeps in flight, at most the ring's stages (0: all of them).
     // Fewer than the ring holds when enough SMs stream that HBM is saturated
     // anyway: the bytes in flight then only lengthen every request's queueing,
@@ -122,6 +119,27 @@ __device__ __forceinline__ int kv_row(int blk, int h, int off, const DecodeArgs 
         return -(1 << 30);  // wholly outside the map: TMA fills zeros, nothing is read
     }
     return ((blk * 2) * a.num_kv_heads + h) * a.block_size + off;
+}
+
+// Decode pieces of segment (sequence s, KV head h) under the split kernel's
+// partition (the first min(NW, T) warps, equal shares of the T tiles): warps
+// g0..g1, and the record of warp g0's piece (its first record unless it began in
+// an earlier segment).  n_dec = 0 for a segment with no own tokens.
+__device__ __forceinline__ void segment_pieces(const int *prefix, int num_seqs, int Hkv,
+                                               long long NW, int s, int h, int &n_dec,
+                                               int &rec0) {
+    const int pre = prefix[s];
+    const int nt = prefix[s + 1] - pre;
+    n_dec = 0;
+    rec0 = -1;
+    if (nt == 0) return;
+    const long long T = (long long)prefix[num_seqs] * Hkv;
+    const long long NWe = NW < T ? NW : T;
+    const long long S0 = (long long)Hkv * pre + (long long)h * nt;
+    const long long g0 = div_floor_small((S0 + 1) * NWe - 1, T);
+    const long long g1 = div_floor_small((S0 + nt) * NWe - 1, T);
+    n_dec = (int)(g1 - g0 + 1);
+    rec0 = (int)(g0 * 2 + (g0 * T < S0 * NWe ? 1 : 0));  // floor(g0 T / NWe) < S0
 }
 
 // The split-context decode of one CTA (index cta of a grid whose warps number
@@ -258,6 +276,8 @@ __device__ __forceinline__ void decode_body(const CUtensorMap &kv_map, const Dec
     const uint32_t q_bytes = (uint32_t)G * D * 2u;
     const int v_row_off = Hkv * bs;
     const uint64_t policy = policy_evict_first();
+    // Records the merge reads back: kept in L2 ahead of the streamed K/V.
+    const uint64_t keep = policy_evict_last();
 
     auto issue = [&](int i) {
         const bool in_a = (i >> 5) == cur_batch;
@@ -592,18 +612,17 @@ __device__ __forceinline__ void decode_body(const CUtensorMap &kv_map, const Dec
 #pragma unroll
                 for (int mt = 0; mt < D / 16; ++mt) {
                     const int d0 = dim_of(mt, 0), d1 = dim_of(mt, 1);
-                    pacc[hh0 * D + d0] = acc[mt][0];
-                    pacc[(hh0 + 1) * D + d0] = acc[mt][1];
-                    pacc[hh0 * D + d1] = acc[mt][2];
-                    pacc[(hh0 + 1) * D + d1] = acc[mt][3];
+                    st_hint(pacc + hh0 * D + d0, acc[mt][0], keep);
+                    st_hint(pacc + (hh0 + 1) * D + d0, acc[mt][1], keep);
+                    st_hint(pacc + hh0 * D + d1, acc[mt][2], keep);
+                    st_hint(pacc + (hh0 + 1) * D + d1, acc[mt][3], keep);
                 }
                 if (lane < 4) {
                     float *pml = whole ? a.cs.whole_ml + wrec * kHeadsPad * 2
                                        : a.part_ml + rec * kHeadsPad * 2;
-                    pml[hh0 * 2 + 0] = m0;
-                    pml[hh0 * 2 + 1] = l0;
-                    pml[(hh0 + 1) * 2 + 0] = m1;
-                    pml[(hh0 + 1) * 2 + 1] = l1;
+                    st_hint(reinterpret_cast<float2 *>(pml + hh0 * 2), make_float2(m0, l0), keep);
+                    st_hint(reinterpret_cast<float2 *>(pml + (hh0 + 1) * 2), make_float2(m1, l1),
+                            keep);
                 }
             }
             first_piece = false;
@@ -690,28 +709,14 @@ __global__ void __launch_bounds__(kHeadsPad * D / 4) decode_merge_kernel(const D
 }
 
 // Cascade: merge segment k (sequence, KV head) from its decode records and the
-// prefix pass's partials (pa_merge.cuh); a whole warp.  Segments of sequences
-// with no own tokens have no decode record.
+// prefix pass's partials (pa_merge.cuh); a whole warp.
 template <int D, int RG>
 __device__ __forceinline__ void cascade_merge_one(const DecodeArgs &a, int k) {
     const int Hkv = a.num_kv_heads;
     const int s = k / Hkv, h = k - s * Hkv;
-    const int pre = a.prefix[s];
-    const int nt = a.prefix[s + 1] - pre;
-    int n_dec = 0, rec0 = -1;
-    if (nt > 0) {
-        // Pieces g0..g1 under the split kernel's partition (the first min(NW, T)
-        // warps, equal shares); warp g0's record of this segment is its first
-        // unless the warp began in an earlier segment.
-        const long long NW = a.plan ? a.plan[1] : a.total_warps;
-        const long long T = (long long)a.prefix[a.num_seqs] * Hkv;
-        const long long NWe = NW < T ? NW : T;
-        const long long S0 = (long long)Hkv * pre + (long long)h * nt;
-        const long long g0 = div_floor_small((S0 + 1) * NWe - 1, T);
-        const long long g1 = div_floor_small((S0 + nt) * NWe - 1, T);
-        n_dec = (int)(g1 - g0 + 1);
-        rec0 = (int)(g0 * 2 + (g0 * T < S0 * NWe ? 1 : 0));  // floor(g0 T / NWe) < S0
-    }
+    int n_dec, rec0;
+    segment_pieces(a.prefix, a.num_seqs, Hkv, a.plan ? a.plan[1] : a.total_warps, s, h, n_dec,
+                   rec0);
     merge_segment<D, RG>(a.cs, s, h, n_dec, rec0);
 }
 
@@ -822,7 +827,6 @@ DecodeArgs make_decode_args(void *out, const void *q, const KvGeom &g, int num_h
     a.cs.group = a.group;
     a.plan = nullptr;
     a.depth = 0;
-    a.grid_bar = nullptr;
     return a;
 }
 
@@ -913,7 +917,7 @@ size_t prefix_partial_bytes(int splits, int num_seqs, int num_heads, int head_si
 size_t cascade_whole_bytes(int num_seqs, int num_kv_heads, int head_size) {
     const size_t segs = (size_t)num_seqs * num_kv_heads;
     return align_up(segs * kHeadsPad * 2 * 4, 256) +
-           align_up(segs * kHeadsPad * (size_t)head_size * 4, 256) + 256;  // + barrier word
+           align_up(segs * kHeadsPad * (size_t)head_size * 4, 256);
 }
 
 }  // namespace pa

@@ -32,12 +32,21 @@ struct CascadeState {
     int pre_splits;        // prefix partials per row (0: no cascade)
 };
 
-// Global loads that bypass L1: records written by other SMs.
-__device__ __forceinline__ float2 ld_cg2(const float *p) {
-    return __ldcg(reinterpret_cast<const float2 *>(p));
+// Global loads that bypass L1 (records written by other SMs), with an L2
+// eviction hint: a record is dead once merged, so its lines go first.
+__device__ __forceinline__ float2 ld_cg2(const float *p, uint64_t policy) {
+    float2 v;
+    asm volatile("ld.global.cg.L2::cache_hint.v2.f32 {%0, %1}, [%2], %3;"
+                 : "=f"(v.x), "=f"(v.y)
+                 : "l"(p), "l"(policy));
+    return v;
 }
-__device__ __forceinline__ float4 ld_cg4(const float *p) {
-    return __ldcg(reinterpret_cast<const float4 *>(p));
+__device__ __forceinline__ float4 ld_cg4(const float *p, uint64_t policy) {
+    float4 v;
+    asm volatile("ld.global.cg.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p), "l"(policy));
+    return v;
 }
 
 // floor(a / b) for 0 <= a < 2^62, 0 < b, when the quotient is below 2^20 (a warp
@@ -93,6 +102,7 @@ __device__ __forceinline__ void merge_segment(const CascadeState &c, int s, int 
     constexpr int kQuads = D / 4;
     const int nslot = (G * kQuads + 31) / 32;
     const int kk = lane >> 3, hh = lane & 7;  // the (m, l) this lane holds: record kk, head hh
+    const uint64_t drop = policy_evict_first();
     int hi[8], off[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -109,20 +119,22 @@ __device__ __forceinline__ void merge_segment(const CascadeState &c, int s, int 
             const float *a = base_acc(k0 + (j < nk ? j : 0));
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-                if (i < nslot && j < nk) v[j][i] = ld_cg4(a + off[i]);
+                if (i < nslot && j < nk) v[j][i] = ld_cg4(a + off[i], drop);
         }
     };
     auto load_ml = [&](int k0, int nk) {
-        return kk < nk && hh < G ? ld_cg2(base_ml(k0 + kk) + 2 * hh)
+        return kk < nk && hh < G ? ld_cg2(base_ml(k0 + kk) + 2 * hh, drop)
                                  : make_float2(-INFINITY, 0.f);
     };
     const int nk0 = R < RG ? R : RG;
     load_group(0, nk0);
     const float2 ml0 = load_ml(0, nk0);
-    // Reference max per head over all records.
-    float M = ml0.x;
-    for (int k = 4 + kk; k < R; k += 4)
-        if (hh < G) M = fmaxf(M, ld_cg2(base_ml(k) + 2 * hh).x);
+    // Reference max per head over all records: lane (kk, hh) covers records
+    // kk, kk + 4, ... (the first of them already in ml0 when kk < nk0).
+    float M = -INFINITY;
+    for (int k = kk; k < R; k += 4)
+        M = fmaxf(M, k < nk0 ? ml0.x
+                             : (hh < G ? ld_cg2(base_ml(k) + 2 * hh, drop).x : -INFINITY));
     M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 8));
     M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 16));
     float4 num[8];
@@ -166,41 +178,6 @@ __device__ __forceinline__ void merge_segment(const CascadeState &c, int s, int 
                                             pack_bf16(num[i].z * inv, num[i].w * inv));
         }
     }
-}
-
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-// Barrier over every CTA of a cooperatively launched grid (all resident at once),
-// on a word that is zero when the launch starts.  Every thread of every CTA calls
-// it; each CTA's writes before it are visible to every CTA after it.  The wait is
-// bounded: false (for the whole CTA) if the other CTAs did not all arrive within
-// kWaitLimitNs.
-__device__ __forceinline__ bool grid_barrier(unsigned *bar, unsigned nctas) {
-    __shared__ int s_ok;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        atomicAdd(bar, 1u);
-        bool ok = true;
-        if (ld_acquire_u32(bar) < nctas) {
-            const unsigned long long t0 = globaltimer_ns();
-            while (ld_acquire_u32(bar) < nctas) {
-                if (globaltimer_ns() - t0 > kWaitLimitNs) {
-                    ok = false;
-                    break;
-                }
-                __nanosleep(100);
-            }
-        }
-        __threadfence();
-        s_ok = ok ? 1 : 0;
-    }
-    __syncthreads();
-    return s_ok != 0;
 }
 
 }  // namespace pa

@@ -33,6 +33,8 @@
 // the other tile's products instead of sharing the exponential units with the
 // other softmax.  Keys past a row's position are masked; tiles past the CTA's
 // causal limit are never fetched.
+#pragma once
+
 #include <algorithm>
 #include <cmath>
 
@@ -626,6 +628,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &kv_map, const Pr
                 const size_t rec =
                     ((size_t)bid.z * q_len + (t0 + tok)) * a.num_heads + (size_t)h * G + gq;
                 float4 *pacc = reinterpret_cast<float4 *>(a.part_acc + rec * D);
+                const uint64_t keep = policy_evict_last();  // read back by the merge
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
                     float o[32];
@@ -634,11 +637,14 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &kv_map, const Pr
                     if (real) {
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
-                            pacc[c * 8 + e] = make_float4(o[4 * e] * vsc, o[4 * e + 1] * vsc,
-                                                          o[4 * e + 2] * vsc, o[4 * e + 3] * vsc);
+                            st_hint(pacc + c * 8 + e,
+                                    make_float4(o[4 * e] * vsc, o[4 * e + 1] * vsc,
+                                                o[4 * e + 2] * vsc, o[4 * e + 3] * vsc),
+                                    keep);
                     }
                 }
-                if (real) reinterpret_cast<float2 *>(a.part_ml)[rec] = make_float2(m, l);
+                if (real)
+                    st_hint(reinterpret_cast<float2 *>(a.part_ml) + rec, make_float2(m, l), keep);
             } else {
             const float inv = (KV8 ? a.v_scale : 1.f) / l;
             uint4 *dst = reinterpret_cast<uint4 *>(

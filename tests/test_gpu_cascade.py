@@ -283,9 +283,9 @@ def test_cascade_where_the_prefix_pass_arrives_last(fp8):
     """One long own suffix makes the host run the prefix pass beside the own
     tokens' decode in one launch; the other 63 sequences own 1-16 tokens, which
     the decode finishes within microseconds, long before the prefix pass over
-    2048 shared tokens ends.  So the prefix pass's arrival completes almost every
-    segment, and its CTAs do those merges (the long sequence's segments, split
-    over many decode warps, included); deterministic and equal to the oracle."""
+    2048 shared tokens ends.  The merge kernel, a programmatic dependent of that
+    launch, then merges every segment (the long sequence's, split over many
+    decode warps, included): deterministic and equal to the oracle."""
     pb, bs = 128, 16
     g = torch.Generator().manual_seed(97)
     suffix = [8192] + torch.randint(1, 17, (63,), generator=g).tolist()
