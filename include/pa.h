@@ -175,7 +175,11 @@ size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, 
  *                 share one workspace
  * out[s][h] = sum_t softmax_t(scale * q[s][h].K[t][h/G]) V[t][h/G], computed
  * with an online softmax in fp32 over bf16 products; contexts are split evenly
- * over the whole GPU and the pieces merged by log-sum-exp.  num_seqs == 0 is a
+ * over the whole GPU and the pieces merged by log-sum-exp (a second, dependent
+ * kernel).  A batch of at most one (sequence, KV head) pair per SM whose
+ * max_seq_len is at most 12 tiles of 16 tokens runs as one kernel instead: a CTA
+ * per pair, its warps splitting the pair's tiles, merged in the CTA
+ * (pa_decode_cascade_kernels with shared_len 0 says which).  num_seqs == 0 is a
  * no-op.
  */
 pa_status pa_decode(void *out, const void *q, const void *kv_cache, int num_blocks,
@@ -225,10 +229,11 @@ size_t pa_decode_cascade_workspace_bytes(int num_seqs, int num_heads, int num_kv
  * Kernels one pa_decode_cascade call (pa_decode_cascade_fp8 when kv8 != 0) with
  * these shapes launches on the current device: 2 when the shared prefix and the
  * sequences' own tokens are attended side by side in one launch on disjoint
- * SMs, then merged (chosen from the shapes and the pool's type), or when
- * shared_len is 0 (pa_decode); 3 when the prefix is attended by its own launch
- * before the own tokens and the merge; 0 when num_seqs is 0; -1 for invalid
- * shapes.  For planning only (e.g. counting a CUDA graph's nodes): the results
+ * SMs, then merged (chosen from the shapes and the pool's type); 3 when the
+ * prefix is attended by its own launch before the own tokens and the merge;
+ * when shared_len is 0, pa_decode's count: 1 (a CTA per segment, merged in
+ * place) or 2 (split kernel and merge kernel); 0 when num_seqs is 0; -1 for
+ * invalid shapes.  For planning only (e.g. counting a CUDA graph's nodes): the results
  * are the same either way, up to floating-point summation order.
  */
 int pa_decode_cascade_kernels(int num_seqs, int num_heads, int num_kv_heads, int head_size,

@@ -107,9 +107,10 @@ def lib(path: Optional[str] = None):
 def _stream(stream) -> int:
     if stream is None:
         return torch.cuda.current_stream().cuda_stream
-    if isinstance(stream, torch.cuda.Stream):
-        return stream.cuda_stream
-    return int(stream)
+    try:
+        return stream.cuda_stream  # torch.cuda.Stream
+    except AttributeError:
+        return int(stream)
 
 
 def _check(status: int, where: str):
@@ -118,6 +119,12 @@ def _check(status: int, where: str):
 
 
 def _need(t: torch.Tensor, name: str, dtype, dims: Optional[int] = None):
+    try:  # the common case in one expression (torch dtypes are singletons)
+        if (t.is_cuda and t.dtype is dtype and (dims is None or t.dim() == dims)
+                and t.is_contiguous() and isinstance(t, torch.Tensor)):
+            return
+    except AttributeError:
+        pass
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
     if t.dtype != dtype:

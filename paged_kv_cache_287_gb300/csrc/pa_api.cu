@@ -358,7 +358,10 @@ int pa_decode_cascade_kernels(int num_seqs, int num_heads, int num_kv_heads, int
     if (head_size != 64 && head_size != 128) return -1;
     if (block_size != 8 && block_size != 16 && block_size != 32) return -1;
     if (num_seqs == 0) return 0;
-    if (shared_len == 0) return 2;  // pa_decode: split kernel and merge kernel
+    if (shared_len == 0)  // pa_decode: one CTA per segment, or the split kernel and its merge
+        return pa::decode_seg_ctas(num_seqs, num_kv_heads, max_seq_len, pa::device_sm_count())
+                   ? 1
+                   : 2;
     const pa::KvGeom g{1, block_size, num_kv_heads, head_size};
     return pa::cascade_one_launch_ctas(num_seqs, num_heads, g, max_seq_len, shared_len, kv8 != 0,
                                        pa::device_sm_count()) > 0

@@ -101,6 +101,13 @@ struct DecodeArgs {
     // anyway: the bytes in flight then only lengthen every request's queueing,
     // the loads of the kernel's other role included.
     int depth;
+    // Segment-per-CTA mode (1): CTA c covers segment c (sequence c / num_kv_heads,
+    // KV head c % num_kv_heads), its warps taking equal shares of the segment's
+    // tiles; the CTA's last warp to finish merges the pieces and writes the rows
+    // (zeros for a sequence of no tokens), so no merge kernel follows.  For
+    // batches of at most one segment per SM, each a few tiles long: the split
+    // partition would leave a merge launch on the step's critical path.
+    int seg_ctas;
 };
 
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -209,8 +216,18 @@ __device__ __forceinline__ void decode_body(const CUtensorMap &kv_map, const Dec
     const long long NW = total_warps;
     const long long NWe = NW < T ? NW : (T > 0 ? T : 1);
     const long long g = (long long)cta * W + warp;
-    const int t_begin = g < NWe ? (int)((g * T) / NWe) : 0;
-    const int t_end = g < NWe ? (int)(((g + 1) * T) / NWe) : 0;
+    int t_begin = g < NWe ? (int)((g * T) / NWe) : 0;
+    int t_end = g < NWe ? (int)(((g + 1) * T) / NWe) : 0;
+    if (a.seg_ctas) {
+        const int s = cta / Hkv, h = cta - (cta / Hkv) * Hkv;
+        const int nt = s_pre[s + 1] - s_pre[s];
+        const int ne = nt < W ? nt : W;
+        t_begin = t_end = 0;
+        if (warp < ne) {
+            t_begin = Hkv * s_pre[s] + h * nt + warp * nt / ne;
+            t_end = Hkv * s_pre[s] + h * nt + (warp + 1) * nt / ne;
+        }
+    }
     const int n = t_end - t_begin;
     // Cascade: the prefix pass reads the shared blocks through sequence 0's table,
     // so every other sequence's first shared_len / block_size entries must equal
@@ -645,10 +662,33 @@ __device__ __forceinline__ void decode_body(const CUtensorMap &kv_map, const Dec
     }
 }
 
+// Segment-per-CTA mode, once every warp of CTA cta has left decode_body: warp 0
+// merges the segment's pieces (slot 0 of warps cta W .. cta W + ne - 1) and
+// writes its rows; a segment of one tile is already written by its warp, and a
+// sequence of no tokens gets zero rows.  The tile count is recomputed from the
+// length exactly as decode_body clamps it.
+template <int D, int W>
+__device__ __forceinline__ void seg_cta_merge(const DecodeArgs &a, int cta) {
+    __syncthreads();  // every piece's record written (visible to this CTA)
+    if (threadIdx.x >= 32) return;
+    const int Hkv = a.num_kv_heads, s = cta / Hkv, h = cta - s * Hkv;
+    const int len = min(max(a.seq_lens[s], 0), a.max_blocks * a.block_size);
+    const int nt = (len + kTile - 1) / kTile;
+    const int ne = nt < W ? nt : W;
+    if (nt == 0) {
+        uint4 *dst =
+            reinterpret_cast<uint4 *>(a.out + ((size_t)s * a.num_heads + (size_t)h * a.group) * D);
+        for (int v = threadIdx.x; v < a.group * D / 8; v += 32) dst[v] = make_uint4(0u, 0u, 0u, 0u);
+    } else if (ne > 1) {
+        merge_segment<D>(a.cs, s, h, ne, cta * W * 2);
+    }
+}
+
 template <int D, int W, int S, bool KV8>
 __global__ void __launch_bounds__(W * 32, 1)
     decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
     decode_body<D, W, S, KV8>(kv_map, a, blockIdx.x, a.total_warps);
+    if (a.seg_ctas) seg_cta_merge<D, W>(a, blockIdx.x);
 }
 
 // Merge the pieces of segments that were split across warps; zero empty
@@ -740,7 +780,7 @@ cudaError_t launch_decode_d(const DecodeArgs &a0, const CUtensorMap &map, int gr
     if (e != cudaSuccess) return e;
     kern<<<grid, kDecodeWarps * 32, smem, stream>>>(map, a0);
     e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess || a0.seg_ctas) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(a0.num_seqs * a0.num_kv_heads));
     cfg.blockDim = dim3((unsigned)(a0.group * D / 4));
@@ -767,6 +807,14 @@ int decode_max_seqs(int head_size, int group, bool kv8) {
                          : head_size == 128 ? decode_smem_bytes<128>(0, group)
                                             : decode_smem_bytes<64>(0, group);
     return fixed >= limit ? 0 : (int)((limit - fixed) / 8);
+}
+
+bool decode_seg_ctas(int num_seqs, int num_kv_heads, int max_seq_len, int sm_count) {
+    // At most one segment per SM, each at most a tile per warp: a CTA per segment,
+    // merged in place (one launch).
+    const long long segs = (long long)num_seqs * num_kv_heads;
+    const long long seg_tiles = ((long long)std::max(max_seq_len, 1) + kTile - 1) / kTile;
+    return segs >= 1 && segs <= sm_count && seg_tiles <= kDecodeWarps;
 }
 
 size_t decode_workspace_bytes(int num_seqs, int head_size, int sm_count) {
@@ -827,6 +875,7 @@ DecodeArgs make_decode_args(void *out, const void *q, const KvGeom &g, int num_h
     a.cs.group = a.group;
     a.plan = nullptr;
     a.depth = 0;
+    a.seg_ctas = 0;
     return a;
 }
 
@@ -859,15 +908,20 @@ cudaError_t launch_decode_impl(void *out, const void *q, const void *kv_cache, c
     // As many warps as there can be tiles, at most one CTA per SM.  A warp has a
     // single stage, so a small batch finishes soonest with one tile per warp; a
     // large one fills every SM and each warp streams its share.
-    const long long tmax = (long long)num_seqs * g.num_kv_heads *
-                           ((std::max(max_seq_len - shared_len, 1) + kTile - 1) / kTile);
+    const long long seg_tiles = (std::max(max_seq_len - shared_len, 1) + kTile - 1) / kTile;
+    const long long segs = (long long)num_seqs * g.num_kv_heads;
+    const long long tmax = segs * seg_tiles;
     long long ctas = (tmax + kDecodeWarps - 1) / kDecodeWarps;
     ctas = std::max(1LL, std::min<long long>(ctas, sms));
+    const bool seg_ctas = !whole && shared_len == 0 && decode_seg_ctas(num_seqs, g.num_kv_heads,
+                                                                        max_seq_len, sms);
+    if (seg_ctas) ctas = segs;
     DecodeArgs a = make_decode_args(out, q, g, num_heads, block_tables, max_blocks_per_seq,
                                     seq_lens, num_seqs, scale, workspace, kv8, (int)ctas);
     a.k_scale = k_scale;
     a.v_scale = v_scale;
     a.shared_len = shared_len;
+    a.seg_ctas = seg_ctas ? 1 : 0;
     if (whole) set_cascade(a, whole, pre_ml, pre_acc, pre_splits);
     if (kv8) return launch_decode_d<128, true>(a, map, (int)ctas, stream);
     if (D == 128) return launch_decode_d<128, false>(a, map, (int)ctas, stream);

@@ -59,6 +59,9 @@ cudaError_t launch_cache_write(void *kv_cache, const KvGeom &g, const void *k_ne
                                const void *v_new, int64_t new_row_stride,
                                const int32_t *slot_mapping, int num_tokens, cudaStream_t stream);
 
+// Whether pa_decode (no shared prefix) over this shape runs one CTA per segment
+// and merges in place: one launch instead of the split kernel and its merge.
+bool decode_seg_ctas(int num_seqs, int num_kv_heads, int max_seq_len, int sm_count);
 // Decode workspace bytes for num_seqs sequences on a device with sm_count SMs.
 size_t decode_workspace_bytes(int num_seqs, int head_size, int sm_count);
 // Largest num_seqs the decode kernel's shared-memory tables hold (kv8: FP8 pool).

@@ -131,7 +131,12 @@ def test_cascade_host_checks(lib):
 def test_cascade_kernel_count_query(lib):
     q = lib.pa_decode_cascade_kernels
     assert q(0, 32, 8, 128, 16, 64, 32, 0) == 0            # no sequences: nothing launched
-    assert q(5, 32, 8, 128, 16, 64, 0, 0) == 2             # no shared tokens: pa_decode
+    # No shared tokens: pa_decode, one launch when every (sequence, KV head) gets an
+    # SM and is at most 12 tiles long (one tile per warp), else split + merge.
+    assert q(1, 8, 1, 128, 16, 192, 0, 0) == 1             # one segment of 12 tiles
+    assert q(1, 8, 1, 128, 16, 193, 0, 0) == 2             # 13 tiles
+    assert q(5, 32, 8, 128, 16, 4096, 0, 0) == 2
+    assert q(5, 32, 8, 128, 16, 64, 0, 0) in (1, 2)        # 40 segments: the SM count decides
     assert q(5, 32, 8, 128, 16, 64, 32, 0) in (2, 3)       # depends on the device's SMs
     assert q(5, 32, 8, 128, 16, 64, 32, 1) in (2, 3)       # FP8 pool: the same choice
     assert q(5, 32, 8, 128, 16, 64, 65, 0) == -1           # shared_len beyond max_seq_len
