@@ -312,19 +312,23 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &kv_map, const Pr
         const uint32_t idesc_s =
             KV8 ? tc_idesc_f16(kTcRows, kTcKeys, 0) : tc_idesc_bf16(kTcRows, kTcKeys, 0);
         const uint32_t idesc_pv = KV8 ? tc_idesc_f16(kTcRows, D, 1) : tc_idesc_bf16(kTcRows, D, 1);
-        const uint32_t q_base = smem_u32(sQ) + t * L::kQTile;
-        const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV);
+        // Operand descriptors are built once: an offset within an operand is added
+        // to the start-address field (bits 0-13, address / 16), which cannot carry
+        // out since shared-memory addresses stay below 2^18.  The issuing thread's
+        // per-product work is then one add, not a descriptor rebuilt from scratch,
+        // and the products reach the tensor pipe as fast as it takes them.
+        const uint64_t q_desc = tc_desc_sw128(smem_u32(sQ) + t * L::kQTile, 16, 1024);
+        const uint64_t k_desc = tc_desc_sw128(smem_u32(sK), 16, 1024);
+        const uint64_t v_desc = tc_desc_sw128(smem_u32(sV), L::kKvPanel, 1024);
         // S_t = Q_t . K_j^T into tensor-memory columns [128 t, 128 t + 128).
         auto issue_s = [&](int j) {
             if (lane == 0) {
-                const uint32_t kb = k_base + (j % kKSlots) * L::kKBytes;
+                const uint64_t kd = k_desc + (uint64_t)(((j % kKSlots) * L::kKBytes) >> 4);
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = (k >> 2) * L::kQPanel + (k & 3) * 32;
-                    const uint64_t ad = tc_desc_sw128(q_base + off, 16, 1024);
-                    const uint64_t bd = tc_desc_sw128(kb + (k >> 2) * L::kKvPanel + (k & 3) * 32,
-                                                      16, 1024);
-                    tc_mma_ss(tmem + t * kTcRows, ad, bd, idesc_s, k > 0 ? 1u : 0u);
+                    const uint32_t qo = ((k >> 2) * L::kQPanel + (k & 3) * 32) >> 4;
+                    const uint32_t ko = ((k >> 2) * L::kKvPanel + (k & 3) * 32) >> 4;
+                    tc_mma_ss(tmem + t * kTcRows, q_desc + qo, kd + ko, idesc_s, k > 0 ? 1u : 0u);
                 }
                 tc_commit(&s_full[t]);
                 tc_commit(&k_empty[j % kKSlots]);
@@ -335,13 +339,12 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &kv_map, const Pr
         // per column in the first 64 columns of its scores (16 keys per 8 columns).
         auto issue_pv = [&](int j, int h) {
             if (lane == 0) {
-                const uint32_t vb = v_base + (j % kVSlots) * L::kKBytes;
+                const uint64_t vd = v_desc + (uint64_t)(((j % kVSlots) * L::kKBytes) >> 4);
 #pragma unroll
-                for (int kk = 4 * h; kk < 4 * h + 4; ++kk) {
-                    const uint64_t bd = tc_desc_sw128(vb + kk * 16 * 128, L::kKvPanel, 1024);
-                    tc_mma_ts(tmem + kColO + t * kTcRows, tmem + t * kTcRows + kk * 8, bd,
-                              idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
+                    tc_mma_ts(tmem + kColO + t * kTcRows, tmem + t * kTcRows + kk * 8,
+                              vd + (uint64_t)((kk * 16 * 128) >> 4), idesc_pv,
+                              (j > 0 || kk > 0) ? 1u : 0u);
                 if (h == 1) {
                     tc_commit(&pv_done[t]);
                     tc_commit(&v_empty[j % kVSlots]);
@@ -445,17 +448,23 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &kv_map, const Pr
             const uint32_t flip = a.negate_q ? 0x80008000u : 0u;  // exact bf16 negation
             uint8_t *qt_smem = sQ + t * L::kQTile;
             if constexpr (!KV8) {
+                // Every load is issued before the first store: the stores go through
+                // generic pointers the compiler cannot tell apart from the loads', so
+                // interleaved they would wait for one global round trip each.
+                uint4 v[D / 8];
+#pragma unroll
+                for (int c = 0; c < D / 8; ++c) v[c] = real ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
 #pragma unroll
                 for (int p = 0; p < L::kPanels; ++p)
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
-                        uint4 v = real ? src[p * 8 + c] : make_uint4(0, 0, 0, 0);
-                        v.x ^= flip;
-                        v.y ^= flip;
-                        v.z ^= flip;
-                        v.w ^= flip;
+                        uint4 w = v[p * 8 + c];
+                        w.x ^= flip;
+                        w.y ^= flip;
+                        w.z ^= flip;
+                        w.w ^= flip;
                         *reinterpret_cast<uint4 *>(qt_smem + p * L::kQPanel + row * 128 +
-                                                   ((c ^ (row & 7)) << 4)) = v;
+                                                   ((c ^ (row & 7)) << 4)) = w;
                     }
             } else {
                 // f16 query: the row times the power of two that puts its largest
@@ -465,7 +474,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &kv_map, const Pr
                 float mx = 0.f;
 #pragma unroll
                 for (int c = 0; c < D / 8; ++c) {
-                    v[c] = real ? src[c] : make_uint4(0, 0, 0, 0);
+                    v[c] = real ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
                     v[c].x ^= flip;
                     v[c].y ^= flip;
                     v[c].z ^= flip;
