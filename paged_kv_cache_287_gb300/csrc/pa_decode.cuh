@@ -666,9 +666,10 @@ __device__ __forceinline__ void decode_body(const CUtensorMap &kv_map, const Dec
 // merges the segment's pieces (slot 0 of warps cta W .. cta W + ne - 1) and
 // writes its rows; a segment of one tile is already written by its warp, and a
 // sequence of no tokens gets zero rows.  The tile count is recomputed from the
-// length exactly as decode_body clamps it.
+// length exactly as decode_body clamps it.  Kept out of line: inlined, its
+// record registers made the streaming loop of every decode kernel spill.
 template <int D, int W>
-__device__ __forceinline__ void seg_cta_merge(const DecodeArgs &a, int cta) {
+__device__ __noinline__ void seg_cta_merge(const DecodeArgs &a, int cta) {
     __syncthreads();  // every piece's record written (visible to this CTA)
     if (threadIdx.x >= 32) return;
     const int Hkv = a.num_kv_heads, s = cta / Hkv, h = cta - s * Hkv;
@@ -680,7 +681,7 @@ __device__ __forceinline__ void seg_cta_merge(const DecodeArgs &a, int cta) {
             reinterpret_cast<uint4 *>(a.out + ((size_t)s * a.num_heads + (size_t)h * a.group) * D);
         for (int v = threadIdx.x; v < a.group * D / 8; v += 32) dst[v] = make_uint4(0u, 0u, 0u, 0u);
     } else if (ne > 1) {
-        merge_segment<D>(a.cs, s, h, ne, cta * W * 2);
+        merge_segment<D, 2>(a.cs, s, h, ne, cta * W * 2);
     }
 }
 
