@@ -749,26 +749,71 @@ __global__ void __launch_bounds__(kHeadsPad * D / 4) decode_merge_kernel(const D
     orow[d4] = make_uint2(pack_bf16(num.x * inv, num.y * inv), pack_bf16(num.z * inv, num.w * inv));
 }
 
-// Cascade: merge segment k (sequence, KV head) from its decode records and the
-// prefix pass's partials (pa_merge.cuh); a whole warp.
-template <int D, int RG>
-__device__ __forceinline__ void cascade_merge_one(const DecodeArgs &a, int k) {
-    const int Hkv = a.num_kv_heads;
-    const int s = k / Hkv, h = k - s * Hkv;
-    int n_dec, rec0;
-    segment_pieces(a.prefix, a.num_seqs, Hkv, a.plan ? a.plan[1] : a.total_warps, s, h, n_dec,
-                   rec0);
-    merge_segment<D, RG>(a.cs, s, h, n_dec, rec0);
-}
+// Batches of at most this many sequences have their tile prefix rebuilt by each
+// merge CTA (16 KB of shared memory) instead of read from the decode's table.
+constexpr int kMergeOwnPrefix = 4096;
 
 // The cascade's merge as its own launch, one warp per segment; launched as a
 // programmatic dependent of the kernel that wrote the records: it waits for that
-// grid's completion before reading anything.
+// grid's completion before reading any record.  What the segment's pieces are
+// depends only on the inputs (the lengths) and the decode grid's shape, so for
+// batches up to kMergeOwnPrefix sequences each CTA rebuilds the tile prefix of
+// the own tokens, clamped exactly as decode_body clamps them, before the wait,
+// while the decode grid's last warps still run: after the wait only the records
+// are loaded.
 template <int D>
 __global__ void __launch_bounds__(256) cascade_merge_kernel(const DecodeArgs a) {
+    __shared__ int s_pre[kMergeOwnPrefix + 1];
+    __shared__ int s_warp[8];
+    const int B = a.num_seqs, Hkv = a.num_kv_heads;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int k = blockIdx.x * 8 + warp;
+    const int s = k / Hkv, h = k - (k / Hkv) * Hkv;
+    const bool own_prefix = B <= kMergeOwnPrefix && a.plan == nullptr;
+    int n_dec = 0, rec0 = -1;
+    if (own_prefix) {
+        const int per = (B + 255) / 256;  // consecutive sequences per thread
+        const int sh = a.shared_len, max_len = a.max_blocks * a.block_size;
+        int t[16];
+        int sum = 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int q = tid * per + i;
+            int nt = 0;
+            if (i < per && q < B) {
+                int len = a.seq_lens[q];
+                if (len < sh || len > max_len) len = len < sh ? sh : max_len;
+                nt = (len - sh + kTile - 1) / kTile;
+            }
+            t[i] = nt;
+            sum += nt;
+        }
+        int v = sum;  // inclusive scan over the warp, then over the warps
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += u;
+        }
+        if (lane == 31) s_warp[warp] = v;
+        __syncthreads();
+        int base = 0;
+        for (int w = 0; w < warp; ++w) base += s_warp[w];
+        int run = base + v - sum;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int q = tid * per + i;
+            if (i < per && q < B) s_pre[q] = run;
+            run += t[i];
+        }
+        if (tid == 255) s_pre[B] = run;
+        __syncthreads();
+        if (k < B * Hkv) segment_pieces(s_pre, B, Hkv, a.total_warps, s, h, n_dec, rec0);
+    }
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int k = blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (k < a.num_seqs * a.num_kv_heads) cascade_merge_one<D, 4>(a, k);
+    if (k >= B * Hkv) return;
+    if (!own_prefix)
+        segment_pieces(a.prefix, B, Hkv, a.plan ? a.plan[1] : a.total_warps, s, h, n_dec, rec0);
+    merge_segment<D, 4>(a.cs, s, h, n_dec, rec0);
 }
 
 template <int D, bool KV8>
