@@ -384,7 +384,7 @@ def pa_attention_varlen(out: torch.Tensor, q: torch.Tensor, k_new: Optional[torc
     """One step over a flattened mixed batch (chunks first, then decode tokens):
     optional cache write, chunked prefill, decode.  A uint8 kv_cache is an FP8
     (e4m3) pool and needs kv_scales = (k_scale, v_scale)."""
-    fp8 = kv_cache.dtype == torch.uint8
+    fp8 = kv_cache.dtype is torch.uint8
     if fp8:
         if kv_scales is None:
             raise ValueError("an FP8 pool needs kv_scales=(k_scale, v_scale)")
@@ -415,13 +415,17 @@ def pa_attention_varlen(out: torch.Tensor, q: torch.Tensor, k_new: Optional[torc
               int(num_prefill_tokens), int(max_prefill_q_len), kv_cache.data_ptr(), NB, bs, Hq,
               Hkv, D, block_tables.data_ptr(), block_tables.shape[1], seq_lens.data_ptr(),
               int(max_seq_len), float(scale))
+    L = _lib if _lib is not None else lib()
     if fp8:
-        _check(lib().pa_attention_varlen_fp8(*common, float(kv_scales[0]), float(kv_scales[1]),
-                                             workspace.data_ptr(), workspace.numel(),
-                                             _stream(stream)), "pa_attention_varlen_fp8")
+        st = L.pa_attention_varlen_fp8(*common, float(kv_scales[0]), float(kv_scales[1]),
+                                       workspace.data_ptr(), workspace.numel(), _stream(stream))
+        if st:
+            raise PaError(st, "pa_attention_varlen_fp8")
     else:
-        _check(lib().pa_attention_varlen(*common, workspace.data_ptr(), workspace.numel(),
-                                         _stream(stream)), "pa_attention_varlen")
+        st = L.pa_attention_varlen(*common, workspace.data_ptr(), workspace.numel(),
+                                   _stream(stream))
+        if st:
+            raise PaError(st, "pa_attention_varlen")
 
 
 def pa_error_check(stream=None) -> None:
