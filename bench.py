@@ -199,6 +199,24 @@ def median_launch_ms(fn, stream, runs: int = 50, flush=None) -> float:
     return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
 
 
+def back_to_back_ms(fn, stream, n: int = 20, runs: int = 10) -> float:
+    """Device time per call of a short kernel: n calls back to back between one
+    pair of CUDA events, queued behind a bounded sleep kernel (about 100 us) so
+    that the host's submission stays ahead of the GPU; the median over runs."""
+    ts = []
+    for _ in range(runs):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        torch.cuda._sleep(200000)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1) / n)
+    return statistics.median(ts)
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -462,7 +480,7 @@ def by_workload(args, dev, stream) -> dict:
     torch.cuda.synchronize(dev)
     with torch.cuda.graph(graph, stream=cap):
         for _ in range(20):
-            step1(cap)
+            step1u(cap)
     torch.cuda.synchronize(dev)
     replay, clk_g = timed(graph.replay, 20 * per_step)
     res[1] = {"workload": CONFIG_NAMES[1], "value": b.num_seqs / (eager / 1e3),
@@ -472,7 +490,9 @@ def by_workload(args, dev, stream) -> dict:
                             "ms_per_step": eager2, "step": "pa_cache_write + pa_decode, eager",
                             "clocks": clk2},
               "graph": {"value": b.num_seqs / (replay / 20 / 1e3), "unit": "seqs/s",
-                        "ms_per_step": replay / 20, "steps_per_replay": 20, "clocks": clk_g},
+                        "ms_per_step": replay / 20, "steps_per_replay": 20,
+                        "step": "the one-call step, 20 captured in one CUDA graph",
+                        "clocks": clk_g},
               "roofline": {"bound": "launch", "frac": None,
                            "note": "264 KB of KV: launch latency, not HBM, bounds the step"},
               "clocks": clk}
@@ -528,7 +548,7 @@ def by_workload(args, dev, stream) -> dict:
         kw = {"kv_scales": sc} if kind == "fp8" else {}
         step_ms, clk = timed(lambda: binding.pa_attention_varlen(
             out_all, b.q, b.k_new, b.v_new, b.slot_mapping, cu_pre, n_pre, r_pre, max_q, pool,
-            b.block_tables, b.seq_lens, max_dec, b.scale, ws, stream, **kw), 4)
+            b.block_tables, b.seq_lens, max_dec, b.scale, ws, stream, **kw), 3)
         if kind == "fp8":
             pre = lambda: binding.pa_prefill_chunk_fp8(out_pre, b.q[:r_pre], cu_pre, max_q, pool,
                                                        b.block_tables[:n_pre],
@@ -541,7 +561,8 @@ def by_workload(args, dev, stream) -> dict:
         tf = flops / (pre_ms / 1e3) / 1e12
         e = {"value": step_ms, "unit": "ms", "higher_is_better": False, "ms_per_step": step_ms,
              "step": "pa_attention_varlen" + ("_fp8" if kind == "fp8" else "") +
-                     ": cache write, then chunked prefill and decode side by side in one launch",
+                     ": cache write (its extra block splits the SMs), then chunked prefill "
+                     "and decode side by side in one launch, then the decode's merge",
              "prefill": {"tflops": tf, "launch_ms": pre_ms, "flops_per_launch": flops,
                          "clocks": clk_p},
              "roofline": {"bound": "tensor", "achieved": tf, "peak": tfl, "unit": "TFLOP/s",
@@ -963,6 +984,15 @@ def run_mixed(args, world, rank, local):
     runs = max(50, args.median_runs)
     pre_med_ms = median_launch_ms(prefill_only, stream, runs)
 
+    def write_only():
+        if fp8:
+            binding.pa_cache_write_fp8(pool8, b.k_new, b.v_new, b.slot_mapping, FP8_K_SCALE,
+                                       FP8_V_SCALE, stream)
+        else:
+            binding.pa_cache_write(b.kv_cache, b.k_new, b.v_new, b.slot_mapping, stream)
+
+    write_b2b_ms = back_to_back_ms(write_only, stream)
+
     # The same step through the one unified call (write, chunks, decode tokens).
     out_all = torch.empty_like(b.q)
     ws_all = torch.empty(binding.pa_attention_varlen_workspace_bytes(
@@ -1071,6 +1101,8 @@ def run_mixed(args, world, rank, local):
     with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
         pk = json.load(f)
     pre_tflops = flops / (pre_med_ms / 1e3) / 1e12
+    # bf16 rows read, pool bytes written (one byte per element in an FP8 pool)
+    wbytes = 2 * b.k_new.numel() * (2 + (1 if fp8 else 2))
     line = {"metric": "mixed chunked-prefill + decode step",
             "value": unified_ms, "unit": "ms", "ms_per_step": unified_ms,
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
@@ -1078,8 +1110,9 @@ def run_mixed(args, world, rank, local):
             "warmup": args.warmup, "dtype": "f16" if fp8 else "bf16", "data": "synthetic",
             "config": dict(workload_config(4),
                            kv_cache="fp8-e4m3 (per-tensor k/v scale 1/64)" if fp8 else "bf16"),
-            "step": "pa_attention_varlen: cache write, then chunked prefill and decode side "
-                    "by side in one launch (decode SMs chosen on the device)"
+            "step": "pa_attention_varlen: cache write (one extra block of its launch chooses "
+                    "the decode SMs), then chunked prefill and decode side by side in one "
+                    "launch, then the decode's merge"
                     + ("; FP8 pool" if fp8 else ""),
             "kernels_ms": {"pa_cache_write": ms[0], "pa_prefill_chunk": ms[1], "pa_decode": ms[2]},
             "sequential_step_ms": sum(ms),
@@ -1090,9 +1123,15 @@ def run_mixed(args, world, rank, local):
                         "frac": flops / (ms[1] / 1e3) / 1e12 / pk["bf16_tflops"]},
             "decode": {"kv_gbs": kv_dec / (2 if fp8 else 1) / (ms[2] / 1e3) / 1e9,
                        "frac": kv_dec / (2 if fp8 else 1) / (ms[2] / 1e3) / 1e9 / pk["hbm_gbs"]},
-            # bf16 rows read, pool bytes written (one byte per element in an FP8 pool)
-            "cache_write": {"gbs": 2 * b.k_new.numel() * (2 + (1 if fp8 else 2)) /
-                                   (ms[0] / 1e3) / 1e9},
+            # In the step (after the decode's 2 GB stream, L2 clean; the event
+            # clock's step is about 2 us) and back to back (20 launches per event
+            # pair): device time of one launch.
+            "cache_write": {"gbs": wbytes / (ms[0] / 1e3) / 1e9,
+                            "back_to_back_us": write_b2b_ms * 1e3,
+                            "gbs_back_to_back": wbytes / (write_b2b_ms / 1e3) / 1e9,
+                            "frac_back_to_back": wbytes / (write_b2b_ms / 1e3) / 1e9 /
+                                                 pk["hbm_gbs"],
+                            "bytes_per_launch": wbytes},
             # The tensor-bound kernel of the step, timed alone in the separate calls
             # (so against the burst bf16 peak; its f16 MMAs run at the same rate).
             "roofline": {"bound": "tensor", "achieved": pre_tflops,
@@ -1110,8 +1149,8 @@ def run_mixed(args, world, rank, local):
                             "host memory and its output copied out, one stream per copy "
                             "direction, two buffer sets; the KV pool resident; host wall "
                             "clock over all steps"},
-            "clocks": sampler.summary(), "gpu_launches": 4 * args.steps,
-            "unified_gpu_launches_per_step": 4}
+            "clocks": sampler.summary(), "gpu_launches": 3 * args.steps,
+            "unified_gpu_launches_per_step": 3}
     if world == 1 and not args.no_cpu_baseline and not fp8:
         est, nrows, allrows, threads = cpu_mixed_step_ms(
             type(b)(**{**b.__dict__, **{k: getattr(b, k).cpu()

@@ -368,6 +368,45 @@ pa_status pa_attention_varlen_fp8(void *out, const void *q, const void *k_new,
                                   void *workspace, size_t workspace_bytes, pa_stream_t stream);
 
 /*
+ * pa_varlen_args - every argument of pa_attention_varlen(_fp8) in one struct,
+ * for callers whose per-argument marshalling costs more than the call itself
+ * (an interpreter's foreign-function layer).  Each field means what the
+ * parameter of the same name means; kv8 != 0 selects the FP8 pool form
+ * (k_scale and v_scale are read only then).  Natural C layout, as declared: on
+ * a 64-bit target 12 eight-byte fields, 12 int32, 3 float (pa_varlen_args_bytes
+ * reports its size).
+ */
+typedef struct pa_varlen_args {
+    void *out;
+    const void *q;
+    const void *k_new;
+    const void *v_new;
+    const int32_t *slot_mapping;
+    const int32_t *cu_q_lens;
+    void *kv_cache;
+    const int32_t *block_tables;
+    const int32_t *seq_lens;
+    void *workspace;
+    size_t workspace_bytes;
+    pa_stream_t stream;
+    int32_t num_seqs, num_prefills, num_prefill_tokens, max_prefill_q_len;
+    int32_t num_blocks, block_size, num_heads, num_kv_heads, head_size;
+    int32_t max_blocks_per_seq, max_seq_len, kv8;
+    float scale, k_scale, v_scale;
+} pa_varlen_args;
+
+/* sizeof(pa_varlen_args), for callers that lay the struct out themselves. */
+size_t pa_varlen_args_bytes(void);
+
+/*
+ * pa_attention_varlen_packed - pa_attention_varlen (kv8 == 0) or
+ * pa_attention_varlen_fp8 (kv8 != 0) with the arguments read from *args, which
+ * the call does not keep.  Same checks and statuses; PA_ERR_INVALID_ARG for a
+ * NULL args.
+ */
+pa_status pa_attention_varlen_packed(const pa_varlen_args *args);
+
+/*
  * Synchronise `stream`, then read and clear the device error word the kernels
  * of this library set on the current device.  Returns PA_OK, PA_ERR_TIMEOUT,
  * PA_ERR_OOB or PA_ERR_PRECONDITION (the first of these that was set, in this

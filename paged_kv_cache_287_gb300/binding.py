@@ -11,6 +11,8 @@ from __future__ import annotations
 
 import ctypes
 import os
+import struct
+import threading
 from typing import Optional
 
 import torch
@@ -30,7 +32,16 @@ EXPORTS = ("pa_status_string", "pa_kv_block_bytes", "pa_kv_block_bytes_dtype", "
            "pa_decode_cascade_fp8",
            "pa_prefill_chunk",
            "pa_attention_varlen_workspace_bytes", "pa_attention_varlen",
-           "pa_attention_varlen_fp8", "pa_error_check")
+           "pa_attention_varlen_fp8", "pa_varlen_args_bytes", "pa_attention_varlen_packed",
+           "pa_error_check")
+
+# pa_varlen_args as laid out on a 64-bit little-endian target: out, q, k_new,
+# v_new, slot_mapping, cu_q_lens, kv_cache, block_tables, seq_lens, workspace,
+# workspace_bytes, stream; num_seqs, num_prefills, num_prefill_tokens,
+# max_prefill_q_len, num_blocks, block_size, num_heads, num_kv_heads, head_size,
+# max_blocks_per_seq, max_seq_len, kv8; scale, k_scale, v_scale.
+VARLEN_ARGS = struct.Struct("<12Q12i3f")
+_tls = threading.local()  # one packed-argument buffer per thread
 
 
 class PaError(RuntimeError):
@@ -97,6 +108,12 @@ def lib(path: Optional[str] = None):
     L.pa_attention_varlen_fp8.argtypes = [P, P, P, P, P, P, i, i, i, i, P, i, i, i, i, i, P, i, P,
                                           i, ctypes.c_float, ctypes.c_float, ctypes.c_float, P,
                                           sz, P]
+    L.pa_varlen_args_bytes.restype = sz
+    L.pa_varlen_args_bytes.argtypes = []
+    L.pa_attention_varlen_packed.restype = i
+    L.pa_attention_varlen_packed.argtypes = [P]
+    if L.pa_varlen_args_bytes() < VARLEN_ARGS.size:
+        raise RuntimeError("pa_varlen_args is smaller than this binding's layout")
     L.pa_error_check.restype = i
     L.pa_error_check.argtypes = [P]
     if path is None:
@@ -402,7 +419,7 @@ def pa_attention_varlen(out: torch.Tensor, q: torch.Tensor, k_new: Optional[torc
     if Dq != D or out.shape != q.shape or block_tables.shape[0] != B or \
             rows != num_prefill_tokens + B - num_prefills:
         raise ValueError("inconsistent varlen shapes")
-    kp = vp = sp = None
+    kp = vp = sp = 0
     if slot_mapping is not None:
         _need(k_new, "k_new", torch.bfloat16, 3)
         _need(v_new, "v_new", torch.bfloat16, 3)
@@ -411,21 +428,28 @@ def pa_attention_varlen(out: torch.Tensor, q: torch.Tensor, k_new: Optional[torc
                 slot_mapping.shape[0] != rows:
             raise ValueError("k_new/v_new/slot_mapping must have one row per query row")
         kp, vp, sp = k_new.data_ptr(), v_new.data_ptr(), slot_mapping.data_ptr()
-    common = (out.data_ptr(), q.data_ptr(), kp, vp, sp, cu_q_lens.data_ptr(), B, int(num_prefills),
-              int(num_prefill_tokens), int(max_prefill_q_len), kv_cache.data_ptr(), NB, bs, Hq,
-              Hkv, D, block_tables.data_ptr(), block_tables.shape[1], seq_lens.data_ptr(),
-              int(max_seq_len), float(scale))
     L = _lib if _lib is not None else lib()
+    try:
+        buf, addr = _tls.varlen
+    except AttributeError:
+        buf = ctypes.create_string_buffer(L.pa_varlen_args_bytes())
+        addr = ctypes.addressof(buf)
+        _tls.varlen = (buf, addr)
     if fp8:
-        st = L.pa_attention_varlen_fp8(*common, float(kv_scales[0]), float(kv_scales[1]),
-                                       workspace.data_ptr(), workspace.numel(), _stream(stream))
-        if st:
-            raise PaError(st, "pa_attention_varlen_fp8")
+        ks, vs = float(kv_scales[0]), float(kv_scales[1])
     else:
-        st = L.pa_attention_varlen(*common, workspace.data_ptr(), workspace.numel(),
-                                   _stream(stream))
-        if st:
-            raise PaError(st, "pa_attention_varlen")
+        ks = vs = 1.0
+    # One struct and one foreign call: per-argument conversion would cost more
+    # than the call itself.
+    VARLEN_ARGS.pack_into(
+        buf, 0, out.data_ptr(), q.data_ptr(), kp, vp, sp, cu_q_lens.data_ptr(),
+        kv_cache.data_ptr(), block_tables.data_ptr(), seq_lens.data_ptr(), workspace.data_ptr(),
+        workspace.numel(), _stream(stream) or 0, B, int(num_prefills), int(num_prefill_tokens),
+        int(max_prefill_q_len), NB, bs, Hq, Hkv, D, block_tables.shape[1], int(max_seq_len), fp8,
+        float(scale), ks, vs)
+    st = L.pa_attention_varlen_packed(addr)
+    if st:
+        raise PaError(st, "pa_attention_varlen_fp8" if fp8 else "pa_attention_varlen")
 
 
 def pa_error_check(stream=None) -> None:

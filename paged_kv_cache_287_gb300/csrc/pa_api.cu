@@ -548,15 +548,23 @@ static pa_status varlen_impl(void *out, const void *q, const void *k_new, const 
             return PA_ERR_WORKSPACE;
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // With chunks and decode tokens in one launch, the split of its SMs is
+    // computed by one extra block of the write's launch.
+    pa::MixPlanArgs plan_job;
+    const bool plan_in_write =
+        one && !none_w && pa::mixed_plan_args(&plan_job, cu_q_lens, num_prefills, g, num_heads,
+                                              max_blocks_per_seq, seq_lens, num_seqs, workspace,
+                                              kv8);
     // The step's new K/V into their slots (one row per query row).
     if (!none_w) {
+        const pa::MixPlanArgs *job = plan_in_write ? &plan_job : nullptr;
         const cudaError_t e =
             kv8 ? pa::launch_cache_write_fp8(kv_cache, g, k_new, v_new,
                                              (int64_t)num_kv_heads * head_size, slot_mapping,
-                                             (int)rows, k_scale, v_scale, s)
+                                             (int)rows, k_scale, v_scale, s, job)
                 : pa::launch_cache_write(kv_cache, g, k_new, v_new,
                                          (int64_t)num_kv_heads * head_size, slot_mapping,
-                                         (int)rows, s);
+                                         (int)rows, s, job);
         if (e != cudaSuccess) return PA_ERR_CUDA;
     }
     // Chunks and decode tokens in one launch when both are present: side by side
@@ -565,7 +573,8 @@ static pa_status varlen_impl(void *out, const void *q, const void *k_new, const 
         return from_cuda(pa::launch_mixed(out, q, cu_q_lens, num_prefills, num_prefill_tokens,
                                           max_prefill_q_len, kv_cache, g, num_heads,
                                           block_tables, max_blocks_per_seq, seq_lens, num_seqs,
-                                          scale, workspace, kv8, k_scale, v_scale, s));
+                                          scale, workspace, kv8, k_scale, v_scale, s,
+                                          plan_in_write));
     // Otherwise one part at a time: the chunks (sequences [0, num_prefills), query
     // rows [0, num_prefill_tokens)), then the decode tokens (one row each).
     if (!none_p) {
@@ -579,13 +588,15 @@ static pa_status varlen_impl(void *out, const void *q, const void *k_new, const 
         if (e != cudaSuccess) return PA_ERR_CUDA;
     }
     if (!none_d) {
+        // Right after the write (no chunks between): the decode's set-up overlaps it.
+        const bool after_write = !none_w && none_p;
         const cudaError_t e =
             kv8 ? pa::launch_decode_fp8(dec_out, dec_q, kv_cache, g, num_heads, dec_tables,
                                         max_blocks_per_seq, dec_lens, num_decodes, max_seq_len,
-                                        scale, k_scale, v_scale, workspace, s)
+                                        scale, k_scale, v_scale, workspace, s, after_write)
                 : pa::launch_decode(dec_out, dec_q, kv_cache, g, num_heads, dec_tables,
                                     max_blocks_per_seq, dec_lens, num_decodes, max_seq_len, scale,
-                                    workspace, s);
+                                    workspace, s, after_write);
         if (e != cudaSuccess) return PA_ERR_CUDA;
     }
     return PA_OK;
@@ -620,6 +631,18 @@ pa_status pa_attention_varlen_fp8(void *out, const void *q, const void *k_new,
                        num_heads, num_kv_heads, head_size, block_tables, max_blocks_per_seq,
                        seq_lens, max_seq_len, scale, true, k_scale, v_scale, workspace,
                        workspace_bytes, stream);
+}
+
+size_t pa_varlen_args_bytes(void) { return sizeof(pa_varlen_args); }
+
+pa_status pa_attention_varlen_packed(const pa_varlen_args *a) {
+    if (!a) return PA_ERR_INVALID_ARG;
+    return varlen_impl(a->out, a->q, a->k_new, a->v_new, a->slot_mapping, a->cu_q_lens,
+                       a->num_seqs, a->num_prefills, a->num_prefill_tokens, a->max_prefill_q_len,
+                       a->kv_cache, a->num_blocks, a->block_size, a->num_heads, a->num_kv_heads,
+                       a->head_size, a->block_tables, a->max_blocks_per_seq, a->seq_lens,
+                       a->max_seq_len, a->scale, a->kv8 != 0, a->k_scale, a->v_scale,
+                       a->workspace, a->workspace_bytes, a->stream);
 }
 
 pa_status pa_prefill_chunk_fp8(void *out, const void *q, const int32_t *cu_q_lens,

@@ -4,6 +4,7 @@
 #include <type_traits>
 
 #include "pa_decode.cuh"
+#include "pa_plan.cuh"
 #include "pa_prefill.cuh"
 
 // ----------------------------------------------------------------------------
@@ -34,74 +35,10 @@ constexpr float kMixDecodeSmGBs = 96.0f, kMixHbmGBs = 7000.0f, kMixPrefillSmTflo
 // within 1 % of its best for 52 to 70 decode SMs on the mixed workload).
 constexpr float kMixDecodeSmGBsFp8 = 46.0f;
 
-struct MixPlanArgs {
-    const int32_t *seq_lens;   // all sequences, chunks first
-    const int32_t *cu_q_lens;  // chunk row offsets [num_prefills + 1]
-    int num_prefills, num_seqs, sms, max_len;
-    float dec_bytes_per_token;  // K+V bytes per decode token: 2 * Hkv * D * 2
-    float pre_flops_per_pair;   // flops per visible (query, key) pair: 4 * Hq * D
-    float dec_sm_gbs, hbm_gbs, pre_sm_tflops;  // rates of the two parts
-    int dec_warps;               // decode warps per decode CTA
-    int *plan;                   // out: {decode CTAs, decode warps}
-};
-
-// Decode bytes and prefill flops of the batch, then the number of decode SMs k
-// that makes both parts finish together: min over k of
-// max(bytes / min(k * decode rate, HBM), flops / ((sms - k) * prefill rate)).
-// fp32 throughout (the choice needs no more; this GPU's fp64 rate is low), the
-// search spread over one warp.
+// The split as a launch of its own, where no cache write precedes the mixed
+// launch.
 __global__ void __launch_bounds__(256) mix_plan_kernel(const MixPlanArgs a) {
-    __shared__ float s_dec[256], s_pre[256];
-    const int tid = threadIdx.x;
-    float dec = 0.f, pre = 0.f;
-    for (int s = tid; s < a.num_seqs; s += 256) {
-        const long long len = max(0, min(a.seq_lens[s], a.max_len));
-        if (s < a.num_prefills) {
-            const long long ql = a.cu_q_lens[s + 1] - a.cu_q_lens[s];
-            const long long ctx = max(0LL, len - ql);
-            pre += (float)(ql * ctx + ql * (ql + 1) / 2);
-        } else {
-            dec += (float)len;
-        }
-    }
-    s_dec[tid] = dec;
-    s_pre[tid] = pre;
-    __syncthreads();
-    for (int o = 128; o > 0; o >>= 1) {
-        if (tid < o) {
-            s_dec[tid] += s_dec[tid + o];
-            s_pre[tid] += s_pre[tid + o];
-        }
-        __syncthreads();
-    }
-    if (tid < 32) {
-        // times in microseconds: bytes / (GB/s * 1e3), flops / (TFLOP/s * 1e6)
-        const float bytes = s_dec[0] * a.dec_bytes_per_token;
-        const float flops = s_pre[0] * a.pre_flops_per_pair;
-        int best = 1;
-        float best_t = 3.0e38f;
-        for (int k = 1 + tid; k < a.sms; k += 32) {
-            const float td = bytes / (fminf(k * a.dec_sm_gbs, a.hbm_gbs) * 1e3f);
-            const float tp = flops / ((a.sms - k) * a.pre_sm_tflops * 1e6f);
-            const float t = fmaxf(td, tp);
-            if (t < best_t) {
-                best_t = t;
-                best = k;
-            }
-        }
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ot = __shfl_xor_sync(0xffffffffu, best_t, o);
-            const int ok = __shfl_xor_sync(0xffffffffu, best, o);
-            if (ot < best_t || (ot == best_t && ok < best)) {
-                best_t = ot;
-                best = ok;
-            }
-        }
-        if (tid == 0) {
-            a.plan[0] = best;
-            a.plan[1] = best * a.dec_warps;
-        }
-    }
+    mix_plan_block(a);
 }
 
 // KV8: an FP8 pool for both roles (the prefill role's converter is warp 11).
@@ -202,12 +139,41 @@ bool mixed_supported(int num_decodes, int num_heads, const KvGeom &g, bool kv8) 
     return mixed_decode_warps(num_decodes, num_heads, g, kv8) > 0;
 }
 
+bool mixed_plan_args(MixPlanArgs *pl, const int32_t *cu_q_lens, int num_prefills,
+                     const KvGeom &g, int num_heads, int max_blocks_per_seq,
+                     const int32_t *seq_lens, int num_seqs, void *workspace, bool kv8) {
+    const int sms = device_sm_count();
+    const int D = g.head_size, num_decodes = num_seqs - num_prefills;
+    // The decode's rate per SM scales with its warps (each holds the same bytes
+    // in flight).
+    const int dw = mixed_decode_warps(num_decodes, num_heads, g, kv8);
+    if (dw == 0) return false;
+    pl->seq_lens = seq_lens;
+    pl->cu_q_lens = cu_q_lens;
+    pl->num_prefills = num_prefills;
+    pl->num_seqs = num_seqs;
+    pl->sms = sms;
+    pl->max_len = max_blocks_per_seq * g.block_size;
+    pl->dec_bytes_per_token = 2.0f * g.num_kv_heads * D * (kv8 ? 1 : 2);
+    pl->pre_flops_per_pair = 4.0f * num_heads * D;
+    // FP8 pool (measured on GB300): decode about kMixDecodeSmGBsFp8 per SM with 12
+    // warps x 3 stages, 6.3 TB/s at most; the prefill, with its conversion, about
+    // 7.1 TFLOP/s per SM.
+    pl->dec_warps = dw;
+    pl->dec_sm_gbs = (kv8 ? kMixDecodeSmGBsFp8 : kMixDecodeSmGBs) * dw / kDecodeWarps;
+    pl->hbm_gbs = kv8 ? 6300.f : kMixHbmGBs;
+    pl->pre_sm_tflops = kv8 ? 7.1f : kMixPrefillSmTflops;
+    pl->plan = reinterpret_cast<int *>(static_cast<uint8_t *>(workspace) +
+                                       decode_workspace_bytes(num_decodes, D, sms));
+    return true;
+}
+
 cudaError_t launch_mixed(void *out, const void *q, const int32_t *cu_q_lens, int num_prefills,
                          int num_prefill_tokens, int max_prefill_q_len, const void *kv_cache,
                          const KvGeom &g, int num_heads, const int32_t *block_tables,
                          int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs,
                          float scale, void *workspace, bool kv8, float k_scale, float v_scale,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, bool plan_done) {
     const int sms = device_sm_count();
     const int D = g.head_size, num_decodes = num_seqs - num_prefills;
     CUtensorMap map;
@@ -215,32 +181,17 @@ cudaError_t launch_mixed(void *out, const void *q, const int32_t *cu_q_lens, int
     if (!(kv8 ? encode_kv_map_fp8(&map, kv_cache, g, box_rows)
               : encode_kv_map(&map, kv_cache, g, box_rows)))
         return cudaErrorInvalidValue;
-    int *plan = reinterpret_cast<int *>(static_cast<uint8_t *>(workspace) +
-                                        decode_workspace_bytes(num_decodes, D, sms));
     MixPlanArgs pl;
-    pl.seq_lens = seq_lens;
-    pl.cu_q_lens = cu_q_lens;
-    pl.num_prefills = num_prefills;
-    pl.num_seqs = num_seqs;
-    pl.sms = sms;
-    pl.max_len = max_blocks_per_seq * g.block_size;
-    pl.dec_bytes_per_token = 2.0f * g.num_kv_heads * D * (kv8 ? 1 : 2);
-    pl.pre_flops_per_pair = 4.0f * num_heads * D;
-    // FP8 pool (measured on GB300): decode about kMixDecodeSmGBsFp8 per SM with 12
-    // warps x 3 stages, 6.3 TB/s at most; the prefill, with its conversion, about
-    // 7.1 TFLOP/s per SM.
-    // The decode's rate per SM scales with its warps (each holds the same bytes
-    // in flight).
-    const int dw = mixed_decode_warps(num_decodes, num_heads, g, kv8);
-    if (dw == 0) return cudaErrorInvalidValue;
-    pl.dec_warps = dw;
-    pl.dec_sm_gbs = (kv8 ? kMixDecodeSmGBsFp8 : kMixDecodeSmGBs) * dw / kDecodeWarps;
-    pl.hbm_gbs = kv8 ? 6300.f : kMixHbmGBs;
-    pl.pre_sm_tflops = kv8 ? 7.1f : kMixPrefillSmTflops;
-    pl.plan = plan;
-    mix_plan_kernel<<<1, 256, 0, stream>>>(pl);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    if (!mixed_plan_args(&pl, cu_q_lens, num_prefills, g, num_heads, max_blocks_per_seq,
+                         seq_lens, num_seqs, workspace, kv8))
+        return cudaErrorInvalidValue;
+    const int dw = pl.dec_warps;
+    int *plan = pl.plan;
+    if (!plan_done) {
+        mix_plan_kernel<<<1, 256, 0, stream>>>(pl);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     const size_t off = (size_t)num_prefill_tokens * num_heads * D * 2;
     DecodeArgs da = make_decode_args(static_cast<uint8_t *>(out) + off,
                                      static_cast<const uint8_t *>(q) + off, g, num_heads,

@@ -339,6 +339,10 @@ __device__ __forceinline__ void decode_body(const CUtensorMap &kv_map, const Dec
 
     const int ahead = a.depth > 0 && a.depth < S ? a.depth : S;
     const int first_issue = n < ahead ? n : ahead;
+    // Launched as a programmatic dependent of the cache write that fills the
+    // pool, the set-up above overlaps that write; the pool is read only after it
+    // has completed (a no-op in any other launch).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int i = 0; i < first_issue; ++i) issue(i);
     int issued = first_issue;
     // While the first tiles are in flight.
@@ -816,16 +820,34 @@ __global__ void __launch_bounds__(256) cascade_merge_kernel(const DecodeArgs a) 
     merge_segment<D, 4>(a.cs, s, h, n_dec, rec0);
 }
 
+// after_write: the kernel just before on the stream is this library's cache write
+// of the pool (it triggers its dependents at its start), so the decode launches
+// as its programmatic dependent.  Its inputs other than the pool were written
+// before that write began.
 template <int D, bool KV8>
 cudaError_t launch_decode_d(const DecodeArgs &a0, const CUtensorMap &map, int grid,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, bool after_write) {
     constexpr int S = KV8 ? kDecodeStagesFp8 : kDecodeStages;
     const size_t smem = decode_smem_bytes<D, KV8, S>(a0.num_seqs, a0.group);
     auto kern = decode_kernel<D, kDecodeWarps, S, KV8>;
     cudaError_t e = ensure_smem<decode_kernel<D, kDecodeWarps, S, KV8>>(smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kDecodeWarps * 32, smem, stream>>>(map, a0);
-    e = cudaGetLastError();
+    if (after_write) {
+        cudaLaunchConfig_t dcfg = {};
+        dcfg.gridDim = dim3((unsigned)grid);
+        dcfg.blockDim = dim3(kDecodeWarps * 32);
+        dcfg.dynamicSmemBytes = smem;
+        dcfg.stream = stream;
+        cudaLaunchAttribute dattr[1];
+        dattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        dattr[0].val.programmaticStreamSerializationAllowed = 1;
+        dcfg.attrs = dattr;
+        dcfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&dcfg, kern, map, a0);
+    } else {
+        kern<<<grid, kDecodeWarps * 32, smem, stream>>>(map, a0);
+        e = cudaGetLastError();
+    }
     if (e != cudaSuccess || a0.seg_ctas) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(a0.num_seqs * a0.num_kv_heads));
@@ -943,7 +965,8 @@ cudaError_t launch_decode_impl(void *out, const void *q, const void *kv_cache, c
                                const int32_t *seq_lens, int num_seqs, int max_seq_len,
                                int shared_len, float scale, void *workspace, const float *pre_ml,
                                const float *pre_acc, int pre_splits, void *whole, bool kv8,
-                               float k_scale, float v_scale, cudaStream_t stream) {
+                               float k_scale, float v_scale, cudaStream_t stream,
+                               bool after_write = false) {
     const int sms = device_sm_count();
     const int D = g.head_size;
     CUtensorMap map;
@@ -969,9 +992,9 @@ cudaError_t launch_decode_impl(void *out, const void *q, const void *kv_cache, c
     a.shared_len = shared_len;
     a.seg_ctas = seg_ctas ? 1 : 0;
     if (whole) set_cascade(a, whole, pre_ml, pre_acc, pre_splits);
-    if (kv8) return launch_decode_d<128, true>(a, map, (int)ctas, stream);
-    if (D == 128) return launch_decode_d<128, false>(a, map, (int)ctas, stream);
-    return launch_decode_d<64, false>(a, map, (int)ctas, stream);
+    if (kv8) return launch_decode_d<128, true>(a, map, (int)ctas, stream, after_write);
+    if (D == 128) return launch_decode_d<128, false>(a, map, (int)ctas, stream, after_write);
+    return launch_decode_d<64, false>(a, map, (int)ctas, stream, after_write);
 }
 
 
@@ -981,19 +1004,20 @@ cudaError_t launch_decode_impl(void *out, const void *q, const void *kv_cache, c
 cudaError_t launch_decode(void *out, const void *q, const void *kv_cache, const KvGeom &g,
                           int num_heads, const int32_t *block_tables, int max_blocks_per_seq,
                           const int32_t *seq_lens, int num_seqs, int max_seq_len, float scale,
-                          void *workspace, cudaStream_t stream) {
+                          void *workspace, cudaStream_t stream, bool after_write) {
     return launch_decode_impl(out, q, kv_cache, g, num_heads, block_tables, max_blocks_per_seq,
                               seq_lens, num_seqs, max_seq_len, 0, scale, workspace, nullptr,
-                              nullptr, 0, nullptr, false, 1.f, 1.f, stream);
+                              nullptr, 0, nullptr, false, 1.f, 1.f, stream, after_write);
 }
 
 cudaError_t launch_decode_fp8(void *out, const void *q, const void *kv_cache, const KvGeom &g,
                               int num_heads, const int32_t *block_tables, int max_blocks_per_seq,
                               const int32_t *seq_lens, int num_seqs, int max_seq_len, float scale,
-                              float k_scale, float v_scale, void *workspace, cudaStream_t stream) {
+                              float k_scale, float v_scale, void *workspace, cudaStream_t stream,
+                              bool after_write) {
     return launch_decode_impl(out, q, kv_cache, g, num_heads, block_tables, max_blocks_per_seq,
                               seq_lens, num_seqs, max_seq_len, 0, scale, workspace, nullptr,
-                              nullptr, 0, nullptr, true, k_scale, v_scale, stream);
+                              nullptr, 0, nullptr, true, k_scale, v_scale, stream, after_write);
 }
 
 cudaError_t launch_decode_suffix(void *out, const void *q, const void *kv_cache, const KvGeom &g,

@@ -55,9 +55,24 @@ bool encode_kv_map_fp8(CUtensorMap *map, const void *kv_cache, const KvGeom &g, 
 
 int device_sm_count();
 
+// Inputs of the device-side split of a mixed launch's SMs (pa_plan.cuh).
+struct MixPlanArgs {
+    const int32_t *seq_lens;   // all sequences, chunks first
+    const int32_t *cu_q_lens;  // chunk row offsets [num_prefills + 1]
+    int num_prefills, num_seqs, sms, max_len;
+    float dec_bytes_per_token;  // K+V bytes per decode token: 2 * Hkv * D * element bytes
+    float pre_flops_per_pair;   // flops per visible (query, key) pair: 4 * Hq * D
+    float dec_sm_gbs, hbm_gbs, pre_sm_tflops;  // rates of the two parts
+    int dec_warps;               // decode warps per decode CTA
+    int *plan;                   // out: {decode CTAs, decode warps}
+};
+
+// plan_job (optional): the split of the mixed launch that follows, computed by
+// one extra block of the same launch (no block waits on another).
 cudaError_t launch_cache_write(void *kv_cache, const KvGeom &g, const void *k_new,
                                const void *v_new, int64_t new_row_stride,
-                               const int32_t *slot_mapping, int num_tokens, cudaStream_t stream);
+                               const int32_t *slot_mapping, int num_tokens, cudaStream_t stream,
+                               const MixPlanArgs *plan_job = nullptr);
 
 // Whether pa_decode (no shared prefix) over this shape runs one CTA per segment
 // and merges in place: one launch instead of the split kernel and its merge.
@@ -71,16 +86,21 @@ int decode_max_seqs(int head_size, int group, bool kv8 = false);
 cudaError_t launch_cache_write_fp8(void *kv_cache, const KvGeom &g, const void *k_new,
                                    const void *v_new, int64_t new_row_stride,
                                    const int32_t *slot_mapping, int num_tokens, float k_scale,
-                                   float v_scale, cudaStream_t stream);
+                                   float v_scale, cudaStream_t stream,
+                                   const MixPlanArgs *plan_job = nullptr);
 cudaError_t launch_decode_fp8(void *out, const void *q, const void *kv_cache, const KvGeom &g,
                               int num_heads, const int32_t *block_tables, int max_blocks_per_seq,
                               const int32_t *seq_lens, int num_seqs, int max_seq_len, float scale,
-                              float k_scale, float v_scale, void *workspace, cudaStream_t stream);
+                              float k_scale, float v_scale, void *workspace, cudaStream_t stream,
+                              bool after_write = false);
 
+// after_write: the launch just before on the stream is launch_cache_write(_fp8)
+// of this pool; the decode then starts as its programmatic dependent (its set-up
+// overlaps the write, its reads of the pool wait for the write to complete).
 cudaError_t launch_decode(void *out, const void *q, const void *kv_cache, const KvGeom &g,
                           int num_heads, const int32_t *block_tables, int max_blocks_per_seq,
                           const int32_t *seq_lens, int num_seqs, int max_seq_len, float scale,
-                          void *workspace, cudaStream_t stream);
+                          void *workspace, cudaStream_t stream, bool after_write = false);
 
 // Shared-prefix (cascade) decode.  The first shared_len tokens of every sequence
 // sit in sequence 0's first blocks.  The prefix pass computes, per key-range split,
@@ -127,12 +147,18 @@ cudaError_t launch_decode_suffix(void *out, const void *q, const void *kv_cache,
 // mixed_supported: whether the decode part's shared memory fits the launch.
 size_t mixed_workspace_bytes(int num_decodes, int head_size, int sm_count);
 bool mixed_supported(int num_decodes, int num_heads, const KvGeom &g, bool kv8);
+// The split's inputs for launch_mixed's batch (false: no mixed launch for it).
+bool mixed_plan_args(MixPlanArgs *pl, const int32_t *cu_q_lens, int num_prefills,
+                     const KvGeom &g, int num_heads, int max_blocks_per_seq,
+                     const int32_t *seq_lens, int num_seqs, void *workspace, bool kv8);
+// plan_done: a launch earlier on the stream ran mixed_plan_args' job (the cache
+// write's extra block), so no plan kernel is launched here.
 cudaError_t launch_mixed(void *out, const void *q, const int32_t *cu_q_lens, int num_prefills,
                          int num_prefill_tokens, int max_prefill_q_len, const void *kv_cache,
                          const KvGeom &g, int num_heads, const int32_t *block_tables,
                          int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs,
                          float scale, void *workspace, bool kv8, float k_scale, float v_scale,
-                         cudaStream_t stream);
+                         cudaStream_t stream, bool plan_done = false);
 
 // Chunked prefill over an FP8 pool (head_size 128).
 cudaError_t launch_prefill_fp8(void *out, const void *q, const int32_t *cu_q_lens,

@@ -205,3 +205,51 @@ def test_varlen_checks_everything_before_enqueueing(lib):
     bad[5] = FAKE
     bad[21] = FAKE + 64                         # workspace not 256-byte aligned
     assert lib.pa_attention_varlen(*bad) == 6
+
+
+def _packed(lib, args, kv8=0, k_scale=1.0, v_scale=1.0):
+    """pa_attention_varlen's argument list (as in the tests above) through
+    pa_attention_varlen_packed."""
+    (out, q, kn, vn, sm, cu, B, npf, npt, mq, kv, NB, bs, Hq, Hkv, D, bt, mb, sl, ml, scale, ws,
+     wsb, stream) = args
+    buf = ctypes.create_string_buffer(lib.pa_varlen_args_bytes())
+    binding.VARLEN_ARGS.pack_into(buf, 0, out or 0, q or 0, kn or 0, vn or 0, sm or 0, cu or 0,
+                                  kv or 0, bt or 0, sl or 0, ws or 0, wsb, stream or 0, B, npf,
+                                  npt, mq, NB, bs, Hq, Hkv, D, mb, ml, kv8, scale, k_scale,
+                                  v_scale)
+    return lib.pa_attention_varlen_packed(ctypes.addressof(buf))
+
+
+def test_packed_varlen_layout_and_host_checks(lib):
+    """The packed struct's layout (12 eight-byte fields, 12 int32, 3 float) and
+    the same statuses as the unpacked calls, each decided by a different field."""
+    assert lib.pa_varlen_args_bytes() == 160 and binding.VARLEN_ARGS.size == 156
+    assert lib.pa_attention_varlen_packed(None) == 1
+    args = [FAKE, FAKE, None, None, None, FAKE, 4, 2, 100, 64, FAKE, 10, 16, 32, 8, 128, FAKE, 4,
+            FAKE, 64, 0.1, FAKE, 1 << 30, None]
+    for i, v in ((7, 5), (8, 1)):               # num_prefills > num_seqs; too few chunk rows
+        bad = list(args)
+        bad[i] = v
+        assert _packed(lib, bad) == lib.pa_attention_varlen(*bad) == 1
+    bad = list(args)
+    bad[6] = bad[7] = bad[8] = 0                # empty batch: no-op
+    assert _packed(lib, bad) == 0
+    w = [FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 2, 4, 2, 100, 64, FAKE, 10, 16, 32, 8, 128, FAKE, 4,
+         FAKE, 64, 0.1, FAKE, 1 << 30, None]
+    assert _packed(lib, w) == 1                 # misaligned cu_q_lens
+    assert _packed(lib, w, kv8=1, k_scale=0.5, v_scale=0.5) == 1
+    bad = list(w)
+    bad[5] = FAKE
+    bad[21] = FAKE + 64                         # workspace not 256-byte aligned
+    assert _packed(lib, bad) == lib.pa_attention_varlen(*bad) == 6
+    small = list(w)
+    small[5] = FAKE
+    small[22] = 1                               # workspace too small: all else valid
+    assert _packed(lib, small) == lib.pa_attention_varlen(*small) == 6
+    assert _packed(lib, small, kv8=1, k_scale=0.5, v_scale=0.5) == 6
+    assert _packed(lib, small, kv8=1, k_scale=0.0, v_scale=0.5) == 1   # scales must be > 0
+    assert _packed(lib, small, kv8=1, k_scale=0.5, v_scale=-1.0) == 1
+    bad = list(small)
+    bad[15] = 64                                # FP8 pool: head size 128 only
+    assert _packed(lib, bad, kv8=1, k_scale=0.5, v_scale=0.5) == 2
+    assert _packed(lib, bad) == 6               # a bf16 pool takes head size 64

@@ -86,6 +86,30 @@ def test_fp8_cache_write_saturates_rounds_ties_and_keeps_signs():
     assert np.array_equal(pool8.cpu().numpy(), want)
 
 
+@pytest.mark.parametrize("ks,vs", [
+    (2.0 ** -100, 2.0 ** 100),  # powers of two: the write multiplies by 1 / scale
+    (2.0 ** 126, 2.0 ** -126),  # reciprocals at the ends of the normal range
+    (2.0 ** 127, 0.75),         # 2^-127 is subnormal, 0.75 no power of two: division
+    (0.25, 3.0),
+])
+def test_fp8_cache_write_bit_exact_over_the_whole_exponent_range(ks, vs):
+    """x / scale, rounded to e4m3, for bf16 inputs of every binary32 exponent;
+    a power-of-two scale takes the multiply by its exact reciprocal, which must
+    give the same codes as the division."""
+    b = make_batch(name="w8e", seq_lens=[64], q_lens=[64], num_heads=4, num_kv_heads=4,
+                   head_size=128, block_size=16, scale=0.1, seed=811, device=DEV)
+    pool8 = fp8_pool_of(b)
+    g = torch.Generator().manual_seed(5)
+    e = torch.randint(-133, 128, b.k_new.shape, generator=g).float()
+    x = torch.sign(torch.randn(b.k_new.shape, generator=g)) * torch.exp2(e) * \
+        (1 + torch.randint(0, 16, b.k_new.shape, generator=g).float() / 16)
+    x = x.clamp(-3.0e38, 3.0e38)
+    b.k_new.copy_(x.to(torch.bfloat16).to(DEV))
+    b.v_new.copy_(x.flip(0).to(torch.bfloat16).to(DEV))
+    want = _write(b, pool8, ks, vs)
+    assert np.array_equal(pool8.cpu().numpy(), want)
+
+
 DECODE_SHAPES = [
     # seq_lens, Hq, Hkv, bs
     ([1, 15, 16, 17, 31, 32, 33, 100], 8, 8, 16),      # group 1

@@ -50,3 +50,39 @@ def test_graph_replay_of_write_and_decode_matches_eager(n):
         assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
     binding.pa_error_check()
     compare(out, oracle_rows(b, pool), f"graph replay, workload {n}")
+
+
+@pytest.mark.parametrize("n", [1, 2, 4])
+def test_graph_replay_of_the_varlen_step_matches_eager(n):
+    """The one-call step, captured: decode tokens only (1, 2: the decode starts
+    as a programmatic dependent of the write, a dependency the capture keeps) and
+    the mixed batch (4: the write's extra block chooses the split read by the
+    attention launch)."""
+    b = make_config(n, device=DEV)
+    n_pre = int((b.q_lens > 1).sum())
+    npt = int(b.cu_q_lens[n_pre])
+    max_q = int(b.q_lens[:n_pre].max()) if n_pre else 0
+    max_dec = int(b.seq_lens[n_pre:].max())
+    cu = b.cu_q_lens[:n_pre + 1].contiguous()
+    ws = torch.empty(binding.pa_attention_varlen_workspace_bytes(
+        b.num_seqs, n_pre, b.num_heads, b.num_kv_heads, b.head_size), dtype=torch.uint8,
+        device=DEV)
+    eager = torch.empty_like(b.q)
+    out = torch.empty_like(b.q)
+
+    def step(dst):
+        binding.pa_attention_varlen(dst, b.q, b.k_new, b.v_new, b.slot_mapping, cu, n_pre, npt,
+                                    max_q, b.kv_cache, b.block_tables, b.seq_lens, max_dec,
+                                    b.scale, ws)
+
+    step(eager)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step(out)
+    for _ in range(3):
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+    binding.pa_error_check()

@@ -10,7 +10,8 @@ import torch
 
 from paged_kv_cache_287_gb300 import binding
 from paged_kv_cache_287_gb300.workloads import make_batch, make_config
-from tests._gpu import bits, compare, gpu_decode, gpu_prefill, oracle_pool, oracle_rows
+from tests._gpu import (bits, compare, gpu_decode, gpu_prefill, gpu_write, oracle_pool,
+                        oracle_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -82,6 +83,41 @@ def test_varlen_mixed_workload_one_launch():
     rows = np.concatenate([np.arange(0, 4096, 97), np.arange(4096, 4344)]).astype(np.int32)
     compare(out[torch.as_tensor(rows, device=DEV).long()], oracle_rows(b, pool, rows),
             "mixed workload, unified call (sampled chunk rows, every decode row)")
+
+
+def test_varlen_split_from_the_write_launch_equals_its_own_launch():
+    """With a cache write in the call, the split of the mixed launch's SMs is
+    computed by one extra block of the write's launch; without one, by a launch
+    of its own.  Both compute the same split (256-thread blocks at 8 KV heads of
+    128), so the rows are equal bit for bit."""
+    a = make_config(4, device=DEV)
+    b = make_config(4, device=DEV)
+    out_a = varlen(a, 8)
+    gpu_write(b)
+    out_b = varlen(b, 8, write=False)
+    assert np.array_equal(bits(a.kv_cache), bits(b.kv_cache)), "same pool"
+    assert np.array_equal(bits(out_a), bits(out_b))
+
+
+@pytest.mark.parametrize("num_seqs", [4, 300])
+def test_varlen_decode_reads_the_tokens_its_call_just_wrote(num_seqs):
+    """Decode tokens only: the decode starts as a programmatic dependent of the
+    cache write and must read the pool only after that write completes.  With
+    one token per sequence the softmax has a single key, so each query head's
+    row is exactly its KV head's new V row; fresh V rows every call show a stale
+    read at once.  4 sequences: one CTA per (sequence, KV head); 300: the split
+    kernel and its merge kernel."""
+    b = make_batch(name=f"vw{num_seqs}", seq_lens=[1] * num_seqs, q_lens=[1] * num_seqs,
+                   num_heads=32, num_kv_heads=8, head_size=128, block_size=16,
+                   scale=128 ** -0.5, seed=990 + num_seqs, device=DEV)
+    G = b.num_heads // b.num_kv_heads
+    g = torch.Generator(device="cpu").manual_seed(num_seqs)
+    for it in range(12):
+        b.k_new.copy_(torch.randn(b.k_new.shape, generator=g).to(torch.bfloat16))
+        b.v_new.copy_(torch.randn(b.v_new.shape, generator=g).to(torch.bfloat16))
+        out = varlen(b, 0)
+        want = b.v_new.repeat_interleave(G, dim=1)  # [N, Hq, D]
+        assert torch.equal(out.view(torch.int16), want.view(torch.int16)), f"call {it}"
 
 
 @pytest.mark.parametrize("n_dec", [1, 31, 600])
