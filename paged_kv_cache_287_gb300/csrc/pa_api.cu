@@ -574,7 +574,7 @@ static pa_status varlen_impl(void *out, const void *q, const void *k_new, const 
                                           max_prefill_q_len, kv_cache, g, num_heads,
                                           block_tables, max_blocks_per_seq, seq_lens, num_seqs,
                                           scale, workspace, kv8, k_scale, v_scale, s,
-                                          plan_in_write));
+                                          plan_in_write, !none_w));
     // Otherwise one part at a time: the chunks (sequences [0, num_prefills), query
     // rows [0, num_prefill_tokens)), then the decode tokens (one row each).
     if (!none_p) {

@@ -49,6 +49,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     mixed_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs da,
                  const PrefillArgs pa, int dec_slots, uint3 pre_grid) {
     if ((int)blockIdx.x < dec_slots) {
+        // The plan may come from the cache write this launch depends on.
+        if (da.plan) asm volatile("griddepcontrol.wait;" ::: "memory");
         // Without a device plan every decode slot streams (da.total_warps warps).
         const int dec_ctas = da.plan ? da.plan[0] : dec_slots;
         if ((int)blockIdx.x < dec_ctas)
@@ -68,11 +70,14 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
 // the grid (one CTA per SM) is resident at once, and the merge CTAs take SMs as
 // this grid's CTAs leave them.  Otherwise the plain merge kernel follows as a
 // plain launch (the prefill CTAs come in waves, and early merge CTAs would hold
-// SMs they need).
+// SMs they need).  after_write: the launch just before on the stream is the
+// step's cache write (which triggers its dependents at its start); this launch
+// is then its programmatic dependent, and every read of the pool or of the
+// plan waits for the write to complete.
 template <int D, bool KV8, int DW = kDecodeWarps>
 cudaError_t launch_mixed_d(const CUtensorMap &map, const DecodeArgs &da, const PrefillArgs &pa,
                            dim3 pgrid, int dec_slots, size_t smem, cudaStream_t stream,
-                           bool cascade = false) {
+                           bool cascade = false, bool after_write = false) {
     auto kern = mixed_kernel<D, KV8, DW>;
     cudaError_t e = ensure_smem<mixed_kernel<D, KV8, DW>>(smem);
     if (e != cudaSuccess) return e;
@@ -84,12 +89,12 @@ cudaError_t launch_mixed_d(const CUtensorMap &map, const DecodeArgs &da, const P
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 0;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = after_write ? 1 : 0;
     e = cudaLaunchKernelEx(&cfg, kern, map, da, pa, dec_slots,
                            make_uint3(pgrid.x, pgrid.y, pgrid.z));
     if (e != cudaSuccess) return e;
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t mcfg = {};
     mcfg.stream = stream;
     mcfg.attrs = attr;
@@ -173,7 +178,7 @@ cudaError_t launch_mixed(void *out, const void *q, const int32_t *cu_q_lens, int
                          const KvGeom &g, int num_heads, const int32_t *block_tables,
                          int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs,
                          float scale, void *workspace, bool kv8, float k_scale, float v_scale,
-                         cudaStream_t stream, bool plan_done) {
+                         cudaStream_t stream, bool plan_done, bool after_write) {
     const int sms = device_sm_count();
     const int D = g.head_size, num_decodes = num_seqs - num_prefills;
     CUtensorMap map;
@@ -207,14 +212,18 @@ cudaError_t launch_mixed(void *out, const void *q, const int32_t *cu_q_lens, int
                           block_tables, max_blocks_per_seq, seq_lens, scale, &pgrid);
     pa.k_scale = k_scale;
     pa.v_scale = v_scale;
+    const bool aw = after_write;
     if (kv8)
-        return launch_mixed_d<128, true>(map, da, pa, pgrid, sms, TcLay<128>::kSmem, stream);
+        return launch_mixed_d<128, true>(map, da, pa, pgrid, sms, TcLay<128>::kSmem, stream,
+                                         false, aw);
     if (D == 128 && dw < kDecodeWarps)
         return launch_mixed_d<128, false, kDecodeWarps - 1>(map, da, pa, pgrid, sms,
-                                                            TcLay<128>::kSmem, stream);
+                                                            TcLay<128>::kSmem, stream, false, aw);
     if (D == 128)
-        return launch_mixed_d<128, false>(map, da, pa, pgrid, sms, TcLay<128>::kSmem, stream);
-    return launch_mixed_d<64, false>(map, da, pa, pgrid, sms, TcLay<64>::kSmem, stream);
+        return launch_mixed_d<128, false>(map, da, pa, pgrid, sms, TcLay<128>::kSmem, stream,
+                                          false, aw);
+    return launch_mixed_d<64, false>(map, da, pa, pgrid, sms, TcLay<64>::kSmem, stream, false,
+                                     aw);
 }
 
 // ----------------------------------------------------------------------------

@@ -152,13 +152,15 @@ bool mixed_plan_args(MixPlanArgs *pl, const int32_t *cu_q_lens, int num_prefills
                      const KvGeom &g, int num_heads, int max_blocks_per_seq,
                      const int32_t *seq_lens, int num_seqs, void *workspace, bool kv8);
 // plan_done: a launch earlier on the stream ran mixed_plan_args' job (the cache
-// write's extra block), so no plan kernel is launched here.
+// write's extra block), so no plan kernel is launched here.  after_write: the
+// launch just before on the stream is launch_cache_write(_fp8) of this pool; the
+// attention launch then starts as its programmatic dependent.
 cudaError_t launch_mixed(void *out, const void *q, const int32_t *cu_q_lens, int num_prefills,
                          int num_prefill_tokens, int max_prefill_q_len, const void *kv_cache,
                          const KvGeom &g, int num_heads, const int32_t *block_tables,
                          int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs,
                          float scale, void *workspace, bool kv8, float k_scale, float v_scale,
-                         cudaStream_t stream, bool plan_done = false);
+                         cudaStream_t stream, bool plan_done = false, bool after_write = false);
 
 // Chunked prefill over an FP8 pool (head_size 128).
 cudaError_t launch_prefill_fp8(void *out, const void *q, const int32_t *cu_q_lens,

@@ -253,6 +253,10 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &kv_map, const Pr
         };
         int nxt = box_row(0);
         int issued = 0;
+        // As a programmatic dependent of the cache write that fills the pool (the
+        // mixed launch of a step), the set-up above overlapped that write; the
+        // pool is read only after it has completed (a no-op in any other launch).
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         auto load = [&](uint8_t *dst, uint64_t *bar, int row) {
             if constexpr (KV8) {
                 // The tile's codes (128 bytes per key) into the slot's upper half.
