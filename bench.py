@@ -678,16 +678,25 @@ def run_ours(args, world, rank, local):
         else:
             binding.pa_cache_write(pool, k_new, v_new, slots, st)
 
-    def step(ev=None, st=None):
+    cu0 = b.cu_q_lens[:1].contiguous()  # no chunks: decode tokens only
+
+    def one_call(k_new, v_new, slots, q, tables, lens, st, dst=None):
+        """The step through the library's one call: the cache write, then the
+        decode as a programmatic dependent of the write (its set-up overlaps it)."""
+        dst = out if dst is None else dst
+        kw = {"kv_scales": (FP8_K_SCALE, FP8_V_SCALE)} if fp8 else {}
+        binding.pa_attention_varlen(dst, q, k_new, v_new, slots, cu0, 0, 0, 0, pool, tables,
+                                    lens, max_len, b.scale, ws, st, **kw)
+
+    def step(st=None, calls=None):
+        """One step: write the new tokens, then decode.  The shared-prefix decode
+        has no one-call form, so it (and calls == 2) runs the two calls."""
         st = stream if st is None else st
-        if ev is not None:
-            ev[0].record(st)
-        write(b.k_new, b.v_new, b.slot_mapping, st)
-        if ev is not None:
-            ev[1].record(st)
-        attend(b.q, b.block_tables, b.seq_lens, st)
-        if ev is not None:
-            ev[2].record(st)
+        if args.cascade or calls == 2:
+            write(b.k_new, b.v_new, b.slot_mapping, st)
+            attend(b.q, b.block_tables, b.seq_lens, st)
+        else:
+            one_call(b.k_new, b.v_new, b.slot_mapping, b.q, b.block_tables, b.seq_lens, st)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -708,9 +717,9 @@ def run_ours(args, world, rank, local):
                 step(st=cap)
         torch.cuda.synchronize(dev)
 
-    def timed():
+    def timed(calls=None):
+        """K steps (graph replays) between one pair of events on the stream."""
         n_rep = args.steps // per_graph if graph is not None else args.steps
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_rep)]
         start = torch.cuda.Event(enable_timing=True)
         stop = torch.cuda.Event(enable_timing=True)
         barrier(world)
@@ -721,36 +730,35 @@ def run_ours(args, world, rank, local):
         start.record(stream)
         for i in range(n_rep):
             if graph is not None:
-                evs[i][0].record(stream)
                 graph.replay()
-                evs[i][2].record(stream)
             else:
-                step(evs[i])
+                step(calls=calls)
         stop.record(stream)
         torch.cuda.synchronize(dev)
         if sampler:
             sampler.__exit__(None, None, None)
         barrier(world)
-        total_ms = start.elapsed_time(stop)
-        if graph is not None:  # the per-kernel split is not visible inside a replay
-            write_ms = float("nan")
-            decode_ms = sum(e[0].elapsed_time(e[2]) for e in evs) / args.steps
-        else:
-            write_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
-            decode_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
-        return total_ms, write_ms, decode_ms, (sampler.summary() if sampler else {})
+        return start.elapsed_time(stop), (sampler.summary() if sampler else {})
 
-    total_ms, write_ms, decode_ms, clocks = timed()
+    total_ms, clocks = timed()
     if rank == 0 and rejected_clocks(clocks):
-        total_ms, write_ms, decode_ms, clocks = timed()
+        total_ms, clocks = timed()
         clocks["remeasured"] = True
     binding.pa_error_check(stream)
     total_ms = max_over_ranks(total_ms, world, dev)
+    # The same steps as the two separate calls (eager only), for comparison.
+    two_calls_ms = None
+    if graph is None and not args.cascade:
+        for _ in range(3):
+            step(calls=2)
+        two_calls_ms = max_over_ranks(timed(calls=2)[0], world, dev)
     # The attention call alone: the median of individually event-timed launches
-    # (the roofline's duration), after the timed steps.
+    # (the roofline's duration); the cache write's device time back to back.
     runs = max(50, args.median_runs)
-    decode_med_ms = decode_ms if graph is not None else median_launch_ms(
+    decode_med_ms = median_launch_ms(
         lambda: attend(b.q, b.block_tables, b.seq_lens, stream), stream, runs)
+    write_ms = back_to_back_ms(lambda: write(b.k_new, b.v_new, b.slot_mapping, stream), stream)
+    decode_ms = decode_med_ms
 
     # End to end: every step's inputs from pinned host memory, its output back to
     # pinned host memory.  Two buffer sets and one stream per copy direction:
@@ -800,9 +808,13 @@ def run_ours(args, world, rank, local):
             dev_buf[p].copy_(host_buf, non_blocking=True)
         landed[p].record(copy_in)
         stream.wait_event(landed[p])
-        write(dev_in[p]["k_new"], dev_in[p]["v_new"], dev_in[p]["slot_mapping"], stream)
-        attend(dev_in[p]["q"], dev_in[p]["block_tables"], dev_in[p]["seq_lens"], stream,
-               dst=dev_out[p])
+        x = dev_in[p]
+        if args.cascade:
+            write(x["k_new"], x["v_new"], x["slot_mapping"], stream)
+            attend(x["q"], x["block_tables"], x["seq_lens"], stream, dst=dev_out[p])
+        else:
+            one_call(x["k_new"], x["v_new"], x["slot_mapping"], x["q"], x["block_tables"],
+                     x["seq_lens"], stream, dst=dev_out[p])
         done[p].record(stream)
         copy_out.wait_event(done[p])
         with torch.cuda.stream(copy_out):
@@ -862,12 +874,20 @@ def run_ours(args, world, rank, local):
                      "frac": achieved / peak, "traffic": profile_traffic(traffic_file),
                      "kernel": kernel,
                      "algorithmic_bytes_per_launch": alg, "launch_ms": decode_med_ms,
-                     "launch_ms_how": (f"median of {runs} individually event-timed launches"
-                                       if graph is None else "mean over the graph replays"),
-                     "launch_ms_mean_in_steps": decode_ms,
+                     "launch_ms_how": f"median of {runs} individually event-timed launches",
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s"},
+        "step": ("pa_cache_write, then " + kernel if args.cascade else
+                 "pa_attention_varlen on the decode tokens: the cache write, then the decode "
+                 "as its programmatic dependent (one call)"),
         "kernels_ms": {"pa_cache_write": write_ms, "pa_decode": decode_ms},
+        "kernels_ms_how": "the write: 20 launches back to back per pair of events; the "
+                          "decode: median of individually event-timed launches",
+        **({"two_calls": {"ms_per_step": two_calls_ms / args.steps,
+                          "value": world * kv * args.steps / (two_calls_ms / 1e3) / 1e9,
+                          "step": "pa_cache_write + pa_decode"
+                                  + ("_fp8" if fp8 else "") + ", two calls"}}
+           if two_calls_ms is not None else {}),
         "e2e": {"value": world * kv * n_e2e / e2e_s / 1e9, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
                 "note": "KV pool resident in HBM (the cache); every step's inputs copied in "
