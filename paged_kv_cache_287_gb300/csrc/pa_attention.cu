@@ -27,9 +27,12 @@ constexpr int kMixStages = 2;
 // An FP8 tile is half the bytes: three stages per warp.
 constexpr int kMixStagesFp8 = 3;
 // Rates measured on GB300 for the split (bf16 pool): decode with 12 warps x 2
-// stages streams about 96 GB/s per SM, 7.0 TB/s at most in all; chunked prefill
-// does about 7.5 TFLOP/s per SM.  FP8 pool: see launch_mixed.
-constexpr float kMixDecodeSmGBs = 96.0f, kMixHbmGBs = 7000.0f, kMixPrefillSmTflops = 7.5f;
+// stages streams about 88 GB/s per SM beside the prefill (whose CTAs start while
+// the step's cache write runs), 7.0 TB/s at most in all; chunked prefill does
+// about 7.5 TFLOP/s per SM.  On the mixed workload the step is fastest with 56
+// decode SMs (433-436 us against 461-466 with 52 and 445 with 60), which these
+// rates choose.  FP8 pool: see launch_mixed.
+constexpr float kMixDecodeSmGBs = 88.0f, kMixHbmGBs = 7000.0f, kMixPrefillSmTflops = 7.5f;
 // FP8 pool: the decode issues about 2.6 times the instructions per byte and
 // streams about 46 GB/s per SM on part of the GPU (measured: the mixed step is
 // within 1 % of its best for 52 to 70 decode SMs on the mixed workload).
