@@ -211,3 +211,51 @@ def test_varlen_host_fault_leaves_the_pool_untouched(fp8):
     torch.cuda.synchronize()
     assert binding.STATUS[status] == "PA_ERR_INVALID_ARG"
     assert torch.equal(pool.view(torch.uint8), before.view(torch.uint8))
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_unpacked_and_packed_entry_points_agree_bitwise(fp8):
+    """pa_attention_varlen(_fp8) with its 24 (26) arguments and
+    pa_attention_varlen_packed (which the binding calls) run the same step: the
+    same pool bytes and the same output bits, chunks and decode tokens in one
+    launch."""
+    import ctypes
+    from paged_kv_cache_287_gb300.workloads import FP8_K_SCALE, FP8_V_SCALE, fp8_pool_of
+    lens, qls = [300, 40, 513, 90, 17, 1], [129, 40, 1, 1, 1, 1]
+    kw = dict(name="vpk", seq_lens=lens, q_lens=qls, num_heads=32, num_kv_heads=8,
+              head_size=128, block_size=16, scale=128 ** -0.5, seed=981, device=DEV)
+    outs, pools = [], []
+    for packed in (False, True):
+        b = make_batch(**kw)
+        pool = fp8_pool_of(b) if fp8 else b.kv_cache
+        cu = b.cu_q_lens[:3].contiguous()
+        npt = int(b.cu_q_lens[2])
+        max_dec = int(b.seq_lens[2:].max())
+        ws = torch.empty(binding.pa_attention_varlen_workspace_bytes(
+            b.num_seqs, 2, b.num_heads, b.num_kv_heads, b.head_size), dtype=torch.uint8,
+            device=DEV)
+        out = torch.full_like(b.q, float("nan"))
+        if packed:
+            kv = {"kv_scales": (FP8_K_SCALE, FP8_V_SCALE)} if fp8 else {}
+            binding.pa_attention_varlen(out, b.q, b.k_new, b.v_new, b.slot_mapping, cu, 2, npt,
+                                        129, pool, b.block_tables, b.seq_lens, max_dec,
+                                        b.scale, ws, **kv)
+        else:
+            L = binding.lib()
+            args = [out.data_ptr(), b.q.data_ptr(), b.k_new.data_ptr(), b.v_new.data_ptr(),
+                    b.slot_mapping.data_ptr(), cu.data_ptr(), b.num_seqs, 2, npt, 129,
+                    pool.data_ptr(), b.num_blocks, 16, 32, 8, 128, b.block_tables.data_ptr(),
+                    b.block_tables.shape[1], b.seq_lens.data_ptr(), max_dec,
+                    ctypes.c_float(b.scale)]
+            tail = [ws.data_ptr(), ws.numel(), torch.cuda.current_stream().cuda_stream]
+            if fp8:
+                st = L.pa_attention_varlen_fp8(*args, ctypes.c_float(FP8_K_SCALE),
+                                               ctypes.c_float(FP8_V_SCALE), *tail)
+            else:
+                st = L.pa_attention_varlen(*args, *tail)
+            assert st == 0
+        binding.pa_error_check()
+        outs.append(out)
+        pools.append(pool)
+    assert torch.equal(pools[0].view(torch.uint8), pools[1].view(torch.uint8))
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
