@@ -41,6 +41,7 @@ EXPORTS = ("pa_status_string", "pa_kv_block_bytes", "pa_kv_block_bytes_dtype", "
 # max_prefill_q_len, num_blocks, block_size, num_heads, num_kv_heads, head_size,
 # max_blocks_per_seq, max_seq_len, kv8; scale, k_scale, v_scale.
 VARLEN_ARGS = struct.Struct("<12Q12i3f")
+_BF16, _I32, _U8 = torch.bfloat16, torch.int32, torch.uint8
 _tls = threading.local()  # one packed-argument buffer per thread
 
 
@@ -401,32 +402,61 @@ def pa_attention_varlen(out: torch.Tensor, q: torch.Tensor, k_new: Optional[torc
     """One step over a flattened mixed batch (chunks first, then decode tokens):
     optional cache write, chunked prefill, decode.  A uint8 kv_cache is an FP8
     (e4m3) pool and needs kv_scales = (k_scale, v_scale)."""
-    fp8 = kv_cache.dtype is torch.uint8
-    if fp8:
-        if kv_scales is None:
-            raise ValueError("an FP8 pool needs kv_scales=(k_scale, v_scale)")
-        NB, bs, Hkv, D = _pool8_geom(kv_cache)
-    else:
-        NB, bs, Hkv, D = _pool_geom(kv_cache)
-    _need(q, "q", torch.bfloat16, 3)
-    _need(out, "out", torch.bfloat16, 3)
-    _need(cu_q_lens, "cu_q_lens", torch.int32, 1)
-    _need(block_tables, "block_tables", torch.int32, 2)
-    _need(seq_lens, "seq_lens", torch.int32, 1)
-    _need(workspace, "workspace", torch.uint8, 1)
+    fp8 = kv_cache.dtype is _U8
+    if fp8 and kv_scales is None:
+        raise ValueError("an FP8 pool needs kv_scales=(k_scale, v_scale)")
+    # Every tensor's device, dtype, rank and contiguity in one expression (this
+    # call runs once per step of a serving loop); any failure re-runs the
+    # argument-by-argument checks, which name the offending tensor.
+    try:
+        ks, qs, bts = kv_cache.shape, q.shape, block_tables.shape
+        ok = (len(ks) == 5 and ks[1] == 2 and len(qs) == 3 and len(bts) == 2
+              and kv_cache.is_cuda and kv_cache.is_contiguous()
+              and q.dtype is _BF16 and q.is_cuda and q.is_contiguous()
+              and out.dtype is _BF16 and out.is_cuda and out.is_contiguous()
+              and cu_q_lens.dtype is _I32 and cu_q_lens.is_cuda and cu_q_lens.dim() == 1
+              and cu_q_lens.is_contiguous()
+              and block_tables.dtype is _I32 and block_tables.is_cuda
+              and block_tables.is_contiguous()
+              and seq_lens.dtype is _I32 and seq_lens.is_cuda and seq_lens.dim() == 1
+              and seq_lens.is_contiguous()
+              and workspace.dtype is _U8 and workspace.is_cuda and workspace.dim() == 1
+              and workspace.is_contiguous()
+              and (fp8 or kv_cache.dtype is _BF16))
+    except (AttributeError, TypeError):
+        ok = False
+    if not ok:
+        (_pool8_geom if fp8 else _pool_geom)(kv_cache)
+        _need(q, "q", torch.bfloat16, 3)
+        _need(out, "out", torch.bfloat16, 3)
+        _need(cu_q_lens, "cu_q_lens", torch.int32, 1)
+        _need(block_tables, "block_tables", torch.int32, 2)
+        _need(seq_lens, "seq_lens", torch.int32, 1)
+        _need(workspace, "workspace", torch.uint8, 1)
+        ks, qs, bts = kv_cache.shape, q.shape, block_tables.shape
+    NB, _, Hkv, bs, D = ks
     B = seq_lens.shape[0]
-    rows, Hq, Dq = q.shape
-    if Dq != D or out.shape != q.shape or block_tables.shape[0] != B or \
+    rows, Hq, Dq = qs
+    if Dq != D or out.shape != qs or bts[0] != B or \
             rows != num_prefill_tokens + B - num_prefills:
         raise ValueError("inconsistent varlen shapes")
     kp = vp = sp = 0
     if slot_mapping is not None:
-        _need(k_new, "k_new", torch.bfloat16, 3)
-        _need(v_new, "v_new", torch.bfloat16, 3)
-        _need(slot_mapping, "slot_mapping", torch.int32, 1)
-        if k_new.shape != (rows, Hkv, D) or v_new.shape != (rows, Hkv, D) or \
-                slot_mapping.shape[0] != rows:
-            raise ValueError("k_new/v_new/slot_mapping must have one row per query row")
+        try:
+            ok = (k_new.dtype is _BF16 and k_new.is_cuda and k_new.is_contiguous()
+                  and v_new.dtype is _BF16 and v_new.is_cuda and v_new.is_contiguous()
+                  and slot_mapping.dtype is _I32 and slot_mapping.is_cuda
+                  and slot_mapping.is_contiguous())
+        except (AttributeError, TypeError):
+            ok = False
+        if not ok:
+            _need(k_new, "k_new", torch.bfloat16, 3)
+            _need(v_new, "v_new", torch.bfloat16, 3)
+            _need(slot_mapping, "slot_mapping", torch.int32, 1)
+        kv_rows = (rows, Hkv, D)
+        if k_new.shape != kv_rows or v_new.shape != kv_rows or slot_mapping.shape != (rows,):
+            raise ValueError("k_new/v_new [rows, num_kv_heads, head_size] and slot_mapping "
+                             "[rows]: one row per query row")
         kp, vp, sp = k_new.data_ptr(), v_new.data_ptr(), slot_mapping.data_ptr()
     L = _lib if _lib is not None else lib()
     try:
@@ -445,7 +475,7 @@ def pa_attention_varlen(out: torch.Tensor, q: torch.Tensor, k_new: Optional[torc
         buf, 0, out.data_ptr(), q.data_ptr(), kp, vp, sp, cu_q_lens.data_ptr(),
         kv_cache.data_ptr(), block_tables.data_ptr(), seq_lens.data_ptr(), workspace.data_ptr(),
         workspace.numel(), _stream(stream) or 0, B, int(num_prefills), int(num_prefill_tokens),
-        int(max_prefill_q_len), NB, bs, Hq, Hkv, D, block_tables.shape[1], int(max_seq_len), fp8,
+        int(max_prefill_q_len), NB, bs, Hq, Hkv, D, bts[1], int(max_seq_len), fp8,
         float(scale), ks, vs)
     st = L.pa_attention_varlen_packed(addr)
     if st:

@@ -253,3 +253,22 @@ def test_packed_varlen_layout_and_host_checks(lib):
     bad[15] = 64                                # FP8 pool: head size 128 only
     assert _packed(lib, bad, kv8=1, k_scale=0.5, v_scale=0.5) == 2
     assert _packed(lib, bad) == 6               # a bf16 pool takes head size 64
+
+
+def test_varlen_binding_checks_its_tensors_before_the_call(lib):
+    """The binding's one-expression check of every tensor falls back to the
+    argument-by-argument checks, which name the tensor at fault (here: host
+    tensors, so no call reaches the library)."""
+    import torch
+    from paged_kv_cache_287_gb300.workloads import make_config
+    b = make_config(1, device="cpu")
+    ws = torch.empty(1 << 16, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="kv_cache must be a CUDA tensor"):
+        binding.pa_attention_varlen(torch.empty_like(b.q), b.q, b.k_new, b.v_new,
+                                    b.slot_mapping, b.cu_q_lens[:1].contiguous(), 0, 0, 0,
+                                    b.kv_cache, b.block_tables, b.seq_lens, 80, b.scale, ws)
+    with pytest.raises(ValueError, match="kv_scales"):
+        binding.pa_attention_varlen(torch.empty_like(b.q), b.q, None, None, None,
+                                    b.cu_q_lens[:1].contiguous(), 0, 0, 0,
+                                    b.kv_cache.view(torch.uint8)[..., :64], b.block_tables,
+                                    b.seq_lens, 80, b.scale, ws)

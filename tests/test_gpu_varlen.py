@@ -259,3 +259,30 @@ def test_unpacked_and_packed_entry_points_agree_bitwise(fp8):
         pools.append(pool)
     assert torch.equal(pools[0].view(torch.uint8), pools[1].view(torch.uint8))
     assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+
+
+def test_varlen_binding_names_the_tensor_at_fault():
+    """Wrong shapes, dtypes or layouts raise ValueError before any launch."""
+    b = make_batch(name="vbad", seq_lens=[40, 20], q_lens=[8, 1], num_heads=8, num_kv_heads=2,
+                   head_size=128, block_size=16, scale=0.1, seed=951, device=DEV)
+    ws = torch.empty(binding.pa_attention_varlen_workspace_bytes(2, 1, 8, 2, 128),
+                     dtype=torch.uint8, device=DEV)
+    out = torch.empty_like(b.q)
+    cu = b.cu_q_lens[:2].contiguous()
+
+    def call(**kw):
+        a = dict(out=out, q=b.q, k_new=b.k_new, v_new=b.v_new, slot_mapping=b.slot_mapping)
+        a.update(kw)
+        binding.pa_attention_varlen(a["out"], a["q"], a["k_new"], a["v_new"], a["slot_mapping"],
+                                    cu, 1, 8, 8, b.kv_cache, b.block_tables, b.seq_lens, 20,
+                                    b.scale, ws)
+
+    with pytest.raises(ValueError, match="one row per query row"):
+        call(k_new=b.k_new[:-1])
+    with pytest.raises(ValueError, match="slot_mapping must be torch.int32"):
+        call(slot_mapping=b.slot_mapping.long())
+    with pytest.raises(ValueError, match="q must be contiguous"):
+        call(q=b.q.transpose(0, 1).contiguous().transpose(0, 1))
+    with pytest.raises(ValueError, match="inconsistent varlen shapes"):
+        call(out=out[:-1])
+    binding.pa_error_check()
