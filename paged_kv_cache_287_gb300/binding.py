@@ -168,16 +168,31 @@ def pa_kv_block_bytes(block_size: int, num_kv_heads: int, head_size: int) -> int
 def pa_cache_write(kv_cache: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
                    slot_mapping: torch.Tensor, stream=None) -> None:
     """Scatter k_new/v_new [N, Hkv, D] rows into kv_cache at slot_mapping [N]."""
-    NB, bs, Hkv, D = _pool_geom(kv_cache)
-    _need(k_new, "k_new", torch.bfloat16, 3)
-    _need(v_new, "v_new", torch.bfloat16, 3)
-    _need(slot_mapping, "slot_mapping", torch.int32, 1)
+    try:  # every tensor at once; on failure the per-argument checks name the culprit
+        ks = kv_cache.shape
+        ok = (len(ks) == 5 and ks[1] == 2
+              and kv_cache.dtype is _BF16 and kv_cache.is_cuda and kv_cache.is_contiguous()
+              and k_new.dtype is _BF16 and k_new.is_cuda and k_new.is_contiguous()
+              and v_new.dtype is _BF16 and v_new.is_cuda and v_new.is_contiguous()
+              and slot_mapping.dtype is _I32 and slot_mapping.is_cuda
+              and slot_mapping.dim() == 1 and slot_mapping.is_contiguous())
+    except (AttributeError, TypeError):
+        ok = False
+    if not ok:
+        _pool_geom(kv_cache)
+        _need(k_new, "k_new", torch.bfloat16, 3)
+        _need(v_new, "v_new", torch.bfloat16, 3)
+        _need(slot_mapping, "slot_mapping", torch.int32, 1)
+        ks = kv_cache.shape
+    NB, _, Hkv, bs, D = ks
     N = slot_mapping.shape[0]
-    if k_new.shape != (N, Hkv, D) or v_new.shape != (N, Hkv, D):
+    rows = (N, Hkv, D)
+    if k_new.shape != rows or v_new.shape != rows:
         raise ValueError("k_new/v_new must be [num_tokens, num_kv_heads, head_size]")
-    _check(lib().pa_cache_write(kv_cache.data_ptr(), NB, bs, Hkv, D, k_new.data_ptr(),
-                                v_new.data_ptr(), Hkv * D, slot_mapping.data_ptr(), N,
-                                _stream(stream)), "pa_cache_write")
+    L = _lib if _lib is not None else lib()
+    _check(L.pa_cache_write(kv_cache.data_ptr(), NB, bs, Hkv, D, k_new.data_ptr(),
+                            v_new.data_ptr(), Hkv * D, slot_mapping.data_ptr(), N,
+                            _stream(stream)), "pa_cache_write")
 
 
 def _pool8_geom(kv_cache: torch.Tensor):
@@ -264,19 +279,37 @@ def pa_decode(out: torch.Tensor, q: torch.Tensor, kv_cache: torch.Tensor,
               block_tables: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
               scale: float, workspace: torch.Tensor, stream=None) -> None:
     """Decode attention: q/out [B, Hq, D], block_tables [B, MB], seq_lens [B]."""
-    NB, bs, Hkv, D = _pool_geom(kv_cache)
-    _need(q, "q", torch.bfloat16, 3)
-    _need(out, "out", torch.bfloat16, 3)
-    _need(block_tables, "block_tables", torch.int32, 2)
-    _need(seq_lens, "seq_lens", torch.int32, 1)
-    _need(workspace, "workspace", torch.uint8, 1)
-    B, Hq, Dq = q.shape
-    if Dq != D or out.shape != q.shape or seq_lens.shape[0] != B or block_tables.shape[0] != B:
+    try:  # every tensor at once; on failure the per-argument checks name the culprit
+        ks, qs, bts = kv_cache.shape, q.shape, block_tables.shape
+        ok = (len(ks) == 5 and ks[1] == 2 and len(qs) == 3 and len(bts) == 2
+              and kv_cache.dtype is _BF16 and kv_cache.is_cuda and kv_cache.is_contiguous()
+              and q.dtype is _BF16 and q.is_cuda and q.is_contiguous()
+              and out.dtype is _BF16 and out.is_cuda and out.is_contiguous()
+              and block_tables.dtype is _I32 and block_tables.is_cuda
+              and block_tables.is_contiguous()
+              and seq_lens.dtype is _I32 and seq_lens.is_cuda and seq_lens.dim() == 1
+              and seq_lens.is_contiguous()
+              and workspace.dtype is _U8 and workspace.is_cuda and workspace.dim() == 1
+              and workspace.is_contiguous())
+    except (AttributeError, TypeError):
+        ok = False
+    if not ok:
+        _pool_geom(kv_cache)
+        _need(q, "q", torch.bfloat16, 3)
+        _need(out, "out", torch.bfloat16, 3)
+        _need(block_tables, "block_tables", torch.int32, 2)
+        _need(seq_lens, "seq_lens", torch.int32, 1)
+        _need(workspace, "workspace", torch.uint8, 1)
+        ks, qs, bts = kv_cache.shape, q.shape, block_tables.shape
+    NB, _, Hkv, bs, D = ks
+    B, Hq, Dq = qs
+    if Dq != D or out.shape != qs or seq_lens.shape[0] != B or bts[0] != B:
         raise ValueError("inconsistent decode shapes")
-    _check(lib().pa_decode(out.data_ptr(), q.data_ptr(), kv_cache.data_ptr(), NB, bs, Hq, Hkv, D,
-                           block_tables.data_ptr(), block_tables.shape[1], seq_lens.data_ptr(),
-                           B, int(max_seq_len), float(scale), workspace.data_ptr(),
-                           workspace.numel(), _stream(stream)), "pa_decode")
+    L = _lib if _lib is not None else lib()
+    _check(L.pa_decode(out.data_ptr(), q.data_ptr(), kv_cache.data_ptr(), NB, bs, Hq, Hkv, D,
+                       block_tables.data_ptr(), bts[1], seq_lens.data_ptr(), B,
+                       int(max_seq_len), float(scale), workspace.data_ptr(), workspace.numel(),
+                       _stream(stream)), "pa_decode")
 
 
 def pa_decode_noalloc(out: torch.Tensor, q: torch.Tensor, kv_cache: torch.Tensor,
