@@ -1,8 +1,11 @@
 """Benchmark: paged decode attention on GB300 through the C ABI.
 
 One step = one pass of the hot path over one batch: the cache write of every
-sequence's new token (pa_cache_write) followed by decode attention over the
-paged KV cache (pa_decode: the split-context kernel plus its merge kernel).
+sequence's new token followed by decode attention over the paged KV cache, as
+the library's one call for it (pa_attention_varlen on decode tokens: the write,
+then the split-context decode as the write's programmatic dependent, then its
+merge kernel); the same step as the two calls pa_cache_write + pa_decode is
+timed beside it.
 Default workload: the Llama-3-8B-shaped decode layer (256 sequences, 32 query /
 8 KV heads, head_size 128, block_size 16, lengths U{512..4096}).
 
