@@ -479,6 +479,24 @@ def by_workload(args, dev, stream) -> dict:
                                     wsv, st)
 
     eager, clk = timed(step1u, per_step)
+    # The same call as a C caller makes it: the argument struct filled once, one
+    # foreign call per step (no Python-side checks or marshalling).
+    L = binding.lib()
+    cbuf = ctypes.create_string_buffer(L.pa_varlen_args_bytes())
+    binding.VARLEN_ARGS.pack_into(
+        cbuf, 0, out.data_ptr(), b.q.data_ptr(), b.k_new.data_ptr(), b.v_new.data_ptr(),
+        b.slot_mapping.data_ptr(), cu0.data_ptr(), b.kv_cache.data_ptr(),
+        b.block_tables.data_ptr(), b.seq_lens.data_ptr(), wsv.data_ptr(), wsv.numel(),
+        stream.cuda_stream, b.num_seqs, 0, 0, 0, b.kv_cache.shape[0], b.block_size,
+        b.num_heads, b.num_kv_heads, b.head_size, b.block_tables.shape[1], max_len, 0,
+        b.scale, 1.0, 1.0)
+    caddr = ctypes.addressof(cbuf)
+
+    def step1c():
+        if L.pa_attention_varlen_packed(caddr):
+            raise RuntimeError("pa_attention_varlen_packed failed")
+
+    eager_c, clk_c = timed(step1c, per_step)
     graph, cap = torch.cuda.CUDAGraph(), torch.cuda.Stream(dev)
     torch.cuda.synchronize(dev)
     with torch.cuda.graph(graph, stream=cap):
@@ -492,6 +510,11 @@ def by_workload(args, dev, stream) -> dict:
               "two_calls": {"value": b.num_seqs / (eager2 / 1e3), "unit": "seqs/s",
                             "ms_per_step": eager2, "step": "pa_cache_write + pa_decode, eager",
                             "clocks": clk2},
+              "c_abi": {"value": b.num_seqs / (eager_c / 1e3), "unit": "seqs/s",
+                        "ms_per_step": eager_c,
+                        "step": "pa_attention_varlen_packed with the argument struct filled "
+                                "once (a C caller's cost: no Python-side checks), eager",
+                        "clocks": clk_c},
               "graph": {"value": b.num_seqs / (replay / 20 / 1e3), "unit": "seqs/s",
                         "ms_per_step": replay / 20, "steps_per_replay": 20,
                         "step": "the one-call step, 20 captured in one CUDA graph",

@@ -623,6 +623,27 @@ __device__ __forceinline__ void decode_body(const CUtensorMap &kv_map, const Dec
                 const uint4 *srcv = reinterpret_cast<const uint4 *>(stage_out);
                 for (int v = lane; v < G * D / 8; v += 32) dst[v] = srcv[v];
                 wrote_smem = true;
+            } else if (a.seg_ctas) {
+                // Segment-per-CTA mode: this warp's piece (its one tile is consumed)
+                // stays in its stage, [8 heads][D] of acc then [8 heads] of (m, l),
+                // for the CTA's merge after its barrier.
+                float *sacc = reinterpret_cast<float *>(stg);
+                float *sml = sacc + kHeadsPad * D;
+#pragma unroll
+                for (int mt = 0; mt < D / 16; ++mt) {
+                    const int d0 = dim_of(mt, 0), d1 = dim_of(mt, 1);
+                    sacc[hh0 * D + d0] = acc[mt][0];
+                    sacc[(hh0 + 1) * D + d0] = acc[mt][1];
+                    sacc[hh0 * D + d1] = acc[mt][2];
+                    sacc[(hh0 + 1) * D + d1] = acc[mt][3];
+                }
+                if (lane < 4) {
+                    sml[hh0 * 2] = m0;
+                    sml[hh0 * 2 + 1] = l0;
+                    sml[(hh0 + 1) * 2] = m1;
+                    sml[(hh0 + 1) * 2 + 1] = l1;
+                }
+                wrote_smem = true;
             } else {
                 // A piece of a split segment, or (cascade) a whole one: unnormalised
                 // (m, l, acc) for the merge kernel.
@@ -667,25 +688,57 @@ __device__ __forceinline__ void decode_body(const CUtensorMap &kv_map, const Dec
 }
 
 // Segment-per-CTA mode, once every warp of CTA cta has left decode_body: warp 0
-// merges the segment's pieces (slot 0 of warps cta W .. cta W + ne - 1) and
-// writes its rows; a segment of one tile is already written by its warp, and a
-// sequence of no tokens gets zero rows.  The tile count is recomputed from the
-// length exactly as decode_body clamps it.  Kept out of line: inlined, its
-// record registers made the streaming loop of every decode kernel spill.
-template <int D, int W>
+// merges the segment's pieces, which the warps left in their stages (warps
+// 0 .. ne - 1, one tile each), by log-sum-exp and writes its rows; a segment of
+// one tile is already written by its warp, and a sequence of no tokens gets
+// zero rows.  The tile counts come from the tables decode_body built in shared
+// memory.  Kept out of line: inlined, its registers made the streaming loop of
+// every decode kernel spill.
+template <int D, int W, int S, bool KV8>
 __device__ __noinline__ void seg_cta_merge(const DecodeArgs &a, int cta) {
-    __syncthreads();  // every piece's record written (visible to this CTA)
+    __syncthreads();  // every piece's record is in its warp's stage
     if (threadIdx.x >= 32) return;
+    extern __shared__ uint8_t smem_raw[];
+    const uint8_t *ring =
+        reinterpret_cast<const uint8_t *>(align_up(reinterpret_cast<size_t>(smem_raw), 1024));
+    const int *s_len = reinterpret_cast<const int *>(ring + (size_t)W * S * a.stage_bytes +
+                                                     (size_t)W * S * 8);
+    const int *s_pre = s_len + a.num_seqs;
+    const int lane = threadIdx.x, G = a.group;
     const int Hkv = a.num_kv_heads, s = cta / Hkv, h = cta - s * Hkv;
-    const int len = min(max(a.seq_lens[s], 0), a.max_blocks * a.block_size);
-    const int nt = (len + kTile - 1) / kTile;
+    const int nt = s_pre[s + 1] - s_pre[s];
     const int ne = nt < W ? nt : W;
+    __nv_bfloat16 *orow = a.out + ((size_t)s * a.num_heads + (size_t)h * G) * D;
     if (nt == 0) {
-        uint4 *dst =
-            reinterpret_cast<uint4 *>(a.out + ((size_t)s * a.num_heads + (size_t)h * a.group) * D);
-        for (int v = threadIdx.x; v < a.group * D / 8; v += 32) dst[v] = make_uint4(0u, 0u, 0u, 0u);
-    } else if (ne > 1) {
-        merge_segment<D, 2>(a.cs, s, h, ne, cta * W * 2);
+        uint4 *dst = reinterpret_cast<uint4 *>(orow);
+        for (int v = lane; v < G * D / 8; v += 32) dst[v] = make_uint4(0u, 0u, 0u, 0u);
+        return;
+    }
+    if (ne <= 1) return;
+    const size_t stride = (size_t)S * a.stage_bytes;  // between two warps' first stages
+    for (int e = lane; e < G * D / 4; e += 32) {
+        const int hh = e / (D / 4), c4 = 4 * (e - hh * (D / 4));
+        float M = -INFINITY;
+        for (int k = 0; k < ne; ++k) {
+            const float *ml = reinterpret_cast<const float *>(ring + k * stride) + kHeadsPad * D;
+            M = fmaxf(M, ml[hh * 2]);
+        }
+        float den = 0.f;
+        float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = 0; k < ne; ++k) {
+            const float *acc = reinterpret_cast<const float *>(ring + k * stride);
+            const float *ml = acc + kHeadsPad * D;
+            const float w = fast_exp2(ml[hh * 2] - M);
+            den += w * ml[hh * 2 + 1];
+            const float4 v = *reinterpret_cast<const float4 *>(acc + hh * D + c4);
+            num.x += w * v.x;
+            num.y += w * v.y;
+            num.z += w * v.z;
+            num.w += w * v.w;
+        }
+        const float inv = 1.f / den;
+        *reinterpret_cast<uint2 *>(orow + hh * D + c4) =
+            make_uint2(pack_bf16(num.x * inv, num.y * inv), pack_bf16(num.z * inv, num.w * inv));
     }
 }
 
@@ -693,7 +746,7 @@ template <int D, int W, int S, bool KV8>
 __global__ void __launch_bounds__(W * 32, 1)
     decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
     decode_body<D, W, S, KV8>(kv_map, a, blockIdx.x, a.total_warps);
-    if (a.seg_ctas) seg_cta_merge<D, W>(a, blockIdx.x);
+    if (a.seg_ctas) seg_cta_merge<D, W, S, KV8>(a, blockIdx.x);
 }
 
 // Merge the pieces of segments that were split across warps; zero empty
