@@ -202,6 +202,19 @@ def test_prefill_of_single_token_chunks_matches_decode():
     compare(gpu_decode(b), oracle_rows(b, pool), "decode")
 
 
+def test_prefill_more_chunks_than_the_ranking_holds():
+    """300 chunks: more than the kernel ranks by cached context (256), so the
+    CTAs take chunks in index order; short ragged chunks, some without context."""
+    g = np.random.default_rng(77)
+    qls = [int(x) for x in g.integers(2, 25, 300)]
+    lens = [q + int(c) for q, c in zip(qls, g.integers(0, 200, 300))]
+    b = make_batch(name="p300", seq_lens=lens, q_lens=qls, num_heads=8, num_kv_heads=2,
+                   head_size=128, block_size=16, scale=128 ** -0.5, seed=78, device=DEV)
+    pool = oracle_pool(b)
+    gpu_write(b)
+    compare(gpu_prefill(b), oracle_rows(b, pool), "prefill, 300 chunks")
+
+
 def test_prefill_long_context_and_empty_chunk():
     """A chunk after a 40 000-token cached context (316 K/V tiles through each
     query tile's hand-over chain), an empty chunk between two others, and a

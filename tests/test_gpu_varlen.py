@@ -65,6 +65,20 @@ def test_varlen_small_batches(shape):
     compare(out, oracle_rows(b, pool), f"varlen {lens}")
 
 
+def test_varlen_more_chunks_than_the_ranking_holds():
+    """270 prefill chunks (more than the 256 the kernel ranks by context) and 10
+    decode tokens in one call."""
+    g = np.random.default_rng(79)
+    qls = [int(x) for x in g.integers(2, 20, 270)] + [1] * 10
+    lens = [q + int(c) for q, c in zip(qls, g.integers(0, 300, 280))]
+    b = make_batch(name="v280", seq_lens=lens, q_lens=qls, num_heads=16, num_kv_heads=4,
+                   head_size=128, block_size=16, scale=128 ** -0.5, seed=80, device=DEV)
+    pool = oracle_pool(b)
+    out = varlen(b, 270)
+    assert np.array_equal(bits(b.kv_cache), pool), "cache write"
+    compare(out, oracle_rows(b, pool), "varlen, 270 chunks + 10 decode tokens")
+
+
 def test_varlen_mixed_workload_one_launch():
     """Chunks and decode tokens in one launch: the chunk rows equal the separate
     prefill call bit for bit (same kernel body), the decode rows match the oracle
