@@ -215,6 +215,19 @@ def test_prefill_more_chunks_than_the_ranking_holds():
     compare(gpu_prefill(b), oracle_rows(b, pool), "prefill, 300 chunks")
 
 
+def test_prefill_one_long_chunk():
+    """One 3000-token chunk after 1000 cached tokens (47 query-tile pairs, the
+    last ragged; the latest rows see 4000 keys); rows sampled across tiles."""
+    b = make_batch(name="pl1", seq_lens=[4000, 70], q_lens=[3000, 70], num_heads=32,
+                   num_kv_heads=8, head_size=128, block_size=16, scale=128 ** -0.5, seed=81,
+                   device=DEV)
+    pool = oracle_pool(b)
+    gpu_write(b)
+    out = gpu_prefill(b)
+    rows = [0, 1, 63, 64, 127, 128, 1000, 1999, 2047, 2048, 2943, 2944, 2998, 2999, 3000, 3069]
+    compare(out[rows], oracle_rows(b, pool, rows=rows), "prefill, one 3000-token chunk")
+
+
 def test_prefill_long_context_and_empty_chunk():
     """A chunk after a 40 000-token cached context (316 K/V tiles through each
     query tile's hand-over chain), an empty chunk between two others, and a
