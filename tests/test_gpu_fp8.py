@@ -207,6 +207,28 @@ def test_fp8_prefill_small_shapes(case):
     compare(out, _oracle(b, codes, FP8_K_SCALE, FP8_V_SCALE), f"fp8 prefill case {case}")
 
 
+def test_fp8_prefill_more_chunks_than_the_ranking_holds_and_one_long_chunk():
+    """300 short ragged chunks (past the 256 the kernel ranks by context), then
+    one 3000-token chunk after 1000 cached tokens, from an FP8 pool."""
+    g = np.random.default_rng(83)
+    qls = [int(x) for x in g.integers(2, 25, 300)]
+    lens = [q + int(c) for q, c in zip(qls, g.integers(0, 200, 300))]
+    for name, lens, qls, seed, rows in (
+            ("p8many", lens, qls, 84, None),
+            ("p8one", [4000, 70], [3000, 70], 85,
+             [0, 1, 63, 64, 127, 128, 1000, 2047, 2048, 2944, 2999, 3000, 3069])):
+        b = make_batch(name=name, seq_lens=lens, q_lens=qls, num_heads=16, num_kv_heads=4,
+                       head_size=128, block_size=16, scale=128 ** -0.5, seed=seed, device=DEV)
+        pool8 = fp8_pool_of(b)
+        codes = _write(b, pool8, FP8_K_SCALE, FP8_V_SCALE)
+        out = torch.full_like(b.q, float("nan"))
+        binding.pa_prefill_chunk_fp8(out, b.q, b.cu_q_lens, max(qls), pool8, b.block_tables,
+                                     b.seq_lens, b.scale, FP8_K_SCALE, FP8_V_SCALE)
+        binding.pa_error_check()
+        got = out if rows is None else out[rows]
+        compare(got, _oracle(b, codes, FP8_K_SCALE, FP8_V_SCALE, rows=rows), f"fp8 prefill {name}")
+
+
 def test_fp8_prefill_long_context_and_empty_chunk():
     """The FP8 prefill (conversion warp in the loop) over a 40 000-token cached
     context, with an empty chunk between two others."""
