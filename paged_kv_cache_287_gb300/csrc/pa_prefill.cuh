@@ -143,6 +143,8 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &kv_map, const Pr
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 26);
     // FP8 pool: a tile's codes have landed in its slot's upper half.
     uint64_t *k_staged = bars + 27, *v_staged = bars + 30;
+    static_assert(kKSlots <= 3 && kVSlots <= 2 && kTcTiles <= 2,
+                  "the fixed barrier offsets above hold 3 K slots, 2 V slots and 2 tiles");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // Grid (query tile, head, chunk rank): CTAs are dispatched in that order, so
