@@ -442,9 +442,10 @@ def by_workload(args, dev, stream) -> dict:
         launches += kernels * runs
         return ms, clk.summary()
 
-    def hbm_roof(alg, ms):
+    def hbm_roof(alg, ms, traffic_file=None):
         a = alg / (ms / 1e3) / 1e9
         return {"bound": "hbm", "achieved": a, "peak": hbm, "unit": "GB/s", "frac": a / hbm,
+                "traffic": profile_traffic(traffic_file) if traffic_file else None,
                 "algorithmic_bytes_per_launch": alg, "launch_ms": ms,
                 "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)"}
 
@@ -539,7 +540,8 @@ def by_workload(args, dev, stream) -> dict:
                                                  b.head_size) / (ms / 1e3) / 1e9,
                           "unit": "GB/s", "ms_per_step": ms,
                           "seqs_per_s": b.num_seqs / (ms / 1e3), "kernel": "pa_decode",
-                          "roofline": hbm_roof(decode_algorithmic_bytes(b), ms), "clocks": clk})
+                          "roofline": hbm_roof(decode_algorithmic_bytes(b), ms,
+                                               f"decode_{b.name}.traffic.txt"), "clocks": clk})
         pool8 = fp8_pool_of(b)
         b.kv_cache = torch.empty(0, device=dev)
         torch.cuda.empty_cache()
@@ -551,7 +553,8 @@ def by_workload(args, dev, stream) -> dict:
                                                b.head_size) / 2 / (ms / 1e3) / 1e9,
                         "unit": "GB/s", "ms_per_step": ms, "seqs_per_s": b.num_seqs / (ms / 1e3),
                         "kernel": "pa_decode_fp8",
-                        "roofline": hbm_roof(decode_algorithmic_bytes(b, 1), ms), "clocks": clk}
+                        "roofline": hbm_roof(decode_algorithmic_bytes(b, 1), ms,
+                                             f"decode_fp8_{b.name}.traffic.txt"), "clocks": clk}
         res[n] = entry
         del b, out, ws, pool8
         torch.cuda.empty_cache()
@@ -594,6 +597,8 @@ def by_workload(args, dev, stream) -> dict:
              "roofline": {"bound": "tensor", "achieved": tf, "peak": tfl, "unit": "TFLOP/s",
                           "frac": tf / tfl, "kernel": "pa_prefill_chunk" +
                           ("_fp8" if kind == "fp8" else ""),
+                          "traffic": profile_traffic(
+                              f"prefill{'_fp8' if kind == 'fp8' else ''}_{b.name}.traffic.txt"),
                           "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops)"},
              "clocks": clk}
         if kind == "fp8":
@@ -634,7 +639,8 @@ def by_workload(args, dev, stream) -> dict:
             ms, clk = timed(call, 2, flushed=timing == "cold")
             e[timing] = {"value": alg / (ms / 1e3) / 1e9, "unit": "GB/s (unique bytes)",
                          "ms_per_step": ms, "seqs_per_s": b.num_seqs / (ms / 1e3),
-                         "roofline": hbm_roof(alg, ms), "clocks": clk}
+                         "roofline": hbm_roof(alg, ms, f"cascade{'_fp8' if kind == 'fp8' else ''}"
+                                                       f"_{b.name}.traffic.txt"), "clocks": clk}
         c = dict(e["cold"], kernel="pa_decode_cascade" + ("_fp8" if kind == "fp8" else ""),
                  timing="cold (L2 flushed by writing 512 MB before each call)", warm=e["warm"])
         entry["cascade" if kind == "bf16" else "cascade_fp8"] = c
